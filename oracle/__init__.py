@@ -1,0 +1,161 @@
+"""CPU fp64 oracle for row-wise RMSNorm and fused residual Add + RMSNorm (forward, backward).
+
+TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the benchmark's CPU-baseline
+leg may import this package; the product path (the GPU library and its Python binding) never
+does, and this package imports nothing from it.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, single-threaded); this module only
+loads it with ctypes and marshals numpy arrays. Input encodings are taken from the numpy
+dtype: ``uint16`` arrays hold raw bf16 bit patterns, ``float32`` and ``float64`` arrays hold
+values. Every output is a float64 array.
+
+What each function computes, with the passage it follows, is stated in ``oracle.c``:
+  rmsnorm_fwd      y = x * rstd * w, rstd = 1/sqrt(mean(x^2) + eps)  (Machete, "Built-In Areas")
+  add_rmsnorm_fwd  the same on r = x + residual, also returning r  (KernelAgent page, Oink)
+  rmsnorm_bwd      dx and dw, the exact derivative of rmsnorm_fwd
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+import numpy as np
+
+from . import libbuild as _build
+
+BF16, F32, F64 = 0, 1, 2
+_CODES = {np.dtype(np.uint16): BF16, np.dtype(np.float32): F32, np.dtype(np.float64): F64}
+
+_dbl_p = ctypes.POINTER(ctypes.c_double)
+
+
+def _code(a: np.ndarray) -> int:
+    try:
+        return _CODES[a.dtype]
+    except KeyError:
+        raise TypeError(f"oracle input dtype {a.dtype} is not uint16 (bf16 bits), float32 or float64")
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _out(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(_dbl_p)
+
+
+class Oracle:
+    """ctypes handle on one compiled copy of ``oracle.c`` (the default build, or a test's)."""
+
+    def __init__(self, path: Optional[str] = None):
+        self.path = path or _build.build()
+        lib = ctypes.CDLL(self.path)
+        vp, i32, i64, dbl = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        lib.oracle_decode.argtypes = [vp, i32, i64, _dbl_p]
+        lib.oracle_add_rmsnorm_fwd.argtypes = [vp, i32, vp, i32, vp, i32, i64, i64, dbl,
+                                               _dbl_p, _dbl_p, _dbl_p]
+        lib.oracle_rmsnorm_fwd.argtypes = [vp, i32, vp, i32, i64, i64, dbl, _dbl_p, _dbl_p]
+        lib.oracle_rmsnorm_bwd.argtypes = [vp, i32, vp, i32, vp, i32, i64, i64, dbl,
+                                           _dbl_p, _dbl_p]
+        for name in ("oracle_decode", "oracle_add_rmsnorm_fwd", "oracle_rmsnorm_fwd",
+                     "oracle_rmsnorm_bwd"):
+            getattr(lib, name).restype = i32
+        self.lib = lib
+
+    @staticmethod
+    def _check(status: int, what: str) -> None:
+        if status != 0:
+            raise RuntimeError(f"{what}: oracle returned status {status}")
+
+    def decode(self, a: np.ndarray) -> np.ndarray:
+        """Exact fp64 values of ``a`` (bf16 bit patterns, float32 or float64)."""
+        a = np.ascontiguousarray(a)
+        out = np.empty(a.shape, dtype=np.float64)
+        self._check(self.lib.oracle_decode(_ptr(a), _code(a), a.size, _out(out)), "decode")
+        return out
+
+    def add_rmsnorm_fwd(self, x: np.ndarray, residual: Optional[np.ndarray], w: np.ndarray,
+                        eps: float) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+        """Return ``(r, y, rstd)`` for r = x + residual (residual None: r = x)."""
+        x = np.ascontiguousarray(x)
+        w = np.ascontiguousarray(w)
+        M, N = x.shape
+        if w.shape != (N,):
+            raise ValueError("w must have shape (N,)")
+        if residual is not None:
+            residual = np.ascontiguousarray(residual)
+            if residual.shape != x.shape:
+                raise ValueError("residual must have the shape of x")
+        r = np.empty((M, N), dtype=np.float64)
+        y = np.empty((M, N), dtype=np.float64)
+        rstd = np.empty((M,), dtype=np.float64)
+        self._check(self.lib.oracle_add_rmsnorm_fwd(
+            _ptr(x), _code(x), _ptr(residual), 0 if residual is None else _code(residual),
+            _ptr(w), _code(w), M, N, float(eps), _out(r), _out(y), _out(rstd)),
+            "add_rmsnorm_fwd")
+        return r, y, rstd
+
+    def rmsnorm_fwd(self, x: np.ndarray, w: np.ndarray, eps: float) -> Tuple[np.ndarray, np.ndarray]:
+        """Return ``(y, rstd)``."""
+        x = np.ascontiguousarray(x)
+        w = np.ascontiguousarray(w)
+        M, N = x.shape
+        if w.shape != (N,):
+            raise ValueError("w must have shape (N,)")
+        y = np.empty((M, N), dtype=np.float64)
+        rstd = np.empty((M,), dtype=np.float64)
+        self._check(self.lib.oracle_rmsnorm_fwd(_ptr(x), _code(x), _ptr(w), _code(w), M, N,
+                                                float(eps), _out(y), _out(rstd)), "rmsnorm_fwd")
+        return y, rstd
+
+    def rmsnorm_bwd(self, dy: np.ndarray, x: np.ndarray, w: np.ndarray, eps: float,
+                    want_dx: bool = True) -> Tuple[Optional[np.ndarray], np.ndarray]:
+        """Return ``(dx, dw)``; ``dx`` is None when ``want_dx`` is False (dw alone)."""
+        dy = np.ascontiguousarray(dy)
+        x = np.ascontiguousarray(x)
+        w = np.ascontiguousarray(w)
+        M, N = x.shape
+        if dy.shape != x.shape or w.shape != (N,):
+            raise ValueError("dy must have the shape of x and w shape (N,)")
+        dx = np.empty((M, N), dtype=np.float64) if want_dx else None
+        dw = np.empty((N,), dtype=np.float64)
+        self._check(self.lib.oracle_rmsnorm_bwd(_ptr(dy), _code(dy), _ptr(x), _code(x), _ptr(w),
+                                                _code(w), M, N, float(eps), _out(dx), _out(dw)),
+                    "rmsnorm_bwd")
+        return dx, dw
+
+
+_DEFAULT: Optional[Oracle] = None
+
+
+def default() -> Oracle:
+    """The oracle built from this directory's ``oracle.c`` (compiled on first use)."""
+    global _DEFAULT
+    if _DEFAULT is None:
+        _DEFAULT = Oracle()
+    return _DEFAULT
+
+
+def decode(a):
+    return default().decode(a)
+
+
+def add_rmsnorm_fwd(x, residual, w, eps):
+    return default().add_rmsnorm_fwd(x, residual, w, eps)
+
+
+def rmsnorm_fwd(x, w, eps):
+    return default().rmsnorm_fwd(x, w, eps)
+
+
+def rmsnorm_bwd(dy, x, w, eps, want_dx=True):
+    return default().rmsnorm_bwd(dy, x, w, eps, want_dx)
+
+
+def build(force: bool = False) -> str:
+    """Compile ``liboracle.so`` (used by the package's build step)."""
+    return _build.build(force)
+
+
+__all__ = ["Oracle", "default", "decode", "add_rmsnorm_fwd", "rmsnorm_fwd", "rmsnorm_bwd",
+           "build", "BF16", "F32", "F64"]

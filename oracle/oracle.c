@@ -1,0 +1,166 @@
+/*
+ * CPU oracle for row-wise RMSNorm and fused residual Add + RMSNorm, forward and backward.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the slow, plain, fp64 statement of what the GPU
+ * library computes. Only the test suite, the smoke check and the benchmark's CPU-baseline
+ * leg may load it; the product path never does. It shares no code, header, table or helper
+ * with the CUDA library, and it never reads a value produced by the CUDA library.
+ *
+ * What it follows.
+ *   - The operation: the RMSNorm op listed among Machete's built-in ops ("Machete", section
+ *     "Built-In Areas"), the "RMSNorm SM100" CuTe DSL example (CuTe DSL skill page, example
+ *     index of "Workflow 0"), and KernelAgent-Oink's "RMSNorm and fused Add + RMSNorm" custom
+ *     ops for SM100/SM103 (KernelAgent page, repository summary). None of the pages writes the
+ *     formula out, so this file uses the standard definition of row-wise RMSNorm:
+ *         r      = x + residual            (fused op only; plain op: r = x)
+ *         rstd_i = 1 / sqrt( (1/N) sum_j r_ij^2 + eps )
+ *         y_ij   = r_ij * rstd_i * w_j
+ *   - The backward pass is the exact derivative of that definition (per row, with
+ *     xhat = x * rstd and g = dy * w):
+ *         dx_j = rstd * ( g_j - xhat_j * (1/N) sum_k g_k xhat_k )
+ *         dw_j = sum over rows of dy_j * xhat_j
+ *     which follows from d(rstd)/d(x_k) = -rstd^3 * x_k / N.
+ *
+ * Precision. Inputs arrive as raw bf16 bit patterns, fp32 or fp64 values; each element is
+ * decoded exactly to fp64 and every step is done in fp64, in the order the definition reads
+ * (sums run over j = 0..N-1 and over rows i = 0..M-1 in order). Outputs stay fp64: the
+ * oracle never rounds to the GPU's storage type.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -shared -fPIC oracle.c -lm (see libbuild.py).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Element encodings accepted for every input tensor. */
+enum { ORACLE_BF16 = 0, ORACLE_F32 = 1, ORACLE_F64 = 2 };
+
+/* Return codes. */
+enum { ORACLE_OK = 0, ORACLE_BAD_ARG = 1, ORACLE_NO_MEMORY = 2 };
+
+/* A bf16 value is the upper 16 bits of an IEEE-754 binary32 value: widening it is exact. */
+static double decode_bf16(uint16_t bits)
+{
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static int valid_dtype(int dt) { return dt == ORACLE_BF16 || dt == ORACLE_F32 || dt == ORACLE_F64; }
+
+/* Element `i` of a tensor stored with encoding `dt`, as an exact fp64 value. */
+static double element(const void *base, int dt, int64_t i)
+{
+    if (dt == ORACLE_BF16) return decode_bf16(((const uint16_t *)base)[i]);
+    if (dt == ORACLE_F32) return (double)((const float *)base)[i];
+    return ((const double *)base)[i];
+}
+
+/* Decode n elements to fp64 (exposed so the tests can pin the decoding on its own). */
+int oracle_decode(const void *src, int dt, int64_t n, double *dst)
+{
+    if (!src || !dst || n < 0 || !valid_dtype(dt)) return ORACLE_BAD_ARG;
+    for (int64_t i = 0; i < n; ++i) dst[i] = element(src, dt, i);
+    return ORACLE_OK;
+}
+
+/* rstd = 1 / sqrt(mean(r^2) + eps) over one row r[0..N-1]. */
+static double row_rstd(const double *r, int64_t N, double eps)
+{
+    double sum_sq = 0.0;
+    for (int64_t j = 0; j < N; ++j) sum_sq += r[j] * r[j];
+    double mean_sq = sum_sq / (double)N;
+    return 1.0 / sqrt(mean_sq + eps);
+}
+
+/*
+ * Fused residual Add + RMSNorm forward (KernelAgent page, repository summary: "fused Add +
+ * RMSNorm"). `res` may be NULL, which gives the plain RMSNorm forward (Machete, "Built-In
+ * Areas"). x, res: [M, N] row-major; w: [N]. Outputs (fp64, caller-owned, any may be NULL):
+ * r_out [M, N] = x + res, y [M, N], rstd [M].
+ */
+int oracle_add_rmsnorm_fwd(const void *x, int x_dt, const void *res, int res_dt,
+                           const void *w, int w_dt, int64_t M, int64_t N, double eps,
+                           double *r_out, double *y, double *rstd)
+{
+    if (!x || !w || M < 0 || N < 1 || !valid_dtype(x_dt) || !valid_dtype(w_dt)) return ORACLE_BAD_ARG;
+    if (res && !valid_dtype(res_dt)) return ORACLE_BAD_ARG;
+    double *r = (double *)malloc((size_t)N * sizeof(double));
+    double *wd = (double *)malloc((size_t)N * sizeof(double));
+    if (!r || !wd) { free(r); free(wd); return ORACLE_NO_MEMORY; }
+    for (int64_t j = 0; j < N; ++j) wd[j] = element(w, w_dt, j);
+
+    for (int64_t i = 0; i < M; ++i) {
+        /* r = x + residual (or x alone), exactly in fp64. */
+        for (int64_t j = 0; j < N; ++j) {
+            double v = element(x, x_dt, i * N + j);
+            if (res) v += element(res, res_dt, i * N + j);
+            r[j] = v;
+        }
+        double s = row_rstd(r, N, eps);
+        if (rstd) rstd[i] = s;
+        for (int64_t j = 0; j < N; ++j) {
+            if (r_out) r_out[i * N + j] = r[j];
+            if (y) y[i * N + j] = r[j] * s * wd[j];
+        }
+    }
+    free(r);
+    free(wd);
+    return ORACLE_OK;
+}
+
+/* Plain RMSNorm forward: the fused op without a residual. */
+int oracle_rmsnorm_fwd(const void *x, int x_dt, const void *w, int w_dt, int64_t M, int64_t N,
+                       double eps, double *y, double *rstd)
+{
+    return oracle_add_rmsnorm_fwd(x, x_dt, NULL, 0, w, w_dt, M, N, eps, NULL, y, rstd);
+}
+
+/*
+ * RMSNorm backward: the derivative of the forward definition above. rstd is recomputed in
+ * fp64 from x and eps (the oracle takes nothing from a GPU forward pass).
+ * dy, x: [M, N]; w: [N]. Outputs (fp64, caller-owned): dx [M, N] (may be NULL), dw [N]
+ * (may be NULL; overwritten with the sum over all M rows, taken in row order).
+ */
+int oracle_rmsnorm_bwd(const void *dy, int dy_dt, const void *x, int x_dt, const void *w,
+                       int w_dt, int64_t M, int64_t N, double eps, double *dx, double *dw)
+{
+    if (!dy || !x || !w || M < 0 || N < 1 || !valid_dtype(dy_dt) || !valid_dtype(x_dt) ||
+        !valid_dtype(w_dt))
+        return ORACLE_BAD_ARG;
+    double *xr = (double *)malloc((size_t)N * sizeof(double));
+    double *dyr = (double *)malloc((size_t)N * sizeof(double));
+    double *wd = (double *)malloc((size_t)N * sizeof(double));
+    double *xhat = (double *)malloc((size_t)N * sizeof(double));
+    double *g = (double *)malloc((size_t)N * sizeof(double));
+    if (!xr || !dyr || !wd || !xhat || !g) {
+        free(xr); free(dyr); free(wd); free(xhat); free(g);
+        return ORACLE_NO_MEMORY;
+    }
+    for (int64_t j = 0; j < N; ++j) wd[j] = element(w, w_dt, j);
+    if (dw)
+        for (int64_t j = 0; j < N; ++j) dw[j] = 0.0;
+
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            xr[j] = element(x, x_dt, i * N + j);
+            dyr[j] = element(dy, dy_dt, i * N + j);
+        }
+        double s = row_rstd(xr, N, eps);
+        double dot = 0.0; /* sum_k g_k * xhat_k */
+        for (int64_t j = 0; j < N; ++j) {
+            xhat[j] = xr[j] * s;
+            g[j] = dyr[j] * wd[j];
+            dot += g[j] * xhat[j];
+        }
+        double c = dot / (double)N;
+        for (int64_t j = 0; j < N; ++j) {
+            if (dx) dx[i * N + j] = s * (g[j] - xhat[j] * c);
+            if (dw) dw[j] += dyr[j] * xhat[j];
+        }
+    }
+    free(xr); free(dyr); free(wd); free(xhat); free(g);
+    return ORACLE_OK;
+}

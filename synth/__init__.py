@@ -1,0 +1,143 @@
+"""Seeded synthetic workloads for row-wise RMSNorm / fused residual Add + RMSNorm.
+
+This module only draws random inputs. It contains none of the normalisation arithmetic, so
+both the GPU path's tests/benchmark and the CPU oracle can take their inputs from it.
+
+Every workload is drawn on the host with numpy's PCG64 generator, seeded per workload, in a
+fixed order: x, residual, (outlier mask, outlier sign), w, dy. Values are drawn in float32
+and, for bf16 workloads, rounded to bf16 (round to nearest even) by torch's CPU cast. bf16
+tensors are returned as ``uint16`` arrays holding the raw bit patterns; fp32 tensors as
+``float32`` arrays.
+
+The pages name benchmark suites for this op (Quack-suite, DeepSeek-V3/V4 norm workloads on the
+KernelAgent page) whose shapes are not published there; the shapes below stand in for them.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+from typing import Dict, Optional
+
+import numpy as np
+
+BF16 = "bf16"
+F32 = "f32"
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One synthetic problem: op kind, shape, dtype, eps, seed and value distributions."""
+
+    name: str
+    op: str                      # "rmsnorm_fwd" | "add_rmsnorm_fwd" | "rmsnorm_bwd"
+    M: int
+    N: int
+    dtype: str                   # "bf16" | "f32"
+    eps: float
+    seed: int
+    x_sigma: float = 1.0         # x ~ N(0, x_sigma^2)
+    res_sigma: float = 1.0       # residual ~ N(0, res_sigma^2)
+    outlier_frac: float = 0.0    # fraction of residual entries replaced by +/- outlier_value
+    outlier_value: float = 50.0
+    w_kind: str = "normal"       # "normal": 1 + 0.1*N(0,1); "uniform": U(0.5, 1.5)
+    meta: Dict[str, str] = field(default_factory=dict)
+
+    def with_shape(self, M: int, N: Optional[int] = None) -> "Workload":
+        return replace(self, M=M, N=self.N if N is None else N,
+                       name=f"{self.name}@{M}x{self.N if N is None else N}")
+
+    @property
+    def elem_bytes(self) -> int:
+        return 2 if self.dtype == BF16 else 4
+
+
+# The workloads. Names give op, shape and dtype.
+WORKLOADS: Dict[str, Workload] = {}
+
+
+def _add(w: Workload) -> None:
+    WORKLOADS[w.name] = w
+
+
+_add(Workload("rmsnorm_fwd_256x1024_bf16", "rmsnorm_fwd", 256, 1024, BF16, 1e-6, 0))
+_add(Workload("add_rmsnorm_fwd_4096x4096_bf16", "add_rmsnorm_fwd", 4096, 4096, BF16, 1e-6, 1))
+_add(Workload("add_rmsnorm_fwd_16384x4096_bf16", "add_rmsnorm_fwd", 16384, 4096, BF16, 1e-6, 1))
+_add(Workload("add_rmsnorm_fwd_16384x7168_bf16", "add_rmsnorm_fwd", 16384, 7168, BF16, 1e-6, 2,
+              res_sigma=2.0, outlier_frac=0.01, outlier_value=50.0, w_kind="uniform"))
+for _dt in (BF16, F32):
+    for _m in (1, 8, 32, 64):
+        _add(Workload(f"rmsnorm_fwd_{_m}x8192_{_dt}", "rmsnorm_fwd", _m, 8192, _dt, 1e-5, 3))
+    _add(Workload(f"rmsnorm_fwd_65536x2048_{_dt}", "rmsnorm_fwd", 65536, 2048, _dt, 1e-5, 3))
+_add(Workload("rmsnorm_bwd_16384x4096_bf16", "rmsnorm_bwd", 16384, 4096, BF16, 1e-6, 4))
+
+
+def get(name: str) -> Workload:
+    return WORKLOADS[name]
+
+
+def to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest even) with torch's CPU cast; return the bits."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def _store(a: np.ndarray, dtype: str) -> np.ndarray:
+    return to_bf16_bits(a) if dtype == BF16 else np.ascontiguousarray(a, dtype=np.float32)
+
+
+def make(w: Workload) -> Dict[str, np.ndarray]:
+    """Draw the host inputs of ``w``: x, w and, per op, residual or dy.
+
+    The result maps tensor names to host arrays in the workload's storage encoding (uint16
+    bf16 bits or float32). For the fused op it also holds ``outliers``, the number of
+    residual entries replaced by outliers.
+    """
+    rng = np.random.default_rng(w.seed)
+    shape = (w.M, w.N)
+    out: Dict[str, np.ndarray] = {}
+    x = rng.standard_normal(shape, dtype=np.float32)
+    if w.x_sigma != 1.0:
+        x *= np.float32(w.x_sigma)
+    out["x"] = _store(x, w.dtype)
+    del x
+    if w.op == "add_rmsnorm_fwd":
+        res = rng.standard_normal(shape, dtype=np.float32)
+        if w.res_sigma != 1.0:
+            res *= np.float32(w.res_sigma)
+        if w.outlier_frac > 0.0:
+            mask = rng.random(shape, dtype=np.float32) < w.outlier_frac
+            sign = rng.integers(0, 2, size=shape, dtype=np.int8)
+            res[mask] = np.where(sign[mask] == 1, w.outlier_value, -w.outlier_value)
+            out["outliers"] = np.array(int(mask.sum()))
+            del mask, sign
+        out["residual"] = _store(res, w.dtype)
+        del res
+    if w.w_kind == "uniform":
+        wt = rng.uniform(0.5, 1.5, size=w.N).astype(np.float32)
+    else:
+        wt = (np.float32(1.0) + np.float32(0.1) * rng.standard_normal(w.N, dtype=np.float32))
+    out["w"] = _store(wt, w.dtype)
+    if w.op == "rmsnorm_bwd":
+        out["dy"] = _store(rng.standard_normal(shape, dtype=np.float32), w.dtype)
+    return out
+
+
+def min_bytes(w: Workload) -> int:
+    """Minimum HBM bytes one call moves: every input read once, every output written once.
+
+    rmsnorm_fwd: x, y (M*N each), w (N), rstd (M, fp32).
+    add_rmsnorm_fwd: x, residual, residual_out, y (M*N each), w (N), rstd (M, fp32).
+    rmsnorm_bwd: x, dy, dx (M*N each), w (N), rstd (M, fp32), dw (N, fp32).
+    """
+    e = w.elem_bytes
+    if w.op == "rmsnorm_fwd":
+        return 2 * w.M * w.N * e + w.N * e + 4 * w.M
+    if w.op == "add_rmsnorm_fwd":
+        return 4 * w.M * w.N * e + w.N * e + 4 * w.M
+    if w.op == "rmsnorm_bwd":
+        return 3 * w.M * w.N * e + w.N * e + 4 * w.M + 4 * w.N
+    raise ValueError(w.op)
+
+
+__all__ = ["Workload", "WORKLOADS", "get", "make", "min_bytes", "to_bf16_bits", "BF16", "F32"]
