@@ -1,0 +1,436 @@
+"""Benchmark: fused residual Add + RMSNorm and RMSNorm backward on GB300, as achieved HBM GB/s.
+
+One step is one pass of the whole hot path over one batch of synthetic input:
+    add_rmsnorm_fwd  (x, residual -> residual_out, y, rstd)              16384 x 4096 bf16
+    rmsnorm_bwd      (dy, x, w, rstd -> dx, dw; stage 1 + stage 2)       16384 x 4096 bf16
+Throughput is counted in minimum HBM bytes (every input read once, every output written once):
+536,944,640 B for the forward and 402,743,296 B for the backward, 939,687,936 B per step.
+
+Output: one JSON line on rank 0 (see the keys below). ``--impl reference`` times the CPU fp64
+oracle on a bounded sample of the same workload instead (the reference arm).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs its own replica of the step on its own GPU (rows are
+independent; no data-path collective), and the timed region is bracketed by barriers.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "fused Add+RMSNorm bf16 achieved HBM GB/s and % of GB300 peak, by M×N"
+FWD_WL = "add_rmsnorm_fwd_16384x4096_bf16"
+BWD_WL = "rmsnorm_bwd_16384x4096_bf16"
+FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "residual_rmsnorm_row_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ------------------------------------------------------------------ helpers
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(kernel_key: str):
+    """dram bytes per launch from the committed ncu summary, if it matches these sources."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            doc = json.load(f)
+        ent = doc[kernel_key]
+        if ent.get("source_hash") != kernel_source_hash():
+            return None
+        return int(ent["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 100 ms while the benchmark runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = []
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9], parts[4]))
+            except ValueError:
+                continue
+        self.file.close()
+        os.unlink(self.file.name)
+        return rows
+
+    @staticmethod
+    def summarise(rows, t0, t1):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        inside = [r for r in rows if t0 - 1.0 <= r[0] <= t1 + 1.0]
+        use = inside or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([r[1] for r in use])), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(use),
+                "window": "timed region" if inside else "whole run"}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def as_dev(a: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def step_bytes():
+    fwd = synth.min_bytes(synth.get(FWD_WL))
+    bwd = synth.min_bytes(synth.get(BWD_WL))
+    return fwd, bwd
+
+
+def base_config(world):
+    f, b = synth.get(FWD_WL), synth.get(BWD_WL)
+    return {
+        "workload": f"fused Add+RMSNorm forward {f.M}x{f.N} bf16 (eps {f.eps}) + RMSNorm backward "
+                    f"{b.M}x{b.N} bf16 per step",
+        "M": f.M, "N": f.N,
+        "step": "add_rmsnorm_fwd then rmsnorm_bwd (two-stage dw)",
+        "bytes_per_step": sum(step_bytes()),
+        "l2": "inputs larger than L2: two rotating buffer sets, 1.8 GB per set pair",
+        "parallelism": "replicas" if world == 1 else f"dp{world} replicas (rows sharded, no collective)",
+        "inputs": "seeded synthetic: x, residual, dy ~ N(0,1); w ~ 1+0.1 N(0,1)",
+    }
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, world, rank, local):
+    import residual_rmsnorm_row_gb300 as rrn
+
+    rrn.load_library()
+    dev = torch.device("cuda", local)
+    fw, bw = synth.get(FWD_WL), synth.get(BWD_WL)
+    hf = synth.make(fw)
+    hb = synth.make(bw)
+    w = as_dev(hf["w"], dev)
+    wb = as_dev(hb["w"], dev)
+    sets = []
+    for s in range(2):
+        x = as_dev(hf["x"], dev)
+        res = as_dev(hf["residual"], dev)
+        xb = as_dev(hb["x"], dev)
+        dy = as_dev(hb["dy"], dev)
+        if s == 1:   # a second, different buffer set (rows rolled) so no step re-reads L2 lines
+            x, res, xb, dy = (t.roll(1, 0).contiguous() for t in (x, res, xb, dy))
+        _, rstd_b = rrn.rms_norm(xb, wb, bw.eps)
+        sets.append(dict(x=x, res=res, ro=torch.empty_like(x), y=torch.empty_like(x),
+                         rstd=torch.empty(fw.M, device=dev), xb=xb, dy=dy, rstd_b=rstd_b,
+                         dx=torch.empty_like(xb), dw=torch.empty(bw.N, device=dev)))
+    ws = torch.empty(max(rrn.rmsnorm_bwd_workspace_bytes(bw.M, bw.N, torch.bfloat16), 16) // 4,
+                     device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fwd_plan = rrn.plan_fwd(sets[0]["x"], sets[0]["res"], sets[0]["ro"], w, sets[0]["y"])
+    bwd_plan = rrn.plan_bwd(sets[0]["dy"], sets[0]["xb"], wb, sets[0]["dx"])
+
+    do_fwd = args.only in ("step", "fwd")
+    do_bwd = args.only in ("step", "bwd")
+
+    def step(i, ev=None):
+        s = sets[i & 1]
+        if ev is not None:
+            ev[0].record(stream)
+        if do_fwd:
+            rrn.add_rmsnorm_fwd(s["x"], s["res"], s["ro"], w, s["y"], s["rstd"], fw.eps, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        if do_bwd:
+            rrn.rmsnorm_bwd(s["dy"], s["xb"], wb, s["rstd_b"], s["dx"], s["dw"], ws, bw.eps, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0.0)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i, evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier(world)
+    elapsed_ms = max_over_ranks(world, start.elapsed_time(end))
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    clocks = ClockSampler.summarise(sampler.stop(), t0, t1) if sampler else None
+
+    # End to end through the public API: pinned host inputs -> device, fwd + bwd, results
+    # (y, residual_out, dx, dw) -> pinned host, every step.
+    e2e_steps = 0 if args.no_e2e else max(1, min(args.steps, 20))
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    h_x, h_res, h_dy = pin(sets[0]["x"]), pin(sets[0]["res"]), pin(sets[0]["dy"])
+    h_y, h_ro, h_dx = (torch.empty_like(h_x).pin_memory() for _ in range(3))
+    h_dw = torch.empty(bw.N).pin_memory()
+    d_x, d_res, d_dy = (torch.empty_like(sets[0]["x"]) for _ in range(3))
+    d_ro, d_y, d_dx = (torch.empty_like(sets[0]["x"]) for _ in range(3))
+    d_rstd, d_dw = torch.empty(fw.M, device=dev), torch.empty(bw.N, device=dev)
+
+    def e2e_step():
+        d_x.copy_(h_x, non_blocking=True)
+        d_res.copy_(h_res, non_blocking=True)
+        d_dy.copy_(h_dy, non_blocking=True)
+        rrn.add_rmsnorm_fwd(d_x, d_res, d_ro, w, d_y, d_rstd, fw.eps, stream)
+        rrn.rmsnorm_bwd(d_dy, d_ro, w, d_rstd, d_dx, d_dw, ws, bw.eps, stream)
+        h_y.copy_(d_y, non_blocking=True)
+        h_ro.copy_(d_ro, non_blocking=True)
+        h_dx.copy_(d_dx, non_blocking=True)
+        h_dw.copy_(d_dw, non_blocking=True)
+
+    e2e_ms = 0.0
+    if e2e_steps:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        es.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        ee.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(world, es.elapsed_time(ee))
+        barrier(world)
+
+    fb, bb = step_bytes()
+    per_step = (fb if do_fwd else 0) + (bb if do_bwd else 0)
+    ms_per_step = elapsed_ms / args.steps
+    value = per_step * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+    fwd_us = float(np.mean(fwd_ms)) * 1e3 if do_fwd else float("nan")
+    bwd_us = float(np.mean(bwd_ms)) * 1e3 if do_bwd else float("nan")
+    peak, peak_kind = hbm_peak()
+    fwd_gbs = fb / (fwd_us * 1e-6) / 1e9
+    bwd_gbs = bb / (bwd_us * 1e-6) / 1e9
+    h2d = sum(t.numel() * t.element_size() for t in (h_x, h_res, h_dy))
+    d2h = sum(t.numel() * t.element_size() for t in (h_y, h_ro, h_dx, h_dw))
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": base_config(world),
+        "kernels": {
+            "add_rmsnorm_fwd": {"us": round(fwd_us, 2), "gbps": round(fwd_gbs, 1),
+                                "frac_of_peak": round(fwd_gbs / peak, 4),
+                                "rows_per_s": round(fw.M / (fwd_us * 1e-6), 1),
+                                "launch": fwd_plan.name, "launches_per_step": 1},
+            "rmsnorm_bwd": {"us": round(bwd_us, 2), "gbps": round(bwd_gbs, 1),
+                            "frac_of_peak": round(bwd_gbs / peak, 4),
+                            "rows_per_s": round(bw.M / (bwd_us * 1e-6), 1),
+                            "launch": bwd_plan.name, "launches_per_step": 2},
+        },
+        "roofline": {"bound": "hbm", "kernel": "add_rmsnorm_fwd (fwd_row_cta)",
+                     "achieved": round(fwd_gbs, 1), "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs",
+                     "unit": "GB/s", "frac": round(fwd_gbs / peak, 4),
+                     "traffic": recorded_traffic("add_rmsnorm_fwd_16384x4096_bf16"),
+                     "algorithmic_bytes": fb},
+        "e2e": ({"value": round((fb + bb) * e2e_steps * world / (e2e_ms * 1e-3) / 1e9, 1),
+                 "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                 "steps": e2e_steps, "ms_per_step": round(e2e_ms / e2e_steps, 4)}
+                if e2e_steps else None),
+        "gpu_launches": (int(do_fwd) + 2 * int(do_bwd)) * args.steps,
+        "clocks": clocks,
+    }
+    return out
+
+
+# ------------------------------------------------------------------ the oracle (CPU)
+def oracle_sample(target_s: float, rows_cap: int = 16384):
+    """Time the fp64 CPU oracle on row samples of the same workload until ~target_s seconds."""
+    import oracle
+
+    fw, bw = synth.get(FWD_WL), synth.get(BWD_WL)
+    rows = 256
+    hf = synth.make(fw.with_shape(rows))
+    hb = synth.make(bw.with_shape(rows))
+    fb, bb = step_bytes()
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.add_rmsnorm_fwd(hf["x"], hf["residual"], hf["w"], fw.eps)
+        oracle.rmsnorm_bwd(hb["dy"], hb["x"], hb["w"], bw.eps)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= target_s:
+            break
+    bytes_done = n * rows * (fb + bb) / fw.M
+    return {"value": round(bytes_done / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} x {rows} of {fw.M} rows (fused fwd + bwd, N={fw.N}, bf16 in, fp64 "
+                      f"arithmetic), single-threaded C, {el:.1f} s wall"}
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle as it stands, timed step by step on host cores."""
+    import oracle
+
+    if rank != 0:
+        return None
+    fw, bw = synth.get(FWD_WL), synth.get(BWD_WL)
+    fb, bb = step_bytes()
+    # size each step so warmup + steps end within about two minutes
+    probe_rows = 64
+    hf = synth.make(fw.with_shape(probe_rows))
+    hb = synth.make(bw.with_shape(probe_rows))
+    t = time.perf_counter()
+    oracle.add_rmsnorm_fwd(hf["x"], hf["residual"], hf["w"], fw.eps)
+    oracle.rmsnorm_bwd(hb["dy"], hb["x"], hb["w"], bw.eps)
+    per_row = (time.perf_counter() - t) / probe_rows
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(fw.M, budget / max(per_row, 1e-9))))
+    hf = synth.make(fw.with_shape(rows))
+    hb = synth.make(bw.with_shape(rows))
+
+    def step():
+        oracle.add_rmsnorm_fwd(hf["x"], hf["residual"], hf["w"], fw.eps)
+        oracle.rmsnorm_bwd(hb["dy"], hb["x"], hb["w"], bw.eps)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    bytes_done = args.steps * rows * (fb + bb) / fw.M
+    value = bytes_done / el / 1e9
+    sample = (f"{rows} of {fw.M} rows per step (fused fwd + bwd, N={fw.N}, bf16 in, fp64 "
+              f"arithmetic), single-threaded C oracle")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": base_config(world),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=10.0,
+                    help="seconds of CPU oracle work for cpu_baseline (0: skip)")
+    ap.add_argument("--only", choices=["step", "fwd", "bwd"], default="step",
+                    help="time the whole step (default) or one kernel alone (for profiling)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        out = run_reference(args, world, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    out = run_ours(args, world, rank, local)
+    if rank == 0:
+        out["cpu_baseline"] = (oracle_sample(args.cpu_baseline_seconds)
+                               if world == 1 and args.cpu_baseline_seconds > 0 else None)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+/*
+ * rrn.h - C ABI of the GB300 (sm_103a) row-wise RMSNorm / fused residual Add + RMSNorm library.
+ *
+ * The operation (none of the source pages writes the formula out; this is the standard
+ * definition of the op they name - the RMSNorm op of the Machete page, section "Built-In
+ * Areas"; the "RMSNorm SM100" example of the CuTe DSL skill page, "Workflow 0" example index;
+ * KernelAgent-Oink's "RMSNorm and fused Add + RMSNorm" custom ops, KernelAgent page,
+ * repository summary), per row i of an [M, N] row-major matrix:
+ *
+ *     r_i    = x_i + residual_i                 (fused op; written back as residual_out)
+ *     rstd_i = 1 / sqrt( mean_j(r_ij^2) + eps )
+ *     y_ij   = r_ij * rstd_i * w_j
+ *
+ * and the backward pass of the plain op (x -> y), with xhat = x * rstd and g = dy * w:
+ *
+ *     dx_ij = rstd_i * ( g_ij - xhat_ij * mean_k(g_ik * xhat_ik) )
+ *     dw_j  = sum_i dy_ij * xhat_ij
+ *
+ * Arithmetic: inputs are widened to fp32; the sum of squares (and the backward dot product)
+ * is accumulated in fp32 with warp shuffles followed by a cross-warp shared-memory step (the
+ * reduction pattern the CuTe DSL skill page prescribes for RMSNorm: "Workflow 0", paragraph on
+ * reduction kernels); y is computed from the UNROUNDED fp32 r and rounded once (round to
+ * nearest even) to the storage type. residual_out is r rounded once to the storage type.
+ * dw is reduced in two stages in a fixed order, so it is bitwise reproducible for a given
+ * (M, N, dtype, device).
+ *
+ * Conventions shared by every entry point below:
+ *   - Pointers are DEVICE pointers (cudaMalloc / torch CUDA tensors) on the current device,
+ *     except where stated. The caller owns every buffer; the library allocates nothing,
+ *     never synchronises and compiles nothing at run time.
+ *   - Layout: x, residual, residual_out, y, dy, dx are contiguous row-major [M, N] (row stride
+ *     N elements) of `dtype`; w is [N] of `dtype`; rstd is [M] fp32; dw is [N] fp32.
+ *   - dtype: RRN_BF16 (bfloat16) or RRN_F32 (float); all dtype-typed tensors of a call share it.
+ *   - Alignment: elements must be naturally aligned (2 bytes for bf16, 4 for fp32; rstd and
+ *     dw 4 bytes). When every matrix pointer is 16-byte aligned and N * sizeof(dtype) is a
+ *     multiple of 16 the 128-bit vector kernels run; otherwise an element-wise GPU kernel
+ *     runs. There is no CPU fallback.
+ *   - Aliasing: an output may be the same buffer as an input of the same shape
+ *     (residual_out == residual or x; y == x; dx == dy or x). Any other overlap is undefined.
+ *   - M == 0 is a no-op that returns RRN_OK and launches nothing.
+ *   - Work is enqueued on `stream` (NULL: the legacy default stream) and the call returns
+ *     without waiting. Argument errors return a nonzero code before anything is launched;
+ *     a failed launch returns RRN_ERR_CUDA (rrn_last_cuda_error() gives the cudaError_t);
+ *     errors during execution surface on the stream like any CUDA error.
+ *   - Thread safety: every entry point may be called from several host threads at once.
+ */
+#ifndef RRN_H_
+#define RRN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define RRN_API __attribute__((visibility("default")))
+#else
+#define RRN_API
+#endif
+
+/* A CUDA stream handle: the same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *rrn_stream_t;
+
+/* Storage types. */
+typedef enum { RRN_BF16 = 0, RRN_F32 = 1 } rrn_dtype;
+
+/* Return codes. */
+typedef enum {
+    RRN_OK = 0,
+    RRN_ERR_NULL = 1,      /* a required pointer is NULL */
+    RRN_ERR_SHAPE = 2,     /* M < 0, N < 1, or M * N too large */
+    RRN_ERR_EPS = 3,       /* eps negative, infinite or NaN */
+    RRN_ERR_DTYPE = 4,     /* dtype not RRN_BF16 / RRN_F32 */
+    RRN_ERR_ALIGN = 5,     /* a pointer is not aligned to its element size */
+    RRN_ERR_WORKSPACE = 6, /* backward workspace NULL or smaller than required */
+    RRN_ERR_CUDA = 7,      /* a CUDA runtime call or kernel launch failed */
+    RRN_ERR_CONFIG = 8     /* an explicit launch configuration cannot cover the row */
+} rrn_status;
+
+/*
+ * rmsnorm_fwd - RMSNorm forward: y = x * rstd * w per row (Machete page, "Built-In Areas").
+ *   x     [M, N] dtype, read.
+ *   w     [N] dtype, read.
+ *   y     [M, N] dtype, written (may be x).
+ *   rstd  [M] fp32, written; may be NULL (not stored).
+ *   eps   >= 0, finite; added to the mean square inside the square root.
+ * Returns an rrn_status.
+ */
+RRN_API int rmsnorm_fwd(const void *x, const void *w, void *y, float *rstd, int64_t M, int64_t N,
+                        float eps, int dtype, rrn_stream_t stream);
+
+/*
+ * add_rmsnorm_fwd - fused residual Add + RMSNorm forward (KernelAgent page, repository
+ * summary: KernelAgent-Oink's "fused Add + RMSNorm"): r = x + residual in fp32,
+ * residual_out = r (rounded to dtype), y = r * rstd * w (from the unrounded r).
+ *   x, residual   [M, N] dtype, read.
+ *   residual_out  [M, N] dtype, written (may be residual or x: the in-place update).
+ *   w             [N] dtype, read.
+ *   y             [M, N] dtype, written.
+ *   rstd          [M] fp32, written; may be NULL.
+ * Returns an rrn_status.
+ */
+RRN_API int add_rmsnorm_fwd(const void *x, const void *residual, void *residual_out, const void *w,
+                            void *y, float *rstd, int64_t M, int64_t N, float eps, int dtype,
+                            rrn_stream_t stream);
+
+/*
+ * rmsnorm_bwd_workspace_bytes - device workspace rmsnorm_bwd needs for (M, N, dtype) on the
+ * CURRENT device (it depends on the device's SM count). Writes the size to *bytes (0 when
+ * M == 0). Returns an rrn_status (RRN_ERR_CUDA if the device cannot be queried).
+ */
+RRN_API int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t *bytes);
+
+/*
+ * rmsnorm_bwd - RMSNorm backward of rmsnorm_fwd, with a two-stage deterministic dw.
+ *   dy        [M, N] dtype, read (upstream gradient of y).
+ *   x         [M, N] dtype, read (the forward input).
+ *   w         [N] dtype, read.
+ *   rstd      [M] fp32, read (as written by the forward pass).
+ *   dx        [M, N] dtype, written (may be dy or x).
+ *   dw        [N] fp32, overwritten (not accumulated) with the sum over all M rows.
+ *   workspace device buffer of at least rmsnorm_bwd_workspace_bytes(M, N, dtype) bytes,
+ *             16-byte aligned, owned by the caller; its contents on entry are ignored and
+ *             on return are unspecified. Calls that share a workspace must be ordered on
+ *             one stream.
+ *   eps       validated (>= 0, finite) and otherwise unused: rstd carries it.
+ * Stage 1 writes per-CTA fp32 partial sums of dy * xhat to the workspace; stage 2 adds
+ * them in a fixed order. With M == 0 nothing is launched and dw is left untouched.
+ * Returns an rrn_status.
+ */
+RRN_API int rmsnorm_bwd(const void *dy, const void *x, const void *w, const float *rstd, void *dx,
+                        float *dw, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
+                        float eps, int dtype, rrn_stream_t stream);
+
+/* rrn_status_string - static, NUL-terminated description of a status code. */
+RRN_API const char *rrn_status_string(int status);
+
+/* rrn_last_cuda_error - the cudaError_t behind this thread's last RRN_ERR_CUDA (0 if none). */
+RRN_API int rrn_last_cuda_error(void);
+
+/* ------------------------------------------------------------------------------------------
+ * Launch control, for benchmarking and tuning. The entry points above choose these
+ * automatically from (M, N, dtype, SM count); the _ex forms below take them explicitly.
+ * ------------------------------------------------------------------------------------------ */
+
+/* Kernel variants. */
+typedef enum {
+    RRN_VARIANT_AUTO = 0,    /* let the library choose */
+    RRN_VARIANT_ROW_CTA = 1, /* one row per CTA, row held in registers, 128-bit vectors */
+    RRN_VARIANT_ROW_WARP = 2,/* one row per warp, row held in registers, 128-bit vectors */
+    RRN_VARIANT_STREAM = 3   /* one row per CTA, two passes over the row (any N / alignment) */
+} rrn_variant;
+
+/* A launch configuration. Zero fields mean "choose automatically". */
+typedef struct {
+    int variant; /* rrn_variant */
+    int vpt;     /* 128-bit vectors per thread for the register variants: 1, 2, 4 or 8 */
+    int threads; /* threads per CTA (a multiple of 32, at most 1024) */
+    int ctas;    /* CTAs in the grid; each walks rows with a grid-sized stride */
+    int vec;     /* output of rrn_plan_*: 1 when the 128-bit vector path is used */
+} rrn_launch;
+
+/*
+ * rrn_plan_fwd / rrn_plan_bwd - the configuration the automatic entry points would use for
+ * these arguments (the pointers only matter for their alignment; they are not dereferenced).
+ * `residual` NULL plans the plain forward. Returns an rrn_status.
+ */
+RRN_API int rrn_plan_fwd(const void *x, const void *residual, const void *residual_out,
+                         const void *w, const void *y, int64_t M, int64_t N, int dtype,
+                         rrn_launch *out);
+RRN_API int rrn_plan_bwd(const void *dy, const void *x, const void *w, const void *dx, int64_t M,
+                         int64_t N, int dtype, rrn_launch *out);
+
+/*
+ * add_rmsnorm_fwd_ex - add_rmsnorm_fwd (residual != NULL) or rmsnorm_fwd (residual == NULL,
+ * residual_out ignored) with an explicit launch configuration `cfg` (NULL: automatic).
+ * Fields left at 0 are filled in automatically; a configuration whose threads * vpt vectors
+ * cannot cover a row, or that the chosen variant cannot run, returns RRN_ERR_CONFIG.
+ */
+RRN_API int add_rmsnorm_fwd_ex(const void *x, const void *residual, void *residual_out,
+                               const void *w, void *y, float *rstd, int64_t M, int64_t N,
+                               float eps, int dtype, const rrn_launch *cfg, rrn_stream_t stream);
+
+/* rmsnorm_bwd_ex - rmsnorm_bwd with an explicit stage-1 launch configuration (see above).
+ * The workspace must hold cfg->ctas * N fp32 values (rrn_plan_bwd reports the default). */
+RRN_API int rmsnorm_bwd_ex(const void *dy, const void *x, const void *w, const float *rstd,
+                           void *dx, float *dw, void *workspace, size_t workspace_bytes,
+                           int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,
+                           rrn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RRN_H_ */

@@ -1,0 +1,268 @@
+"""ctypes binding of ``librrn.so`` (C ABI in ``include/rrn.h``): argument marshalling only.
+
+Each function here has the name of the C entry point it calls, takes torch CUDA tensors,
+passes their device pointers, sizes and the stream to the library, and raises ``RRNError``
+on a nonzero status. No arithmetic of the operation happens in Python; there is no CPU
+fallback - if the library is missing, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY_PATH = os.path.join(_HERE, "librrn.so")
+
+BF16, F32 = 0, 1
+_DTYPES = {torch.bfloat16: BF16, torch.float32: F32}
+
+VARIANT_AUTO, VARIANT_ROW_CTA, VARIANT_ROW_WARP, VARIANT_STREAM = 0, 1, 2, 3
+VARIANT_NAMES = {VARIANT_ROW_CTA: "row_cta", VARIANT_ROW_WARP: "row_warp",
+                 VARIANT_STREAM: "stream"}
+
+STATUS_NAMES = {0: "RRN_OK", 1: "RRN_ERR_NULL", 2: "RRN_ERR_SHAPE", 3: "RRN_ERR_EPS",
+                4: "RRN_ERR_DTYPE", 5: "RRN_ERR_ALIGN", 6: "RRN_ERR_WORKSPACE",
+                7: "RRN_ERR_CUDA", 8: "RRN_ERR_CONFIG"}
+
+
+class RRNError(RuntimeError):
+    """A nonzero rrn_status from the library."""
+
+    def __init__(self, status: int, message: str, cuda_error: int = 0):
+        self.status = status
+        self.cuda_error = cuda_error
+        extra = f" (cudaError {cuda_error})" if status == 7 else ""
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}{extra}")
+
+
+class rrn_launch(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("vpt", ctypes.c_int), ("threads", ctypes.c_int),
+                ("ctas", ctypes.c_int), ("vec", ctypes.c_int)]
+
+
+@dataclass(frozen=True)
+class Launch:
+    """A launch configuration (0 = automatic), mirroring ``rrn_launch``."""
+
+    variant: int = 0
+    vpt: int = 0
+    threads: int = 0
+    ctas: int = 0
+    vec: int = 0
+
+    def to_c(self) -> rrn_launch:
+        return rrn_launch(self.variant, self.vpt, self.threads, self.ctas, self.vec)
+
+    @staticmethod
+    def from_c(c: rrn_launch) -> "Launch":
+        return Launch(c.variant, c.vpt, c.threads, c.ctas, c.vec)
+
+    @property
+    def name(self) -> str:
+        base = VARIANT_NAMES.get(self.variant, "auto")
+        return f"{base}(vpt={self.vpt},threads={self.threads},ctas={self.ctas},vec={self.vec})"
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+_vp, _i32, _i64, _f32, _sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                              ctypes.c_size_t)
+_SIGNATURES = {
+    "rmsnorm_fwd": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32, _vp]),
+    "add_rmsnorm_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32, _vp]),
+    "rmsnorm_bwd_workspace_bytes": (_i32, [_i64, _i64, _i32, ctypes.POINTER(_sz)]),
+    "rmsnorm_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _f32, _i32, _vp]),
+    "rrn_status_string": (ctypes.c_char_p, [_i32]),
+    "rrn_last_cuda_error": (_i32, []),
+    "rrn_plan_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, ctypes.POINTER(rrn_launch)]),
+    "rrn_plan_bwd": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, ctypes.POINTER(rrn_launch)]),
+    "add_rmsnorm_fwd_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32,
+                                  ctypes.POINTER(rrn_launch), _vp]),
+    "rmsnorm_bwd_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _f32, _i32,
+                              ctypes.POINTER(rrn_launch), _vp]),
+}
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load ``librrn.so`` (once) and declare the C signatures. Raises if it is missing."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    p = path or LIBRARY_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"the GPU library {p} is not built: run `python -c \"import __graft_entry__ as g; "
+            f"g.build()\"` (or residual_rmsnorm_row_gb300/build.py) first")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _LIB = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        lib = load_library()
+        msg = lib.rrn_status_string(status).decode()
+        raise RRNError(status, msg, lib.rrn_last_cuda_error() if status == 7 else 0)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"dtype {t.dtype} is not supported (bfloat16 or float32)") from None
+
+
+def _mat(t: torch.Tensor, name: str, N: Optional[int] = None) -> int:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (row-major)")
+    if N is not None and (t.dim() == 0 or t.shape[-1] != N):
+        raise ValueError(f"{name} must have last dimension {N}")
+    return t.data_ptr()
+
+
+def _same(a: torch.Tensor, b: torch.Tensor, name: str) -> None:
+    if b.shape != a.shape or b.dtype != a.dtype:
+        raise ValueError(f"{name} must have the shape and dtype of x")
+
+
+def _rows(x: torch.Tensor):
+    N = int(x.shape[-1])
+    return (x.numel() // N if N else 0), N
+
+
+def _vec(t: Optional[torch.Tensor], name: str) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    return t.data_ptr()
+
+
+def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, rstd: Optional[torch.Tensor],
+                eps: float, stream=None) -> None:
+    """C ``rmsnorm_fwd``: y = x * rstd * w per row of x ([..., N]); rstd optional ([M] fp32)."""
+    M, N = _rows(x)
+    _same(x, y, "y")
+    if w.shape != (N,) or w.dtype != x.dtype:
+        raise ValueError("w must have shape (N,) and the dtype of x")
+    if rstd is not None and rstd.numel() != M:
+        raise ValueError("rstd must hold M values")
+    _check(load_library().rmsnorm_fwd(_mat(x, "x", N), _mat(w, "w"), _mat(y, "y"),
+                                      _vec(rstd, "rstd"), M, N, float(eps), _dtype(x),
+                                      _stream(stream)))
+
+
+def add_rmsnorm_fwd(x: torch.Tensor, residual: torch.Tensor, residual_out: torch.Tensor,
+                    w: torch.Tensor, y: torch.Tensor, rstd: Optional[torch.Tensor], eps: float,
+                    stream=None) -> None:
+    """C ``add_rmsnorm_fwd``: residual_out = x + residual, y = RMSNorm(x + residual) * w."""
+    M, N = _rows(x)
+    _same(x, residual, "residual")
+    _same(x, residual_out, "residual_out")
+    _same(x, y, "y")
+    if w.shape != (N,) or w.dtype != x.dtype:
+        raise ValueError("w must have shape (N,) and the dtype of x")
+    if rstd is not None and rstd.numel() != M:
+        raise ValueError("rstd must hold M values")
+    _check(load_library().add_rmsnorm_fwd(
+        _mat(x, "x", N), _mat(residual, "residual"), _mat(residual_out, "residual_out"),
+        _mat(w, "w"), _mat(y, "y"), _vec(rstd, "rstd"), M, N, float(eps), _dtype(x),
+        _stream(stream)))
+
+
+def add_rmsnorm_fwd_ex(x: torch.Tensor, residual: Optional[torch.Tensor],
+                       residual_out: Optional[torch.Tensor], w: torch.Tensor, y: torch.Tensor,
+                       rstd: Optional[torch.Tensor], eps: float, launch: Optional[Launch] = None,
+                       stream=None) -> None:
+    """C ``add_rmsnorm_fwd_ex``: either forward with an explicit launch configuration."""
+    M, N = _rows(x)
+    _same(x, y, "y")
+    if residual is not None:
+        _same(x, residual, "residual")
+        _same(x, residual_out, "residual_out")
+    if w.shape != (N,) or w.dtype != x.dtype:
+        raise ValueError("w must have shape (N,) and the dtype of x")
+    cfg = ctypes.byref(launch.to_c()) if launch is not None else None
+    _check(load_library().add_rmsnorm_fwd_ex(
+        _mat(x, "x", N), None if residual is None else _mat(residual, "residual"),
+        None if residual is None else _mat(residual_out, "residual_out"), _mat(w, "w"),
+        _mat(y, "y"), _vec(rstd, "rstd"), M, N, float(eps), _dtype(x), cfg, _stream(stream)))
+
+
+def rmsnorm_bwd_workspace_bytes(M: int, N: int, dtype: torch.dtype) -> int:
+    """C ``rmsnorm_bwd_workspace_bytes`` for the current device."""
+    out = ctypes.c_size_t(0)
+    _check(load_library().rmsnorm_bwd_workspace_bytes(int(M), int(N), _DTYPES[dtype],
+                                                      ctypes.byref(out)))
+    return int(out.value)
+
+
+def rmsnorm_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, rstd: torch.Tensor,
+                dx: torch.Tensor, dw: torch.Tensor, workspace: torch.Tensor, eps: float,
+                stream=None) -> None:
+    """C ``rmsnorm_bwd``: dx (dtype of x) and dw ([N] fp32, overwritten)."""
+    M, N = _rows(x)
+    _same(x, dy, "dy")
+    _same(x, dx, "dx")
+    if w.shape != (N,) or w.dtype != x.dtype:
+        raise ValueError("w must have shape (N,) and the dtype of x")
+    if rstd.numel() != M or dw.numel() != N:
+        raise ValueError("rstd must hold M values and dw N values")
+    _check(load_library().rmsnorm_bwd(
+        _mat(dy, "dy", N), _mat(x, "x"), _mat(w, "w"), _vec(rstd, "rstd"), _mat(dx, "dx"),
+        _vec(dw, "dw"), _mat(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        M, N, float(eps), _dtype(x), _stream(stream)))
+
+
+def rmsnorm_bwd_ex(dy, x, w, rstd, dx, dw, workspace, eps, launch: Optional[Launch] = None,
+                   stream=None) -> None:
+    """C ``rmsnorm_bwd_ex``: backward with an explicit stage-1 launch configuration."""
+    M, N = _rows(x)
+    _same(x, dy, "dy")
+    _same(x, dx, "dx")
+    cfg = ctypes.byref(launch.to_c()) if launch is not None else None
+    _check(load_library().rmsnorm_bwd_ex(
+        _mat(dy, "dy", N), _mat(x, "x"), _mat(w, "w"), _vec(rstd, "rstd"), _mat(dx, "dx"),
+        _vec(dw, "dw"), _mat(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        M, N, float(eps), _dtype(x), cfg, _stream(stream)))
+
+
+def plan_fwd(x: torch.Tensor, residual: Optional[torch.Tensor] = None,
+             residual_out: Optional[torch.Tensor] = None, w: Optional[torch.Tensor] = None,
+             y: Optional[torch.Tensor] = None) -> Launch:
+    """C ``rrn_plan_fwd``: the launch the automatic forward would use for these tensors."""
+    M, N = _rows(x)
+    out = rrn_launch()
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    _check(load_library().rrn_plan_fwd(ptr(x), ptr(residual), ptr(residual_out),
+                                       ptr(w if w is not None else x), ptr(y if y is not None else x),
+                                       M, N, _dtype(x), ctypes.byref(out)))
+    return Launch.from_c(out)
+
+
+def plan_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, dx: torch.Tensor) -> Launch:
+    """C ``rrn_plan_bwd``: the stage-1 launch the automatic backward would use."""
+    M, N = _rows(x)
+    out = rrn_launch()
+    _check(load_library().rrn_plan_bwd(dy.data_ptr(), x.data_ptr(), w.data_ptr(), dx.data_ptr(),
+                                       M, N, _dtype(x), ctypes.byref(out)))
+    return Launch.from_c(out)

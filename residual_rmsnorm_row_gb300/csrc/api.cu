@@ -1,0 +1,427 @@
+// C ABI of the RMSNorm library: argument validation, launch planning, dispatch.
+//
+// Every entry point validates all of its arguments before touching the GPU, picks a kernel
+// variant from (dtype, M, N, alignment, SM count), launches on the caller's stream and
+// returns. Nothing here allocates device memory, synchronises, or compiles code at run time
+// (the CuTe DSL skill page's rule for a kernel wrapper - no per-call allocation, copy or
+// recompilation, "Workflow 0" step 4 and "Workflow 1" step 5 - applied to a prebuilt
+// library).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <initializer_list>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "launch.h"
+#include "rrn.h"
+
+namespace rrn {
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return RRN_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- device properties (cached)
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+int current_sm_count(int *sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev >= 0 && dev < kMaxDevices) {
+        int cached = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (cached > 0) {
+            *sms = cached;
+            return RRN_OK;
+        }
+    }
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(n, std::memory_order_relaxed);
+    *sms = n;
+    return RRN_OK;
+}
+
+// Occupancy per (device, kernel instance, block size), computed once.
+std::mutex g_occ_mutex;
+std::map<std::tuple<int, int, int, int, int, int, int, int>, int> g_occ;
+
+int occupancy(bool bwd, int dtype, bool fused, const Launch &l) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    const auto key = std::make_tuple(dev, bwd ? 1 : 0, dtype, fused ? 1 : 0, l.variant, l.vpt,
+                                     l.threads, l.vec ? 1 : 0);
+    {
+        std::lock_guard<std::mutex> g(g_occ_mutex);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) return it->second;
+    }
+    int n = bwd ? (dtype == RRN_BF16 ? occupancy_bwd_bf16(l) : occupancy_bwd_f32(l))
+                : (dtype == RRN_BF16 ? occupancy_fwd_bf16(fused, l) : occupancy_fwd_f32(fused, l));
+    std::lock_guard<std::mutex> g(g_occ_mutex);
+    g_occ[key] = n;
+    return n;
+}
+
+// ---------------------------------------------------------------- argument checks
+int elem_size(int dtype) { return dtype == RRN_BF16 ? 2 : dtype == RRN_F32 ? 4 : 0; }
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_common(int64_t M, int64_t N, float eps, int dtype) {
+    if (elem_size(dtype) == 0) return RRN_ERR_DTYPE;
+    if (M < 0 || N < 1 || N > INT32_MAX) return RRN_ERR_SHAPE;
+    if (M > 0 && M > (INT64_MAX / 16) / N) return RRN_ERR_SHAPE;
+    if (!std::isfinite(eps) || eps < 0.f) return RRN_ERR_EPS;
+    return RRN_OK;
+}
+
+int round_up32(int64_t v) { return static_cast<int>((v + 31) / 32 * 32); }
+
+int ceil_pow2_vpt(int64_t need, int max_vpt) {
+    int v = 1;
+    while (v < need && v < max_vpt) v *= 2;
+    return v;
+}
+
+int clamp_grid(int64_t v) {
+    if (v < 1) return 1;
+    return v > INT32_MAX ? INT32_MAX : static_cast<int>(v);
+}
+
+// Threads per CTA the row-per-CTA forward aims for on large M: 8 CTAs of 256 threads fill an
+// SM, each with one 128-bit load per tensor per VPT in flight.
+constexpr int kFwdTargetThreads = 256;
+constexpr int kBwdTargetThreads = 256;
+
+// ---------------------------------------------------------------- forward planning
+// True when every row of every matrix starts on a 16-byte boundary (128-bit vector path).
+bool vec_path_ok(std::initializer_list<const void *> ptrs, int64_t N, int dtype) {
+    for (const void *p : ptrs)
+        if (p && !aligned(p, 16)) return false;
+    return N % (16 / elem_size(dtype)) == 0;
+}
+
+int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const rrn_launch *cfg,
+                  Launch *out) {
+    const int V = 16 / elem_size(dtype);
+    const int64_t nvec = N / V;
+    int sms = 0;
+    int st = current_sm_count(&sms);
+    if (st != RRN_OK) return st;
+
+    Launch l{};
+    l.variant = cfg && cfg->variant ? cfg->variant : RRN_VARIANT_AUTO;
+    if (l.variant == RRN_VARIANT_AUTO) {
+        if (!vec_ok) l.variant = RRN_VARIANT_STREAM;
+        else if (nvec <= 32 * kMaxVpt && M >= 4LL * sms) l.variant = RRN_VARIANT_ROW_WARP;
+        else if (nvec <= 2048) l.variant = RRN_VARIANT_ROW_CTA;
+        else l.variant = RRN_VARIANT_STREAM;
+    }
+    l.vec = (l.variant == RRN_VARIANT_STREAM) ? vec_ok : true;
+
+    switch (l.variant) {
+        case RRN_VARIANT_ROW_CTA: {
+            if (!vec_ok) return RRN_ERR_CONFIG;
+            if (cfg && cfg->vpt) {
+                l.vpt = cfg->vpt;
+            } else if (M < 2LL * sms) {
+                // Few rows (decode shapes): the widest CTA, so each row arrives in one round trip.
+                l.vpt = 1;
+                while (l.vpt < kMaxVpt && nvec > static_cast<int64_t>(l.vpt) * fwd_max_threads(l.vpt)) l.vpt *= 2;
+            } else {
+                l.vpt = ceil_pow2_vpt((nvec + kFwdTargetThreads - 1) / kFwdTargetThreads, kMaxVpt);
+                while (l.vpt < kMaxVpt && nvec > static_cast<int64_t>(l.vpt) * fwd_max_threads(l.vpt)) l.vpt *= 2;
+            }
+            l.threads = cfg && cfg->threads ? cfg->threads : round_up32((nvec + l.vpt - 1) / l.vpt);
+            if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4 && l.vpt != 8) return RRN_ERR_CONFIG;
+            if (l.threads < 32 || l.threads % 32 || l.threads > fwd_max_threads(l.vpt)) return RRN_ERR_CONFIG;
+            if (static_cast<int64_t>(l.vpt) * l.threads < nvec) return RRN_ERR_CONFIG;
+            l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid(M);
+            break;
+        }
+        case RRN_VARIANT_ROW_WARP: {
+            if (!vec_ok) return RRN_ERR_CONFIG;
+            l.vpt = cfg && cfg->vpt ? cfg->vpt : ceil_pow2_vpt((nvec + 31) / 32, kMaxVpt);
+            if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4 && l.vpt != 8) return RRN_ERR_CONFIG;
+            if (static_cast<int64_t>(l.vpt) * 32 < nvec) return RRN_ERR_CONFIG;
+            l.threads = cfg && cfg->threads ? cfg->threads : 128;
+            if (l.threads < 32 || l.threads % 32 || l.threads > 256) return RRN_ERR_CONFIG;
+            l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid((M + l.threads / 32 - 1) / (l.threads / 32));
+            break;
+        }
+        case RRN_VARIANT_STREAM: {
+            l.vpt = 1;
+            const int64_t chunks = l.vec ? nvec : N;
+            l.threads = cfg && cfg->threads ? cfg->threads
+                                            : (chunks >= 512 ? 512 : round_up32(chunks));
+            if (l.threads < 32 || l.threads % 32 || l.threads > 1024) return RRN_ERR_CONFIG;
+            if (cfg && cfg->ctas) {
+                l.ctas = cfg->ctas;
+            } else {
+                const int occ = occupancy(false, dtype, fused, l);
+                l.ctas = clamp_grid(M < static_cast<int64_t>(sms) * (occ > 0 ? occ : 1)
+                                        ? M
+                                        : static_cast<int64_t>(sms) * (occ > 0 ? occ : 1));
+            }
+            break;
+        }
+        default:
+            return RRN_ERR_CONFIG;
+    }
+    if (l.ctas < 1) return RRN_ERR_CONFIG;
+    *out = l;
+    return RRN_OK;
+}
+
+int check_fwd(const void *x, const void *res, const void *res_out, const void *w, const void *y,
+              const float *rstd, int64_t M, int64_t N, float eps, int dtype) {
+    int st = check_common(M, N, eps, dtype);
+    if (st != RRN_OK) return st;
+    if (!x || !w || !y || (res && !res_out)) return RRN_ERR_NULL;
+    const uintptr_t es = elem_size(dtype);
+    if (!aligned(x, es) || !aligned(w, es) || !aligned(y, es) || (res && !aligned(res, es)) ||
+        (res && !aligned(res_out, es)) || (rstd && !aligned(rstd, 4)))
+        return RRN_ERR_ALIGN;
+    return RRN_OK;
+}
+
+int run_fwd(const void *x, const void *res, void *res_out, const void *w, void *y, float *rstd,
+            int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg, cudaStream_t stream) {
+    int st = check_fwd(x, res, res_out, w, y, rstd, M, N, eps, dtype);
+    if (st != RRN_OK) return st;
+    if (M == 0) return RRN_OK;
+    Launch l;
+    st = plan_fwd_impl(vec_path_ok({x, res, res_out, w, y}, N, dtype), res != nullptr, M, N, dtype,
+                       cfg, &l);
+    if (st != RRN_OK) return st;
+    FwdArgs a{x, res, res ? res_out : nullptr, w, y, rstd, M, static_cast<int>(N), eps};
+    cudaError_t e = dtype == RRN_BF16 ? launch_fwd_bf16(a, l, stream) : launch_fwd_f32(a, l, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return RRN_OK;
+}
+
+// ---------------------------------------------------------------- backward planning
+int plan_bwd_impl(bool vec_ok, int64_t M, int64_t N, int dtype, const rrn_launch *cfg, Launch *out,
+                  int64_t *rows_per_cta) {
+    const int V = 16 / elem_size(dtype);
+    const int64_t nvec = N / V;
+    int sms = 0;
+    int st = current_sm_count(&sms);
+    if (st != RRN_OK) return st;
+
+    Launch l{};
+    l.variant = cfg && cfg->variant ? cfg->variant : RRN_VARIANT_AUTO;
+    if (l.variant == RRN_VARIANT_AUTO)
+        l.variant = (vec_ok && nvec <= static_cast<int64_t>(kBwdMaxVpt) * bwd_max_threads(kBwdMaxVpt))
+                        ? RRN_VARIANT_ROW_CTA
+                        : RRN_VARIANT_STREAM;
+    l.vec = (l.variant == RRN_VARIANT_STREAM) ? vec_ok : true;
+    switch (l.variant) {
+        case RRN_VARIANT_ROW_CTA: {
+            if (!vec_ok) return RRN_ERR_CONFIG;
+            if (cfg && cfg->vpt) {
+                l.vpt = cfg->vpt;
+            } else {
+                l.vpt = ceil_pow2_vpt((nvec + kBwdTargetThreads - 1) / kBwdTargetThreads, kBwdMaxVpt);
+                while (l.vpt < kBwdMaxVpt && nvec > static_cast<int64_t>(l.vpt) * bwd_max_threads(l.vpt)) l.vpt *= 2;
+            }
+            if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4) return RRN_ERR_CONFIG;
+            l.threads = cfg && cfg->threads ? cfg->threads : round_up32((nvec + l.vpt - 1) / l.vpt);
+            if (l.threads < 32 || l.threads % 32 || l.threads > bwd_max_threads(l.vpt)) return RRN_ERR_CONFIG;
+            if (static_cast<int64_t>(l.vpt) * l.threads < nvec) return RRN_ERR_CONFIG;
+            break;
+        }
+        case RRN_VARIANT_STREAM: {
+            l.vpt = 1;
+            const int64_t chunks = l.vec ? nvec : N;
+            l.threads = cfg && cfg->threads ? cfg->threads
+                                            : (chunks >= 512 ? 512 : round_up32(chunks));
+            if (l.threads < 32 || l.threads % 32 || l.threads > 1024) return RRN_ERR_CONFIG;
+            break;
+        }
+        default:
+            return RRN_ERR_CONFIG;
+    }
+    int64_t want = 0;
+    if (cfg && cfg->ctas) {
+        want = cfg->ctas;
+    } else {
+        const int occ = occupancy(true, dtype, false, l);
+        want = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
+    }
+    if (want < 1) return RRN_ERR_CONFIG;
+    if (M == 0) {
+        l.ctas = 0;
+        *rows_per_cta = 0;
+    } else {
+        if (want > M) want = M;
+        const int64_t rpc = (M + want - 1) / want;
+        l.ctas = clamp_grid((M + rpc - 1) / rpc);  // every CTA owns at least one row
+        *rows_per_cta = rpc;
+    }
+    *out = l;
+    return RRN_OK;
+}
+
+int check_bwd(const void *dy, const void *x, const void *w, const float *rstd, const void *dx,
+              const float *dw, int64_t M, int64_t N, float eps, int dtype) {
+    int st = check_common(M, N, eps, dtype);
+    if (st != RRN_OK) return st;
+    if (!dy || !x || !w || !rstd || !dx || !dw) return RRN_ERR_NULL;
+    const uintptr_t es = elem_size(dtype);
+    if (!aligned(dy, es) || !aligned(x, es) || !aligned(w, es) || !aligned(dx, es) ||
+        !aligned(rstd, 4) || !aligned(dw, 4))
+        return RRN_ERR_ALIGN;
+    return RRN_OK;
+}
+
+int run_bwd(const void *dy, const void *x, const void *w, const float *rstd, void *dx, float *dw,
+            void *workspace, size_t workspace_bytes, int64_t M, int64_t N, float eps, int dtype,
+            const rrn_launch *cfg, cudaStream_t stream) {
+    int st = check_bwd(dy, x, w, rstd, dx, dw, M, N, eps, dtype);
+    if (st != RRN_OK) return st;
+    if (M == 0) return RRN_OK;
+    Launch l;
+    int64_t rpc = 0;
+    st = plan_bwd_impl(vec_path_ok({dy, x, w, dx}, N, dtype), M, N, dtype, cfg, &l, &rpc);
+    if (st != RRN_OK) return st;
+    const size_t need = static_cast<size_t>(l.ctas) * static_cast<size_t>(N) * sizeof(float);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return RRN_ERR_WORKSPACE;
+    BwdArgs a{dy, x, w, rstd, dx, dw, static_cast<float *>(workspace), M, static_cast<int>(N), rpc};
+    cudaError_t e = dtype == RRN_BF16 ? launch_bwd_bf16(a, l, stream) : launch_bwd_f32(a, l, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return RRN_OK;
+}
+
+void to_public(const Launch &l, rrn_launch *out) {
+    out->variant = l.variant;
+    out->vpt = l.vpt;
+    out->threads = l.threads;
+    out->ctas = l.ctas;
+    out->vec = l.vec ? 1 : 0;
+}
+
+}  // namespace
+}  // namespace rrn
+
+using namespace rrn;
+
+extern "C" {
+
+RRN_API int rmsnorm_fwd(const void *x, const void *w, void *y, float *rstd, int64_t M, int64_t N,
+                        float eps, int dtype, rrn_stream_t stream) {
+    return run_fwd(x, nullptr, nullptr, w, y, rstd, M, N, eps, dtype, nullptr,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+RRN_API int add_rmsnorm_fwd(const void *x, const void *residual, void *residual_out, const void *w,
+                            void *y, float *rstd, int64_t M, int64_t N, float eps, int dtype,
+                            rrn_stream_t stream) {
+    if (!residual) return RRN_ERR_NULL;
+    return run_fwd(x, residual, residual_out, w, y, rstd, M, N, eps, dtype, nullptr,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+RRN_API int add_rmsnorm_fwd_ex(const void *x, const void *residual, void *residual_out,
+                               const void *w, void *y, float *rstd, int64_t M, int64_t N,
+                               float eps, int dtype, const rrn_launch *cfg, rrn_stream_t stream) {
+    return run_fwd(x, residual, residual_out, w, y, rstd, M, N, eps, dtype, cfg,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+RRN_API int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t *bytes) {
+    if (!bytes) return RRN_ERR_NULL;
+    int st = check_common(M, N, 0.f, dtype);
+    if (st != RRN_OK) return st;
+    if (M == 0) {
+        *bytes = 0;
+        return RRN_OK;
+    }
+    // The caller's buffers are not known here: size for both the 128-bit vector plan and the
+    // element-wise plan (unaligned buffers) and return the larger.
+    Launch l, l2;
+    int64_t rpc = 0, rpc2 = 0;
+    st = plan_bwd_impl(true, M, N, dtype, nullptr, &l, &rpc);
+    if (st != RRN_OK) return st;
+    st = plan_bwd_impl(false, M, N, dtype, nullptr, &l2, &rpc2);
+    if (st != RRN_OK) return st;
+    const int ctas = l.ctas > l2.ctas ? l.ctas : l2.ctas;
+    *bytes = static_cast<size_t>(ctas) * static_cast<size_t>(N) * sizeof(float);
+    return RRN_OK;
+}
+
+RRN_API int rmsnorm_bwd(const void *dy, const void *x, const void *w, const float *rstd, void *dx,
+                        float *dw, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
+                        float eps, int dtype, rrn_stream_t stream) {
+    return run_bwd(dy, x, w, rstd, dx, dw, workspace, workspace_bytes, M, N, eps, dtype, nullptr,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+RRN_API int rmsnorm_bwd_ex(const void *dy, const void *x, const void *w, const float *rstd,
+                           void *dx, float *dw, void *workspace, size_t workspace_bytes,
+                           int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,
+                           rrn_stream_t stream) {
+    return run_bwd(dy, x, w, rstd, dx, dw, workspace, workspace_bytes, M, N, eps, dtype, cfg,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+RRN_API int rrn_plan_fwd(const void *x, const void *residual, const void *residual_out,
+                         const void *w, const void *y, int64_t M, int64_t N, int dtype,
+                         rrn_launch *out) {
+    if (!out) return RRN_ERR_NULL;
+    int st = check_fwd(x, residual, residual_out, w, y, nullptr, M, N, 0.f, dtype);
+    if (st != RRN_OK) return st;
+    Launch l;
+    st = plan_fwd_impl(vec_path_ok({x, residual, residual_out, w, y}, N, dtype), residual != nullptr,
+                       M, N, dtype, nullptr, &l);
+    if (st != RRN_OK) return st;
+    to_public(l, out);
+    return RRN_OK;
+}
+
+RRN_API int rrn_plan_bwd(const void *dy, const void *x, const void *w, const void *dx, int64_t M,
+                         int64_t N, int dtype, rrn_launch *out) {
+    if (!out) return RRN_ERR_NULL;
+    int st = check_common(M, N, 0.f, dtype);
+    if (st != RRN_OK) return st;
+    if (!dy || !x || !w || !dx) return RRN_ERR_NULL;
+    Launch l;
+    int64_t rpc = 0;
+    st = plan_bwd_impl(vec_path_ok({dy, x, w, dx}, N, dtype), M, N, dtype, nullptr, &l, &rpc);
+    if (st != RRN_OK) return st;
+    to_public(l, out);
+    return RRN_OK;
+}
+
+RRN_API const char *rrn_status_string(int status) {
+    switch (status) {
+        case RRN_OK: return "success";
+        case RRN_ERR_NULL: return "a required pointer is NULL";
+        case RRN_ERR_SHAPE: return "invalid shape: need M >= 0, 1 <= N <= INT32_MAX, M*N bounded";
+        case RRN_ERR_EPS: return "eps must be finite and >= 0";
+        case RRN_ERR_DTYPE: return "dtype must be RRN_BF16 or RRN_F32";
+        case RRN_ERR_ALIGN: return "a pointer is not aligned to its element size";
+        case RRN_ERR_WORKSPACE: return "workspace is NULL, unaligned or smaller than required";
+        case RRN_ERR_CUDA: return "a CUDA call or kernel launch failed (see rrn_last_cuda_error)";
+        case RRN_ERR_CONFIG: return "the launch configuration cannot run this problem";
+        default: return "unknown status";
+    }
+}
+
+RRN_API int rrn_last_cuda_error(void) { return t_last_cuda_error; }
+
+}  // extern "C"

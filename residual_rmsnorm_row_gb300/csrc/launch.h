@@ -1,0 +1,69 @@
+// Host-side interface between the C ABI (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "rrn.h"
+
+namespace rrn {
+
+// Arguments of one forward call (fused when res != nullptr).
+struct FwdArgs {
+    const void *x;
+    const void *res;  // nullptr: plain RMSNorm
+    void *res_out;    // ignored when res == nullptr
+    const void *w;
+    void *y;
+    float *rstd;      // may be nullptr
+    int64_t M;
+    int N;
+    float eps;
+};
+
+// Arguments of one backward call. `partial` is the [P, N] fp32 workspace (P = ctas).
+struct BwdArgs {
+    const void *dy;
+    const void *x;
+    const void *w;
+    const float *rstd;
+    void *dx;
+    float *dw;
+    float *partial;
+    int64_t M;
+    int N;
+    int64_t rows_per_cta;
+};
+
+// A resolved launch (all fields set).
+struct Launch {
+    int variant;  // rrn_variant, never AUTO here
+    int vpt;
+    int threads;
+    int ctas;
+    bool vec;     // 128-bit vectors (else element-wise)
+};
+
+// Largest vectors-per-thread the register variants are compiled for, and the thread limit
+// each VPT is compiled with (__launch_bounds__), which bounds registers per thread.
+constexpr int kMaxVpt = 8;
+constexpr int fwd_max_threads(int vpt) { return vpt >= 8 ? 256 : vpt >= 4 ? 512 : 1024; }
+constexpr int bwd_max_threads(int vpt) { return vpt >= 4 ? 256 : 512; }
+constexpr int kBwdMaxVpt = 4;
+constexpr int kReduceThreads = 256;  // dw stage-2 CTA size: 32 columns x 8 row groups
+
+// Kernel launchers, one per dtype (defined in fwd_bf16.cu, fwd_f32.cu and bwd.cu). They
+// enqueue on `stream` and return the cudaError_t of the launch.
+cudaError_t launch_fwd_bf16(const FwdArgs &a, const Launch &l, cudaStream_t stream);
+cudaError_t launch_fwd_f32(const FwdArgs &a, const Launch &l, cudaStream_t stream);
+cudaError_t launch_bwd_bf16(const BwdArgs &a, const Launch &l, cudaStream_t stream);
+cudaError_t launch_bwd_f32(const BwdArgs &a, const Launch &l, cudaStream_t stream);
+
+// Occupancy (resident CTAs per SM) of the kernel a launch would run; 0 on error.
+int occupancy_fwd_bf16(bool fused, const Launch &l);
+int occupancy_fwd_f32(bool fused, const Launch &l);
+int occupancy_bwd_bf16(const Launch &l);
+int occupancy_bwd_f32(const Launch &l);
+
+}  // namespace rrn

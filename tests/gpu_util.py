@@ -1,0 +1,85 @@
+"""Helpers for the GPU parity tests: host <-> device transfer of raw encodings, and the
+acceptance bounds, written once.
+
+Bounds (each compares a GPU output, decoded exactly to fp64, with the oracle's fp64 value):
+  bf16 outputs (y, residual_out, dx): |err| <= 2^-8 * |ref| + 1e-6
+  fp32 outputs (y, residual_out):     |err| <= 1e-5 * |ref| + 1e-6
+  rstd (fp32):                        |err| <= 1e-5 * |ref|
+  dw (fp32):                          |err| <= 1e-3 * max(|ref|, 1)
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+BF16_REL = 2.0 ** -8
+ABS = 1e-6
+F32_REL = 1e-5
+RSTD_REL = 1e-5
+DW_REL = 1e-3
+
+TORCH = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def to_dev(a: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
+    """Host array in its storage encoding (uint16 bf16 bits / float32) -> CUDA tensor."""
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+
+
+def to_host(t: torch.Tensor) -> np.ndarray:
+    """CUDA tensor -> host array in its storage encoding."""
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def values(t: torch.Tensor) -> np.ndarray:
+    """Exact fp64 values of a CUDA tensor's elements."""
+    return oracle.decode(to_host(t))
+
+
+def _worst(err, bound, got, ref, what):
+    ratio = np.where(bound > 0, err / np.where(bound > 0, bound, 1.0), np.inf)
+    bad = ~(err <= bound)
+    i = np.unravel_index(np.argmax(np.where(bad, np.inf, ratio)) if bad.any()
+                         else np.argmax(ratio), err.shape)
+    return (f"{what}: {int(bad.sum())} of {err.size} outside the bound; worst at {tuple(int(k) for k in i)}: "
+            f"got {got[i]!r}, want {ref[i]!r}, err/bound {ratio[i]:.3g}")
+
+
+def check_out(got: np.ndarray, ref: np.ndarray, dtype: str, what: str) -> float:
+    """Assert the storage-type bound elementwise; return max err/bound."""
+    rel = BF16_REL if dtype == "bf16" else F32_REL
+    err = np.abs(got - ref)
+    bound = rel * np.abs(ref) + ABS
+    ok = err <= bound
+    assert ok.all(), _worst(err, bound, got, ref, what)
+    return float(np.max(err / bound)) if err.size else 0.0
+
+
+def check_rstd(got: np.ndarray, ref: np.ndarray, what: str = "rstd") -> float:
+    err = np.abs(got - ref)
+    bound = RSTD_REL * np.abs(ref)
+    ok = err <= bound
+    assert ok.all(), _worst(err, bound, got, ref, what)
+    return float(np.max(err / np.where(bound > 0, bound, 1.0))) if err.size else 0.0
+
+
+def check_dw(got: np.ndarray, ref: np.ndarray, what: str = "dw") -> float:
+    err = np.abs(got - ref)
+    bound = DW_REL * np.maximum(np.abs(ref), 1.0)
+    ok = err <= bound
+    assert ok.all(), _worst(err, bound, got, ref, what)
+    return float(np.max(err / bound)) if err.size else 0.0
+
+
+def bits_of(values_f32: np.ndarray, dtype: str) -> np.ndarray:
+    """Storage encoding of float32 values (bf16 rounded to nearest even by torch's cast)."""
+    import synth
+
+    return synth.to_bf16_bits(values_f32) if dtype == "bf16" else np.asarray(values_f32, np.float32)

@@ -1,0 +1,394 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU fp64 oracle.
+
+Every comparison is element by element on the same seeded host inputs, with the bounds of
+``gpu_util``. The named workloads run at their full sizes in the automatic launch
+configuration (the one the benchmark times); the full-size forward outputs are compared in row
+chunks against the oracle, so every element is checked.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import residual_rmsnorm_row_gb300 as rrn
+import synth
+from gpu_util import (check_dw, check_out, check_rstd, to_dev, to_host, values, bits_of, TORCH)
+
+pytestmark = pytest.mark.gpu
+
+CHUNK_ROWS = 2048
+
+
+def fwd_case(x_h, res_h, w_h, dtype, eps, launch=None, inplace=None):
+    """Run one forward on the GPU; return device tensors (y, residual_out or None, rstd)."""
+    x = to_dev(x_h, dtype)
+    w = to_dev(w_h, dtype)
+    M = x.shape[0]
+    y = torch.full_like(x, float("nan"))
+    rstd = torch.full((M,), float("nan"), device="cuda")
+    if res_h is None:
+        rrn.add_rmsnorm_fwd_ex(x, None, None, w, y, rstd, eps, launch)
+        ro = None
+    else:
+        res = to_dev(res_h, dtype)
+        ro = torch.full_like(x, float("nan"))
+        rrn.add_rmsnorm_fwd_ex(x, res, ro, w, y, rstd, eps, launch)
+    torch.cuda.synchronize()
+    return y, ro, rstd
+
+
+def compare_fwd(x_h, res_h, w_h, dtype, eps, y, ro, rstd, rows=None):
+    """Compare GPU outputs with the oracle over all rows (in chunks) or the given rows."""
+    M = x_h.shape[0]
+    worst = 0.0
+    starts = range(0, M, CHUNK_ROWS) if rows is None else [None]
+    for s in starts:
+        idx = np.arange(s, min(M, s + CHUNK_ROWS)) if rows is None else np.asarray(rows)
+        r_ref, y_ref, rs_ref = oracle.add_rmsnorm_fwd(x_h[idx], None if res_h is None else res_h[idx],
+                                                      w_h, eps)
+        ti = torch.from_numpy(idx).cuda()
+        worst = max(worst, check_out(values(y.index_select(0, ti)), y_ref, dtype, "y"))
+        worst = max(worst, check_rstd(rstd.index_select(0, ti).cpu().numpy().astype(np.float64), rs_ref))
+        if res_h is not None:
+            got_r = values(ro.index_select(0, ti))
+            worst = max(worst, check_out(got_r, r_ref, dtype, "residual_out"))
+            # residual_out is the sum rounded once: it must equal the correctly rounded sum.
+            # The fp64 sum of two bf16/fp32 values is exact here, so rounding it to fp32 gives
+            # the kernel's fp32 r bit for bit, and rounding that to bf16 its residual_out.
+            want = bits_of(r_ref.astype(np.float32), dtype)
+            assert np.array_equal(to_host(ro.index_select(0, ti)), want), \
+                "residual_out is not the sum rounded once to the storage type"
+    return worst
+
+
+# ------------------------------------------------------------------ the named workloads
+FWD_WORKLOADS = [n for n, w in synth.WORKLOADS.items() if w.op != "rmsnorm_bwd"]
+
+
+@pytest.mark.parametrize("name", FWD_WORKLOADS)
+def test_forward_workload_full_size(name):
+    wl = synth.get(name)
+    h = synth.make(wl)
+    res_h = h.get("residual")
+    y, ro, rstd = fwd_case(h["x"], res_h, h["w"], wl.dtype, wl.eps)
+    worst = compare_fwd(h["x"], res_h, h["w"], wl.dtype, wl.eps, y, ro, rstd)
+    print(f"{name}: max err/bound {worst:.3f}")
+
+
+def test_backward_workload_full_size():
+    wl = synth.get("rmsnorm_bwd_16384x4096_bf16")
+    h = synth.make(wl)
+    x, w, dy = to_dev(h["x"], "bf16"), to_dev(h["w"], "bf16"), to_dev(h["dy"], "bf16")
+    _, rstd = rrn.rms_norm(x, w, wl.eps)          # rstd from the GPU forward, as in training
+    dx, dw = rrn.rms_norm_backward(dy, x, w, rstd, wl.eps)
+    torch.cuda.synchronize()
+    dx_ref, dw_ref = oracle.rmsnorm_bwd(h["dy"], h["x"], h["w"], wl.eps)
+    a = check_out(values(dx), dx_ref, "bf16", "dx")
+    b = check_dw(dw.cpu().numpy().astype(np.float64), dw_ref)
+    print(f"bwd 16384x4096: dx max err/bound {a:.3f}, dw max err/bound {b:.3f}")
+
+
+# ------------------------------------------------------------------ every kernel variant
+def _variants(dtype, N, M):
+    V = 8 if dtype == "bf16" else 4
+    nvec = N // V
+    out = []
+    for vpt in (1, 2, 4, 8):
+        lim = 256 if vpt == 8 else 512 if vpt == 4 else 1024
+        thr = -(-nvec // vpt)
+        thr = -(-thr // 32) * 32
+        if N % V == 0 and thr <= lim:
+            out.append(rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0))
+            out.append(rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 37))     # persistent, ragged
+        if N % V == 0 and nvec <= 32 * vpt:
+            out.append(rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 128, 0))
+            out.append(rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 64, 5))
+    out.append(rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0))
+    out.append(rrn.Launch(rrn.VARIANT_STREAM, 0, 1024, 11))
+    return out
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("N", [1024, 2048, 4096, 7168])
+@pytest.mark.parametrize("fused", [False, True])
+def test_every_variant(dtype, N, fused):
+    M = 333
+    wl = synth.Workload("variants", "add_rmsnorm_fwd" if fused else "rmsnorm_fwd", M, N, dtype,
+                        1e-6, 7, res_sigma=2.0)
+    h = synth.make(wl)
+    for launch in _variants(dtype, N, M):
+        y, ro, rstd = fwd_case(h["x"], h.get("residual"), h["w"], dtype, wl.eps, launch)
+        compare_fwd(h["x"], h.get("residual"), h["w"], dtype, wl.eps, y, ro, rstd)
+
+
+# ------------------------------------------------------------------ edge shapes
+EDGE_N = [1, 7, 8, 9, 1000, 1024, 4095, 7168, 8192, 16384, 20000, 65536]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("N", EDGE_N)
+@pytest.mark.parametrize("M", [1, 3, 130])
+def test_edge_shapes_forward(dtype, N, M):
+    for fused in (False, True):
+        wl = synth.Workload("edge", "add_rmsnorm_fwd" if fused else "rmsnorm_fwd", M, N, dtype,
+                            1e-5, 100 + N)
+        h = synth.make(wl)
+        y, ro, rstd = fwd_case(h["x"], h.get("residual"), h["w"], dtype, wl.eps)
+        compare_fwd(h["x"], h.get("residual"), h["w"], dtype, wl.eps, y, ro, rstd)
+
+
+def test_empty_matrix_writes_nothing():
+    x = torch.zeros(0, 4096, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(4096, dtype=torch.bfloat16, device="cuda")
+    rrn.rmsnorm_fwd(x, w, x, None, 1e-6)
+    rrn.add_rmsnorm_fwd(x, x, x, w, x, None, 1e-6)
+    dw = torch.full((4096,), 7.0, device="cuda")
+    rrn.rmsnorm_bwd(x, x, w, torch.zeros(0, device="cuda"), x, dw,
+                    torch.zeros(4, device="cuda"), 1e-6)
+    torch.cuda.synchronize()
+    assert torch.all(dw == 7.0)
+
+
+# ------------------------------------------------------------------ alignment and aliasing
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_unaligned_base_pointers(dtype):
+    M, N = 65, 4096
+    wl = synth.Workload("unaligned", "add_rmsnorm_fwd", M, N, dtype, 1e-6, 21)
+    h = synth.make(wl)
+    t = TORCH[dtype]
+    big = [torch.empty(M * N + 1, dtype=t, device="cuda") for _ in range(5)]
+    x, res, ro, y = (b[1:].view(M, N) for b in big[:4])
+    wbuf = torch.empty(N + 1, dtype=t, device="cuda")
+    w = wbuf[1:]
+    x.copy_(to_dev(h["x"], dtype))
+    res.copy_(to_dev(h["residual"], dtype))
+    w.copy_(to_dev(h["w"], dtype))
+    rstd = torch.empty(M, device="cuda")
+    plan = rrn.plan_fwd(x, res, ro, w, y)
+    assert plan.vec == 0, "an unaligned base must take the element-wise path"
+    rrn.add_rmsnorm_fwd(x, res, ro, w, y, rstd, wl.eps)
+    torch.cuda.synchronize()
+    compare_fwd(h["x"], h["residual"], h["w"], dtype, wl.eps, y, ro, rstd)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("N", [2048, 4096, 20000, 4095])
+def test_in_place_forms(dtype, N):
+    M = 77
+    wl = synth.Workload("alias", "add_rmsnorm_fwd", M, N, dtype, 1e-6, 31)
+    h = synth.make(wl)
+    r_ref, y_ref, rs_ref = oracle.add_rmsnorm_fwd(h["x"], h["residual"], h["w"], wl.eps)
+    w = to_dev(h["w"], dtype)
+    # residual_out written over residual
+    x, res = to_dev(h["x"], dtype), to_dev(h["residual"], dtype)
+    y = torch.empty_like(x)
+    rstd = torch.empty(M, device="cuda")
+    rrn.add_rmsnorm_fwd(x, res, res, w, y, rstd, wl.eps)
+    torch.cuda.synchronize()
+    check_out(values(res), r_ref, dtype, "residual_out==residual")
+    check_out(values(y), y_ref, dtype, "y (residual_out==residual)")
+    # residual_out written over x, y over residual
+    x, res = to_dev(h["x"], dtype), to_dev(h["residual"], dtype)
+    rrn.add_rmsnorm_fwd(x, res, x, w, res, rstd, wl.eps)
+    torch.cuda.synchronize()
+    check_out(values(x), r_ref, dtype, "residual_out==x")
+    check_out(values(res), y_ref, dtype, "y==residual")
+    # plain forward in place
+    y_ref2, _ = oracle.rmsnorm_fwd(h["x"], h["w"], wl.eps)
+    x = to_dev(h["x"], dtype)
+    rrn.rmsnorm_fwd(x, w, x, None, wl.eps)
+    torch.cuda.synchronize()
+    check_out(values(x), y_ref2, dtype, "y==x")
+
+
+# ------------------------------------------------------------------ bounds: guard bands
+SENTINEL = 0x5A
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("N", [7, 1024, 2048, 4096, 7168, 20000])
+def test_outputs_stay_in_bounds(dtype, N):
+    M, G = 37, 4096  # G guard bytes before and after every output
+    wl = synth.Workload("guard", "add_rmsnorm_fwd", M, N, dtype, 1e-6, 41)
+    h = synth.make(wl)
+    es = 2 if dtype == "bf16" else 4
+    t = TORCH[dtype]
+
+    def guarded(nbytes):
+        buf = torch.full((G + nbytes + G,), SENTINEL, dtype=torch.uint8, device="cuda")
+        return buf, buf[G:G + nbytes]
+
+    bufs = {}
+    for name in ("ro", "y"):
+        bufs[name] = guarded(M * N * es)
+    bufs["rstd"] = guarded(M * 4)
+    ro = bufs["ro"][1].view(t).view(M, N)
+    y = bufs["y"][1].view(t).view(M, N)
+    rstd = bufs["rstd"][1].view(torch.float32)
+    x, res, w = to_dev(h["x"], dtype), to_dev(h["residual"], dtype), to_dev(h["w"], dtype)
+    rrn.add_rmsnorm_fwd(x, res, ro, w, y, rstd, wl.eps)
+    torch.cuda.synchronize()
+    for name, (buf, _) in bufs.items():
+        host = buf.cpu().numpy()
+        assert np.all(host[:G] == SENTINEL) and np.all(host[-G:] == SENTINEL), f"{name} guard band written"
+    compare_fwd(h["x"], h["residual"], h["w"], dtype, wl.eps, y, ro, rstd)
+    # backward
+    dxb = guarded(M * N * es)
+    dwb = guarded(N * 4)
+    dx = dxb[1].view(t).view(M, N)
+    dw = dwb[1].view(torch.float32)
+    ws_bytes = rrn.rmsnorm_bwd_workspace_bytes(M, N, t)
+    wsb = guarded(max(ws_bytes, 16))
+    ws = wsb[1].view(torch.float32)
+    dy = to_dev(h["residual"], dtype)
+    rrn.rmsnorm_bwd(dy, x, w, rstd, dx, dw, ws, wl.eps)
+    torch.cuda.synchronize()
+    for name, (buf, _) in {"dx": dxb, "dw": dwb, "workspace": wsb}.items():
+        host = buf.cpu().numpy()
+        assert np.all(host[:G] == SENTINEL) and np.all(host[-G:] == SENTINEL), f"{name} guard band written"
+
+
+# ------------------------------------------------------------------ extreme values
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("N", [1024, 4096, 20000, 4095])
+def test_extreme_rows(dtype, N):
+    rng = np.random.default_rng(51)
+    base = rng.standard_normal((8, N)).astype(np.float32)
+    rows = np.stack([
+        base[0] * 1e37,                                   # sum of squares overflows fp32
+        base[1] * 1e-30,                                  # squares underflow fp32
+        np.zeros(N, np.float32),                          # all-zero row: rstd = eps^-1/2
+        np.where(rng.random(N) < 0.01, 50.0, base[3]).astype(np.float32),   # outliers
+        np.full(N, 3.0, np.float32),                      # constant row
+        base[5] * 1e19,                                   # squares just past fp32 range
+        np.where(np.arange(N) == 0, 1e30, 1e-30).astype(np.float32),        # one huge value
+        base[7],
+    ]).astype(np.float32)
+    x_h = bits_of(rows, dtype)
+    w_h = bits_of((1.0 + 0.1 * rng.standard_normal(N)).astype(np.float32), dtype)
+    for eps in (1e-6, 0.0):
+        keep = np.arange(8) if eps > 0 else np.array([0, 1, 3, 4, 5, 6, 7])  # eps = 0: no zero row
+        xs = x_h[keep]
+        for launch in (None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0)):
+            y, _, rstd = fwd_case(xs, None, w_h, dtype, eps, launch)
+            compare_fwd(xs, None, w_h, dtype, eps, y, None, rstd)
+
+
+# ------------------------------------------------------------------ backward variants
+def _bwd_case(h, dtype, eps, launch=None, M=None):
+    x, w, dy = to_dev(h["x"], dtype), to_dev(h["w"], dtype), to_dev(h["dy"], dtype)
+    _, rstd = rrn.rms_norm(x, w, eps)
+    dx = torch.full_like(x, float("nan"))
+    dw = torch.full((x.shape[1],), float("nan"), device="cuda")
+    # An explicit launch may pick more CTAs than the automatic plan; M * N floats always suffice.
+    ws = torch.empty(max(rrn.rmsnorm_bwd_workspace_bytes(x.shape[0], x.shape[1], x.dtype),
+                         4 * x.numel()) // 4, device="cuda")
+    if launch is None:
+        rrn.rmsnorm_bwd(dy, x, w, rstd, dx, dw, ws, eps)
+    else:
+        rrn.rmsnorm_bwd_ex(dy, x, w, rstd, dx, dw, ws, eps, launch)
+    torch.cuda.synchronize()
+    return dx, dw
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("N", [1, 7, 9, 1000, 1024, 4095, 4096, 7168, 8192, 16384])
+def test_backward_shapes(dtype, N):
+    M = 203
+    wl = synth.Workload("bwd", "rmsnorm_bwd", M, N, dtype, 1e-6, 61)
+    h = synth.make(wl)
+    dx_ref, dw_ref = oracle.rmsnorm_bwd(h["dy"], h["x"], h["w"], wl.eps)
+    launches = [None, rrn.Launch(rrn.VARIANT_STREAM, 0, 128, 0), rrn.Launch(rrn.VARIANT_STREAM, 0, 512, 3)]
+    V = 8 if dtype == "bf16" else 4
+    if N % V == 0:
+        nvec = N // V
+        for vpt in (1, 2, 4):
+            thr = -(-(-(-nvec // vpt)) // 32) * 32
+            if thr <= (256 if vpt == 4 else 512):
+                launches += [rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0),
+                             rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 13)]
+    for launch in launches:
+        dx, dw = _bwd_case(h, dtype, wl.eps, launch)
+        check_out(values(dx), dx_ref, dtype, f"dx {launch}")
+        check_dw(dw.cpu().numpy().astype(np.float64), dw_ref, f"dw {launch}")
+
+
+def test_backward_is_deterministic():
+    wl = synth.get("rmsnorm_bwd_16384x4096_bf16").with_shape(4096)
+    h = synth.make(wl)
+    a_dx, a_dw = _bwd_case(h, "bf16", wl.eps)
+    b_dx, b_dw = _bwd_case(h, "bf16", wl.eps)
+    assert torch.equal(a_dx.view(torch.int16), b_dx.view(torch.int16))
+    assert torch.equal(a_dw.view(torch.int32), b_dw.view(torch.int32))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_backward_in_place(dtype):
+    M, N = 50, 4096
+    wl = synth.Workload("bwd-alias", "rmsnorm_bwd", M, N, dtype, 1e-6, 71)
+    h = synth.make(wl)
+    dx_ref, dw_ref = oracle.rmsnorm_bwd(h["dy"], h["x"], h["w"], wl.eps)
+    x, w, dy = to_dev(h["x"], dtype), to_dev(h["w"], dtype), to_dev(h["dy"], dtype)
+    _, rstd = rrn.rms_norm(x, w, wl.eps)
+    dw = torch.empty(N, device="cuda")
+    ws = torch.empty(rrn.rmsnorm_bwd_workspace_bytes(M, N, x.dtype) // 4, device="cuda")
+    rrn.rmsnorm_bwd(dy, x, w, rstd, dy, dw, ws, wl.eps)      # dx over dy
+    torch.cuda.synchronize()
+    check_out(values(dy), dx_ref, dtype, "dx==dy")
+    rrn.rmsnorm_bwd(to_dev(h["dy"], dtype), x, w, rstd, x, dw, ws, wl.eps)  # dx over x
+    torch.cuda.synchronize()
+    check_out(values(x), dx_ref, dtype, "dx==x")
+    check_dw(dw.cpu().numpy().astype(np.float64), dw_ref)
+
+
+def test_backward_workspace_too_small_is_rejected():
+    x = torch.zeros(64, 4096, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(4096, dtype=torch.bfloat16, device="cuda")
+    rstd = torch.ones(64, device="cuda")
+    dw = torch.empty(4096, device="cuda")
+    need = rrn.rmsnorm_bwd_workspace_bytes(64, 4096, torch.bfloat16)
+    ws = torch.empty(need // 4 - 1, device="cuda")
+    with pytest.raises(rrn.RRNError) as e:
+        rrn.rmsnorm_bwd(x, x, w, rstd, x, dw, ws, 1e-6)
+    assert e.value.status == 6
+
+
+def test_bad_launch_configuration_is_rejected():
+    x = torch.zeros(8, 4096, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(4096, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(rrn.RRNError) as e:   # 64 threads x 1 vector cannot cover 512 vectors
+        rrn.add_rmsnorm_fwd_ex(x, None, None, w, x, None, 1e-6, rrn.Launch(rrn.VARIANT_ROW_CTA, 1, 64, 0))
+    assert e.value.status == 8
+
+
+# ------------------------------------------------------------------ streams and graphs
+def test_side_stream_and_graph_capture():
+    wl = synth.get("add_rmsnorm_fwd_4096x4096_bf16").with_shape(1024)
+    h = synth.make(wl)
+    x, res, w = to_dev(h["x"], "bf16"), to_dev(h["residual"], "bf16"), to_dev(h["w"], "bf16")
+    y = torch.empty_like(x)
+    ro = torch.empty_like(x)
+    rstd = torch.empty(x.shape[0], device="cuda")
+    dx = torch.empty_like(x)
+    dw = torch.empty(x.shape[1], device="cuda")
+    ws = torch.empty(rrn.rmsnorm_bwd_workspace_bytes(*x.shape, x.dtype) // 4, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        rrn.add_rmsnorm_fwd(x, res, ro, w, y, rstd, wl.eps)           # current stream = s
+        rrn.rmsnorm_bwd(y, ro, w, rstd, dx, dw, ws, wl.eps, stream=s)
+    s.synchronize()
+    ref = [t.clone() for t in (y, ro, rstd, dx, dw)]
+    for t in (y, ro, rstd, dx, dw):
+        t.fill_(0)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):   # the library neither allocates nor synchronises: capturable
+        rrn.add_rmsnorm_fwd(x, res, ro, w, y, rstd, wl.eps)
+        rrn.rmsnorm_bwd(y, ro, w, rstd, dx, dw, ws, wl.eps)
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(ref, (y, ro, rstd, dx, dw)):
+        assert torch.equal(a, b)
+    compare_fwd(h["x"], h["residual"], h["w"], "bf16", wl.eps, y, ro, rstd)
