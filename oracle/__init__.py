@@ -13,6 +13,7 @@ What each function computes, with the passage it follows, is stated in ``oracle.
   rmsnorm_fwd      y = x * rstd * w, rstd = 1/sqrt(mean(x^2) + eps)  (Machete, "Built-In Areas")
   add_rmsnorm_fwd  the same on r = x + residual, also returning r  (KernelAgent page, Oink)
   rmsnorm_bwd      dx and dw, the exact derivative of rmsnorm_fwd
+  add_rmsnorm_bwd  d_r (gradient w.r.t. x + residual) and dw, the derivative of add_rmsnorm_fwd
 """
 from __future__ import annotations
 
@@ -57,8 +58,10 @@ class Oracle:
         lib.oracle_rmsnorm_fwd.argtypes = [vp, i32, vp, i32, i64, i64, dbl, _dbl_p, _dbl_p]
         lib.oracle_rmsnorm_bwd.argtypes = [vp, i32, vp, i32, vp, i32, i64, i64, dbl,
                                            _dbl_p, _dbl_p]
+        lib.oracle_add_rmsnorm_bwd.argtypes = [vp, i32, vp, i32, vp, i32, vp, i32, i64, i64, dbl,
+                                               _dbl_p, _dbl_p]
         for name in ("oracle_decode", "oracle_add_rmsnorm_fwd", "oracle_rmsnorm_fwd",
-                     "oracle_rmsnorm_bwd"):
+                     "oracle_rmsnorm_bwd", "oracle_add_rmsnorm_bwd"):
             getattr(lib, name).restype = i32
         self.lib = lib
 
@@ -125,6 +128,29 @@ class Oracle:
         return dx, dw
 
 
+    def add_rmsnorm_bwd(self, dy: np.ndarray, d_residual_out: Optional[np.ndarray],
+                        residual_out: np.ndarray, w: np.ndarray, eps: float,
+                        want_dr: bool = True) -> Tuple[Optional[np.ndarray], np.ndarray]:
+        """Return ``(d_r, dw)``: the gradient w.r.t. r = x + residual and w."""
+        dy = np.ascontiguousarray(dy)
+        r = np.ascontiguousarray(residual_out)
+        w = np.ascontiguousarray(w)
+        M, N = r.shape
+        if dy.shape != r.shape or w.shape != (N,):
+            raise ValueError("dy must have the shape of residual_out and w shape (N,)")
+        if d_residual_out is not None:
+            d_residual_out = np.ascontiguousarray(d_residual_out)
+            if d_residual_out.shape != r.shape:
+                raise ValueError("d_residual_out must have the shape of residual_out")
+        d_r = np.empty((M, N), dtype=np.float64) if want_dr else None
+        dw = np.empty((N,), dtype=np.float64)
+        self._check(self.lib.oracle_add_rmsnorm_bwd(
+            _ptr(dy), _code(dy), _ptr(d_residual_out),
+            0 if d_residual_out is None else _code(d_residual_out), _ptr(r), _code(r), _ptr(w),
+            _code(w), M, N, float(eps), _out(d_r), _out(dw)), "add_rmsnorm_bwd")
+        return d_r, dw
+
+
 _DEFAULT: Optional[Oracle] = None
 
 
@@ -152,10 +178,14 @@ def rmsnorm_bwd(dy, x, w, eps, want_dx=True):
     return default().rmsnorm_bwd(dy, x, w, eps, want_dx)
 
 
+def add_rmsnorm_bwd(dy, d_residual_out, residual_out, w, eps, want_dr=True):
+    return default().add_rmsnorm_bwd(dy, d_residual_out, residual_out, w, eps, want_dr)
+
+
 def build(force: bool = False) -> str:
     """Compile ``liboracle.so`` (used by the package's build step)."""
     return _build.build(force)
 
 
 __all__ = ["Oracle", "default", "decode", "add_rmsnorm_fwd", "rmsnorm_fwd", "rmsnorm_bwd",
-           "build", "BF16", "F32", "F64"]
+           "add_rmsnorm_bwd", "build", "BF16", "F32", "F64"]

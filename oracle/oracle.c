@@ -123,12 +123,32 @@ int oracle_rmsnorm_fwd(const void *x, int x_dt, const void *w, int w_dt, int64_t
  * fp64 from x and eps (the oracle takes nothing from a GPU forward pass).
  * dy, x: [M, N]; w: [N]. Outputs (fp64, caller-owned): dx [M, N] (may be NULL), dw [N]
  * (may be NULL; overwritten with the sum over all M rows, taken in row order).
+ * It is the fused backward below with no gradient arriving at residual_out.
  */
+/*
+ * Fused residual Add + RMSNorm backward (the backward of the KernelAgent page's "fused Add +
+ * RMSNorm", whose forward returns both y and residual_out = r = x + residual). Given the
+ * gradient dy arriving at y and the gradient d_ro arriving at residual_out (may be NULL: zero),
+ * the gradient with respect to r - and so with respect to both x and residual - is
+ *     d_r = d_ro + (RMSNorm backward of dy at r)
+ * and dw is the same as for the plain op. `r` is the forward's residual_out as stored.
+ */
+int oracle_add_rmsnorm_bwd(const void *dy, int dy_dt, const void *d_ro, int d_ro_dt,
+                           const void *r, int r_dt, const void *w, int w_dt, int64_t M, int64_t N,
+                           double eps, double *d_r, double *dw);
+
 int oracle_rmsnorm_bwd(const void *dy, int dy_dt, const void *x, int x_dt, const void *w,
                        int w_dt, int64_t M, int64_t N, double eps, double *dx, double *dw)
 {
+    return oracle_add_rmsnorm_bwd(dy, dy_dt, NULL, 0, x, x_dt, w, w_dt, M, N, eps, dx, dw);
+}
+
+int oracle_add_rmsnorm_bwd(const void *dy, int dy_dt, const void *d_ro, int d_ro_dt,
+                           const void *x, int x_dt, const void *w, int w_dt, int64_t M, int64_t N,
+                           double eps, double *dx, double *dw)
+{
     if (!dy || !x || !w || M < 0 || N < 1 || !valid_dtype(dy_dt) || !valid_dtype(x_dt) ||
-        !valid_dtype(w_dt))
+        !valid_dtype(w_dt) || (d_ro && !valid_dtype(d_ro_dt)))
         return ORACLE_BAD_ARG;
     double *xr = (double *)malloc((size_t)N * sizeof(double));
     double *dyr = (double *)malloc((size_t)N * sizeof(double));
@@ -157,7 +177,9 @@ int oracle_rmsnorm_bwd(const void *dy, int dy_dt, const void *x, int x_dt, const
         }
         double c = dot / (double)N;
         for (int64_t j = 0; j < N; ++j) {
-            if (dx) dx[i * N + j] = s * (g[j] - xhat[j] * c);
+            double grad = s * (g[j] - xhat[j] * c);
+            if (d_ro) grad += element(d_ro, d_ro_dt, i * N + j);
+            if (dx) dx[i * N + j] = grad;
             if (dw) dw[j] += dyr[j] * xhat[j];
         }
     }

@@ -75,7 +75,8 @@ def pin_golden_worked_examples(o):
     for c in cases:
         for enc in ("f64", "bf16"):
             conv = (lambda v: np.asarray(v, dtype=np.float64)) if enc == "f64" else _bf16_bits
-            x, w = conv(c["x"]), conv(c["w"])
+            x = conv(c["x"]) if "x" in c else None
+            w = conv(c["w"])
             tag = f"{c['name']} ({enc})"
             if c["op"] == "rmsnorm_fwd":
                 y, rstd = o.rmsnorm_fwd(x, w, c["eps"])
@@ -89,6 +90,11 @@ def pin_golden_worked_examples(o):
             elif c["op"] == "rmsnorm_bwd":
                 dx, dw = o.rmsnorm_bwd(conv(c["dy"]), x, w, c["eps"])
                 _close(dx, c["dx"], 1e-13, 1e-15, tag + " dx")
+                _close(dw, c["dw"], 1e-13, 1e-15, tag + " dw")
+            elif c["op"] == "add_rmsnorm_bwd":
+                r = conv(c["residual_out"])
+                d_r, dw = o.add_rmsnorm_bwd(conv(c["dy"]), conv(c["d_residual_out"]), r, w, c["eps"])
+                _close(d_r, c["d_r"], 1e-13, 1e-15, tag + " d_r")
                 _close(dw, c["dw"], 1e-13, 1e-15, tag + " dw")
             else:
                 raise AssertionError(f"unknown op {c['op']}")
@@ -275,6 +281,69 @@ def pin_bwd_matches_torch_autograd(o):
         _close(dw, tw.grad.numpy(), 1e-12, 1e-13, f"torch dw {M}x{N}")
 
 
+def pin_add_bwd_finite_differences(o):
+    """Central differences of L = <dy, y> + <d_ro, r> (r = x + residual) with respect to x and
+    to residual both give the fused backward's d_r; with respect to w, its dw."""
+    rng = np.random.default_rng(21)
+    h = 1e-6
+    M, N, eps = 2, 6, 1e-3
+    x = rng.standard_normal((M, N))
+    res = rng.standard_normal((M, N))
+    w = 1.0 + 0.3 * rng.standard_normal(N)
+    dy = rng.standard_normal((M, N))
+    dro = rng.standard_normal((M, N))
+
+    def loss(xx, rr, ww):
+        r, y, _ = o.add_rmsnorm_fwd(xx, rr, ww, eps)
+        return float(np.sum(dy * y) + np.sum(dro * r))
+
+    d_r, dw = o.add_rmsnorm_bwd(dy, dro, x + res, w, eps)
+    for which in ("x", "residual"):
+        fd = np.empty_like(x)
+        for i in range(M):
+            for j in range(N):
+                a, b = (x.copy(), res.copy()), (x.copy(), res.copy())
+                k = 0 if which == "x" else 1
+                a[k][i, j] += h
+                b[k][i, j] -= h
+                fd[i, j] = (loss(a[0], a[1], w) - loss(b[0], b[1], w)) / (2 * h)
+        _close(d_r, fd, 1e-6, 1e-7, f"d_r vs finite differences in {which}")
+    fdw = np.empty_like(w)
+    for j in range(N):
+        wp, wm = w.copy(), w.copy()
+        wp[j] += h
+        wm[j] -= h
+        fdw[j] = (loss(x, res, wp) - loss(x, res, wm)) / (2 * h)
+    _close(dw, fdw, 1e-6, 1e-7, "fused dw vs finite differences")
+
+
+def pin_add_bwd_matches_torch_autograd(o):
+    """torch autograd in float64 through r = x + residual, y = rms_norm(r) * w, returning both."""
+    import torch
+
+    rng = np.random.default_rng(22)
+    M, N, eps = 4, 96, 1e-5
+    x = rng.standard_normal((M, N))
+    res = rng.standard_normal((M, N))
+    w = 1.0 + 0.1 * rng.standard_normal(N)
+    dy = rng.standard_normal((M, N))
+    dro = rng.standard_normal((M, N))
+    tx = torch.from_numpy(x).requires_grad_(True)
+    tr = torch.from_numpy(res).requires_grad_(True)
+    tw = torch.from_numpy(w).requires_grad_(True)
+    r = tx + tr
+    y = torch.nn.functional.rms_norm(r, (N,), tw, eps)
+    (torch.sum(y * torch.from_numpy(dy)) + torch.sum(r * torch.from_numpy(dro))).backward()
+    d_r, dw = o.add_rmsnorm_bwd(dy, dro, x + res, w, eps)
+    _close(d_r, tx.grad.numpy(), 1e-12, 1e-14, "torch d(x)")
+    _close(d_r, tr.grad.numpy(), 1e-12, 1e-14, "torch d(residual)")
+    _close(dw, tw.grad.numpy(), 1e-12, 1e-13, "torch fused dw")
+    # with no gradient at residual_out it is the plain backward
+    d0, dw0 = o.add_rmsnorm_bwd(dy, None, x + res, w, eps)
+    p0, pw0 = o.rmsnorm_bwd(dy, x + res, w, eps)
+    assert np.array_equal(d0, p0) and np.array_equal(dw0, pw0), "fused bwd without d_ro != plain bwd"
+
+
 ALL_PINS = [
     pin_decode_known_bits,
     pin_decode_matches_torch_cast,
@@ -290,4 +359,6 @@ ALL_PINS = [
     pin_bwd_orthogonality,
     pin_bwd_dw_brute_force,
     pin_bwd_matches_torch_autograd,
+    pin_add_bwd_finite_differences,
+    pin_add_bwd_matches_torch_autograd,
 ]

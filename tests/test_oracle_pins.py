@@ -36,10 +36,13 @@ MUTATIONS = [
     ("weights reversed", "if (y) y[i * N + j] = r[j] * s * wd[j];",
      "if (y) y[i * N + j] = r[j] * s * wd[N - 1 - j];"),
     ("weights dropped", "if (y) y[i * N + j] = r[j] * s * wd[j];", "if (y) y[i * N + j] = r[j] * s;"),
-    ("dx sign flipped", "if (dx) dx[i * N + j] = s * (g[j] - xhat[j] * c);",
-     "if (dx) dx[i * N + j] = s * (g[j] + xhat[j] * c);"),
-    ("dx projection dropped", "if (dx) dx[i * N + j] = s * (g[j] - xhat[j] * c);",
-     "if (dx) dx[i * N + j] = s * g[j];"),
+    ("dx sign flipped", "double grad = s * (g[j] - xhat[j] * c);",
+     "double grad = s * (g[j] + xhat[j] * c);"),
+    ("dx projection dropped", "double grad = s * (g[j] - xhat[j] * c);", "double grad = s * g[j];"),
+    ("residual gradient subtracted", "if (d_ro) grad += element(d_ro, d_ro_dt, i * N + j);",
+     "if (d_ro) grad -= element(d_ro, d_ro_dt, i * N + j);"),
+    ("residual gradient dropped", "if (d_ro) grad += element(d_ro, d_ro_dt, i * N + j);",
+     "if (d_ro) grad += 0.0;"),
     ("bwd weight dropped", "g[j] = dyr[j] * wd[j];", "g[j] = dyr[j];"),
     ("projection not averaged", "double c = dot / (double)N;", "double c = dot;"),
     ("dw uses x, not xhat", "if (dw) dw[j] += dyr[j] * xhat[j];", "if (dw) dw[j] += dyr[j] * xr[j];"),
