@@ -36,7 +36,8 @@
  *     multiple of 16 the 128-bit vector kernels run; otherwise an element-wise GPU kernel
  *     runs. There is no CPU fallback.
  *   - Aliasing: an output may be the same buffer as an input of the same shape
- *     (residual_out == residual or x; y == x; dx == dy or x). Any other overlap is undefined.
+ *     (residual_out == residual or x; y == x; dx == dy or x; d_r == dy, d_residual_out or
+ *     residual_out). Any other overlap is undefined.
  *   - M == 0 is a no-op that returns RRN_OK and launches nothing.
  *   - Work is enqueued on `stream` (NULL: the legacy default stream) and the call returns
  *     without waiting. Argument errors return a nonzero code before anything is launched;
@@ -134,11 +135,50 @@ RRN_API int rmsnorm_bwd(const void *dy, const void *x, const void *w, const floa
                         float *dw, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
                         float eps, int dtype, rrn_stream_t stream);
 
+/*
+ * add_rmsnorm_bwd - backward of the fused residual Add + RMSNorm (add_rmsnorm_fwd), in one pass:
+ *   d_r = d_residual_out + rstd * (g - rhat * mean(g * rhat)),  g = dy * w,  rhat = r * rstd
+ *   dw  = sum over rows of dy * rhat
+ * where r is the forward's residual_out as stored. d_r is the gradient with respect to
+ * r = x + residual, i.e. with respect to both x and residual. (The backward of the KernelAgent
+ * page's fused Add + RMSNorm op; Machete's "Built-In Areas" lists autograd helpers.)
+ *   dy              [M, N] dtype, read (gradient arriving at y).
+ *   d_residual_out  [M, N] dtype, read; may be NULL (no gradient arrives at residual_out).
+ *   residual_out    [M, N] dtype, read (the forward's r).
+ *   w               [N] dtype, read.
+ *   rstd            [M] fp32, read (as written by the forward pass).
+ *   d_r             [M, N] dtype, written (may be dy, d_residual_out or residual_out).
+ *   dw, workspace   as for rmsnorm_bwd (same workspace size query).
+ * Returns an rrn_status.
+ */
+RRN_API int add_rmsnorm_bwd(const void *dy, const void *d_residual_out, const void *residual_out,
+                            const void *w, const float *rstd, void *d_r, float *dw,
+                            void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
+                            float eps, int dtype, rrn_stream_t stream);
+
 /* rrn_status_string - static, NUL-terminated description of a status code. */
 RRN_API const char *rrn_status_string(int status);
 
 /* rrn_last_cuda_error - the cudaError_t behind this thread's last RRN_ERR_CUDA (0 if none). */
 RRN_API int rrn_last_cuda_error(void);
+
+/*
+ * rrn_device_faults - read (and, if `clear` is nonzero, reset) the library's fault word on the
+ * current device. Bit 0 (RRN_FAULT_WAIT_TIMEOUT) is set when a kernel gave up waiting for an
+ * asynchronous copy (a bounded wait of about 2 s ran out); that kernel's outputs are then
+ * invalid. The kernels never trap. This call synchronises with the device (it copies the
+ * word), unlike every other entry point. Returns an rrn_status.
+ */
+#define RRN_FAULT_WAIT_TIMEOUT 1u
+RRN_API int rrn_device_faults(unsigned int *faults, int clear);
+
+/*
+ * rrn_selftest_wait_timeout - exercise the bounded-wait failure path on the current device:
+ * one thread waits on an mbarrier that nothing ever arrives at, gives up after `limit_ns`
+ * nanoseconds (clamped to 1 ms .. 1 s), sets RRN_FAULT_WAIT_TIMEOUT in the fault word and
+ * returns normally; the context stays usable. Enqueued on `stream`. Returns an rrn_status.
+ */
+RRN_API int rrn_selftest_wait_timeout(uint64_t limit_ns, rrn_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * Launch control, for benchmarking and tuning. The entry points above choose these
@@ -150,7 +190,9 @@ typedef enum {
     RRN_VARIANT_AUTO = 0,    /* let the library choose */
     RRN_VARIANT_ROW_CTA = 1, /* one row per CTA, row held in registers, 128-bit vectors */
     RRN_VARIANT_ROW_WARP = 2,/* one row per warp, row held in registers, 128-bit vectors */
-    RRN_VARIANT_STREAM = 3   /* one row per CTA, two passes over the row (any N / alignment) */
+    RRN_VARIANT_STREAM = 3,  /* one row per CTA, two passes over the row (any N / alignment) */
+    RRN_VARIANT_ROW_TMA = 4  /* persistent row per CTA fed by bulk async copies (TMA engine)
+                                into a shared-memory ring of `stages` rows, 128-bit vectors */
 } rrn_variant;
 
 /* A launch configuration. Zero fields mean "choose automatically". */
@@ -159,6 +201,7 @@ typedef struct {
     int vpt;     /* 128-bit vectors per thread for the register variants: 1, 2, 4 or 8 */
     int threads; /* threads per CTA (a multiple of 32, at most 1024) */
     int ctas;    /* CTAs in the grid; each walks rows with a grid-sized stride */
+    int stages;  /* RRN_VARIANT_ROW_TMA: rows in flight per CTA, 1..8 */
     int vec;     /* output of rrn_plan_*: 1 when the 128-bit vector path is used */
 } rrn_launch;
 
@@ -183,12 +226,18 @@ RRN_API int add_rmsnorm_fwd_ex(const void *x, const void *residual, void *residu
                                const void *w, void *y, float *rstd, int64_t M, int64_t N,
                                float eps, int dtype, const rrn_launch *cfg, rrn_stream_t stream);
 
-/* rmsnorm_bwd_ex - rmsnorm_bwd with an explicit stage-1 launch configuration (see above).
- * The workspace must hold cfg->ctas * N fp32 values (rrn_plan_bwd reports the default). */
+/* rmsnorm_bwd_ex / add_rmsnorm_bwd_ex - the backward calls with an explicit stage-1 launch
+ * configuration (see above). The workspace must hold cfg->ctas * N fp32 values (at most M * N;
+ * rrn_plan_bwd reports the default). */
 RRN_API int rmsnorm_bwd_ex(const void *dy, const void *x, const void *w, const float *rstd,
                            void *dx, float *dw, void *workspace, size_t workspace_bytes,
                            int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,
                            rrn_stream_t stream);
+RRN_API int add_rmsnorm_bwd_ex(const void *dy, const void *d_residual_out,
+                               const void *residual_out, const void *w, const float *rstd,
+                               void *d_r, float *dw, void *workspace, size_t workspace_bytes,
+                               int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,
+                               rrn_stream_t stream);
 
 #ifdef __cplusplus
 }

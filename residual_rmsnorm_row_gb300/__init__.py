@@ -23,12 +23,15 @@ from ._binding import (  # noqa: F401  (re-exported API)
     VARIANT_AUTO,
     VARIANT_NAMES,
     VARIANT_ROW_CTA,
+    VARIANT_ROW_TMA,
     VARIANT_ROW_WARP,
     VARIANT_STREAM,
     Launch,
     RRNError,
+    add_rmsnorm_bwd,
     add_rmsnorm_fwd,
     add_rmsnorm_fwd_ex,
+    device_faults,
     load_library,
     plan_bwd,
     plan_fwd,
@@ -36,6 +39,7 @@ from ._binding import (  # noqa: F401  (re-exported API)
     rmsnorm_bwd_ex,
     rmsnorm_bwd_workspace_bytes,
     rmsnorm_fwd,
+    selftest_wait_timeout,
 )
 
 
@@ -61,6 +65,11 @@ def add_rms_norm(x: torch.Tensor, residual: torch.Tensor, w: torch.Tensor, eps: 
     return y, residual_out, rstd
 
 
+def _workspace(M: int, N: int, like: torch.Tensor) -> torch.Tensor:
+    nbytes = rmsnorm_bwd_workspace_bytes(M, N, like.dtype)
+    return torch.empty(max(nbytes, 16) // 4, device=like.device, dtype=torch.float32)
+
+
 def rms_norm_backward(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, rstd: torch.Tensor,
                       eps: float = 1e-6, workspace: Optional[torch.Tensor] = None,
                       stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
@@ -69,14 +78,87 @@ def rms_norm_backward(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, rstd: 
     dx = torch.empty_like(x)
     dw = torch.empty(N, device=x.device, dtype=torch.float32)
     if workspace is None:
-        nbytes = rmsnorm_bwd_workspace_bytes(M, N, x.dtype)
-        workspace = torch.empty(max(nbytes, 16) // 4, device=x.device, dtype=torch.float32)
+        workspace = _workspace(M, N, x)
     rmsnorm_bwd(dy, x, w, rstd, dx, dw, workspace, eps, stream)
     return dx, dw
+
+
+def add_rms_norm_backward(dy: torch.Tensor, d_residual_out: Optional[torch.Tensor],
+                          residual_out: torch.Tensor, w: torch.Tensor, rstd: torch.Tensor,
+                          eps: float = 1e-6, workspace: Optional[torch.Tensor] = None,
+                          stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Return ``(d_r, dw)``: the gradient w.r.t. x + residual (both inputs) and w."""
+    M, N = residual_out.numel() // residual_out.shape[-1], residual_out.shape[-1]
+    d_r = torch.empty_like(residual_out)
+    dw = torch.empty(N, device=residual_out.device, dtype=torch.float32)
+    if workspace is None:
+        workspace = _workspace(M, N, residual_out)
+    add_rmsnorm_bwd(dy, d_residual_out, residual_out, w, rstd, d_r, dw, workspace, eps,
+                    stream=stream)
+    return d_r, dw
+
+
+class RMSNormFunction(torch.autograd.Function):
+    """y = RMSNorm(x) * w with the library's forward and backward kernels."""
+
+    @staticmethod
+    def forward(ctx, x, w, eps):
+        xc = x.contiguous()
+        y, rstd = rms_norm(xc, w, eps)
+        ctx.save_for_backward(xc, w, rstd)
+        ctx.eps = eps
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        x, w, rstd = ctx.saved_tensors
+        dx, dw = rms_norm_backward(dy.contiguous(), x, w, rstd, ctx.eps)
+        return dx, dw.to(w.dtype), None
+
+
+class AddRMSNormFunction(torch.autograd.Function):
+    """(y, residual_out) = (RMSNorm(x + residual) * w, x + residual) with the library's kernels.
+
+    The backward evaluates the gradient at the stored residual_out (rounded to the storage
+    type) with the forward's rstd, as a training framework saves them.
+    """
+
+    @staticmethod
+    def forward(ctx, x, residual, w, eps):
+        y, residual_out, rstd = add_rms_norm(x.contiguous(), residual.contiguous(), w, eps)
+        ctx.save_for_backward(residual_out, w, rstd)
+        ctx.eps = eps
+        return y, residual_out
+
+    @staticmethod
+    def backward(ctx, dy, d_residual_out):
+        residual_out, w, rstd = ctx.saved_tensors
+        if dy is None:
+            dy = torch.zeros_like(residual_out)
+        d_r, dw = add_rms_norm_backward(
+            dy.contiguous(), None if d_residual_out is None else d_residual_out.contiguous(),
+            residual_out, w, rstd, ctx.eps)
+        return d_r, d_r, dw.to(w.dtype), None
+
+
+class RMSNorm(torch.nn.Module):
+    """RMSNorm over the last dimension; with ``residual`` it is the fused Add + RMSNorm and
+    returns ``(y, residual_out)``."""
+
+    def __init__(self, hidden: int, eps: float = 1e-6, dtype=torch.bfloat16, device="cuda"):
+        super().__init__()
+        self.eps = eps
+        self.weight = torch.nn.Parameter(torch.ones(hidden, dtype=dtype, device=device))
+
+    def forward(self, x, residual=None):
+        if residual is None:
+            return RMSNormFunction.apply(x, self.weight, self.eps)
+        return AddRMSNormFunction.apply(x, residual, self.weight, self.eps)
 
 
 __all__ = [
     "rmsnorm_fwd", "add_rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_bwd_workspace_bytes",
     "add_rmsnorm_fwd_ex", "rmsnorm_bwd_ex", "plan_fwd", "plan_bwd", "Launch", "RRNError",
-    "load_library", "rms_norm", "add_rms_norm", "rms_norm_backward",
+    "load_library", "rms_norm", "add_rms_norm", "rms_norm_backward", "device_faults",
+    "add_rmsnorm_bwd", "add_rms_norm_backward", "RMSNormFunction", "AddRMSNormFunction", "RMSNorm",
 ]

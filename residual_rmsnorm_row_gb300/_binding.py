@@ -20,9 +20,9 @@ LIBRARY_PATH = os.path.join(_HERE, "librrn.so")
 BF16, F32 = 0, 1
 _DTYPES = {torch.bfloat16: BF16, torch.float32: F32}
 
-VARIANT_AUTO, VARIANT_ROW_CTA, VARIANT_ROW_WARP, VARIANT_STREAM = 0, 1, 2, 3
+VARIANT_AUTO, VARIANT_ROW_CTA, VARIANT_ROW_WARP, VARIANT_STREAM, VARIANT_ROW_TMA = 0, 1, 2, 3, 4
 VARIANT_NAMES = {VARIANT_ROW_CTA: "row_cta", VARIANT_ROW_WARP: "row_warp",
-                 VARIANT_STREAM: "stream"}
+                 VARIANT_STREAM: "stream", VARIANT_ROW_TMA: "row_tma"}
 
 STATUS_NAMES = {0: "RRN_OK", 1: "RRN_ERR_NULL", 2: "RRN_ERR_SHAPE", 3: "RRN_ERR_EPS",
                 4: "RRN_ERR_DTYPE", 5: "RRN_ERR_ALIGN", 6: "RRN_ERR_WORKSPACE",
@@ -41,7 +41,7 @@ class RRNError(RuntimeError):
 
 class rrn_launch(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("vpt", ctypes.c_int), ("threads", ctypes.c_int),
-                ("ctas", ctypes.c_int), ("vec", ctypes.c_int)]
+                ("ctas", ctypes.c_int), ("stages", ctypes.c_int), ("vec", ctypes.c_int)]
 
 
 @dataclass(frozen=True)
@@ -52,19 +52,21 @@ class Launch:
     vpt: int = 0
     threads: int = 0
     ctas: int = 0
+    stages: int = 0
     vec: int = 0
 
     def to_c(self) -> rrn_launch:
-        return rrn_launch(self.variant, self.vpt, self.threads, self.ctas, self.vec)
+        return rrn_launch(self.variant, self.vpt, self.threads, self.ctas, self.stages, self.vec)
 
     @staticmethod
     def from_c(c: rrn_launch) -> "Launch":
-        return Launch(c.variant, c.vpt, c.threads, c.ctas, c.vec)
+        return Launch(c.variant, c.vpt, c.threads, c.ctas, c.stages, c.vec)
 
     @property
     def name(self) -> str:
         base = VARIANT_NAMES.get(self.variant, "auto")
-        return f"{base}(vpt={self.vpt},threads={self.threads},ctas={self.ctas},vec={self.vec})"
+        st = f",stages={self.stages}" if self.variant == VARIANT_ROW_TMA else ""
+        return f"{base}(vpt={self.vpt},threads={self.threads},ctas={self.ctas}{st},vec={self.vec})"
 
 
 _LIB: Optional[ctypes.CDLL] = None
@@ -78,12 +80,18 @@ _SIGNATURES = {
     "rmsnorm_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _f32, _i32, _vp]),
     "rrn_status_string": (ctypes.c_char_p, [_i32]),
     "rrn_last_cuda_error": (_i32, []),
+    "rrn_device_faults": (_i32, [ctypes.POINTER(ctypes.c_uint), _i32]),
+    "rrn_selftest_wait_timeout": (_i32, [ctypes.c_uint64, _vp]),
     "rrn_plan_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, ctypes.POINTER(rrn_launch)]),
     "rrn_plan_bwd": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, ctypes.POINTER(rrn_launch)]),
     "add_rmsnorm_fwd_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32,
                                   ctypes.POINTER(rrn_launch), _vp]),
     "rmsnorm_bwd_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _f32, _i32,
                               ctypes.POINTER(rrn_launch), _vp]),
+    "add_rmsnorm_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _f32, _i32,
+                               _vp]),
+    "add_rmsnorm_bwd_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _f32,
+                                  _i32, ctypes.POINTER(rrn_launch), _vp]),
 }
 
 
@@ -246,6 +254,31 @@ def rmsnorm_bwd_ex(dy, x, w, rstd, dx, dw, workspace, eps, launch: Optional[Laun
         M, N, float(eps), _dtype(x), cfg, _stream(stream)))
 
 
+def add_rmsnorm_bwd(dy: torch.Tensor, d_residual_out: Optional[torch.Tensor],
+                    residual_out: torch.Tensor, w: torch.Tensor, rstd: torch.Tensor,
+                    d_r: torch.Tensor, dw: torch.Tensor, workspace: torch.Tensor, eps: float,
+                    launch: Optional[Launch] = None, stream=None) -> None:
+    """C ``add_rmsnorm_bwd`` (``_ex`` with ``launch``): d_r w.r.t. x + residual, and dw."""
+    M, N = _rows(residual_out)
+    _same(residual_out, dy, "dy")
+    _same(residual_out, d_r, "d_r")
+    if d_residual_out is not None:
+        _same(residual_out, d_residual_out, "d_residual_out")
+    if w.shape != (N,) or w.dtype != residual_out.dtype:
+        raise ValueError("w must have shape (N,) and the dtype of residual_out")
+    if rstd.numel() != M or dw.numel() != N:
+        raise ValueError("rstd must hold M values and dw N values")
+    args = [_mat(dy, "dy", N), None if d_residual_out is None else _mat(d_residual_out, "d_residual_out"),
+            _mat(residual_out, "residual_out"), _mat(w, "w"), _vec(rstd, "rstd"), _mat(d_r, "d_r"),
+            _vec(dw, "dw"), _mat(workspace, "workspace"),
+            workspace.numel() * workspace.element_size(), M, N, float(eps), _dtype(residual_out)]
+    lib = load_library()
+    if launch is None:
+        _check(lib.add_rmsnorm_bwd(*args, _stream(stream)))
+    else:
+        _check(lib.add_rmsnorm_bwd_ex(*args, ctypes.byref(launch.to_c()), _stream(stream)))
+
+
 def plan_fwd(x: torch.Tensor, residual: Optional[torch.Tensor] = None,
              residual_out: Optional[torch.Tensor] = None, w: Optional[torch.Tensor] = None,
              y: Optional[torch.Tensor] = None) -> Launch:
@@ -257,6 +290,18 @@ def plan_fwd(x: torch.Tensor, residual: Optional[torch.Tensor] = None,
                                        ptr(w if w is not None else x), ptr(y if y is not None else x),
                                        M, N, _dtype(x), ctypes.byref(out)))
     return Launch.from_c(out)
+
+
+def device_faults(clear: bool = True) -> int:
+    """C ``rrn_device_faults``: the device fault word (bit 0: a bounded wait ran out)."""
+    out = ctypes.c_uint(0)
+    _check(load_library().rrn_device_faults(ctypes.byref(out), 1 if clear else 0))
+    return int(out.value)
+
+
+def selftest_wait_timeout(limit_ns: int = 50_000_000, stream=None) -> None:
+    """C ``rrn_selftest_wait_timeout``: make one bounded wait run out on purpose."""
+    _check(load_library().rrn_selftest_wait_timeout(int(limit_ns), _stream(stream)))
 
 
 def plan_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, dx: torch.Tensor) -> Launch:

@@ -18,8 +18,23 @@
 
 #include "launch.h"
 #include "rrn.h"
+#include "tma.cuh"
 
 namespace rrn {
+
+// The fault word kernels report a timed-out wait into (one per device, like every __device__
+// variable). Kernels get its address as an argument.
+__device__ unsigned int g_device_faults = 0;
+
+// One thread waits, with a bound, on an mbarrier that expects an arrival nobody makes.
+__global__ void selftest_wait_timeout_kernel(uint64_t limit_ns, unsigned int *faults) {
+    __shared__ __align__(8) uint64_t bar;
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+    fence_proxy_async();
+    (void)mbar_wait(&bar, 0, faults, limit_ns);
+}
+
 namespace {
 
 thread_local int t_last_cuda_error = 0;
@@ -52,9 +67,32 @@ int current_sm_count(int *sms) {
     return RRN_OK;
 }
 
-// Occupancy per (device, kernel instance, block size), computed once.
+// Device address of the fault word on the current device (looked up once per device).
+std::atomic<uintptr_t> g_fault_addr[kMaxDevices];
+
+int fault_word(unsigned int **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev >= 0 && dev < kMaxDevices) {
+        const uintptr_t a = g_fault_addr[dev].load(std::memory_order_relaxed);
+        if (a) {
+            *out = reinterpret_cast<unsigned int *>(a);
+            return RRN_OK;
+        }
+    }
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_faults);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev >= 0 && dev < kMaxDevices)
+        g_fault_addr[dev].store(reinterpret_cast<uintptr_t>(p), std::memory_order_relaxed);
+    *out = static_cast<unsigned int *>(p);
+    return RRN_OK;
+}
+
+// Occupancy per (device, kernel instance, block size, dynamic shared memory), computed once.
 std::mutex g_occ_mutex;
-std::map<std::tuple<int, int, int, int, int, int, int, int>, int> g_occ;
+std::map<std::tuple<int, int, int, int, int, int, int, int, int>, int> g_occ;
 
 int occupancy(bool bwd, int dtype, bool fused, const Launch &l) {
     int dev = 0;
@@ -63,13 +101,13 @@ int occupancy(bool bwd, int dtype, bool fused, const Launch &l) {
         return 0;
     }
     const auto key = std::make_tuple(dev, bwd ? 1 : 0, dtype, fused ? 1 : 0, l.variant, l.vpt,
-                                     l.threads, l.vec ? 1 : 0);
+                                     l.threads, l.vec ? 1 : 0, l.smem);
     {
         std::lock_guard<std::mutex> g(g_occ_mutex);
         auto it = g_occ.find(key);
         if (it != g_occ.end()) return it->second;
     }
-    int n = bwd ? (dtype == RRN_BF16 ? occupancy_bwd_bf16(l) : occupancy_bwd_f32(l))
+    int n = bwd ? (dtype == RRN_BF16 ? occupancy_bwd_bf16(fused, l) : occupancy_bwd_f32(fused, l))
                 : (dtype == RRN_BF16 ? occupancy_fwd_bf16(fused, l) : occupancy_fwd_f32(fused, l));
     std::lock_guard<std::mutex> g(g_occ_mutex);
     g_occ[key] = n;
@@ -107,6 +145,40 @@ int clamp_grid(int64_t v) {
 constexpr int kFwdTargetThreads = 256;
 constexpr int kBwdTargetThreads = 256;
 
+// Largest dynamic shared memory one CTA may use (sm_100-class parts: 227 KB).
+constexpr int kMaxDynSmem = 227 * 1024;
+// Keep this much of an SM's shared memory free for the static parts and the runtime.
+constexpr int kSmemPerSm = 220 * 1024;
+
+// Pick the ring depth for a TMA variant whose one-row slot takes `slot_bytes`: the depth that
+// keeps the most bytes in flight per SM (resident CTAs x depth x slot), preferring the
+// shallower ring (more CTAs) on ties. Fills l->stages, l->smem; returns CTAs per SM (0: none).
+int plan_ring(bool bwd, int dtype, bool fused, int slot_bytes, int want_stages, Launch *l) {
+    int best_occ = 0, best_s = 0;
+    int64_t best_inflight = -1;
+    for (int S = 1; S <= kMaxStages; ++S) {
+        if (want_stages && S != want_stages) continue;
+        const int64_t smem = static_cast<int64_t>(S) * slot_bytes;
+        if (smem > kMaxDynSmem) break;
+        Launch t = *l;
+        t.stages = S;
+        t.smem = static_cast<int>(smem);
+        const int occ = occupancy(bwd, dtype, fused, t);
+        if (occ < 1) continue;
+        int64_t inflight = static_cast<int64_t>(occ) * S * slot_bytes;
+        if (inflight > kSmemPerSm) inflight = kSmemPerSm;  // beyond this the ring adds nothing
+        if (inflight > best_inflight) {
+            best_inflight = inflight;
+            best_occ = occ;
+            best_s = S;
+        }
+    }
+    if (!best_occ) return 0;
+    l->stages = best_s;
+    l->smem = best_s * slot_bytes;
+    return best_occ;
+}
+
 // ---------------------------------------------------------------- forward planning
 // True when every row of every matrix starts on a 16-byte boundary (128-bit vector path).
 bool vec_path_ok(std::initializer_list<const void *> ptrs, int64_t N, int dtype) {
@@ -132,6 +204,8 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
         else l.variant = RRN_VARIANT_STREAM;
     }
     l.vec = (l.variant == RRN_VARIANT_STREAM) ? vec_ok : true;
+    l.stages = 0;
+    l.smem = 0;
 
     switch (l.variant) {
         case RRN_VARIANT_ROW_CTA: {
@@ -161,6 +235,28 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
             l.threads = cfg && cfg->threads ? cfg->threads : 128;
             if (l.threads < 32 || l.threads % 32 || l.threads > 256) return RRN_ERR_CONFIG;
             l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid((M + l.threads / 32 - 1) / (l.threads / 32));
+            break;
+        }
+        case RRN_VARIANT_ROW_TMA: {
+            if (!vec_ok) return RRN_ERR_CONFIG;
+            if (cfg && cfg->vpt) {
+                l.vpt = cfg->vpt;
+            } else {
+                l.vpt = ceil_pow2_vpt((nvec + kFwdTargetThreads - 1) / kFwdTargetThreads, kMaxVpt);
+                while (l.vpt < kMaxVpt && nvec > static_cast<int64_t>(l.vpt) * fwd_max_threads(l.vpt)) l.vpt *= 2;
+            }
+            l.threads = cfg && cfg->threads ? cfg->threads : round_up32((nvec + l.vpt - 1) / l.vpt);
+            if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4 && l.vpt != 8) return RRN_ERR_CONFIG;
+            if (l.threads < 32 || l.threads % 32 || l.threads > fwd_max_threads(l.vpt)) return RRN_ERR_CONFIG;
+            if (static_cast<int64_t>(l.vpt) * l.threads < nvec) return RRN_ERR_CONFIG;
+            const int want = cfg ? cfg->stages : 0;
+            if (want < 0 || want > kMaxStages) return RRN_ERR_CONFIG;
+            const int64_t slot = (fused ? 2 : 1) * N * elem_size(dtype);
+            if (slot > kMaxDynSmem) return RRN_ERR_CONFIG;
+            const int occ = plan_ring(false, dtype, fused, static_cast<int>(slot), want, &l);
+            if (occ < 1) return RRN_ERR_CONFIG;
+            l.ctas = cfg && cfg->ctas ? cfg->ctas
+                                      : clamp_grid(M < static_cast<int64_t>(sms) * occ ? M : static_cast<int64_t>(sms) * occ);
             break;
         }
         case RRN_VARIANT_STREAM: {
@@ -208,15 +304,19 @@ int run_fwd(const void *x, const void *res, void *res_out, const void *w, void *
     st = plan_fwd_impl(vec_path_ok({x, res, res_out, w, y}, N, dtype), res != nullptr, M, N, dtype,
                        cfg, &l);
     if (st != RRN_OK) return st;
-    FwdArgs a{x, res, res ? res_out : nullptr, w, y, rstd, M, static_cast<int>(N), eps};
+    unsigned int *faults = nullptr;
+    st = fault_word(&faults);
+    if (st != RRN_OK) return st;
+    FwdArgs a{x, res, res ? res_out : nullptr, w, y, rstd, M, static_cast<int>(N), eps, 0, faults};
     cudaError_t e = dtype == RRN_BF16 ? launch_fwd_bf16(a, l, stream) : launch_fwd_f32(a, l, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return RRN_OK;
 }
 
 // ---------------------------------------------------------------- backward planning
-int plan_bwd_impl(bool vec_ok, int64_t M, int64_t N, int dtype, const rrn_launch *cfg, Launch *out,
-                  int64_t *rows_per_cta) {
+// add_grad: the fused backward (a third input row, the gradient at residual_out).
+int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
+                  const rrn_launch *cfg, Launch *out, int64_t *rows_per_cta) {
     const int V = 16 / elem_size(dtype);
     const int64_t nvec = N / V;
     int sms = 0;
@@ -230,7 +330,11 @@ int plan_bwd_impl(bool vec_ok, int64_t M, int64_t N, int dtype, const rrn_launch
                         ? RRN_VARIANT_ROW_CTA
                         : RRN_VARIANT_STREAM;
     l.vec = (l.variant == RRN_VARIANT_STREAM) ? vec_ok : true;
+    l.stages = 0;
+    l.smem = 0;
+    int ring_occ = 0;
     switch (l.variant) {
+        case RRN_VARIANT_ROW_TMA:
         case RRN_VARIANT_ROW_CTA: {
             if (!vec_ok) return RRN_ERR_CONFIG;
             if (cfg && cfg->vpt) {
@@ -243,6 +347,14 @@ int plan_bwd_impl(bool vec_ok, int64_t M, int64_t N, int dtype, const rrn_launch
             l.threads = cfg && cfg->threads ? cfg->threads : round_up32((nvec + l.vpt - 1) / l.vpt);
             if (l.threads < 32 || l.threads % 32 || l.threads > bwd_max_threads(l.vpt)) return RRN_ERR_CONFIG;
             if (static_cast<int64_t>(l.vpt) * l.threads < nvec) return RRN_ERR_CONFIG;
+            if (l.variant == RRN_VARIANT_ROW_TMA) {
+                const int want = cfg ? cfg->stages : 0;
+                if (want < 0 || want > kMaxStages) return RRN_ERR_CONFIG;
+                const int64_t slot = (add_grad ? 3 : 2) * N * elem_size(dtype);
+                if (slot > kMaxDynSmem) return RRN_ERR_CONFIG;
+                ring_occ = plan_ring(true, dtype, add_grad, static_cast<int>(slot), want, &l);
+                if (ring_occ < 1) return RRN_ERR_CONFIG;
+            }
             break;
         }
         case RRN_VARIANT_STREAM: {
@@ -260,7 +372,7 @@ int plan_bwd_impl(bool vec_ok, int64_t M, int64_t N, int dtype, const rrn_launch
     if (cfg && cfg->ctas) {
         want = cfg->ctas;
     } else {
-        const int occ = occupancy(true, dtype, false, l);
+        const int occ = ring_occ ? ring_occ : occupancy(true, dtype, add_grad, l);
         want = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
     }
     if (want < 1) return RRN_ERR_CONFIG;
@@ -277,31 +389,36 @@ int plan_bwd_impl(bool vec_ok, int64_t M, int64_t N, int dtype, const rrn_launch
     return RRN_OK;
 }
 
-int check_bwd(const void *dy, const void *x, const void *w, const float *rstd, const void *dx,
-              const float *dw, int64_t M, int64_t N, float eps, int dtype) {
+int check_bwd(const void *dy, const void *d_ro, const void *x, const void *w, const float *rstd,
+              const void *dx, const float *dw, int64_t M, int64_t N, float eps, int dtype) {
     int st = check_common(M, N, eps, dtype);
     if (st != RRN_OK) return st;
     if (!dy || !x || !w || !rstd || !dx || !dw) return RRN_ERR_NULL;
     const uintptr_t es = elem_size(dtype);
     if (!aligned(dy, es) || !aligned(x, es) || !aligned(w, es) || !aligned(dx, es) ||
-        !aligned(rstd, 4) || !aligned(dw, 4))
+        (d_ro && !aligned(d_ro, es)) || !aligned(rstd, 4) || !aligned(dw, 4))
         return RRN_ERR_ALIGN;
     return RRN_OK;
 }
 
-int run_bwd(const void *dy, const void *x, const void *w, const float *rstd, void *dx, float *dw,
-            void *workspace, size_t workspace_bytes, int64_t M, int64_t N, float eps, int dtype,
-            const rrn_launch *cfg, cudaStream_t stream) {
-    int st = check_bwd(dy, x, w, rstd, dx, dw, M, N, eps, dtype);
+int run_bwd(const void *dy, const void *d_ro, const void *x, const void *w, const float *rstd,
+            void *dx, float *dw, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
+            float eps, int dtype, const rrn_launch *cfg, cudaStream_t stream) {
+    int st = check_bwd(dy, d_ro, x, w, rstd, dx, dw, M, N, eps, dtype);
     if (st != RRN_OK) return st;
     if (M == 0) return RRN_OK;
     Launch l;
     int64_t rpc = 0;
-    st = plan_bwd_impl(vec_path_ok({dy, x, w, dx}, N, dtype), M, N, dtype, cfg, &l, &rpc);
+    st = plan_bwd_impl(vec_path_ok({dy, d_ro, x, w, dx}, N, dtype), d_ro != nullptr, M, N, dtype,
+                       cfg, &l, &rpc);
     if (st != RRN_OK) return st;
     const size_t need = static_cast<size_t>(l.ctas) * static_cast<size_t>(N) * sizeof(float);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return RRN_ERR_WORKSPACE;
-    BwdArgs a{dy, x, w, rstd, dx, dw, static_cast<float *>(workspace), M, static_cast<int>(N), rpc};
+    unsigned int *faults = nullptr;
+    st = fault_word(&faults);
+    if (st != RRN_OK) return st;
+    BwdArgs a{dy, d_ro, x, w, rstd, dx, dw, static_cast<float *>(workspace), M,
+              static_cast<int>(N), rpc, 0, faults};
     cudaError_t e = dtype == RRN_BF16 ? launch_bwd_bf16(a, l, stream) : launch_bwd_f32(a, l, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return RRN_OK;
@@ -312,10 +429,27 @@ void to_public(const Launch &l, rrn_launch *out) {
     out->vpt = l.vpt;
     out->threads = l.threads;
     out->ctas = l.ctas;
+    out->stages = l.stages;
     out->vec = l.vec ? 1 : 0;
 }
 
 }  // namespace
+
+cudaError_t allow_dynamic_smem(const void *kernel, int bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, int> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const auto key = std::make_pair(dev, kernel);
+    std::lock_guard<std::mutex> g(mu);
+    auto it = done.find(key);
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done[key] = bytes;
+    return e;
+}
+
 }  // namespace rrn
 
 using namespace rrn;
@@ -351,15 +485,17 @@ RRN_API int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t 
         *bytes = 0;
         return RRN_OK;
     }
-    // The caller's buffers are not known here: size for both the 128-bit vector plan and the
-    // element-wise plan (unaligned buffers) and return the larger.
-    Launch l, l2;
-    int64_t rpc = 0, rpc2 = 0;
-    st = plan_bwd_impl(true, M, N, dtype, nullptr, &l, &rpc);
-    if (st != RRN_OK) return st;
-    st = plan_bwd_impl(false, M, N, dtype, nullptr, &l2, &rpc2);
-    if (st != RRN_OK) return st;
-    const int ctas = l.ctas > l2.ctas ? l.ctas : l2.ctas;
+    // The caller's buffers are not known here: size for the 128-bit vector plan and the
+    // element-wise plan (unaligned buffers), plain and fused, and return the largest.
+    int ctas = 0;
+    for (int vec = 0; vec < 2; ++vec)
+        for (int add = 0; add < 2; ++add) {
+            Launch l;
+            int64_t rpc = 0;
+            st = plan_bwd_impl(vec != 0, add != 0, M, N, dtype, nullptr, &l, &rpc);
+            if (st != RRN_OK) return st;
+            if (l.ctas > ctas) ctas = l.ctas;
+        }
     *bytes = static_cast<size_t>(ctas) * static_cast<size_t>(N) * sizeof(float);
     return RRN_OK;
 }
@@ -367,16 +503,33 @@ RRN_API int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t 
 RRN_API int rmsnorm_bwd(const void *dy, const void *x, const void *w, const float *rstd, void *dx,
                         float *dw, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
                         float eps, int dtype, rrn_stream_t stream) {
-    return run_bwd(dy, x, w, rstd, dx, dw, workspace, workspace_bytes, M, N, eps, dtype, nullptr,
-                   reinterpret_cast<cudaStream_t>(stream));
+    return run_bwd(dy, nullptr, x, w, rstd, dx, dw, workspace, workspace_bytes, M, N, eps, dtype,
+                   nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 RRN_API int rmsnorm_bwd_ex(const void *dy, const void *x, const void *w, const float *rstd,
                            void *dx, float *dw, void *workspace, size_t workspace_bytes,
                            int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,
                            rrn_stream_t stream) {
-    return run_bwd(dy, x, w, rstd, dx, dw, workspace, workspace_bytes, M, N, eps, dtype, cfg,
-                   reinterpret_cast<cudaStream_t>(stream));
+    return run_bwd(dy, nullptr, x, w, rstd, dx, dw, workspace, workspace_bytes, M, N, eps, dtype,
+                   cfg, reinterpret_cast<cudaStream_t>(stream));
+}
+
+RRN_API int add_rmsnorm_bwd(const void *dy, const void *d_residual_out, const void *residual_out,
+                            const void *w, const float *rstd, void *d_r, float *dw,
+                            void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
+                            float eps, int dtype, rrn_stream_t stream) {
+    return run_bwd(dy, d_residual_out, residual_out, w, rstd, d_r, dw, workspace, workspace_bytes,
+                   M, N, eps, dtype, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+RRN_API int add_rmsnorm_bwd_ex(const void *dy, const void *d_residual_out,
+                               const void *residual_out, const void *w, const float *rstd,
+                               void *d_r, float *dw, void *workspace, size_t workspace_bytes,
+                               int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,
+                               rrn_stream_t stream) {
+    return run_bwd(dy, d_residual_out, residual_out, w, rstd, d_r, dw, workspace, workspace_bytes,
+                   M, N, eps, dtype, cfg, reinterpret_cast<cudaStream_t>(stream));
 }
 
 RRN_API int rrn_plan_fwd(const void *x, const void *residual, const void *residual_out,
@@ -401,7 +554,7 @@ RRN_API int rrn_plan_bwd(const void *dy, const void *x, const void *w, const voi
     if (!dy || !x || !w || !dx) return RRN_ERR_NULL;
     Launch l;
     int64_t rpc = 0;
-    st = plan_bwd_impl(vec_path_ok({dy, x, w, dx}, N, dtype), M, N, dtype, nullptr, &l, &rpc);
+    st = plan_bwd_impl(vec_path_ok({dy, x, w, dx}, N, dtype), false, M, N, dtype, nullptr, &l, &rpc);
     if (st != RRN_OK) return st;
     to_public(l, out);
     return RRN_OK;
@@ -423,5 +576,31 @@ RRN_API const char *rrn_status_string(int status) {
 }
 
 RRN_API int rrn_last_cuda_error(void) { return t_last_cuda_error; }
+
+RRN_API int rrn_selftest_wait_timeout(uint64_t limit_ns, rrn_stream_t stream) {
+    if (limit_ns < 1000000ull) limit_ns = 1000000ull;
+    if (limit_ns > 1000000000ull) limit_ns = 1000000000ull;
+    unsigned int *faults = nullptr;
+    int st = fault_word(&faults);
+    if (st != RRN_OK) return st;
+    selftest_wait_timeout_kernel<<<1, 1, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns, faults);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return RRN_OK;
+}
+
+RRN_API int rrn_device_faults(unsigned int *faults, int clear) {
+    if (!faults) return RRN_ERR_NULL;
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_faults, sizeof v);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (clear && v) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_faults, &zero, sizeof zero);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    *faults = v;
+    return RRN_OK;
+}
 
 }  // extern "C"

@@ -9,7 +9,9 @@ cudaError_t launch_bwd_bf16(const BwdArgs &a, const Launch &l, cudaStream_t stre
 cudaError_t launch_bwd_f32(const BwdArgs &a, const Launch &l, cudaStream_t stream) {
     return launch_bwd<float>(a, l, stream);
 }
-int occupancy_bwd_bf16(const Launch &l) { return occupancy_bwd_t<__nv_bfloat16>(l); }
-int occupancy_bwd_f32(const Launch &l) { return occupancy_bwd_t<float>(l); }
+int occupancy_bwd_bf16(bool add_grad, const Launch &l) {
+    return occupancy_bwd_t<__nv_bfloat16>(add_grad, l);
+}
+int occupancy_bwd_f32(bool add_grad, const Launch &l) { return occupancy_bwd_t<float>(add_grad, l); }
 
 }  // namespace rrn

@@ -9,92 +9,100 @@
 //   stage 2  dw[j] = sum over p of workspace[p, j], in a fixed order (rows p = g, g+G, ...
 //            per group g, then the G group sums in order). No atomics anywhere, so dw is
 //            bitwise reproducible for a given (M, N, dtype, device).
+// The fused op (residual_out = r = x + residual, y = RMSNorm(r) * w) has the same backward with
+// the gradient arriving at residual_out added: d_r = dx + d_ro, the gradient with respect to
+// both x and residual (template flag ADDG; r is the stored residual_out).
 // The pages give the op (Machete "Built-In Areas": RMSNorm and autograd helpers) but no
 // backward formula; the one above is the exact derivative of the forward definition.
 #pragma once
 
 #include "common.cuh"
 #include "launch.h"
+#include "tma.cuh"
 
 namespace rrn {
 
-template <typename T, int VPT>
-__global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_cta(const BwdArgs a) {
+// dx for one row held in registers (x vectors xv, dy vectors dyv; this thread owns vector
+// c = v * blockDim.x + threadIdx.x), and dy * xhat added into this thread's dw registers.
+// `after_reduce` runs right after the CTA-wide dot product, when every thread has consumed
+// its inputs; when it returns false the row is abandoned.
+template <typename T, int VPT, bool ADDG, typename AfterReduce>
+__device__ __forceinline__ bool bwd_row_body(const BwdArgs &a, int64_t row, int nvec,
+                                             const uint4 (&xv)[VPT], const uint4 (&dyv)[VPT],
+                                             const uint4 (&gv)[VPT], const uint4 (&wv)[VPT],
+                                             float (&dw)[VPT][Elem<T>::kPerVec],
+                                             float (&slots)[2][32], int &parity,
+                                             AfterReduce after_reduce) {
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
-    __shared__ float slots[2][32];
-
-    const int nvec = a.N / V;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
-    const uint4 *dy4 = static_cast<const uint4 *>(a.dy);
-    const uint4 *x4 = static_cast<const uint4 *>(a.x);
-    uint4 *dx4 = static_cast<uint4 *>(a.dx);
-    const float n_f = static_cast<float>(a.N);
-
-    uint4 wv[VPT];
-    float dw[VPT][V];
+    const float rs = __ldg(a.rstd + row);
+    float dot = 0.f;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int c = v * nthr + tid;
+        if (c < nvec) {
+            float xf[V], d[V], wf[V];
+            E::unpack(xv[v], xf);
+            E::unpack(dyv[v], d);
+            E::unpack(wv[v], wf);
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                const float xh = xf[k] * rs;
+                dot = fmaf(d[k] * wf[k], xh, dot);
+                dw[v][k] = fmaf(d[k], xh, dw[v][k]);
+            }
+        }
+    }
+    dot = cta_sum(dot, slots[parity]);
+    parity ^= 1;
+    if (!after_reduce()) return false;
+    const float cm = dot / static_cast<float>(a.N);
+    const int64_t base = row * nvec;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * nthr + tid;
+        if (c < nvec) {
+            float xf[V], d[V], wf[V], o[V];
+            E::unpack(xv[v], xf);
+            E::unpack(dyv[v], d);
+            E::unpack(wv[v], wf);
+#pragma unroll
+            for (int k = 0; k < V; ++k) o[k] = rs * (d[k] * wf[k] - (xf[k] * rs) * cm);
+            if constexpr (ADDG) {
+                float g[V];
+                E::unpack(gv[v], g);
+#pragma unroll
+                for (int k = 0; k < V; ++k) o[k] += g[k];
+            }
+            st_stream(static_cast<uint4 *>(a.dx) + base + c, E::pack(o));
+        }
+    }
+    return true;
+}
+
+template <typename T, int VPT>
+__device__ __forceinline__ void bwd_prologue(const BwdArgs &a, int nvec, uint4 (&wv)[VPT],
+                                             float (&dw)[VPT][Elem<T>::kPerVec]) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * blockDim.x + threadIdx.x;
         if (c < nvec) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
 #pragma unroll
-        for (int k = 0; k < V; ++k) dw[v][k] = 0.f;
+        for (int k = 0; k < Elem<T>::kPerVec; ++k) dw[v][k] = 0.f;
     }
+}
 
-    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta;
-    const int64_t row1 = min(a.M, row0 + a.rows_per_cta);
-    int parity = 0;
-    for (int64_t row = row0; row < row1; ++row) {
-        const int64_t base = row * nvec;
-        uint4 xv[VPT], dyv[VPT];
-#pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const int c = v * nthr + tid;
-            if (c < nvec) {
-                xv[v] = ld_stream(x4 + base + c);
-                dyv[v] = ld_stream(dy4 + base + c);
-            }
-        }
-        const float rs = __ldg(a.rstd + row);
-        float xh[VPT][V], g[VPT][V];
-        float dot = 0.f;
-#pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const int c = v * nthr + tid;
-            if (c < nvec) {
-                float d[V], wf[V];
-                E::unpack(xv[v], xh[v]);
-                E::unpack(dyv[v], d);
-                E::unpack(wv[v], wf);
-#pragma unroll
-                for (int k = 0; k < V; ++k) {
-                    xh[v][k] *= rs;
-                    g[v][k] = d[k] * wf[k];
-                    dot = fmaf(g[v][k], xh[v][k], dot);
-                    dw[v][k] = fmaf(d[k], xh[v][k], dw[v][k]);
-                }
-            }
-        }
-        dot = cta_sum(dot, slots[parity]);
-        parity ^= 1;
-        const float cm = dot / n_f;
-#pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const int c = v * nthr + tid;
-            if (c < nvec) {
-                float o[V];
-#pragma unroll
-                for (int k = 0; k < V; ++k) o[k] = rs * (g[v][k] - xh[v][k] * cm);
-                st_stream(dx4 + base + c, E::pack(o));
-            }
-        }
-    }
-
+// This CTA's dw partial sums -> row blockIdx.x of the [P, N] workspace.
+template <typename T, int VPT>
+__device__ __forceinline__ void bwd_store_partial(const BwdArgs &a, int nvec,
+                                                  const float (&dw)[VPT][Elem<T>::kPerVec]) {
+    constexpr int V = Elem<T>::kPerVec;
     float *prow = a.partial + static_cast<int64_t>(blockIdx.x) * a.N;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
-        const int c = v * nthr + tid;
+        const int c = v * blockDim.x + threadIdx.x;
         if (c < nvec) {
             float4 *dst = reinterpret_cast<float4 *>(prow + static_cast<int64_t>(c) * V);
 #pragma unroll
@@ -104,9 +112,124 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_cta(const BwdArg
     }
 }
 
+template <typename T, int VPT, bool ADDG>
+__global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_cta(const BwdArgs a) {
+    constexpr int V = Elem<T>::kPerVec;
+    __shared__ float slots[2][32];
+    const int nvec = a.N / V;
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const uint4 *dy4 = static_cast<const uint4 *>(a.dy);
+    const uint4 *g4 = static_cast<const uint4 *>(a.d_ro);
+    const uint4 *x4 = static_cast<const uint4 *>(a.x);
+
+    uint4 wv[VPT];
+    float dw[VPT][V];
+    bwd_prologue<T, VPT>(a, nvec, wv, dw);
+
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta;
+    const int64_t row1 = min(a.M, row0 + a.rows_per_cta);
+    int parity = 0;
+    for (int64_t row = row0; row < row1; ++row) {
+        const int64_t base = row * nvec;
+        uint4 xv[VPT], dyv[VPT], gv[VPT];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * nthr + tid;
+            if (c < nvec) {
+                xv[v] = ld_stream(x4 + base + c);
+                dyv[v] = ld_stream(dy4 + base + c);
+                if constexpr (ADDG) gv[v] = ld_stream(g4 + base + c);
+            }
+        }
+        bwd_row_body<T, VPT, ADDG>(a, row, nvec, xv, dyv, gv, wv, dw, slots, parity,
+                                   [] { return true; });
+    }
+    bwd_store_partial<T, VPT>(a, nvec, dw);
+}
+
+// Stage 1 fed by the TMA engine: CTA p owns the contiguous rows [p * R, (p + 1) * R) and keeps
+// a.stages of them (x and dy) in flight in a shared-memory ring filled with cp.async.bulk,
+// refilling a slot as soon as the CTA-wide dot product of its row is done.
+template <typename T, int VPT, bool ADDG>
+__global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArgs a) {
+    constexpr int V = Elem<T>::kPerVec;
+    constexpr int NT = ADDG ? 3 : 2;  // rows per slot: x, dy (, d_ro)
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) uint64_t full[kMaxStages];
+    __shared__ float slots[2][32];
+    __shared__ int abort_flag;
+
+    const int nvec = a.N / V;
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const uint32_t row_bytes = static_cast<uint32_t>(a.N) * static_cast<uint32_t>(sizeof(T));
+    const int S = a.stages;
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta;
+    const int64_t nrows = max(static_cast<int64_t>(0), min(a.M, row0 + a.rows_per_cta) - row0);
+
+    auto slot = [&](int s, int t) { return ring + static_cast<size_t>(s * NT + t) * row_bytes; };
+    auto issue = [&](int64_t k) {
+        const int s = static_cast<int>(k % S);
+        const int64_t off = (row0 + k) * static_cast<int64_t>(row_bytes);
+        mbar_arrive_expect_tx(&full[s], NT * row_bytes);
+        bulk_g2s(slot(s, 0), static_cast<const char *>(a.x) + off, row_bytes, &full[s]);
+        bulk_g2s(slot(s, 1), static_cast<const char *>(a.dy) + off, row_bytes, &full[s]);
+        if (ADDG) bulk_g2s(slot(s, 2), static_cast<const char *>(a.d_ro) + off, row_bytes, &full[s]);
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        abort_flag = 0;
+        fence_mbarrier_init();
+        fence_proxy_async();
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int64_t k = 0; k < nrows && k < S; ++k) issue(k);
+
+    uint4 wv[VPT];
+    float dw[VPT][V];
+    bwd_prologue<T, VPT>(a, nvec, wv, dw);
+
+    int parity = 0;
+    int64_t k = 0;
+    for (; k < nrows; ++k) {
+        const int s = static_cast<int>(k % S);
+        if (!mbar_wait(&full[s], static_cast<uint32_t>((k / S) & 1), a.faults)) abort_flag = 1;
+        uint4 xv[VPT], dyv[VPT], gv[VPT];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * nthr + tid;
+            if (c < nvec) {
+                xv[v] = ld_shared_v4(slot(s, 0) + static_cast<size_t>(c) * 16);
+                dyv[v] = ld_shared_v4(slot(s, 1) + static_cast<size_t>(c) * 16);
+                if constexpr (ADDG) gv[v] = ld_shared_v4(slot(s, 2) + static_cast<size_t>(c) * 16);
+            }
+        }
+        const bool done = bwd_row_body<T, VPT, ADDG>(a, row0 + k, nvec, xv, dyv, gv, wv, dw, slots,
+                                                     parity, [&] {
+            if (abort_flag) return false;
+            if (tid == 0 && k + S < nrows) {
+                fence_proxy_async();
+                issue(k + S);
+            }
+            return true;
+        });
+        if (!done) break;
+    }
+    if (k < nrows) {
+        if (tid == 0)
+            for (int64_t j = k; j < nrows && j < k + S; ++j)
+                (void)mbar_wait(&full[j % S], static_cast<uint32_t>((j / S) & 1), nullptr, 100000000ull);
+        return;  // the partial row is not written; the fault word reports the failure
+    }
+    bwd_store_partial<T, VPT>(a, nvec, dw);
+}
+
 // Two passes over each row (any N, any alignment); the dw partials live in the CTA's own
 // workspace row instead of registers. Each workspace element is owned by one thread.
-template <typename T, bool VEC>
+template <typename T, bool VEC, bool ADDG>
 __global__ void __launch_bounds__(1024) bwd_stream(const BwdArgs a) {
     using E = Elem<T>;
     constexpr int W = E::kPerVec;
@@ -165,6 +288,16 @@ __global__ void __launch_bounds__(1024) bwd_stream(const BwdArgs a) {
                 float *pw = prow + static_cast<int64_t>(c) * V + k;
                 *pw = first ? df[k] * xh : fmaf(df[k], xh, *pw);
             }
+            if constexpr (ADDG) {
+                float gf[W];
+                if constexpr (VEC) {
+                    E::unpack(ld_stream(static_cast<const uint4 *>(a.d_ro) + base / W + c), gf);
+                } else {
+                    gf[0] = E::load1(a.d_ro, base + c);
+                }
+#pragma unroll
+                for (int k = 0; k < V; ++k) o[k] += gf[k];
+            }
             if constexpr (VEC) {
                 st_stream(static_cast<uint4 *>(a.dx) + base / W + c, E::pack(o));
             } else {
@@ -197,31 +330,49 @@ __global__ void __launch_bounds__(kReduceThreads)
     }
 }
 
-template <typename T>
+template <typename T, bool ADDG>
 const void *bwd_kernel_ptr(const Launch &l) {
     switch (l.variant) {
         case RRN_VARIANT_ROW_CTA:
             switch (l.vpt) {
-                case 1: return reinterpret_cast<const void *>(&bwd_row_cta<T, 1>);
-                case 2: return reinterpret_cast<const void *>(&bwd_row_cta<T, 2>);
-                case 4: return reinterpret_cast<const void *>(&bwd_row_cta<T, 4>);
+                case 1: return reinterpret_cast<const void *>(&bwd_row_cta<T, 1, ADDG>);
+                case 2: return reinterpret_cast<const void *>(&bwd_row_cta<T, 2, ADDG>);
+                case 4: return reinterpret_cast<const void *>(&bwd_row_cta<T, 4, ADDG>);
                 default: return nullptr;
             }
         case RRN_VARIANT_STREAM:
-            return l.vec ? reinterpret_cast<const void *>(&bwd_stream<T, true>)
-                         : reinterpret_cast<const void *>(&bwd_stream<T, false>);
+            return l.vec ? reinterpret_cast<const void *>(&bwd_stream<T, true, ADDG>)
+                         : reinterpret_cast<const void *>(&bwd_stream<T, false, ADDG>);
+        case RRN_VARIANT_ROW_TMA:
+            switch (l.vpt) {
+                case 1: return reinterpret_cast<const void *>(&bwd_row_tma<T, 1, ADDG>);
+                case 2: return reinterpret_cast<const void *>(&bwd_row_tma<T, 2, ADDG>);
+                case 4: return reinterpret_cast<const void *>(&bwd_row_tma<T, 4, ADDG>);
+                default: return nullptr;
+            }
         default: return nullptr;
     }
+}
+
+template <typename T>
+const void *bwd_kernel_ptr_any(bool add_grad, const Launch &l) {
+    return add_grad ? bwd_kernel_ptr<T, true>(l) : bwd_kernel_ptr<T, false>(l);
 }
 
 // Stage 1 on l.ctas CTAs (each owning a.rows_per_cta rows), then stage 2, on one stream.
 template <typename T>
 cudaError_t launch_bwd(const BwdArgs &a, const Launch &l, cudaStream_t stream) {
-    const void *k = bwd_kernel_ptr<T>(l);
+    const void *k = bwd_kernel_ptr_any<T>(a.d_ro != nullptr, l);
     if (!k) return cudaErrorInvalidConfiguration;
+    if (l.smem > 48 * 1024) {
+        cudaError_t e = allow_dynamic_smem(k, l.smem);
+        if (e != cudaSuccess) return e;
+    }
     BwdArgs args = a;
+    args.stages = l.stages;
     void *params[] = {&args};
-    cudaError_t e = cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, 0, stream);
+    cudaError_t e = cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params,
+                                     static_cast<size_t>(l.smem), stream);
     if (e != cudaSuccess) return e;
     const int blocks = (a.N + 31) / 32;
     bwd_dw_reduce<<<blocks, kReduceThreads, 0, stream>>>(a.partial, a.dw, l.ctas, a.N);
@@ -229,11 +380,13 @@ cudaError_t launch_bwd(const BwdArgs &a, const Launch &l, cudaStream_t stream) {
 }
 
 template <typename T>
-int occupancy_bwd_t(const Launch &l) {
-    const void *k = bwd_kernel_ptr<T>(l);
+int occupancy_bwd_t(bool add_grad, const Launch &l) {
+    const void *k = bwd_kernel_ptr_any<T>(add_grad, l);
     if (!k) return 0;
+    if (l.smem > 48 * 1024 && allow_dynamic_smem(k, l.smem) != cudaSuccess) return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, l.threads, 0) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, l.threads, static_cast<size_t>(l.smem)) !=
+        cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }

@@ -18,32 +18,111 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tma.cuh"
 
 namespace rrn {
+
+// The per-row work of the row-per-CTA variants, on a row already in registers: this thread
+// owns the 128-bit vectors c = v * blockDim.x + threadIdx.x (v < VPT, c < nvec) of x (xv) and
+// residual (rv), and the matching weight vectors (wv). Writes residual_out (fused), y and rstd.
+// `after_reduce` runs right after the CTA-wide sum of squares, when every thread has consumed
+// its inputs; when it returns false the row is abandoned (nothing more is written).
+template <typename T, int VPT, bool FUSED, typename AfterReduce>
+__device__ __forceinline__ bool row_cta_body(const FwdArgs &a, int64_t row, int nvec,
+                                             const uint4 (&xv)[VPT], const uint4 (&rv)[VPT],
+                                             const uint4 (&wv)[VPT], float (&slots)[2][32],
+                                             int &parity, AfterReduce after_reduce) {
+    using E = Elem<T>;
+    constexpr int V = E::kPerVec;
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const int64_t base = row * nvec;
+    const float n_f = static_cast<float>(a.N);
+    float acc[VPT][V];
+    float ss = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * nthr + tid;
+        if (c < nvec) {
+            E::unpack(xv[v], acc[v]);
+            if (FUSED) {
+                float b[V];
+                E::unpack(rv[v], b);
+#pragma unroll
+                for (int k = 0; k < V; ++k) acc[v][k] += b[k];
+                st_stream(static_cast<uint4 *>(a.res_out) + base + c, E::pack(acc[v]));
+            }
+#pragma unroll
+            for (int k = 0; k < V; ++k) ss = fmaf(acc[v][k], acc[v][k], ss);
+        }
+    }
+    ss = cta_sum(ss, slots[parity]);
+    parity ^= 1;
+    if (!after_reduce()) return false;
+    float rs;
+    if (!needs_rescale(ss)) {
+        rs = rstd_plain(ss, n_f, a.eps);
+    } else {  // rare: sum of squares out of fp32 range, or an all-zero row
+        float am = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v)
+            if (v * nthr + tid < nvec)
+#pragma unroll
+                for (int k = 0; k < V; ++k) am = fmaxf(am, fabsf(acc[v][k]));
+        am = cta_max(am, slots[parity]);
+        parity ^= 1;
+        const int e = rescale_exponent(am);
+        float s2 = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v)
+            if (v * nthr + tid < nvec)
+#pragma unroll
+                for (int k = 0; k < V; ++k) {
+                    const float t = ldexpf(acc[v][k], -e);
+                    s2 = fmaf(t, t, s2);
+                }
+        s2 = cta_sum(s2, slots[parity]);
+        parity ^= 1;
+        rs = rstd_rescaled(s2, n_f, a.eps, e);
+    }
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * nthr + tid;
+        if (c < nvec) {
+            float wf[V], o[V];
+            E::unpack(wv[v], wf);
+#pragma unroll
+            for (int k = 0; k < V; ++k) o[k] = acc[v][k] * rs * wf[k];
+            st_stream(static_cast<uint4 *>(a.y) + base + c, E::pack(o));
+        }
+    }
+    if (tid == 0 && a.rstd) a.rstd[row] = rs;
+    return true;
+}
+
+template <typename T, int VPT>
+__device__ __forceinline__ void load_w(const FwdArgs &a, int nvec, uint4 (&wv)[VPT]) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * blockDim.x + threadIdx.x;
+        if (c < nvec) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
+    }
+}
 
 template <typename T, int VPT, bool FUSED>
 __global__ void __launch_bounds__(fwd_max_threads(VPT))
     fwd_row_cta(const FwdArgs a) {
-    using E = Elem<T>;
-    constexpr int V = E::kPerVec;
+    constexpr int V = Elem<T>::kPerVec;
     __shared__ float slots[2][32];
-
     const int nvec = a.N / V;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
     const uint4 *x4 = static_cast<const uint4 *>(a.x);
     const uint4 *r4 = static_cast<const uint4 *>(a.res);
-    uint4 *ro4 = static_cast<uint4 *>(a.res_out);
-    uint4 *y4 = static_cast<uint4 *>(a.y);
-    const float n_f = static_cast<float>(a.N);
 
     // The weight row stays in registers for every row this CTA handles.
     uint4 wv[VPT];
-#pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-        const int c = v * nthr + tid;
-        if (c < nvec) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
-    }
+    load_w<T, VPT>(a, nvec, wv);
 
     int parity = 0;
     for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
@@ -57,64 +136,87 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT))
                 if (FUSED) rv[v] = ld_stream(r4 + base + c);
             }
         }
-        float acc[VPT][V];
-        float ss = 0.f;
+        row_cta_body<T, VPT, FUSED>(a, row, nvec, xv, rv, wv, slots, parity, [] { return true; });
+    }
+}
+
+// Row per CTA, persistent, fed by the TMA engine: CTA b owns rows b, b + G, b + 2G, ...
+// (G = gridDim.x) and keeps a.stages of them in flight in a shared-memory ring, each row (x and,
+// fused, residual) fetched by one thread with cp.async.bulk and counted on that slot's
+// mbarrier. Once the CTA-wide sum of a row is done every thread holds its share of the row in
+// registers, so the slot is refilled right then with the row `stages` iterations ahead.
+// Bytes in flight per SM = resident CTAs x stages x row bytes, independent of registers.
+template <typename T, int VPT, bool FUSED>
+__global__ void __launch_bounds__(fwd_max_threads(VPT))
+    fwd_row_tma(const FwdArgs a) {
+    constexpr int V = Elem<T>::kPerVec;
+    constexpr int NT = FUSED ? 2 : 1;
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) uint64_t full[kMaxStages];
+    __shared__ float slots[2][32];
+    __shared__ int abort_flag;
+
+    const int nvec = a.N / V;
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const uint32_t row_bytes = static_cast<uint32_t>(a.N) * static_cast<uint32_t>(sizeof(T));
+    const int S = a.stages;
+    const int64_t first = blockIdx.x;
+    const int64_t stride = gridDim.x;
+    const int64_t nrows = first < a.M ? (a.M - 1 - first) / stride + 1 : 0;
+
+    auto slot = [&](int s, int t) { return ring + static_cast<size_t>(s * NT + t) * row_bytes; };
+    auto issue = [&](int64_t k) {  // one thread: fetch the k-th row of this CTA into its slot
+        const int s = static_cast<int>(k % S);
+        const int64_t off = (first + k * stride) * static_cast<int64_t>(row_bytes);
+        mbar_arrive_expect_tx(&full[s], NT * row_bytes);
+        bulk_g2s(slot(s, 0), static_cast<const char *>(a.x) + off, row_bytes, &full[s]);
+        if (FUSED) bulk_g2s(slot(s, 1), static_cast<const char *>(a.res) + off, row_bytes, &full[s]);
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        abort_flag = 0;
+        fence_mbarrier_init();
+        fence_proxy_async();
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int64_t k = 0; k < nrows && k < S; ++k) issue(k);
+
+    uint4 wv[VPT];
+    load_w<T, VPT>(a, nvec, wv);
+
+    int parity = 0;
+    int64_t k = 0;
+    for (; k < nrows; ++k) {
+        const int s = static_cast<int>(k % S);
+        if (!mbar_wait(&full[s], static_cast<uint32_t>((k / S) & 1), a.faults)) abort_flag = 1;
+        uint4 xv[VPT], rv[VPT];
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * nthr + tid;
             if (c < nvec) {
-                E::unpack(xv[v], acc[v]);
-                if (FUSED) {
-                    float b[V];
-                    E::unpack(rv[v], b);
-#pragma unroll
-                    for (int k = 0; k < V; ++k) acc[v][k] += b[k];
-                    st_stream(ro4 + base + c, E::pack(acc[v]));
+                xv[v] = ld_shared_v4(slot(s, 0) + static_cast<size_t>(c) * 16);
+                if (FUSED) rv[v] = ld_shared_v4(slot(s, 1) + static_cast<size_t>(c) * 16);
+            }
+        }
+        const bool done = row_cta_body<T, VPT, FUSED>(
+            a, first + k * stride, nvec, xv, rv, wv, slots, parity, [&] {
+                if (abort_flag) return false;  // written before the barrier: uniform
+                if (tid == 0 && k + S < nrows) {
+                    fence_proxy_async();       // our generic reads of the slot come first
+                    issue(k + S);
                 }
-#pragma unroll
-                for (int k = 0; k < V; ++k) ss = fmaf(acc[v][k], acc[v][k], ss);
-            }
-        }
-        ss = cta_sum(ss, slots[parity]);
-        parity ^= 1;
-        float rs;
-        if (!needs_rescale(ss)) {
-            rs = rstd_plain(ss, n_f, a.eps);
-        } else {  // rare: sum of squares out of fp32 range, or an all-zero row
-            float am = 0.f;
-#pragma unroll
-            for (int v = 0; v < VPT; ++v)
-                if (v * nthr + tid < nvec)
-#pragma unroll
-                    for (int k = 0; k < V; ++k) am = fmaxf(am, fabsf(acc[v][k]));
-            am = cta_max(am, slots[parity]);
-            parity ^= 1;
-            const int e = rescale_exponent(am);
-            float s2 = 0.f;
-#pragma unroll
-            for (int v = 0; v < VPT; ++v)
-                if (v * nthr + tid < nvec)
-#pragma unroll
-                    for (int k = 0; k < V; ++k) {
-                        const float t = ldexpf(acc[v][k], -e);
-                        s2 = fmaf(t, t, s2);
-                    }
-            s2 = cta_sum(s2, slots[parity]);
-            parity ^= 1;
-            rs = rstd_rescaled(s2, n_f, a.eps, e);
-        }
-#pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const int c = v * nthr + tid;
-            if (c < nvec) {
-                float wf[V], o[V];
-                E::unpack(wv[v], wf);
-#pragma unroll
-                for (int k = 0; k < V; ++k) o[k] = acc[v][k] * rs * wf[k];
-                st_stream(y4 + base + c, E::pack(o));
-            }
-        }
-        if (tid == 0 && a.rstd) a.rstd[row] = rs;
+                return true;
+            });
+        if (!done) break;
+    }
+    if (k < nrows && tid == 0) {
+        // A wait ran out: let the copies already issued land before the CTA's shared memory is
+        // released (each wait bounded again), then leave; the fault word tells the host.
+        for (int64_t j = k; j < nrows && j < k + S; ++j)
+            (void)mbar_wait(&full[j % S], static_cast<uint32_t>((j / S) & 1), nullptr, 100000000ull);
     }
 }
 
@@ -338,6 +440,14 @@ const void *fwd_kernel_ptr(const Launch &l) {
         case RRN_VARIANT_STREAM:
             return l.vec ? reinterpret_cast<const void *>(&fwd_stream<T, true, FUSED>)
                          : reinterpret_cast<const void *>(&fwd_stream<T, false, FUSED>);
+        case RRN_VARIANT_ROW_TMA:
+            switch (l.vpt) {
+                case 1: return reinterpret_cast<const void *>(&fwd_row_tma<T, 1, FUSED>);
+                case 2: return reinterpret_cast<const void *>(&fwd_row_tma<T, 2, FUSED>);
+                case 4: return reinterpret_cast<const void *>(&fwd_row_tma<T, 4, FUSED>);
+                case 8: return reinterpret_cast<const void *>(&fwd_row_tma<T, 8, FUSED>);
+                default: return nullptr;
+            }
         default: return nullptr;
     }
 }
@@ -351,17 +461,25 @@ template <typename T>
 cudaError_t launch_fwd(const FwdArgs &a, const Launch &l, cudaStream_t stream) {
     const void *k = fwd_kernel_ptr_any<T>(a.res != nullptr, l);
     if (!k) return cudaErrorInvalidConfiguration;
+    if (l.smem > 48 * 1024) {
+        cudaError_t e = allow_dynamic_smem(k, l.smem);
+        if (e != cudaSuccess) return e;
+    }
     FwdArgs args = a;
+    args.stages = l.stages;
     void *params[] = {&args};
-    return cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, 0, stream);
+    return cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, static_cast<size_t>(l.smem),
+                            stream);
 }
 
 template <typename T>
 int occupancy_fwd_t(bool fused, const Launch &l) {
     const void *k = fwd_kernel_ptr_any<T>(fused, l);
     if (!k) return 0;
+    if (l.smem > 48 * 1024 && allow_dynamic_smem(k, l.smem) != cudaSuccess) return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, l.threads, 0) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, l.threads, static_cast<size_t>(l.smem)) !=
+        cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }

@@ -20,11 +20,15 @@ struct FwdArgs {
     int64_t M;
     int N;
     float eps;
+    int stages;              // shared-memory ring depth (TMA variant)
+    unsigned int *faults;    // the library's device fault word
 };
 
 // Arguments of one backward call. `partial` is the [P, N] fp32 workspace (P = ctas).
+// d_ro (nullable) is the gradient arriving at residual_out in the fused op; it is added to dx.
 struct BwdArgs {
     const void *dy;
+    const void *d_ro;
     const void *x;
     const void *w;
     const float *rstd;
@@ -34,6 +38,8 @@ struct BwdArgs {
     int64_t M;
     int N;
     int64_t rows_per_cta;
+    int stages;              // shared-memory ring depth (TMA variant)
+    unsigned int *faults;    // the library's device fault word
 };
 
 // A resolved launch (all fields set).
@@ -43,6 +49,8 @@ struct Launch {
     int threads;
     int ctas;
     bool vec;     // 128-bit vectors (else element-wise)
+    int stages;   // TMA variant: rows in flight per CTA (shared-memory ring depth)
+    int smem;     // dynamic shared memory bytes per CTA
 };
 
 // Largest vectors-per-thread the register variants are compiled for, and the thread limit
@@ -52,6 +60,11 @@ constexpr int fwd_max_threads(int vpt) { return vpt >= 8 ? 256 : vpt >= 4 ? 512 
 constexpr int bwd_max_threads(int vpt) { return vpt >= 4 ? 256 : 512; }
 constexpr int kBwdMaxVpt = 4;
 constexpr int kReduceThreads = 256;  // dw stage-2 CTA size: 32 columns x 8 row groups
+constexpr int kMaxStages = 8;        // deepest shared-memory ring of the TMA variants
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device (done once
+// per kernel, device and size; defined in api.cu).
+cudaError_t allow_dynamic_smem(const void *kernel, int bytes);
 
 // Kernel launchers, one per dtype (defined in fwd_bf16.cu, fwd_f32.cu and bwd.cu). They
 // enqueue on `stream` and return the cudaError_t of the launch.
@@ -60,10 +73,11 @@ cudaError_t launch_fwd_f32(const FwdArgs &a, const Launch &l, cudaStream_t strea
 cudaError_t launch_bwd_bf16(const BwdArgs &a, const Launch &l, cudaStream_t stream);
 cudaError_t launch_bwd_f32(const BwdArgs &a, const Launch &l, cudaStream_t stream);
 
-// Occupancy (resident CTAs per SM) of the kernel a launch would run; 0 on error.
+// Occupancy (resident CTAs per SM) of the kernel a launch would run, with l.smem bytes of
+// dynamic shared memory; 0 on error.
 int occupancy_fwd_bf16(bool fused, const Launch &l);
 int occupancy_fwd_f32(bool fused, const Launch &l);
-int occupancy_bwd_bf16(const Launch &l);
-int occupancy_bwd_f32(const Launch &l);
+int occupancy_bwd_bf16(bool add_grad, const Launch &l);
+int occupancy_bwd_f32(bool add_grad, const Launch &l);
 
 }  // namespace rrn

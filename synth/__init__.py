@@ -4,7 +4,7 @@ This module only draws random inputs. It contains none of the normalisation arit
 both the GPU path's tests/benchmark and the CPU oracle can take their inputs from it.
 
 Every workload is drawn on the host with numpy's PCG64 generator, seeded per workload, in a
-fixed order: x, residual, (outlier mask, outlier sign), w, dy. Values are drawn in float32
+fixed order: x, residual, (outlier mask, outlier sign), w, dy, d_ro. Values are drawn in float32
 and, for bf16 workloads, rounded to bf16 (round to nearest even) by torch's CPU cast. bf16
 tensors are returned as ``uint16`` arrays holding the raw bit patterns; fp32 tensors as
 ``float32`` arrays.
@@ -28,7 +28,7 @@ class Workload:
     """One synthetic problem: op kind, shape, dtype, eps, seed and value distributions."""
 
     name: str
-    op: str                      # "rmsnorm_fwd" | "add_rmsnorm_fwd" | "rmsnorm_bwd"
+    op: str                      # "rmsnorm_fwd" | "add_rmsnorm_fwd" | "rmsnorm_bwd" | "add_rmsnorm_bwd"
     M: int
     N: int
     dtype: str                   # "bf16" | "f32"
@@ -68,6 +68,9 @@ for _dt in (BF16, F32):
         _add(Workload(f"rmsnorm_fwd_{_m}x8192_{_dt}", "rmsnorm_fwd", _m, 8192, _dt, 1e-5, 3))
     _add(Workload(f"rmsnorm_fwd_65536x2048_{_dt}", "rmsnorm_fwd", 65536, 2048, _dt, 1e-5, 3))
 _add(Workload("rmsnorm_bwd_16384x4096_bf16", "rmsnorm_bwd", 16384, 4096, BF16, 1e-6, 4))
+# The fused backward: x plays the stored residual_out; dy and d_ro are the gradients arriving at
+# y and at residual_out.
+_add(Workload("add_rmsnorm_bwd_16384x4096_bf16", "add_rmsnorm_bwd", 16384, 4096, BF16, 1e-6, 5))
 
 
 def get(name: str) -> Workload:
@@ -118,8 +121,10 @@ def make(w: Workload) -> Dict[str, np.ndarray]:
     else:
         wt = (np.float32(1.0) + np.float32(0.1) * rng.standard_normal(w.N, dtype=np.float32))
     out["w"] = _store(wt, w.dtype)
-    if w.op == "rmsnorm_bwd":
+    if w.op in ("rmsnorm_bwd", "add_rmsnorm_bwd"):
         out["dy"] = _store(rng.standard_normal(shape, dtype=np.float32), w.dtype)
+    if w.op == "add_rmsnorm_bwd":
+        out["d_ro"] = _store(rng.standard_normal(shape, dtype=np.float32), w.dtype)
     return out
 
 
@@ -129,6 +134,7 @@ def min_bytes(w: Workload) -> int:
     rmsnorm_fwd: x, y (M*N each), w (N), rstd (M, fp32).
     add_rmsnorm_fwd: x, residual, residual_out, y (M*N each), w (N), rstd (M, fp32).
     rmsnorm_bwd: x, dy, dx (M*N each), w (N), rstd (M, fp32), dw (N, fp32).
+    add_rmsnorm_bwd: residual_out, dy, d_residual_out, d_r (M*N each), w, rstd, dw.
     """
     e = w.elem_bytes
     if w.op == "rmsnorm_fwd":
@@ -137,6 +143,8 @@ def min_bytes(w: Workload) -> int:
         return 4 * w.M * w.N * e + w.N * e + 4 * w.M
     if w.op == "rmsnorm_bwd":
         return 3 * w.M * w.N * e + w.N * e + 4 * w.M + 4 * w.N
+    if w.op == "add_rmsnorm_bwd":
+        return 4 * w.M * w.N * e + w.N * e + 4 * w.M + 4 * w.N
     raise ValueError(w.op)
 
 

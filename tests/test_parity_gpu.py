@@ -64,7 +64,7 @@ def compare_fwd(x_h, res_h, w_h, dtype, eps, y, ro, rstd, rows=None):
 
 
 # ------------------------------------------------------------------ the named workloads
-FWD_WORKLOADS = [n for n, w in synth.WORKLOADS.items() if w.op != "rmsnorm_bwd"]
+FWD_WORKLOADS = [n for n, w in synth.WORKLOADS.items() if w.op in ("rmsnorm_fwd", "add_rmsnorm_fwd")]
 
 
 @pytest.mark.parametrize("name", FWD_WORKLOADS)
@@ -102,6 +102,8 @@ def _variants(dtype, N, M):
         if N % V == 0 and thr <= lim:
             out.append(rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0))
             out.append(rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 37))     # persistent, ragged
+            for stages, ctas in ((0, 0), (1, 0), (2, 37), (3, 5)):
+                out.append(rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, ctas, stages))
         if N % V == 0 and nvec <= 32 * vpt:
             out.append(rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 128, 0))
             out.append(rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 64, 5))
@@ -308,7 +310,10 @@ def test_backward_shapes(dtype, N):
             thr = -(-(-(-nvec // vpt)) // 32) * 32
             if thr <= (256 if vpt == 4 else 512):
                 launches += [rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0),
-                             rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 13)]
+                             rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 13),
+                             rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 0, 0),
+                             rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 13, 1),
+                             rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 7, 3)]
     for launch in launches:
         dx, dw = _bwd_case(h, dtype, wl.eps, launch)
         check_out(values(dx), dx_ref, dtype, f"dx {launch}")
@@ -392,3 +397,18 @@ def test_side_stream_and_graph_capture():
     for a, b in zip(ref, (y, ro, rstd, dx, dw)):
         assert torch.equal(a, b)
     compare_fwd(h["x"], h["residual"], h["w"], "bf16", wl.eps, y, ro, rstd)
+
+
+# ------------------------------------------------------------------ bounded waits
+def test_bounded_wait_reports_and_context_survives():
+    """No kernel above gave up on a wait; a wait made to run out on purpose sets the fault bit
+    and returns, and the context keeps working."""
+    assert rrn.device_faults(clear=True) == 0, "a kernel reported a timed-out wait"
+    rrn.selftest_wait_timeout(50_000_000)
+    torch.cuda.synchronize()
+    assert rrn.device_faults(clear=True) & 1
+    assert rrn.device_faults(clear=False) == 0
+    wl = synth.get("rmsnorm_fwd_256x1024_bf16")
+    h = synth.make(wl)
+    y, _, rstd = fwd_case(h["x"], None, h["w"], "bf16", wl.eps)
+    compare_fwd(h["x"], None, h["w"], "bf16", wl.eps, y, None, rstd)

@@ -9,7 +9,8 @@ def test_every_workload_draws_its_tensors():
         small = w.with_shape(min(w.M, 64))
         t = synth.make(small)
         want = {"x", "w"} | ({"residual"} if w.op == "add_rmsnorm_fwd" else set()) | (
-            {"dy"} if w.op == "rmsnorm_bwd" else set())
+            {"dy"} if w.op in ("rmsnorm_bwd", "add_rmsnorm_bwd") else set()) | (
+            {"d_ro"} if w.op == "add_rmsnorm_bwd" else set())
         assert want <= set(t), name
         enc = np.uint16 if w.dtype == synth.BF16 else np.float32
         for k in want:
