@@ -191,8 +191,11 @@ typedef enum {
     RRN_VARIANT_ROW_CTA = 1, /* one row per CTA, row held in registers, 128-bit vectors */
     RRN_VARIANT_ROW_WARP = 2,/* one row per warp, row held in registers, 128-bit vectors */
     RRN_VARIANT_STREAM = 3,  /* one row per CTA, two passes over the row (any N / alignment) */
-    RRN_VARIANT_ROW_TMA = 4  /* persistent row per CTA fed by bulk async copies (TMA engine)
+    RRN_VARIANT_ROW_TMA = 4, /* persistent row per CTA fed by bulk async copies (TMA engine)
                                 into a shared-memory ring of `stages` rows, 128-bit vectors */
+    RRN_VARIANT_ROW_CLUSTER = 5 /* one row split across the `cluster` CTAs of a thread-block
+                                   cluster; partial sums exchanged in distributed shared memory.
+                                   Forward only. */
 } rrn_variant;
 
 /* A launch configuration. Zero fields mean "choose automatically". */
@@ -202,6 +205,7 @@ typedef struct {
     int threads; /* threads per CTA (a multiple of 32, at most 1024) */
     int ctas;    /* CTAs in the grid; each walks rows with a grid-sized stride */
     int stages;  /* RRN_VARIANT_ROW_TMA: rows in flight per CTA, 1..8 */
+    int cluster; /* RRN_VARIANT_ROW_CLUSTER: CTAs per cluster, 2..8 (ctas: a multiple of it) */
     int vec;     /* output of rrn_plan_*: 1 when the 128-bit vector path is used */
 } rrn_launch;
 

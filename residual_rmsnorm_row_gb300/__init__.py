@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401  (re-exported API)
     LIBRARY_PATH,
     VARIANT_AUTO,
     VARIANT_NAMES,
+    VARIANT_ROW_CLUSTER,
     VARIANT_ROW_CTA,
     VARIANT_ROW_TMA,
     VARIANT_ROW_WARP,

@@ -20,9 +20,11 @@ LIBRARY_PATH = os.path.join(_HERE, "librrn.so")
 BF16, F32 = 0, 1
 _DTYPES = {torch.bfloat16: BF16, torch.float32: F32}
 
-VARIANT_AUTO, VARIANT_ROW_CTA, VARIANT_ROW_WARP, VARIANT_STREAM, VARIANT_ROW_TMA = 0, 1, 2, 3, 4
+(VARIANT_AUTO, VARIANT_ROW_CTA, VARIANT_ROW_WARP, VARIANT_STREAM, VARIANT_ROW_TMA,
+ VARIANT_ROW_CLUSTER) = range(6)
 VARIANT_NAMES = {VARIANT_ROW_CTA: "row_cta", VARIANT_ROW_WARP: "row_warp",
-                 VARIANT_STREAM: "stream", VARIANT_ROW_TMA: "row_tma"}
+                 VARIANT_STREAM: "stream", VARIANT_ROW_TMA: "row_tma",
+                 VARIANT_ROW_CLUSTER: "row_cluster"}
 
 STATUS_NAMES = {0: "RRN_OK", 1: "RRN_ERR_NULL", 2: "RRN_ERR_SHAPE", 3: "RRN_ERR_EPS",
                 4: "RRN_ERR_DTYPE", 5: "RRN_ERR_ALIGN", 6: "RRN_ERR_WORKSPACE",
@@ -41,7 +43,8 @@ class RRNError(RuntimeError):
 
 class rrn_launch(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("vpt", ctypes.c_int), ("threads", ctypes.c_int),
-                ("ctas", ctypes.c_int), ("stages", ctypes.c_int), ("vec", ctypes.c_int)]
+                ("ctas", ctypes.c_int), ("stages", ctypes.c_int), ("cluster", ctypes.c_int),
+                ("vec", ctypes.c_int)]
 
 
 @dataclass(frozen=True)
@@ -53,19 +56,22 @@ class Launch:
     threads: int = 0
     ctas: int = 0
     stages: int = 0
+    cluster: int = 0
     vec: int = 0
 
     def to_c(self) -> rrn_launch:
-        return rrn_launch(self.variant, self.vpt, self.threads, self.ctas, self.stages, self.vec)
+        return rrn_launch(self.variant, self.vpt, self.threads, self.ctas, self.stages,
+                          self.cluster, self.vec)
 
     @staticmethod
     def from_c(c: rrn_launch) -> "Launch":
-        return Launch(c.variant, c.vpt, c.threads, c.ctas, c.stages, c.vec)
+        return Launch(c.variant, c.vpt, c.threads, c.ctas, c.stages, c.cluster, c.vec)
 
     @property
     def name(self) -> str:
         base = VARIANT_NAMES.get(self.variant, "auto")
         st = f",stages={self.stages}" if self.variant == VARIANT_ROW_TMA else ""
+        st += f",cluster={self.cluster}" if self.variant == VARIANT_ROW_CLUSTER else ""
         return f"{base}(vpt={self.vpt},threads={self.threads},ctas={self.ctas}{st},vec={self.vec})"
 
 

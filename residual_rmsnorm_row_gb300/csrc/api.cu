@@ -144,6 +144,8 @@ int clamp_grid(int64_t v) {
 // SM, each with one 128-bit load per tensor per VPT in flight.
 constexpr int kFwdTargetThreads = 256;
 constexpr int kBwdTargetThreads = 256;
+// Widest row (in 128-bit vectors) one CTA holds in registers: 8 vectors x 256 threads.
+constexpr int kRowCtaMaxVec = 2048;
 
 // Largest dynamic shared memory one CTA may use (sm_100-class parts: 227 KB).
 constexpr int kMaxDynSmem = 227 * 1024;
@@ -200,12 +202,14 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
     if (l.variant == RRN_VARIANT_AUTO) {
         if (!vec_ok) l.variant = RRN_VARIANT_STREAM;
         else if (nvec <= 32 * kMaxVpt && M >= 4LL * sms) l.variant = RRN_VARIANT_ROW_WARP;
-        else if (nvec <= 2048) l.variant = RRN_VARIANT_ROW_CTA;
+        else if (nvec <= kRowCtaMaxVec) l.variant = RRN_VARIANT_ROW_CTA;
+        else if (nvec <= static_cast<int64_t>(kMaxCluster) * kRowCtaMaxVec) l.variant = RRN_VARIANT_ROW_CLUSTER;
         else l.variant = RRN_VARIANT_STREAM;
     }
     l.vec = (l.variant == RRN_VARIANT_STREAM) ? vec_ok : true;
     l.stages = 0;
     l.smem = 0;
+    l.cluster = 0;
 
     switch (l.variant) {
         case RRN_VARIANT_ROW_CTA: {
@@ -235,6 +239,39 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
             l.threads = cfg && cfg->threads ? cfg->threads : 128;
             if (l.threads < 32 || l.threads % 32 || l.threads > 256) return RRN_ERR_CONFIG;
             l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid((M + l.threads / 32 - 1) / (l.threads / 32));
+            break;
+        }
+        case RRN_VARIANT_ROW_CLUSTER: {
+            if (!vec_ok) return RRN_ERR_CONFIG;
+            if (cfg && cfg->cluster) {
+                l.cluster = cfg->cluster;
+            } else {
+                l.cluster = 2;
+                while (l.cluster < kMaxCluster && nvec > static_cast<int64_t>(l.cluster) * kRowCtaMaxVec) l.cluster *= 2;
+            }
+            if (l.cluster < 2 || l.cluster > kMaxCluster) return RRN_ERR_CONFIG;
+            const int64_t chunk = (nvec + l.cluster - 1) / l.cluster;
+            if (cfg && cfg->vpt) {
+                l.vpt = cfg->vpt;
+            } else {
+                l.vpt = ceil_pow2_vpt((chunk + kFwdTargetThreads - 1) / kFwdTargetThreads, kMaxVpt);
+                while (l.vpt < kMaxVpt && chunk > static_cast<int64_t>(l.vpt) * fwd_max_threads(l.vpt)) l.vpt *= 2;
+            }
+            l.threads = cfg && cfg->threads ? cfg->threads : round_up32((chunk + l.vpt - 1) / l.vpt);
+            if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4 && l.vpt != 8) return RRN_ERR_CONFIG;
+            if (l.threads < 32 || l.threads % 32 || l.threads > fwd_max_threads(l.vpt)) return RRN_ERR_CONFIG;
+            if (static_cast<int64_t>(l.vpt) * l.threads < chunk) return RRN_ERR_CONFIG;
+            if (cfg && cfg->ctas) {
+                l.ctas = cfg->ctas;
+                if (l.ctas % l.cluster) return RRN_ERR_CONFIG;
+            } else {
+                const int occ = occupancy(false, dtype, fused, l);
+                int64_t clusters = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1) / l.cluster;
+                if (clusters < 1) clusters = 1;
+                if (clusters > M) clusters = M;
+                if (clusters > INT32_MAX / l.cluster) clusters = INT32_MAX / l.cluster;
+                l.ctas = static_cast<int>(clusters) * l.cluster;
+            }
             break;
         }
         case RRN_VARIANT_ROW_TMA: {
@@ -332,6 +369,7 @@ int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
     l.vec = (l.variant == RRN_VARIANT_STREAM) ? vec_ok : true;
     l.stages = 0;
     l.smem = 0;
+    l.cluster = 0;
     int ring_occ = 0;
     switch (l.variant) {
         case RRN_VARIANT_ROW_TMA:
@@ -430,6 +468,7 @@ void to_public(const Launch &l, rrn_launch *out) {
     out->threads = l.threads;
     out->ctas = l.ctas;
     out->stages = l.stages;
+    out->cluster = l.cluster;
     out->vec = l.vec ? 1 : 0;
 }
 
@@ -488,7 +527,8 @@ RRN_API int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t 
     // The caller's buffers are not known here: size for the 128-bit vector plan and the
     // element-wise plan (unaligned buffers), plain and fused, and return the largest.
     int ctas = 0;
-    for (int vec = 0; vec < 2; ++vec)
+    const bool vec_possible = N % (16 / elem_size(dtype)) == 0;
+    for (int vec = 0; vec < (vec_possible ? 2 : 1); ++vec)
         for (int add = 0; add < 2; ++add) {
             Launch l;
             int64_t rpc = 0;

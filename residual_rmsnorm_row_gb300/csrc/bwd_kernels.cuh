@@ -308,18 +308,30 @@ __global__ void __launch_bounds__(1024) bwd_stream(const BwdArgs a) {
 }
 
 // Stage 2: dw[j] = sum_p partial[p, j]. A CTA covers 32 consecutive columns with
-// kReduceThreads / 32 row groups; group g sums rows p = g, g + G, g + 2G, ... in order, then
-// the first warp adds the G group sums in order.
+// G = kReduceThreads / 32 row groups (one warp each); group g adds rows p = g, g + G, g + 2G, ...
+// in that order (eight loads in flight, the additions still in sequence), then one warp adds
+// the G group sums in group order. The order depends only on (P, N), so dw is reproducible.
 __global__ void __launch_bounds__(kReduceThreads)
     bwd_dw_reduce(const float *__restrict__ partial, float *__restrict__ dw, int P, int N) {
     constexpr int G = kReduceThreads / 32;
-    __shared__ float sums[G][32];
+    constexpr int U = 8;
+    __shared__ float sums[G][33];
     const int lane = threadIdx.x & 31;
     const int grp = threadIdx.x >> 5;
     const int col = blockIdx.x * 32 + lane;
     float acc = 0.f;
-    if (col < N)
-        for (int p = grp; p < P; p += G) acc += __ldcg(partial + static_cast<int64_t>(p) * N + col);
+    if (col < N) {
+        const float *src = partial + col;
+        int p = grp;
+        for (; p + (U - 1) * G < P; p += U * G) {
+            float v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) v[u] = __ldcg(src + static_cast<int64_t>(p + u * G) * N);
+#pragma unroll
+            for (int u = 0; u < U; ++u) acc += v[u];
+        }
+        for (; p < P; p += G) acc += __ldcg(src + static_cast<int64_t>(p) * N);
+    }
     sums[grp][lane] = acc;
     __syncthreads();
     if (grp == 0 && col < N) {
@@ -364,7 +376,7 @@ template <typename T>
 cudaError_t launch_bwd(const BwdArgs &a, const Launch &l, cudaStream_t stream) {
     const void *k = bwd_kernel_ptr_any<T>(a.d_ro != nullptr, l);
     if (!k) return cudaErrorInvalidConfiguration;
-    if (l.smem > 48 * 1024) {
+    if (l.smem > 0) {
         cudaError_t e = allow_dynamic_smem(k, l.smem);
         if (e != cudaSuccess) return e;
     }
@@ -383,7 +395,7 @@ template <typename T>
 int occupancy_bwd_t(bool add_grad, const Launch &l) {
     const void *k = bwd_kernel_ptr_any<T>(add_grad, l);
     if (!k) return 0;
-    if (l.smem > 48 * 1024 && allow_dynamic_smem(k, l.smem) != cudaSuccess) return 0;
+    if (l.smem > 0 && allow_dynamic_smem(k, l.smem) != cudaSuccess) return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, l.threads, static_cast<size_t>(l.smem)) !=
         cudaSuccess) {

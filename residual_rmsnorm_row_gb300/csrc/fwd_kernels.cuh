@@ -22,6 +22,22 @@
 
 namespace rrn {
 
+// r = x (+ residual) in fp32 for one 128-bit vector of packed inputs. Recomputing it is exact
+// and cheap, so the kernels keep the row packed (4 registers per vector and tensor) instead of
+// holding an fp32 copy across the reduction.
+template <typename T, bool FUSED>
+__device__ __forceinline__ void r_of(const uint4 &xv, const uint4 &rv,
+                                     float (&f)[Elem<T>::kPerVec]) {
+    using E = Elem<T>;
+    E::unpack(xv, f);
+    if constexpr (FUSED) {
+        float b[E::kPerVec];
+        E::unpack(rv, b);
+#pragma unroll
+        for (int k = 0; k < E::kPerVec; ++k) f[k] += b[k];
+    }
+}
+
 // The per-row work of the row-per-CTA variants, on a row already in registers: this thread
 // owns the 128-bit vectors c = v * blockDim.x + threadIdx.x (v < VPT, c < nvec) of x (xv) and
 // residual (rv), and the matching weight vectors (wv). Writes residual_out (fused), y and rstd.
@@ -38,22 +54,16 @@ __device__ __forceinline__ bool row_cta_body(const FwdArgs &a, int64_t row, int 
     const int nthr = blockDim.x;
     const int64_t base = row * nvec;
     const float n_f = static_cast<float>(a.N);
-    float acc[VPT][V];
     float ss = 0.f;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int c = v * nthr + tid;
         if (c < nvec) {
-            E::unpack(xv[v], acc[v]);
-            if (FUSED) {
-                float b[V];
-                E::unpack(rv[v], b);
+            float f[V];
+            r_of<T, FUSED>(xv[v], rv[v], f);
+            if (FUSED) st_stream(static_cast<uint4 *>(a.res_out) + base + c, E::pack(f));
 #pragma unroll
-                for (int k = 0; k < V; ++k) acc[v][k] += b[k];
-                st_stream(static_cast<uint4 *>(a.res_out) + base + c, E::pack(acc[v]));
-            }
-#pragma unroll
-            for (int k = 0; k < V; ++k) ss = fmaf(acc[v][k], acc[v][k], ss);
+            for (int k = 0; k < V; ++k) ss = fmaf(f[k], f[k], ss);
         }
     }
     ss = cta_sum(ss, slots[parity]);
@@ -66,21 +76,27 @@ __device__ __forceinline__ bool row_cta_body(const FwdArgs &a, int64_t row, int 
         float am = 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v)
-            if (v * nthr + tid < nvec)
+            if (v * nthr + tid < nvec) {
+                float f[V];
+                r_of<T, FUSED>(xv[v], rv[v], f);
 #pragma unroll
-                for (int k = 0; k < V; ++k) am = fmaxf(am, fabsf(acc[v][k]));
+                for (int k = 0; k < V; ++k) am = fmaxf(am, fabsf(f[k]));
+            }
         am = cta_max(am, slots[parity]);
         parity ^= 1;
         const int e = rescale_exponent(am);
         float s2 = 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v)
-            if (v * nthr + tid < nvec)
+            if (v * nthr + tid < nvec) {
+                float f[V];
+                r_of<T, FUSED>(xv[v], rv[v], f);
 #pragma unroll
                 for (int k = 0; k < V; ++k) {
-                    const float t = ldexpf(acc[v][k], -e);
+                    const float t = ldexpf(f[k], -e);
                     s2 = fmaf(t, t, s2);
                 }
+            }
         s2 = cta_sum(s2, slots[parity]);
         parity ^= 1;
         rs = rstd_rescaled(s2, n_f, a.eps, e);
@@ -89,10 +105,11 @@ __device__ __forceinline__ bool row_cta_body(const FwdArgs &a, int64_t row, int 
     for (int v = 0; v < VPT; ++v) {
         const int c = v * nthr + tid;
         if (c < nvec) {
-            float wf[V], o[V];
+            float f[V], wf[V], o[V];
+            r_of<T, FUSED>(xv[v], rv[v], f);
             E::unpack(wv[v], wf);
 #pragma unroll
-            for (int k = 0; k < V; ++k) o[k] = acc[v][k] * rs * wf[k];
+            for (int k = 0; k < V; ++k) o[k] = f[k] * rs * wf[k];
             st_stream(static_cast<uint4 *>(a.y) + base + c, E::pack(o));
         }
     }
@@ -220,6 +237,125 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT))
     }
 }
 
+// One row split across the C CTAs of a thread-block cluster (C = 2..8): CTA rank q owns the
+// vectors [q * chunk, (q + 1) * chunk) of every row its cluster handles (chunk = ceil(nvec / C)),
+// held in registers. The CTAs' partial sums of squares are exchanged through distributed shared
+// memory: each CTA writes its partial into slot q of every peer's array, then one cluster
+// barrier, then every CTA adds the C slots in rank order (the same bits everywhere). Clusters
+// walk rows with a grid-sized stride. For rows too wide for one CTA's registers, and to spread
+// few-row (decode) problems over more SMs.
+template <typename T, int VPT, bool FUSED>
+__global__ void __launch_bounds__(fwd_max_threads(VPT)) fwd_row_cluster(const FwdArgs a) {
+    using E = Elem<T>;
+    constexpr int V = E::kPerVec;
+    __shared__ float slots[2][32];
+    __shared__ float part[2][kMaxCluster];  // one buffer per exchange, alternating
+
+    const int nvec = a.N / V;
+    const int C = static_cast<int>(cluster_nctarank());
+    const int q = static_cast<int>(cluster_ctarank());
+    const int chunk = (nvec + C - 1) / C;
+    const int c0 = q * chunk;
+    const int c1 = min(nvec, c0 + chunk);
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const float n_f = static_cast<float>(a.N);
+    const uint4 *x4 = static_cast<const uint4 *>(a.x);
+    const uint4 *r4 = static_cast<const uint4 *>(a.res);
+
+    uint4 wv[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = c0 + v * nthr + tid;
+        if (c < c1) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
+    }
+    int parity = 0, pbuf = 0;
+    // Cluster-wide total of one float per CTA; every CTA gets the same bits.
+    auto exchange = [&](float mine, bool take_max) {
+        if (tid < C) st_cluster_f32(&part[pbuf][q], static_cast<uint32_t>(tid), mine);
+        cluster_sync();
+        float t = 0.f;
+        for (int i = 0; i < C; ++i) t = take_max ? fmaxf(t, part[pbuf][i]) : t + part[pbuf][i];
+        pbuf ^= 1;
+        return t;
+    };
+
+    const int64_t ncl = cluster_nclusters_x();
+    for (int64_t row = cluster_id_x(); row < a.M; row += ncl) {
+        const int64_t base = row * nvec;
+        uint4 xv[VPT], rv[VPT];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = c0 + v * nthr + tid;
+            if (c < c1) {
+                xv[v] = ld_stream(x4 + base + c);
+                if (FUSED) rv[v] = ld_stream(r4 + base + c);
+            }
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = c0 + v * nthr + tid;
+            if (c < c1) {
+                float f[V];
+                r_of<T, FUSED>(xv[v], rv[v], f);
+                if (FUSED) st_stream(static_cast<uint4 *>(a.res_out) + base + c, E::pack(f));
+#pragma unroll
+                for (int k = 0; k < V; ++k) ss = fmaf(f[k], f[k], ss);
+            }
+        }
+        ss = cta_sum(ss, slots[parity]);
+        parity ^= 1;
+        ss = exchange(ss, false);
+        float rs;
+        if (!needs_rescale(ss)) {
+            rs = rstd_plain(ss, n_f, a.eps);
+        } else {  // rare: sum of squares out of fp32 range, or an all-zero row
+            float am = 0.f;
+#pragma unroll
+            for (int v = 0; v < VPT; ++v)
+                if (c0 + v * nthr + tid < c1) {
+                    float f[V];
+                    r_of<T, FUSED>(xv[v], rv[v], f);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) am = fmaxf(am, fabsf(f[k]));
+                }
+            am = cta_max(am, slots[parity]);
+            parity ^= 1;
+            const int e = rescale_exponent(exchange(am, true));
+            float s2 = 0.f;
+#pragma unroll
+            for (int v = 0; v < VPT; ++v)
+                if (c0 + v * nthr + tid < c1) {
+                    float f[V];
+                    r_of<T, FUSED>(xv[v], rv[v], f);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) {
+                        const float t = ldexpf(f[k], -e);
+                        s2 = fmaf(t, t, s2);
+                    }
+                }
+            s2 = cta_sum(s2, slots[parity]);
+            parity ^= 1;
+            rs = rstd_rescaled(exchange(s2, false), n_f, a.eps, e);
+        }
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = c0 + v * nthr + tid;
+            if (c < c1) {
+                float f[V], wf[V], o[V];
+                r_of<T, FUSED>(xv[v], rv[v], f);
+                E::unpack(wv[v], wf);
+#pragma unroll
+                for (int k = 0; k < V; ++k) o[k] = f[k] * rs * wf[k];
+                st_stream(static_cast<uint4 *>(a.y) + base + c, E::pack(o));
+            }
+        }
+        if (q == 0 && tid == 0 && a.rstd) a.rstd[row] = rs;
+    }
+    cluster_sync();  // no CTA exits while a peer may still write into its shared memory
+}
+
 template <typename T, int VPT, bool FUSED>
 __global__ void __launch_bounds__(256) fwd_row_warp(const FwdArgs a) {
     using E = Elem<T>;
@@ -253,22 +389,16 @@ __global__ void __launch_bounds__(256) fwd_row_warp(const FwdArgs a) {
                 if (FUSED) rv[v] = ld_stream(r4 + base + c);
             }
         }
-        float acc[VPT][V];
         float ss = 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * 32 + lane;
             if (c < nvec) {
-                E::unpack(xv[v], acc[v]);
-                if (FUSED) {
-                    float b[V];
-                    E::unpack(rv[v], b);
+                float f[V];
+                r_of<T, FUSED>(xv[v], rv[v], f);
+                if (FUSED) st_stream(ro4 + base + c, E::pack(f));
 #pragma unroll
-                    for (int k = 0; k < V; ++k) acc[v][k] += b[k];
-                    st_stream(ro4 + base + c, E::pack(acc[v]));
-                }
-#pragma unroll
-                for (int k = 0; k < V; ++k) ss = fmaf(acc[v][k], acc[v][k], ss);
+                for (int k = 0; k < V; ++k) ss = fmaf(f[k], f[k], ss);
             }
         }
         ss = warp_sum(ss);
@@ -279,29 +409,36 @@ __global__ void __launch_bounds__(256) fwd_row_warp(const FwdArgs a) {
             float am = 0.f;
 #pragma unroll
             for (int v = 0; v < VPT; ++v)
-                if (v * 32 + lane < nvec)
+                if (v * 32 + lane < nvec) {
+                    float f[V];
+                    r_of<T, FUSED>(xv[v], rv[v], f);
 #pragma unroll
-                    for (int k = 0; k < V; ++k) am = fmaxf(am, fabsf(acc[v][k]));
+                    for (int k = 0; k < V; ++k) am = fmaxf(am, fabsf(f[k]));
+                }
             const int e = rescale_exponent(warp_max(am));
             float s2 = 0.f;
 #pragma unroll
             for (int v = 0; v < VPT; ++v)
-                if (v * 32 + lane < nvec)
+                if (v * 32 + lane < nvec) {
+                    float f[V];
+                    r_of<T, FUSED>(xv[v], rv[v], f);
 #pragma unroll
                     for (int k = 0; k < V; ++k) {
-                        const float t = ldexpf(acc[v][k], -e);
+                        const float t = ldexpf(f[k], -e);
                         s2 = fmaf(t, t, s2);
                     }
+                }
             rs = rstd_rescaled(warp_sum(s2), n_f, a.eps, e);
         }
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * 32 + lane;
             if (c < nvec) {
-                float wf[V], o[V];
+                float f[V], wf[V], o[V];
+                r_of<T, FUSED>(xv[v], rv[v], f);
                 E::unpack(wv[v], wf);
 #pragma unroll
-                for (int k = 0; k < V; ++k) o[k] = acc[v][k] * rs * wf[k];
+                for (int k = 0; k < V; ++k) o[k] = f[k] * rs * wf[k];
                 st_stream(y4 + base + c, E::pack(o));
             }
         }
@@ -440,6 +577,14 @@ const void *fwd_kernel_ptr(const Launch &l) {
         case RRN_VARIANT_STREAM:
             return l.vec ? reinterpret_cast<const void *>(&fwd_stream<T, true, FUSED>)
                          : reinterpret_cast<const void *>(&fwd_stream<T, false, FUSED>);
+        case RRN_VARIANT_ROW_CLUSTER:
+            switch (l.vpt) {
+                case 1: return reinterpret_cast<const void *>(&fwd_row_cluster<T, 1, FUSED>);
+                case 2: return reinterpret_cast<const void *>(&fwd_row_cluster<T, 2, FUSED>);
+                case 4: return reinterpret_cast<const void *>(&fwd_row_cluster<T, 4, FUSED>);
+                case 8: return reinterpret_cast<const void *>(&fwd_row_cluster<T, 8, FUSED>);
+                default: return nullptr;
+            }
         case RRN_VARIANT_ROW_TMA:
             switch (l.vpt) {
                 case 1: return reinterpret_cast<const void *>(&fwd_row_tma<T, 1, FUSED>);
@@ -461,13 +606,28 @@ template <typename T>
 cudaError_t launch_fwd(const FwdArgs &a, const Launch &l, cudaStream_t stream) {
     const void *k = fwd_kernel_ptr_any<T>(a.res != nullptr, l);
     if (!k) return cudaErrorInvalidConfiguration;
-    if (l.smem > 48 * 1024) {
+    if (l.smem > 0) {
         cudaError_t e = allow_dynamic_smem(k, l.smem);
         if (e != cudaSuccess) return e;
     }
     FwdArgs args = a;
     args.stages = l.stages;
     void *params[] = {&args};
+    if (l.variant == RRN_VARIANT_ROW_CLUSTER) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(l.ctas);
+        cfg.blockDim = dim3(l.threads);
+        cfg.dynamicSmemBytes = static_cast<size_t>(l.smem);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(l.cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelExC(&cfg, k, params);
+    }
     return cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, static_cast<size_t>(l.smem),
                             stream);
 }
@@ -476,7 +636,7 @@ template <typename T>
 int occupancy_fwd_t(bool fused, const Launch &l) {
     const void *k = fwd_kernel_ptr_any<T>(fused, l);
     if (!k) return 0;
-    if (l.smem > 48 * 1024 && allow_dynamic_smem(k, l.smem) != cudaSuccess) return 0;
+    if (l.smem > 0 && allow_dynamic_smem(k, l.smem) != cudaSuccess) return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, l.threads, static_cast<size_t>(l.smem)) !=
         cudaSuccess) {

@@ -51,6 +51,7 @@ struct Launch {
     bool vec;     // 128-bit vectors (else element-wise)
     int stages;   // TMA variant: rows in flight per CTA (shared-memory ring depth)
     int smem;     // dynamic shared memory bytes per CTA
+    int cluster;  // cluster variant: CTAs per cluster (one row split across them)
 };
 
 // Largest vectors-per-thread the register variants are compiled for, and the thread limit
@@ -59,8 +60,9 @@ constexpr int kMaxVpt = 8;
 constexpr int fwd_max_threads(int vpt) { return vpt >= 8 ? 256 : vpt >= 4 ? 512 : 1024; }
 constexpr int bwd_max_threads(int vpt) { return vpt >= 4 ? 256 : 512; }
 constexpr int kBwdMaxVpt = 4;
-constexpr int kReduceThreads = 256;  // dw stage-2 CTA size: 32 columns x 8 row groups
+constexpr int kReduceThreads = 1024; // dw stage-2 CTA size: 32 columns x 32 row groups
 constexpr int kMaxStages = 8;        // deepest shared-memory ring of the TMA variants
+constexpr int kMaxCluster = 8;       // largest (portable) thread-block cluster
 
 // Raise a kernel's dynamic shared-memory limit to `bytes` on the current device (done once
 // per kernel, device and size; defined in api.cu).

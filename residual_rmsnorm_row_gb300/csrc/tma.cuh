@@ -99,3 +99,50 @@ __device__ __forceinline__ uint4 ld_shared_v4(const void *p) {
 }
 
 }  // namespace rrn
+
+namespace rrn {
+
+// ---------------------------------------------------------------------------------------
+// Thread-block clusters: rank, distributed shared memory stores, and the cluster barrier.
+// The cluster barrier is a hardware barrier instruction (no polling loop).
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nclusters_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Store one float into the shared memory of CTA `rank` of this cluster, at the address that
+// `local` has in this CTA.
+__device__ __forceinline__ void st_cluster_f32(const float *local, uint32_t rank, float v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+// All threads of all CTAs of the cluster: release this CTA's prior memory operations (incl.
+// remote shared-memory stores) and acquire everyone else's.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+}  // namespace rrn

@@ -107,6 +107,14 @@ def _variants(dtype, N, M):
         if N % V == 0 and nvec <= 32 * vpt:
             out.append(rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 128, 0))
             out.append(rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 64, 5))
+    if N % V == 0:
+        for C in (2, 4, 8):
+            chunk = -(-nvec // C)
+            for vpt in (1, 4):
+                thr = -(-(-(-chunk // vpt)) // 32) * 32
+                if thr <= (512 if vpt == 4 else 1024):
+                    out.append(rrn.Launch(rrn.VARIANT_ROW_CLUSTER, vpt, thr, 0, 0, C))
+                    out.append(rrn.Launch(rrn.VARIANT_ROW_CLUSTER, vpt, thr, 3 * C, 0, C))
     out.append(rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0))
     out.append(rrn.Launch(rrn.VARIANT_STREAM, 0, 1024, 11))
     return out
