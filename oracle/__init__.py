@@ -14,6 +14,7 @@ What each function computes, with the passage it follows, is stated in ``oracle.
   add_rmsnorm_fwd  the same on r = x + residual, also returning r  (KernelAgent page, Oink)
   rmsnorm_bwd      dx and dw, the exact derivative of rmsnorm_fwd
   add_rmsnorm_bwd  d_r (gradient w.r.t. x + residual) and dw, the derivative of add_rmsnorm_fwd
+  add_layernorm_fwd / add_layernorm_bwd   the LayerNorm variant (mean subtracted, bias added)
 """
 from __future__ import annotations
 
@@ -60,8 +61,13 @@ class Oracle:
                                            _dbl_p, _dbl_p]
         lib.oracle_add_rmsnorm_bwd.argtypes = [vp, i32, vp, i32, vp, i32, vp, i32, i64, i64, dbl,
                                                _dbl_p, _dbl_p]
+        lib.oracle_add_layernorm_fwd.argtypes = [vp, i32, vp, i32, vp, i32, vp, i32, i64, i64, dbl,
+                                                 _dbl_p, _dbl_p, _dbl_p, _dbl_p]
+        lib.oracle_add_layernorm_bwd.argtypes = [vp, i32, vp, i32, vp, i32, vp, i32, i64, i64, dbl,
+                                                 _dbl_p, _dbl_p, _dbl_p]
         for name in ("oracle_decode", "oracle_add_rmsnorm_fwd", "oracle_rmsnorm_fwd",
-                     "oracle_rmsnorm_bwd", "oracle_add_rmsnorm_bwd"):
+                     "oracle_rmsnorm_bwd", "oracle_add_rmsnorm_bwd", "oracle_add_layernorm_fwd",
+                     "oracle_add_layernorm_bwd"):
             getattr(lib, name).restype = i32
         self.lib = lib
 
@@ -150,6 +156,50 @@ class Oracle:
             _code(w), M, N, float(eps), _out(d_r), _out(dw)), "add_rmsnorm_bwd")
         return d_r, dw
 
+    def add_layernorm_fwd(self, x: np.ndarray, residual: Optional[np.ndarray], w: np.ndarray,
+                          b: Optional[np.ndarray], eps: float):
+        """Return ``(r, y, mean, rstd)`` of LayerNorm on r = x (+ residual); b may be None."""
+        x = np.ascontiguousarray(x)
+        w = np.ascontiguousarray(w)
+        M, N = x.shape
+        if w.shape != (N,) or (b is not None and np.shape(b) != (N,)):
+            raise ValueError("w and b must have shape (N,)")
+        if residual is not None:
+            residual = np.ascontiguousarray(residual)
+            if residual.shape != x.shape:
+                raise ValueError("residual must have the shape of x")
+        if b is not None:
+            b = np.ascontiguousarray(b)
+        r = np.empty((M, N))
+        y = np.empty((M, N))
+        mean = np.empty(M)
+        rstd = np.empty(M)
+        self._check(self.lib.oracle_add_layernorm_fwd(
+            _ptr(x), _code(x), _ptr(residual), 0 if residual is None else _code(residual),
+            _ptr(w), _code(w), _ptr(b), 0 if b is None else _code(b), M, N, float(eps),
+            _out(r), _out(y), _out(mean), _out(rstd)), "add_layernorm_fwd")
+        return r, y, mean, rstd
+
+    def add_layernorm_bwd(self, dy: np.ndarray, d_residual_out: Optional[np.ndarray],
+                          x: np.ndarray, w: np.ndarray, eps: float):
+        """Return ``(dx, dw, db)`` of LayerNorm at x (the stored residual_out when fused)."""
+        dy = np.ascontiguousarray(dy)
+        x = np.ascontiguousarray(x)
+        w = np.ascontiguousarray(w)
+        M, N = x.shape
+        if dy.shape != x.shape or w.shape != (N,):
+            raise ValueError("dy must have the shape of x and w shape (N,)")
+        if d_residual_out is not None:
+            d_residual_out = np.ascontiguousarray(d_residual_out)
+        dx = np.empty((M, N))
+        dw = np.empty(N)
+        db = np.empty(N)
+        self._check(self.lib.oracle_add_layernorm_bwd(
+            _ptr(dy), _code(dy), _ptr(d_residual_out),
+            0 if d_residual_out is None else _code(d_residual_out), _ptr(x), _code(x), _ptr(w),
+            _code(w), M, N, float(eps), _out(dx), _out(dw), _out(db)), "add_layernorm_bwd")
+        return dx, dw, db
+
 
 _DEFAULT: Optional[Oracle] = None
 
@@ -182,10 +232,19 @@ def add_rmsnorm_bwd(dy, d_residual_out, residual_out, w, eps, want_dr=True):
     return default().add_rmsnorm_bwd(dy, d_residual_out, residual_out, w, eps, want_dr)
 
 
+def add_layernorm_fwd(x, residual, w, b, eps):
+    return default().add_layernorm_fwd(x, residual, w, b, eps)
+
+
+def add_layernorm_bwd(dy, d_residual_out, x, w, eps):
+    return default().add_layernorm_bwd(dy, d_residual_out, x, w, eps)
+
+
 def build(force: bool = False) -> str:
     """Compile ``liboracle.so`` (used by the package's build step)."""
     return _build.build(force)
 
 
 __all__ = ["Oracle", "default", "decode", "add_rmsnorm_fwd", "rmsnorm_fwd", "rmsnorm_bwd",
-           "add_rmsnorm_bwd", "build", "BF16", "F32", "F64"]
+           "add_rmsnorm_bwd", "add_layernorm_fwd", "add_layernorm_bwd", "build", "BF16", "F32",
+           "F64"]

@@ -186,3 +186,108 @@ int oracle_add_rmsnorm_bwd(const void *dy, int dy_dt, const void *d_ro, int d_ro
     free(xr); free(dyr); free(wd); free(xhat); free(g);
     return ORACLE_OK;
 }
+
+/*
+ * LayerNorm, the mean-subtracting variant of the same row norm (the CuTe DSL skill page lists a
+ * "CTA norm (LayerNorm)" example in its "Workflow 0" example index). Standard definition, per
+ * row of r = x (+ residual):
+ *     mean = (1/N) sum_j r_j,   var = (1/N) sum_j (r_j - mean)^2,   rstd = 1 / sqrt(var + eps)
+ *     y_j  = (r_j - mean) * rstd * w_j + b_j
+ * `res` and `b` may be NULL (no residual, no bias). Outputs (fp64, any may be NULL): r_out,
+ * y [M, N], mean [M], rstd [M].
+ */
+int oracle_add_layernorm_fwd(const void *x, int x_dt, const void *res, int res_dt, const void *w,
+                             int w_dt, const void *b, int b_dt, int64_t M, int64_t N, double eps,
+                             double *r_out, double *y, double *mean, double *rstd)
+{
+    if (!x || !w || M < 0 || N < 1 || !valid_dtype(x_dt) || !valid_dtype(w_dt) ||
+        (res && !valid_dtype(res_dt)) || (b && !valid_dtype(b_dt)))
+        return ORACLE_BAD_ARG;
+    double *r = (double *)malloc((size_t)N * sizeof(double));
+    double *wd = (double *)malloc((size_t)N * sizeof(double));
+    double *bd = (double *)malloc((size_t)N * sizeof(double));
+    if (!r || !wd || !bd) { free(r); free(wd); free(bd); return ORACLE_NO_MEMORY; }
+    for (int64_t j = 0; j < N; ++j) {
+        wd[j] = element(w, w_dt, j);
+        bd[j] = b ? element(b, b_dt, j) : 0.0;
+    }
+    for (int64_t i = 0; i < M; ++i) {
+        double sum = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            double v = element(x, x_dt, i * N + j);
+            if (res) v += element(res, res_dt, i * N + j);
+            r[j] = v;
+            sum += v;
+        }
+        double mu = sum / (double)N;
+        double sq = 0.0;
+        for (int64_t j = 0; j < N; ++j) sq += (r[j] - mu) * (r[j] - mu);
+        double s = 1.0 / sqrt(sq / (double)N + eps);
+        if (mean) mean[i] = mu;
+        if (rstd) rstd[i] = s;
+        for (int64_t j = 0; j < N; ++j) {
+            if (r_out) r_out[i * N + j] = r[j];
+            if (y) y[i * N + j] = (r[j] - mu) * s * wd[j] + bd[j];
+        }
+    }
+    free(r); free(wd); free(bd);
+    return ORACLE_OK;
+}
+
+/*
+ * LayerNorm backward (the exact derivative of the definition above), with xhat = (x - mean) *
+ * rstd and g = dy * w, per row:
+ *     dx_j = rstd * ( g_j - mean_k(g_k) - xhat_j * mean_k(g_k * xhat_k) )  (+ d_ro_j, fused)
+ *     dw_j = sum over rows of dy_j * xhat_j,   db_j = sum over rows of dy_j
+ * mean and rstd are recomputed in fp64 from x (the stored residual_out for the fused op).
+ * d_ro may be NULL. Outputs (fp64, any may be NULL): dx [M, N], dw [N], db [N].
+ */
+int oracle_add_layernorm_bwd(const void *dy, int dy_dt, const void *d_ro, int d_ro_dt,
+                             const void *x, int x_dt, const void *w, int w_dt, int64_t M,
+                             int64_t N, double eps, double *dx, double *dw, double *db)
+{
+    if (!dy || !x || !w || M < 0 || N < 1 || !valid_dtype(dy_dt) || !valid_dtype(x_dt) ||
+        !valid_dtype(w_dt) || (d_ro && !valid_dtype(d_ro_dt)))
+        return ORACLE_BAD_ARG;
+    double *xr = (double *)malloc((size_t)N * sizeof(double));
+    double *dyr = (double *)malloc((size_t)N * sizeof(double));
+    double *wd = (double *)malloc((size_t)N * sizeof(double));
+    double *xhat = (double *)malloc((size_t)N * sizeof(double));
+    double *g = (double *)malloc((size_t)N * sizeof(double));
+    if (!xr || !dyr || !wd || !xhat || !g) {
+        free(xr); free(dyr); free(wd); free(xhat); free(g);
+        return ORACLE_NO_MEMORY;
+    }
+    for (int64_t j = 0; j < N; ++j) wd[j] = element(w, w_dt, j);
+    if (dw) for (int64_t j = 0; j < N; ++j) dw[j] = 0.0;
+    if (db) for (int64_t j = 0; j < N; ++j) db[j] = 0.0;
+    for (int64_t i = 0; i < M; ++i) {
+        double sum = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            xr[j] = element(x, x_dt, i * N + j);
+            dyr[j] = element(dy, dy_dt, i * N + j);
+            sum += xr[j];
+        }
+        double mu = sum / (double)N;
+        double sq = 0.0;
+        for (int64_t j = 0; j < N; ++j) sq += (xr[j] - mu) * (xr[j] - mu);
+        double s = 1.0 / sqrt(sq / (double)N + eps);
+        double sum_g = 0.0, sum_gx = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            xhat[j] = (xr[j] - mu) * s;
+            g[j] = dyr[j] * wd[j];
+            sum_g += g[j];
+            sum_gx += g[j] * xhat[j];
+        }
+        double mg = sum_g / (double)N, mgx = sum_gx / (double)N;
+        for (int64_t j = 0; j < N; ++j) {
+            double grad = s * (g[j] - mg - xhat[j] * mgx);
+            if (d_ro) grad += element(d_ro, d_ro_dt, i * N + j);
+            if (dx) dx[i * N + j] = grad;
+            if (dw) dw[j] += dyr[j] * xhat[j];
+            if (db) db[j] += dyr[j];
+        }
+    }
+    free(xr); free(dyr); free(wd); free(xhat); free(g);
+    return ORACLE_OK;
+}

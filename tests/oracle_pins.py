@@ -91,6 +91,16 @@ def pin_golden_worked_examples(o):
                 dx, dw = o.rmsnorm_bwd(conv(c["dy"]), x, w, c["eps"])
                 _close(dx, c["dx"], 1e-13, 1e-15, tag + " dx")
                 _close(dw, c["dw"], 1e-13, 1e-15, tag + " dw")
+            elif c["op"] == "layernorm_fwd":
+                _, y, mean, rstd = o.add_layernorm_fwd(x, None, w, conv(c["b"]), c["eps"])
+                _close(y, c["y"], 1e-14, 1e-15, tag + " y")
+                _close(mean, c["mean"], 1e-15, 0.0, tag + " mean")
+                _close(rstd, c["rstd"], 1e-14, 0.0, tag + " rstd")
+            elif c["op"] == "layernorm_bwd":
+                dx, dw, db = o.add_layernorm_bwd(conv(c["dy"]), None, x, w, c["eps"])
+                _close(dx, c["dx"], 1e-13, 1e-15, tag + " dx")
+                _close(dw, c["dw"], 1e-13, 1e-15, tag + " dw")
+                _close(db, c["db"], 1e-13, 1e-15, tag + " db")
             elif c["op"] == "add_rmsnorm_bwd":
                 r = conv(c["residual_out"])
                 d_r, dw = o.add_rmsnorm_bwd(conv(c["dy"]), conv(c["d_residual_out"]), r, w, c["eps"])
@@ -344,6 +354,101 @@ def pin_add_bwd_matches_torch_autograd(o):
     assert np.array_equal(d0, p0) and np.array_equal(dw0, pw0), "fused bwd without d_ro != plain bwd"
 
 
+# --------------------------------------------------------------------------- LayerNorm
+def pin_layernorm_matches_torch(o):
+    """torch.nn.functional.layer_norm (forward and autograd) in float64, fused through
+    r = x + residual, with weight and bias."""
+    import torch
+
+    rng = np.random.default_rng(31)
+    for (M, N, eps) in ((3, 1, 1e-5), (4, 77, 1e-5), (2, 2048, 0.3)):
+        x = rng.standard_normal((M, N)) * 2.0 + 0.7
+        res = rng.standard_normal((M, N))
+        w = 1.0 + 0.1 * rng.standard_normal(N)
+        b = 0.1 * rng.standard_normal(N)
+        dy = rng.standard_normal((M, N))
+        dro = rng.standard_normal((M, N))
+        tx = torch.from_numpy(x).requires_grad_(True)
+        tr = torch.from_numpy(res).requires_grad_(True)
+        tw = torch.from_numpy(w).requires_grad_(True)
+        tb = torch.from_numpy(b).requires_grad_(True)
+        r = tx + tr
+        ty = torch.nn.functional.layer_norm(r, (N,), tw, tb, eps)
+        (torch.sum(ty * torch.from_numpy(dy)) + torch.sum(r * torch.from_numpy(dro))).backward()
+        ro, y, mean, rstd = o.add_layernorm_fwd(x, res, w, b, eps)
+        _close(y, ty.detach().numpy(), 1e-12, 1e-14, f"torch layer_norm {M}x{N}")
+        _close(mean, (x + res).mean(-1), 1e-13, 1e-14, "mean")
+        dx, dw, db = o.add_layernorm_bwd(dy, dro, x + res, w, eps)
+        _close(dx, tx.grad.numpy(), 1e-11, 1e-13, f"torch LN d(x) {M}x{N}")
+        _close(dx, tr.grad.numpy(), 1e-11, 1e-13, f"torch LN d(residual) {M}x{N}")
+        _close(dw, tw.grad.numpy(), 1e-11, 1e-12, f"torch LN dw {M}x{N}")
+        _close(db, tb.grad.numpy(), 1e-11, 1e-12, f"torch LN db {M}x{N}")
+
+
+def pin_layernorm_finite_differences(o):
+    """Central differences of L = <dy, y> + <d_ro, r> give dx, dw and db."""
+    rng = np.random.default_rng(32)
+    h = 1e-6
+    M, N, eps = 2, 5, 1e-2
+    x = rng.standard_normal((M, N))
+    w = 1.0 + 0.3 * rng.standard_normal(N)
+    b = rng.standard_normal(N)
+    dy = rng.standard_normal((M, N))
+    dro = rng.standard_normal((M, N))
+
+    def loss(xx, ww, bb):
+        r, y, _, _ = o.add_layernorm_fwd(xx, None, ww, bb, eps)
+        return float(np.sum(dy * y) + np.sum(dro * r))
+
+    dx, dw, db = o.add_layernorm_bwd(dy, dro, x, w, eps)
+    fdx = np.empty_like(x)
+    for i in range(M):
+        for j in range(N):
+            xp, xm = x.copy(), x.copy()
+            xp[i, j] += h
+            xm[i, j] -= h
+            fdx[i, j] = (loss(xp, w, b) - loss(xm, w, b)) / (2 * h)
+    fdw, fdb = np.empty(N), np.empty(N)
+    for j in range(N):
+        wp, wm, bp, bm = w.copy(), w.copy(), b.copy(), b.copy()
+        wp[j] += h
+        wm[j] -= h
+        bp[j] += h
+        bm[j] -= h
+        fdw[j] = (loss(x, wp, b) - loss(x, wm, b)) / (2 * h)
+        fdb[j] = (loss(x, w, bp) - loss(x, w, bm)) / (2 * h)
+    _close(dx, fdx, 1e-6, 1e-7, "LN dx vs finite differences")
+    _close(dw, fdw, 1e-6, 1e-7, "LN dw vs finite differences")
+    _close(db, fdb, 1e-6, 1e-7, "LN db vs finite differences")
+
+
+def pin_layernorm_identities(o):
+    """Per row: sum_j dx_j = 0 and <dx, x - mean> = eps * rstd^2 * <g, xhat> (no d_ro);
+    y(x + c) = y(x) for a constant shift c; with zero-mean rows and no bias LayerNorm equals
+    RMSNorm."""
+    rng = np.random.default_rng(33)
+    M, N = 4, 40
+    x = rng.standard_normal((M, N))
+    w = 1.0 + 0.1 * rng.standard_normal(N)
+    dy = rng.standard_normal((M, N))
+    for eps in (0.0, 0.5):
+        dx, _, _ = o.add_layernorm_bwd(dy, None, x, w, eps)
+        for i in range(M):
+            mu = float(np.mean(x[i]))
+            s = 1.0 / math.sqrt(float(np.mean((x[i] - mu) ** 2)) + eps)
+            g_xhat = float(np.dot(dy[i] * w, (x[i] - mu) * s))
+            assert abs(float(np.sum(dx[i]))) <= 1e-12 * (1 + np.abs(dx[i]).sum()), "sum dx != 0"
+            lhs = float(np.dot(dx[i], x[i] - mu))
+            assert abs(lhs - eps * s * s * g_xhat) <= 1e-12 * (1 + abs(g_xhat)), "<dx, x - mean>"
+    _, y0, _, _ = o.add_layernorm_fwd(x, None, w, None, 1e-5)
+    _, y1, _, _ = o.add_layernorm_fwd(x + 3.0, None, w, None, 1e-5)
+    _close(y1, y0, 1e-12, 1e-13, "shift invariance")
+    xz = x - x.mean(axis=1, keepdims=True)
+    _, yl, _, _ = o.add_layernorm_fwd(xz, None, w, None, 1e-5)
+    yr, _ = o.rmsnorm_fwd(xz - xz.mean(axis=1, keepdims=True), w, 1e-5)
+    _close(yl, yr, 1e-12, 1e-14, "zero-mean LayerNorm vs RMSNorm")
+
+
 ALL_PINS = [
     pin_decode_known_bits,
     pin_decode_matches_torch_cast,
@@ -361,4 +466,7 @@ ALL_PINS = [
     pin_bwd_matches_torch_autograd,
     pin_add_bwd_finite_differences,
     pin_add_bwd_matches_torch_autograd,
+    pin_layernorm_matches_torch,
+    pin_layernorm_finite_differences,
+    pin_layernorm_identities,
 ]

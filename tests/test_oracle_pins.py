@@ -31,24 +31,47 @@ MUTATIONS = [
     ("eps dropped", "return 1.0 / sqrt(mean_sq + eps);", "return 1.0 / sqrt(mean_sq);"),
     ("eps outside the root", "return 1.0 / sqrt(mean_sq + eps);", "return 1.0 / sqrt(mean_sq) + eps;"),
     ("sum instead of mean", "double mean_sq = sum_sq / (double)N;", "double mean_sq = sum_sq;"),
-    ("residual subtracted", "if (res) v += element(res, res_dt, i * N + j);",
-     "if (res) v -= element(res, res_dt, i * N + j);"),
+    ("residual subtracted", "if (res) v += element(res, res_dt, i * N + j);\n            r[j] = v;\n        }",
+     "if (res) v -= element(res, res_dt, i * N + j);\n            r[j] = v;\n        }"),
+    ("LN residual subtracted", "if (res) v += element(res, res_dt, i * N + j);\n            r[j] = v;\n            sum",
+     "if (res) v -= element(res, res_dt, i * N + j);\n            r[j] = v;\n            sum"),
     ("weights reversed", "if (y) y[i * N + j] = r[j] * s * wd[j];",
      "if (y) y[i * N + j] = r[j] * s * wd[N - 1 - j];"),
     ("weights dropped", "if (y) y[i * N + j] = r[j] * s * wd[j];", "if (y) y[i * N + j] = r[j] * s;"),
     ("dx sign flipped", "double grad = s * (g[j] - xhat[j] * c);",
      "double grad = s * (g[j] + xhat[j] * c);"),
     ("dx projection dropped", "double grad = s * (g[j] - xhat[j] * c);", "double grad = s * g[j];"),
-    ("residual gradient subtracted", "if (d_ro) grad += element(d_ro, d_ro_dt, i * N + j);",
-     "if (d_ro) grad -= element(d_ro, d_ro_dt, i * N + j);"),
-    ("residual gradient dropped", "if (d_ro) grad += element(d_ro, d_ro_dt, i * N + j);",
-     "if (d_ro) grad += 0.0;"),
-    ("bwd weight dropped", "g[j] = dyr[j] * wd[j];", "g[j] = dyr[j];"),
+    ("residual gradient subtracted",
+     "double grad = s * (g[j] - xhat[j] * c);\n            if (d_ro) grad += element(d_ro, d_ro_dt, i * N + j);",
+     "double grad = s * (g[j] - xhat[j] * c);\n            if (d_ro) grad -= element(d_ro, d_ro_dt, i * N + j);"),
+    ("residual gradient dropped",
+     "double grad = s * (g[j] - xhat[j] * c);\n            if (d_ro) grad += element(d_ro, d_ro_dt, i * N + j);",
+     "double grad = s * (g[j] - xhat[j] * c);\n            if (d_ro) grad += 0.0;"),
+    ("LN residual gradient dropped",
+     "double grad = s * (g[j] - mg - xhat[j] * mgx);\n            if (d_ro) grad += element(d_ro, d_ro_dt, i * N + j);",
+     "double grad = s * (g[j] - mg - xhat[j] * mgx);\n            if (d_ro) grad += 0.0;"),
+    ("bwd weight dropped", "g[j] = dyr[j] * wd[j];\n            dot", "g[j] = dyr[j];\n            dot"),
+    ("LN bwd weight dropped", "g[j] = dyr[j] * wd[j];\n            sum_g", "g[j] = dyr[j];\n            sum_g"),
     ("projection not averaged", "double c = dot / (double)N;", "double c = dot;"),
-    ("dw uses x, not xhat", "if (dw) dw[j] += dyr[j] * xhat[j];", "if (dw) dw[j] += dyr[j] * xr[j];"),
-    ("dw not summed over rows", "if (dw) dw[j] += dyr[j] * xhat[j];", "if (dw) dw[j] = dyr[j] * xhat[j];"),
-    ("dx and dy rows transposed", "dyr[j] = element(dy, dy_dt, i * N + j);",
-     "dyr[j] = element(dy, dy_dt, j * M + i);"),
+    ("dw uses x, not xhat", "if (dw) dw[j] += dyr[j] * xhat[j];\n        }",
+     "if (dw) dw[j] += dyr[j] * xr[j];\n        }"),
+    ("dw not summed over rows", "if (dw) dw[j] += dyr[j] * xhat[j];\n        }",
+     "if (dw) dw[j] = dyr[j] * xhat[j];\n        }"),
+    ("dx and dy rows transposed", "dyr[j] = element(dy, dy_dt, i * N + j);\n        }\n        double s = row_rstd",
+     "dyr[j] = element(dy, dy_dt, j * M + i);\n        }\n        double s = row_rstd"),
+    ("LN mean not subtracted in y", "if (y) y[i * N + j] = (r[j] - mu) * s * wd[j] + bd[j];",
+     "if (y) y[i * N + j] = r[j] * s * wd[j] + bd[j];"),
+    ("LN bias dropped", "if (y) y[i * N + j] = (r[j] - mu) * s * wd[j] + bd[j];",
+     "if (y) y[i * N + j] = (r[j] - mu) * s * wd[j];"),
+    ("LN variance about zero", "for (int64_t j = 0; j < N; ++j) sq += (r[j] - mu) * (r[j] - mu);",
+     "for (int64_t j = 0; j < N; ++j) sq += r[j] * r[j];"),
+    ("LN bwd mean(g) dropped", "double grad = s * (g[j] - mg - xhat[j] * mgx);",
+     "double grad = s * (g[j] - xhat[j] * mgx);"),
+    ("LN bwd projection sign", "double grad = s * (g[j] - mg - xhat[j] * mgx);",
+     "double grad = s * (g[j] - mg + xhat[j] * mgx);"),
+    ("LN db not summed", "if (db) db[j] += dyr[j];", "if (db) db[j] = dyr[j];"),
+    ("LN dw from x, not xhat", "if (dw) dw[j] += dyr[j] * xhat[j];\n            if (db)",
+     "if (dw) dw[j] += dyr[j] * xr[j];\n            if (db)"),
 ]
 
 
