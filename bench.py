@@ -352,6 +352,99 @@ def run_ours(args, world, rank, local):
     return out
 
 
+# ------------------------------------------------------------------ per-shape table
+BY_SHAPE = [
+    "rmsnorm_fwd_256x1024_bf16", "add_rmsnorm_fwd_4096x4096_bf16",
+    "add_rmsnorm_fwd_16384x4096_bf16", "add_rmsnorm_fwd_16384x7168_bf16",
+    "rmsnorm_fwd_1x8192_bf16", "rmsnorm_fwd_8x8192_bf16", "rmsnorm_fwd_32x8192_bf16",
+    "rmsnorm_fwd_64x8192_bf16", "rmsnorm_fwd_1x8192_f32", "rmsnorm_fwd_8x8192_f32",
+    "rmsnorm_fwd_32x8192_f32", "rmsnorm_fwd_64x8192_f32", "rmsnorm_fwd_65536x2048_bf16",
+    "rmsnorm_fwd_65536x2048_f32", "rmsnorm_bwd_16384x4096_bf16", "add_rmsnorm_bwd_16384x4096_bf16",
+    "add_layernorm_fwd_16384x4096_bf16", "layernorm_bwd_16384x4096_bf16",
+]
+L2_BYTES = 129 * 2 ** 20
+
+
+def dev_tensor(a: np.ndarray, device) -> torch.Tensor:
+    if a.dtype == np.float32:
+        return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    return as_dev(a, device)
+
+
+def measure_shape(name: str, dev, reps: int):
+    """Median per-launch time of one workload through the C ABI (automatic launch). Inputs
+    are rotated across enough buffer sets to exceed 3x L2, or L2 is flushed (a 512 MB write
+    outside the timed launch) when one set is too small for that."""
+    import residual_rmsnorm_row_gb300 as rrn
+
+    wl = synth.get(name)
+    h = synth.make(wl)
+    nbytes = synth.min_bytes(wl)
+    nsets = int(min(8, max(1, -(-3 * L2_BYTES // max(nbytes, 1)))))
+    flush = nbytes * nsets < 3 * L2_BYTES
+    scrub = torch.empty(512 * 2 ** 20, dtype=torch.uint8, device=dev) if flush else None
+    w = dev_tensor(h["w"], dev)
+    b = dev_tensor(h["b"], dev) if "b" in h else None
+    M, N = wl.M, wl.N
+    sets = []
+    for k in range(nsets):
+        t = {key: dev_tensor(h[key], dev).roll(k, 0).contiguous()
+             for key in ("x", "residual", "dy", "d_ro") if key in h}
+        sets.append(t)
+    ws = torch.empty(max(rrn.rmsnorm_bwd_workspace_bytes(M, N, w.dtype),
+                         rrn.layernorm_bwd_workspace_bytes(M, N, w.dtype), 16) // 4, device=dev)
+    f32 = lambda n: torch.empty(n, device=dev)  # noqa: E731
+    outs = [dict(y=torch.empty_like(s["x"]), ro=torch.empty_like(s["x"]), rstd=f32(M), mean=f32(M),
+                 dw=f32(N), db=f32(N)) for s in sets]
+    if wl.op in ("rmsnorm_bwd", "add_rmsnorm_bwd", "layernorm_bwd"):
+        for s in sets:   # the forward statistics the backward consumes
+            if wl.op == "layernorm_bwd":
+                _, s["mean"], s["rstd"] = rrn.layer_norm(s["x"], w, None, wl.eps)
+            else:
+                _, s["rstd"] = rrn.rms_norm(s["x"], w, wl.eps)
+
+    def run(i):
+        s, o = sets[i % nsets], outs[i % nsets]
+        if wl.op == "rmsnorm_fwd":
+            rrn.rmsnorm_fwd(s["x"], w, o["y"], o["rstd"], wl.eps)
+        elif wl.op == "add_rmsnorm_fwd":
+            rrn.add_rmsnorm_fwd(s["x"], s["residual"], o["ro"], w, o["y"], o["rstd"], wl.eps)
+        elif wl.op == "rmsnorm_bwd":
+            rrn.rmsnorm_bwd(s["dy"], s["x"], w, s["rstd"], o["y"], o["dw"], ws, wl.eps)
+        elif wl.op == "add_rmsnorm_bwd":
+            rrn.add_rmsnorm_bwd(s["dy"], s["d_ro"], s["x"], w, s["rstd"], o["y"], o["dw"], ws, wl.eps)
+        elif wl.op == "add_layernorm_fwd":
+            rrn.layernorm_fwd(s["x"], w, b, o["y"], o["mean"], o["rstd"], wl.eps,
+                              residual=s["residual"], residual_out=o["ro"])
+        elif wl.op == "layernorm_bwd":
+            rrn.layernorm_bwd(s["dy"], s["d_ro"], s["x"], w, s["mean"], s["rstd"], o["y"], o["dw"],
+                              o["db"], ws, wl.eps)
+
+    for i in range(3):
+        run(i)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        if flush:
+            scrub.zero_()
+        ev[i][0].record()
+        run(i)
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    us = float(np.median([a.elapsed_time(c) for a, c in ev])) * 1e3
+    peak, _ = hbm_peak()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    if "layernorm" in wl.op:
+        plan = "layernorm planner (row_cta or stream)"
+    elif wl.op in ("rmsnorm_bwd", "add_rmsnorm_bwd"):
+        plan = rrn.plan_bwd(sets[0]["dy"], sets[0]["x"], w, outs[0]["y"]).name
+    else:
+        plan = rrn.plan_fwd(sets[0]["x"], sets[0].get("residual"), outs[0]["ro"], w, outs[0]["y"]).name
+    return {"workload": name, "op": wl.op, "M": M, "N": N, "dtype": wl.dtype, "us": round(us, 2),
+            "gbps": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "rows_per_s": round(M / (us * 1e-6), 1), "min_bytes": nbytes,
+            "l2": "flushed" if flush else f"{nsets} rotating sets", "launch": plan}
+
+
 # ------------------------------------------------------------------ the oracle (CPU)
 def oracle_sample(target_s: float, rows_cap: int = 16384):
     """Time the fp64 CPU oracle on row samples of the same workload until ~target_s seconds."""
@@ -436,6 +529,9 @@ def main():
     ap.add_argument("--only", choices=["step", "fwd", "bwd"], default="step",
                     help="time the whole step (default) or one kernel alone (for profiling)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    ap.add_argument("--no-by-shape", action="store_true",
+                    help="skip the per-shape table (every named workload timed alone)")
+    ap.add_argument("--by-shape-reps", type=int, default=50)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -446,6 +542,10 @@ def main():
             print(json.dumps(out), flush=True)
         return
     out = run_ours(args, world, rank, local)
+    if not args.no_by_shape and args.only == "step":
+        dev = torch.device("cuda", local)
+        out["by_shape"] = [measure_shape(n, dev, args.by_shape_reps) for n in BY_SHAPE]
+        torch.cuda.empty_cache()
     if rank == 0:
         out["cpu_baseline"] = (oracle_sample(args.cpu_baseline_seconds)
                                if world == 1 and args.cpu_baseline_seconds > 0 else None)

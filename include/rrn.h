@@ -156,6 +156,44 @@ RRN_API int add_rmsnorm_bwd(const void *dy, const void *d_residual_out, const vo
                             void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
                             float eps, int dtype, rrn_stream_t stream);
 
+/*
+ * LayerNorm, the mean-subtracting variant (the CuTe DSL skill page lists a "CTA norm
+ * (LayerNorm)" example in its "Workflow 0" example index). Per row of r = x (+ residual):
+ *     mean = mean_j(r_j),  rstd = 1 / sqrt( mean_j((r_j - mean)^2) + eps ),
+ *     y_j  = (r_j - mean) * rstd * w_j + b_j
+ * computed in fp32 with the variance taken about the mean (two passes over the row).
+ *
+ * layernorm_fwd / add_layernorm_fwd
+ *   x, residual, residual_out, w, y, rstd   as for rmsnorm_fwd / add_rmsnorm_fwd.
+ *   b      [N] dtype, read; may be NULL (no bias).
+ *   mean   [M] fp32, written; may be NULL.
+ * add_layernorm_fwd_ex takes residual == NULL for the plain op and an explicit launch
+ * configuration (RRN_VARIANT_ROW_CTA or RRN_VARIANT_STREAM).
+ *
+ * layernorm_bwd - dx = rstd * (g - mean(g) - xhat * mean(g * xhat)) (+ d_residual_out),
+ *   g = dy * w, xhat = (x - mean) * rstd;  dw = sum_rows dy * xhat;  db = sum_rows dy.
+ *   dy              [M, N] dtype, read.
+ *   d_residual_out  [M, N] dtype, read; may be NULL (plain op, or no gradient at residual_out).
+ *   x               [M, N] dtype, read: the forward input (the stored residual_out when fused).
+ *   w               [N] dtype, read.   mean, rstd  [M] fp32, read (as the forward wrote them).
+ *   dx              [M, N] dtype, written (may alias dy, d_residual_out or x).
+ *   dw, db          [N] fp32, overwritten; db may be NULL.
+ *   workspace       at least layernorm_bwd_workspace_bytes(M, N, dtype) bytes (twice the
+ *                   RMSNorm workspace: dw and db partials), 16-byte aligned.
+ * Each returns an rrn_status.
+ */
+RRN_API int layernorm_fwd(const void *x, const void *w, const void *b, void *y, float *mean,
+                          float *rstd, int64_t M, int64_t N, float eps, int dtype,
+                          rrn_stream_t stream);
+RRN_API int add_layernorm_fwd(const void *x, const void *residual, void *residual_out,
+                              const void *w, const void *b, void *y, float *mean, float *rstd,
+                              int64_t M, int64_t N, float eps, int dtype, rrn_stream_t stream);
+RRN_API int layernorm_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t *bytes);
+RRN_API int layernorm_bwd(const void *dy, const void *d_residual_out, const void *x,
+                          const void *w, const float *mean, const float *rstd, void *dx,
+                          float *dw, float *db, void *workspace, size_t workspace_bytes,
+                          int64_t M, int64_t N, float eps, int dtype, rrn_stream_t stream);
+
 /* rrn_status_string - static, NUL-terminated description of a status code. */
 RRN_API const char *rrn_status_string(int status);
 
@@ -229,6 +267,17 @@ RRN_API int rrn_plan_bwd(const void *dy, const void *x, const void *w, const voi
 RRN_API int add_rmsnorm_fwd_ex(const void *x, const void *residual, void *residual_out,
                                const void *w, void *y, float *rstd, int64_t M, int64_t N,
                                float eps, int dtype, const rrn_launch *cfg, rrn_stream_t stream);
+
+/* LayerNorm with an explicit launch configuration (row-per-CTA or two-pass variants). */
+RRN_API int add_layernorm_fwd_ex(const void *x, const void *residual, void *residual_out,
+                                 const void *w, const void *b, void *y, float *mean, float *rstd,
+                                 int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,
+                                 rrn_stream_t stream);
+RRN_API int layernorm_bwd_ex(const void *dy, const void *d_residual_out, const void *x,
+                             const void *w, const float *mean, const float *rstd, void *dx,
+                             float *dw, float *db, void *workspace, size_t workspace_bytes,
+                             int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,
+                             rrn_stream_t stream);
 
 /* rmsnorm_bwd_ex / add_rmsnorm_bwd_ex - the backward calls with an explicit stage-1 launch
  * configuration (see above). The workspace must hold cfg->ctas * N fp32 values (at most M * N;

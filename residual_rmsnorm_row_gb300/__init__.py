@@ -33,6 +33,9 @@ from ._binding import (  # noqa: F401  (re-exported API)
     add_rmsnorm_fwd,
     add_rmsnorm_fwd_ex,
     device_faults,
+    layernorm_bwd,
+    layernorm_bwd_workspace_bytes,
+    layernorm_fwd,
     load_library,
     plan_bwd,
     plan_fwd,
@@ -99,6 +102,36 @@ def add_rms_norm_backward(dy: torch.Tensor, d_residual_out: Optional[torch.Tenso
     return d_r, dw
 
 
+def layer_norm(x: torch.Tensor, w: torch.Tensor, b: Optional[torch.Tensor] = None,
+               eps: float = 1e-5, residual: Optional[torch.Tensor] = None, stream=None):
+    """Return ``(y, mean, rstd)``, or ``(y, residual_out, mean, rstd)`` with ``residual``."""
+    M = x.numel() // x.shape[-1]
+    y = torch.empty_like(x)
+    mean = torch.empty(M, device=x.device, dtype=torch.float32)
+    rstd = torch.empty(M, device=x.device, dtype=torch.float32)
+    if residual is None:
+        layernorm_fwd(x, w, b, y, mean, rstd, eps, stream=stream)
+        return y, mean, rstd
+    residual_out = torch.empty_like(x)
+    layernorm_fwd(x, w, b, y, mean, rstd, eps, residual=residual, residual_out=residual_out,
+                  stream=stream)
+    return y, residual_out, mean, rstd
+
+
+def layer_norm_backward(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, mean: torch.Tensor,
+                        rstd: torch.Tensor, eps: float = 1e-5,
+                        d_residual_out: Optional[torch.Tensor] = None, stream=None):
+    """Return ``(dx, dw, db)`` (dx is the gradient w.r.t. x + residual when fused)."""
+    M, N = x.numel() // x.shape[-1], x.shape[-1]
+    dx = torch.empty_like(x)
+    dw = torch.empty(N, device=x.device, dtype=torch.float32)
+    db = torch.empty(N, device=x.device, dtype=torch.float32)
+    nbytes = layernorm_bwd_workspace_bytes(M, N, x.dtype)
+    ws = torch.empty(max(nbytes, 16) // 4, device=x.device, dtype=torch.float32)
+    layernorm_bwd(dy, d_residual_out, x, w, mean, rstd, dx, dw, db, ws, eps, stream=stream)
+    return dx, dw, db
+
+
 class RMSNormFunction(torch.autograd.Function):
     """y = RMSNorm(x) * w with the library's forward and backward kernels."""
 
@@ -162,4 +195,6 @@ __all__ = [
     "add_rmsnorm_fwd_ex", "rmsnorm_bwd_ex", "plan_fwd", "plan_bwd", "Launch", "RRNError",
     "load_library", "rms_norm", "add_rms_norm", "rms_norm_backward", "device_faults",
     "add_rmsnorm_bwd", "add_rms_norm_backward", "RMSNormFunction", "AddRMSNormFunction", "RMSNorm",
+    "layernorm_fwd", "layernorm_bwd", "layernorm_bwd_workspace_bytes", "layer_norm",
+    "layer_norm_backward",
 ]

@@ -96,6 +96,16 @@ _SIGNATURES = {
                               ctypes.POINTER(rrn_launch), _vp]),
     "add_rmsnorm_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _f32, _i32,
                                _vp]),
+    "layernorm_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32, _vp]),
+    "add_layernorm_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32,
+                                 _vp]),
+    "add_layernorm_fwd_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32,
+                                    ctypes.POINTER(rrn_launch), _vp]),
+    "layernorm_bwd_workspace_bytes": (_i32, [_i64, _i64, _i32, ctypes.POINTER(_sz)]),
+    "layernorm_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64,
+                             _f32, _i32, _vp]),
+    "layernorm_bwd_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64,
+                                _f32, _i32, ctypes.POINTER(rrn_launch), _vp]),
     "add_rmsnorm_bwd_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _f32,
                                   _i32, ctypes.POINTER(rrn_launch), _vp]),
 }
@@ -283,6 +293,75 @@ def add_rmsnorm_bwd(dy: torch.Tensor, d_residual_out: Optional[torch.Tensor],
         _check(lib.add_rmsnorm_bwd(*args, _stream(stream)))
     else:
         _check(lib.add_rmsnorm_bwd_ex(*args, ctypes.byref(launch.to_c()), _stream(stream)))
+
+
+def _opt(t: Optional[torch.Tensor], name: str) -> Optional[int]:
+    return None if t is None else _mat(t, name)
+
+
+def layernorm_fwd(x: torch.Tensor, w: torch.Tensor, b: Optional[torch.Tensor], y: torch.Tensor,
+                  mean: Optional[torch.Tensor], rstd: Optional[torch.Tensor], eps: float,
+                  residual: Optional[torch.Tensor] = None,
+                  residual_out: Optional[torch.Tensor] = None, launch: Optional[Launch] = None,
+                  stream=None) -> None:
+    """C ``layernorm_fwd`` / ``add_layernorm_fwd`` (with ``residual``) / ``add_layernorm_fwd_ex``
+    (with ``launch``): y = (r - mean) * rstd * w + b for r = x (+ residual)."""
+    M, N = _rows(x)
+    _same(x, y, "y")
+    if residual is not None:
+        _same(x, residual, "residual")
+        _same(x, residual_out, "residual_out")
+    for t, n in ((w, "w"), (b, "b")):
+        if t is not None and (t.shape != (N,) or t.dtype != x.dtype):
+            raise ValueError(f"{n} must have shape (N,) and the dtype of x")
+    for t, n in ((mean, "mean"), (rstd, "rstd")):
+        if t is not None and t.numel() != M:
+            raise ValueError(f"{n} must hold M values")
+    lib = load_library()
+    px, pw, pb, py = _mat(x, "x", N), _mat(w, "w"), _opt(b, "b"), _mat(y, "y")
+    pm, pr = _vec(mean, "mean"), _vec(rstd, "rstd")
+    if launch is not None:
+        _check(lib.add_layernorm_fwd_ex(px, _opt(residual, "residual"), _opt(residual_out, "residual_out"),
+                                        pw, pb, py, pm, pr, M, N, float(eps), _dtype(x),
+                                        ctypes.byref(launch.to_c()), _stream(stream)))
+    elif residual is not None:
+        _check(lib.add_layernorm_fwd(px, _mat(residual, "residual"), _mat(residual_out, "residual_out"),
+                                     pw, pb, py, pm, pr, M, N, float(eps), _dtype(x), _stream(stream)))
+    else:
+        _check(lib.layernorm_fwd(px, pw, pb, py, pm, pr, M, N, float(eps), _dtype(x), _stream(stream)))
+
+
+def layernorm_bwd_workspace_bytes(M: int, N: int, dtype: torch.dtype) -> int:
+    """C ``layernorm_bwd_workspace_bytes`` for the current device."""
+    out = ctypes.c_size_t(0)
+    _check(load_library().layernorm_bwd_workspace_bytes(int(M), int(N), _DTYPES[dtype],
+                                                        ctypes.byref(out)))
+    return int(out.value)
+
+
+def layernorm_bwd(dy: torch.Tensor, d_residual_out: Optional[torch.Tensor], x: torch.Tensor,
+                  w: torch.Tensor, mean: torch.Tensor, rstd: torch.Tensor, dx: torch.Tensor,
+                  dw: torch.Tensor, db: Optional[torch.Tensor], workspace: torch.Tensor,
+                  eps: float, launch: Optional[Launch] = None, stream=None) -> None:
+    """C ``layernorm_bwd`` (``_ex`` with ``launch``)."""
+    M, N = _rows(x)
+    _same(x, dy, "dy")
+    _same(x, dx, "dx")
+    if d_residual_out is not None:
+        _same(x, d_residual_out, "d_residual_out")
+    if w.shape != (N,) or w.dtype != x.dtype:
+        raise ValueError("w must have shape (N,) and the dtype of x")
+    if mean.numel() != M or rstd.numel() != M or dw.numel() != N or (db is not None and db.numel() != N):
+        raise ValueError("mean/rstd must hold M values, dw/db N values")
+    args = [_mat(dy, "dy", N), _opt(d_residual_out, "d_residual_out"), _mat(x, "x"), _mat(w, "w"),
+            _vec(mean, "mean"), _vec(rstd, "rstd"), _mat(dx, "dx"), _vec(dw, "dw"), _vec(db, "db"),
+            _mat(workspace, "workspace"), workspace.numel() * workspace.element_size(), M, N,
+            float(eps), _dtype(x)]
+    lib = load_library()
+    if launch is None:
+        _check(lib.layernorm_bwd(*args, _stream(stream)))
+    else:
+        _check(lib.layernorm_bwd_ex(*args, ctypes.byref(launch.to_c()), _stream(stream)))
 
 
 def plan_fwd(x: torch.Tensor, residual: Optional[torch.Tensor] = None,

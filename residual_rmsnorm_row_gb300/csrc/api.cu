@@ -114,6 +114,26 @@ int occupancy(bool bwd, int dtype, bool fused, const Launch &l) {
     return n;
 }
 
+// Occupancy of a LayerNorm kernel (same cache; the key's `bwd` slot holds 2 + bwd).
+int occupancy_ln(bool bwd, int dtype, bool flag, const Launch &l) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    const auto key = std::make_tuple(dev, 2 + (bwd ? 1 : 0), dtype, flag ? 1 : 0, l.variant, l.vpt,
+                                     l.threads, l.vec ? 1 : 0, l.smem);
+    {
+        std::lock_guard<std::mutex> g(g_occ_mutex);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) return it->second;
+    }
+    int n = dtype == RRN_BF16 ? occupancy_ln_bf16(bwd, flag, l) : occupancy_ln_f32(bwd, flag, l);
+    std::lock_guard<std::mutex> g(g_occ_mutex);
+    g_occ[key] = n;
+    return n;
+}
+
 // ---------------------------------------------------------------- argument checks
 int elem_size(int dtype) { return dtype == RRN_BF16 ? 2 : dtype == RRN_F32 ? 4 : 0; }
 
@@ -462,6 +482,147 @@ int run_bwd(const void *dy, const void *d_ro, const void *x, const void *w, cons
     return RRN_OK;
 }
 
+// ---------------------------------------------------------------- LayerNorm
+// Register layout (vpt, threads) for a row of nvec vectors, as the RMSNorm planners choose it:
+// the widest CTA for few rows, about kFwdTargetThreads threads otherwise.
+int pick_row_layout(int64_t nvec, int64_t M, int sms, const rrn_launch *cfg, int max_vpt,
+                    int (*max_threads)(int), Launch *l) {
+    if (cfg && cfg->vpt) {
+        l->vpt = cfg->vpt;
+    } else {
+        l->vpt = M < 2LL * sms ? 1 : ceil_pow2_vpt((nvec + kFwdTargetThreads - 1) / kFwdTargetThreads, max_vpt);
+        while (l->vpt < max_vpt && nvec > static_cast<int64_t>(l->vpt) * max_threads(l->vpt)) l->vpt *= 2;
+    }
+    if (l->vpt < 1 || l->vpt > max_vpt || (l->vpt & (l->vpt - 1))) return RRN_ERR_CONFIG;
+    l->threads = cfg && cfg->threads ? cfg->threads : round_up32((nvec + l->vpt - 1) / l->vpt);
+    if (l->threads < 32 || l->threads % 32 || l->threads > max_threads(l->vpt)) return RRN_ERR_CONFIG;
+    if (static_cast<int64_t>(l->vpt) * l->threads < nvec) return RRN_ERR_CONFIG;
+    return RRN_OK;
+}
+
+int fwd_threads_limit(int vpt) { return fwd_max_threads(vpt); }
+int bwd_threads_limit(int vpt) { return bwd_max_threads(vpt); }
+
+int plan_ln_fwd(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const rrn_launch *cfg,
+                Launch *out) {
+    const int64_t nvec = N / (16 / elem_size(dtype));
+    int sms = 0;
+    int st = current_sm_count(&sms);
+    if (st != RRN_OK) return st;
+    Launch l{};
+    l.variant = cfg && cfg->variant ? cfg->variant : RRN_VARIANT_AUTO;
+    if (l.variant == RRN_VARIANT_AUTO)
+        l.variant = vec_ok && nvec <= kRowCtaMaxVec ? RRN_VARIANT_ROW_CTA : RRN_VARIANT_STREAM;
+    l.vec = l.variant == RRN_VARIANT_STREAM ? vec_ok : true;
+    if (l.variant == RRN_VARIANT_ROW_CTA) {
+        if (!vec_ok) return RRN_ERR_CONFIG;
+        st = pick_row_layout(nvec, M, sms, cfg, kMaxVpt, fwd_threads_limit, &l);
+        if (st != RRN_OK) return st;
+        l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid(M);
+    } else if (l.variant == RRN_VARIANT_STREAM) {
+        l.vpt = 1;
+        const int64_t chunks = l.vec ? nvec : N;
+        l.threads = cfg && cfg->threads ? cfg->threads : (chunks >= 512 ? 512 : round_up32(chunks));
+        if (l.threads < 32 || l.threads % 32 || l.threads > 1024) return RRN_ERR_CONFIG;
+        if (cfg && cfg->ctas) {
+            l.ctas = cfg->ctas;
+        } else {
+            const int occ = occupancy_ln(false, dtype, fused, l);
+            const int64_t cap = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
+            l.ctas = clamp_grid(M < cap ? M : cap);
+        }
+    } else {
+        return RRN_ERR_CONFIG;  // LayerNorm runs the row-per-CTA and two-pass variants
+    }
+    if (l.ctas < 1) return RRN_ERR_CONFIG;
+    *out = l;
+    return RRN_OK;
+}
+
+int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, const rrn_launch *cfg,
+                Launch *out, int64_t *rows_per_cta) {
+    const int64_t nvec = N / (16 / elem_size(dtype));
+    int sms = 0;
+    int st = current_sm_count(&sms);
+    if (st != RRN_OK) return st;
+    Launch l{};
+    l.variant = cfg && cfg->variant ? cfg->variant : RRN_VARIANT_AUTO;
+    if (l.variant == RRN_VARIANT_AUTO)
+        l.variant = vec_ok && nvec <= static_cast<int64_t>(kBwdMaxVpt) * bwd_max_threads(kBwdMaxVpt)
+                        ? RRN_VARIANT_ROW_CTA
+                        : RRN_VARIANT_STREAM;
+    l.vec = l.variant == RRN_VARIANT_STREAM ? vec_ok : true;
+    if (l.variant == RRN_VARIANT_ROW_CTA) {
+        if (!vec_ok) return RRN_ERR_CONFIG;
+        st = pick_row_layout(nvec, 1LL << 40, sms, cfg, kBwdMaxVpt, bwd_threads_limit, &l);
+        if (st != RRN_OK) return st;
+    } else if (l.variant == RRN_VARIANT_STREAM) {
+        l.vpt = 1;
+        const int64_t chunks = l.vec ? nvec : N;
+        l.threads = cfg && cfg->threads ? cfg->threads : (chunks >= 512 ? 512 : round_up32(chunks));
+        if (l.threads < 32 || l.threads % 32 || l.threads > 1024) return RRN_ERR_CONFIG;
+    } else {
+        return RRN_ERR_CONFIG;
+    }
+    int64_t want = cfg && cfg->ctas ? cfg->ctas : 0;
+    if (!want) {
+        const int occ = occupancy_ln(true, dtype, add_grad, l);
+        want = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
+    }
+    if (want < 1) return RRN_ERR_CONFIG;
+    if (M == 0) {
+        l.ctas = 0;
+        *rows_per_cta = 0;
+    } else {
+        if (want > M) want = M;
+        const int64_t rpc = (M + want - 1) / want;
+        l.ctas = clamp_grid((M + rpc - 1) / rpc);
+        *rows_per_cta = rpc;
+    }
+    *out = l;
+    return RRN_OK;
+}
+
+int run_ln_fwd(const void *x, const void *res, void *res_out, const void *w, const void *b,
+               void *y, float *mean, float *rstd, int64_t M, int64_t N, float eps, int dtype,
+               const rrn_launch *cfg, cudaStream_t stream) {
+    int st = check_fwd(x, res, res_out, w, y, rstd, M, N, eps, dtype);
+    if (st != RRN_OK) return st;
+    if ((b && !aligned(b, elem_size(dtype))) || (mean && !aligned(mean, 4))) return RRN_ERR_ALIGN;
+    if (M == 0) return RRN_OK;
+    Launch l;
+    st = plan_ln_fwd(vec_path_ok({x, res, res_out, w, b, y}, N, dtype), res != nullptr, M, N, dtype,
+                     cfg, &l);
+    if (st != RRN_OK) return st;
+    LnFwdArgs a{x, res, res ? res_out : nullptr, w, b, y, mean, rstd, M, static_cast<int>(N), eps};
+    cudaError_t e = dtype == RRN_BF16 ? launch_ln_fwd_bf16(a, l, stream) : launch_ln_fwd_f32(a, l, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return RRN_OK;
+}
+
+int run_ln_bwd(const void *dy, const void *d_ro, const void *x, const void *w, const float *mean,
+               const float *rstd, void *dx, float *dw, float *db, void *workspace,
+               size_t workspace_bytes, int64_t M, int64_t N, float eps, int dtype,
+               const rrn_launch *cfg, cudaStream_t stream) {
+    int st = check_bwd(dy, d_ro, x, w, rstd, dx, dw, M, N, eps, dtype);
+    if (st != RRN_OK) return st;
+    if (!mean) return RRN_ERR_NULL;
+    if (!aligned(mean, 4) || (db && !aligned(db, 4))) return RRN_ERR_ALIGN;
+    if (M == 0) return RRN_OK;
+    Launch l;
+    int64_t rpc = 0;
+    st = plan_ln_bwd(vec_path_ok({dy, d_ro, x, w, dx}, N, dtype), d_ro != nullptr, M, N, dtype, cfg,
+                     &l, &rpc);
+    if (st != RRN_OK) return st;
+    const size_t need = 2 * static_cast<size_t>(l.ctas) * static_cast<size_t>(N) * sizeof(float);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return RRN_ERR_WORKSPACE;
+    LnBwdArgs a{dy, d_ro, x, w, mean, rstd, dx, dw, db, static_cast<float *>(workspace), M,
+                static_cast<int>(N), rpc};
+    cudaError_t e = dtype == RRN_BF16 ? launch_ln_bwd_bf16(a, l, stream) : launch_ln_bwd_f32(a, l, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return RRN_OK;
+}
+
 void to_public(const Launch &l, rrn_launch *out) {
     out->variant = l.variant;
     out->vpt = l.vpt;
@@ -598,6 +759,68 @@ RRN_API int rrn_plan_bwd(const void *dy, const void *x, const void *w, const voi
     if (st != RRN_OK) return st;
     to_public(l, out);
     return RRN_OK;
+}
+
+RRN_API int layernorm_fwd(const void *x, const void *w, const void *b, void *y, float *mean,
+                          float *rstd, int64_t M, int64_t N, float eps, int dtype,
+                          rrn_stream_t stream) {
+    return run_ln_fwd(x, nullptr, nullptr, w, b, y, mean, rstd, M, N, eps, dtype, nullptr,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+RRN_API int add_layernorm_fwd(const void *x, const void *residual, void *residual_out,
+                              const void *w, const void *b, void *y, float *mean, float *rstd,
+                              int64_t M, int64_t N, float eps, int dtype, rrn_stream_t stream) {
+    if (!residual) return RRN_ERR_NULL;
+    return run_ln_fwd(x, residual, residual_out, w, b, y, mean, rstd, M, N, eps, dtype, nullptr,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+RRN_API int add_layernorm_fwd_ex(const void *x, const void *residual, void *residual_out,
+                                 const void *w, const void *b, void *y, float *mean, float *rstd,
+                                 int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,
+                                 rrn_stream_t stream) {
+    return run_ln_fwd(x, residual, residual_out, w, b, y, mean, rstd, M, N, eps, dtype, cfg,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+RRN_API int layernorm_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t *bytes) {
+    if (!bytes) return RRN_ERR_NULL;
+    int st = check_common(M, N, 0.f, dtype);
+    if (st != RRN_OK) return st;
+    if (M == 0) {
+        *bytes = 0;
+        return RRN_OK;
+    }
+    int ctas = 0;
+    const bool vec_possible = N % (16 / elem_size(dtype)) == 0;
+    for (int vec = 0; vec < (vec_possible ? 2 : 1); ++vec)
+        for (int add = 0; add < 2; ++add) {
+            Launch l;
+            int64_t rpc = 0;
+            st = plan_ln_bwd(vec != 0, add != 0, M, N, dtype, nullptr, &l, &rpc);
+            if (st != RRN_OK) return st;
+            if (l.ctas > ctas) ctas = l.ctas;
+        }
+    *bytes = 2 * static_cast<size_t>(ctas) * static_cast<size_t>(N) * sizeof(float);
+    return RRN_OK;
+}
+
+RRN_API int layernorm_bwd(const void *dy, const void *d_residual_out, const void *x,
+                          const void *w, const float *mean, const float *rstd, void *dx,
+                          float *dw, float *db, void *workspace, size_t workspace_bytes,
+                          int64_t M, int64_t N, float eps, int dtype, rrn_stream_t stream) {
+    return run_ln_bwd(dy, d_residual_out, x, w, mean, rstd, dx, dw, db, workspace, workspace_bytes,
+                      M, N, eps, dtype, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+RRN_API int layernorm_bwd_ex(const void *dy, const void *d_residual_out, const void *x,
+                             const void *w, const float *mean, const float *rstd, void *dx,
+                             float *dw, float *db, void *workspace, size_t workspace_bytes,
+                             int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,
+                             rrn_stream_t stream) {
+    return run_ln_bwd(dy, d_residual_out, x, w, mean, rstd, dx, dw, db, workspace, workspace_bytes,
+                      M, N, eps, dtype, cfg, reinterpret_cast<cudaStream_t>(stream));
 }
 
 RRN_API const char *rrn_status_string(int status) {

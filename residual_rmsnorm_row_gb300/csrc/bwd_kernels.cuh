@@ -311,9 +311,10 @@ __global__ void __launch_bounds__(1024) bwd_stream(const BwdArgs a) {
 // G = kReduceThreads / 32 row groups (one warp each); group g adds rows p = g, g + G, g + 2G, ...
 // in that order (eight loads in flight, the additions still in sequence), then one warp adds
 // the G group sums in group order. The order depends only on (P, N), so dw is reproducible.
-__global__ void __launch_bounds__(kReduceThreads)
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS)
     bwd_dw_reduce(const float *__restrict__ partial, float *__restrict__ dw, int P, int N) {
-    constexpr int G = kReduceThreads / 32;
+    constexpr int G = THREADS / 32;
     constexpr int U = 8;
     __shared__ float sums[G][33];
     const int lane = threadIdx.x & 31;
@@ -387,7 +388,7 @@ cudaError_t launch_bwd(const BwdArgs &a, const Launch &l, cudaStream_t stream) {
                                      static_cast<size_t>(l.smem), stream);
     if (e != cudaSuccess) return e;
     const int blocks = (a.N + 31) / 32;
-    bwd_dw_reduce<<<blocks, kReduceThreads, 0, stream>>>(a.partial, a.dw, l.ctas, a.N);
+    bwd_dw_reduce<kReduceThreads><<<blocks, kReduceThreads, 0, stream>>>(a.partial, a.dw, l.ctas, a.N);
     return cudaGetLastError();
 }
 

@@ -72,6 +72,22 @@ struct Elem<float> {
     }
 };
 
+// r = x (+ residual) in fp32 for one 128-bit vector of packed inputs. Recomputing it is exact
+// and cheap, so the kernels keep the row packed (4 registers per vector and tensor) instead of
+// holding an fp32 copy across the reduction.
+template <typename T, bool FUSED>
+__device__ __forceinline__ void r_of(const uint4 &xv, const uint4 &rv,
+                                     float (&f)[Elem<T>::kPerVec]) {
+    using E = Elem<T>;
+    E::unpack(xv, f);
+    if constexpr (FUSED) {
+        float b[E::kPerVec];
+        E::unpack(rv, b);
+#pragma unroll
+        for (int k = 0; k < E::kPerVec; ++k) f[k] += b[k];
+    }
+}
+
 // ----------------------------------------------------------------------------------------
 // Memory access. Row data is touched exactly once, so it is loaded and stored with the
 // streaming (evict-first) hint; the weight vector is re-read by every row and goes through

@@ -22,22 +22,6 @@
 
 namespace rrn {
 
-// r = x (+ residual) in fp32 for one 128-bit vector of packed inputs. Recomputing it is exact
-// and cheap, so the kernels keep the row packed (4 registers per vector and tensor) instead of
-// holding an fp32 copy across the reduction.
-template <typename T, bool FUSED>
-__device__ __forceinline__ void r_of(const uint4 &xv, const uint4 &rv,
-                                     float (&f)[Elem<T>::kPerVec]) {
-    using E = Elem<T>;
-    E::unpack(xv, f);
-    if constexpr (FUSED) {
-        float b[E::kPerVec];
-        E::unpack(rv, b);
-#pragma unroll
-        for (int k = 0; k < E::kPerVec; ++k) f[k] += b[k];
-    }
-}
-
 // The per-row work of the row-per-CTA variants, on a row already in registers: this thread
 // owns the 128-bit vectors c = v * blockDim.x + threadIdx.x (v < VPT, c < nvec) of x (xv) and
 // residual (rv), and the matching weight vectors (wv). Writes residual_out (fused), y and rstd.

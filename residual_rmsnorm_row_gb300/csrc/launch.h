@@ -42,6 +42,39 @@ struct BwdArgs {
     unsigned int *faults;    // the library's device fault word
 };
 
+// Arguments of one LayerNorm forward call (fused when res != nullptr; b may be nullptr).
+struct LnFwdArgs {
+    const void *x;
+    const void *res;
+    void *res_out;
+    const void *w;
+    const void *b;
+    void *y;
+    float *mean;  // may be nullptr
+    float *rstd;  // may be nullptr
+    int64_t M;
+    int N;
+    float eps;
+};
+
+// Arguments of one LayerNorm backward call. `partial` is the [2, P, N] fp32 workspace: dw
+// partials in the first half, db partials in the second. d_ro and db may be nullptr.
+struct LnBwdArgs {
+    const void *dy;
+    const void *d_ro;
+    const void *x;
+    const void *w;
+    const float *mean;
+    const float *rstd;
+    void *dx;
+    float *dw;
+    float *db;
+    float *partial;
+    int64_t M;
+    int N;
+    int64_t rows_per_cta;
+};
+
 // A resolved launch (all fields set).
 struct Launch {
     int variant;  // rrn_variant, never AUTO here
@@ -74,6 +107,14 @@ cudaError_t launch_fwd_bf16(const FwdArgs &a, const Launch &l, cudaStream_t stre
 cudaError_t launch_fwd_f32(const FwdArgs &a, const Launch &l, cudaStream_t stream);
 cudaError_t launch_bwd_bf16(const BwdArgs &a, const Launch &l, cudaStream_t stream);
 cudaError_t launch_bwd_f32(const BwdArgs &a, const Launch &l, cudaStream_t stream);
+
+cudaError_t launch_ln_fwd_bf16(const LnFwdArgs &a, const Launch &l, cudaStream_t stream);
+cudaError_t launch_ln_fwd_f32(const LnFwdArgs &a, const Launch &l, cudaStream_t stream);
+cudaError_t launch_ln_bwd_bf16(const LnBwdArgs &a, const Launch &l, cudaStream_t stream);
+cudaError_t launch_ln_bwd_f32(const LnBwdArgs &a, const Launch &l, cudaStream_t stream);
+// LayerNorm occupancy: bwd selects the kernel family, flag is FUSED (fwd) or ADDG (bwd).
+int occupancy_ln_bf16(bool bwd, bool flag, const Launch &l);
+int occupancy_ln_f32(bool bwd, bool flag, const Launch &l);
 
 // Occupancy (resident CTAs per SM) of the kernel a launch would run, with l.smem bytes of
 // dynamic shared memory; 0 on error.

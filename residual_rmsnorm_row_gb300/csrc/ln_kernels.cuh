@@ -1,0 +1,495 @@
+// LayerNorm kernels: the mean-subtracting variant of the row norm, on the same skeleton as the
+// RMSNorm kernels (the CuTe DSL skill page lists a "CTA norm (LayerNorm)" example in its
+// "Workflow 0" example index; the kernels here are this library's own design).
+//
+// Forward, per row of r = x (+ residual) in fp32:
+//   mean = sum(r) / N;  var = sum((r - mean)^2) / N  (corrected two-pass: no cancellation-prone
+//   sum of squares, and the first pass's rounding error in the mean is corrected);
+//   rstd = rsqrt(var + eps)
+//   y = RN((r - mean) * rstd * w + b);  residual_out = RN(r);  mean, rstd stored as fp32
+// Backward, with xhat = (x - mean) * rstd and g = dy * w:
+//   dx = rstd * (g - mean(g) - xhat * mean(g * xhat))  (+ d_ro, fused)
+//   dw = sum over rows of dy * xhat,  db = sum over rows of dy  (two fixed-order stages)
+#pragma once
+
+#include "bwd_kernels.cuh"
+#include "common.cuh"
+#include "launch.h"
+
+namespace rrn {
+
+// Sum of two floats over the CTA (one barrier); same fixed order as cta_sum.
+__device__ __forceinline__ float2 cta_sum2(float a, float b, float (*slots)[32]) {
+    a = warp_sum(a);
+    b = warp_sum(b);
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        slots[0][warp] = a;
+        slots[1][warp] = b;
+    }
+    __syncthreads();
+    const int nwarps = blockDim.x >> 5;
+    float2 t = make_float2(0.f, 0.f);
+    for (int i = 0; i < nwarps; ++i) {
+        t.x += slots[0][i];
+        t.y += slots[1][i];
+    }
+    return t;
+}
+
+// ------------------------------------------------------------------------------ forward
+// The row statistics from per-thread access to the row values: `each(fn)` calls fn(v) for
+// every fp32 value of the row this thread owns. Returns (mean, rstd).
+// Pass 1 gives a first mean m0 = sum(r) / N. Pass 2 sums d = r - m0 and d^2 together (one
+// barrier) and corrects both: mean = m0 + sum(d) / N and
+// sum((r - mean)^2) = sum(d^2) - sum(d)^2 / N (the corrected two-pass algorithm), so the
+// rounding error of m0 - which grows with |mean|, not with the spread - cancels out.
+// Reductions alternate between the two slot pairs (parity), as cta_sum callers do.
+template <typename Each>
+__device__ __forceinline__ float2 ln_stats(Each each, float n_f, float eps,
+                                           float (&slots)[2][2][32], int &parity) {
+    float s1 = 0.f;
+    each([&](float v) { s1 += v; });
+    s1 = cta_sum(s1, slots[parity][0]);
+    parity ^= 1;
+    float m0;
+    if (isfinite(s1)) {
+        m0 = s1 / n_f;
+    } else {  // rare: the sum overflowed fp32 - add the row scaled by a power of two
+        float am = 0.f;
+        each([&](float v) { am = fmaxf(am, fabsf(v)); });
+        am = cta_max(am, slots[parity][0]);
+        parity ^= 1;
+        const int e = rescale_exponent(am);
+        float t = 0.f;
+        each([&](float v) { t += ldexpf(v, -e); });
+        t = cta_sum(t, slots[parity][0]);
+        parity ^= 1;
+        m0 = ldexpf(t / n_f, e);
+    }
+    float d1 = 0.f, d2 = 0.f;
+    each([&](float v) {
+        const float d = v - m0;
+        d1 += d;
+        d2 = fmaf(d, d, d2);
+    });
+    const float2 t2 = cta_sum2(d1, d2, slots[parity]);
+    parity ^= 1;
+    const float mu = isfinite(t2.x) ? m0 + t2.x / n_f : m0;
+    float rs;
+    if (!needs_rescale(t2.y)) {
+        const float ssd = fmaxf(t2.y - t2.x * (t2.x / n_f), 0.f);
+        rs = rstd_plain(ssd, n_f, eps);
+    } else {  // rare: squared deviations out of fp32 range, or a constant row
+        float am = 0.f;
+        each([&](float v) { am = fmaxf(am, fabsf(v - mu)); });
+        am = cta_max(am, slots[parity][0]);
+        parity ^= 1;
+        const int e = rescale_exponent(am);
+        float t = 0.f;
+        each([&](float v) {
+            const float d = ldexpf(v - mu, -e);
+            t = fmaf(d, d, t);
+        });
+        t = cta_sum(t, slots[parity][0]);
+        parity ^= 1;
+        rs = rstd_rescaled(t, n_f, eps, e);
+    }
+    return make_float2(mu, rs);
+}
+
+template <typename T, int VPT, bool FUSED>
+__global__ void __launch_bounds__(fwd_max_threads(VPT)) ln_fwd_row_cta(const LnFwdArgs a) {
+    using E = Elem<T>;
+    constexpr int V = E::kPerVec;
+    __shared__ float slots[2][2][32];
+    const int nvec = a.N / V;
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const float n_f = static_cast<float>(a.N);
+
+    uint4 wv[VPT], bv[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * nthr + tid;
+        if (c < nvec) {
+            wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
+            bv[v] = a.b ? ld_keep(static_cast<const uint4 *>(a.b) + c) : make_uint4(0, 0, 0, 0);
+        }
+    }
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
+        const int64_t base = row * nvec;
+        uint4 xv[VPT], rv[VPT];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * nthr + tid;
+            if (c < nvec) {
+                xv[v] = ld_stream(static_cast<const uint4 *>(a.x) + base + c);
+                if (FUSED) rv[v] = ld_stream(static_cast<const uint4 *>(a.res) + base + c);
+            }
+        }
+        if (FUSED) {
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int c = v * nthr + tid;
+                if (c < nvec) {
+                    float f[V];
+                    r_of<T, FUSED>(xv[v], rv[v], f);
+                    st_stream(static_cast<uint4 *>(a.res_out) + base + c, E::pack(f));
+                }
+            }
+        }
+        auto each = [&](auto fn) {
+#pragma unroll
+            for (int v = 0; v < VPT; ++v)
+                if (v * nthr + tid < nvec) {
+                    float f[V];
+                    r_of<T, FUSED>(xv[v], rv[v], f);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) fn(f[k]);
+                }
+        };
+        const float2 st = ln_stats(each, n_f, a.eps, slots, parity);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * nthr + tid;
+            if (c < nvec) {
+                float f[V], wf[V], bf[V], o[V];
+                r_of<T, FUSED>(xv[v], rv[v], f);
+                E::unpack(wv[v], wf);
+                E::unpack(bv[v], bf);
+#pragma unroll
+                for (int k = 0; k < V; ++k) o[k] = fmaf((f[k] - st.x) * st.y, wf[k], bf[k]);
+                st_stream(static_cast<uint4 *>(a.y) + base + c, E::pack(o));
+            }
+        }
+        if (tid == 0) {
+            if (a.mean) a.mean[row] = st.x;
+            if (a.rstd) a.rstd[row] = st.y;
+        }
+    }
+}
+
+// Any N, any alignment: every pass re-reads the row (from L2); VEC selects 128-bit vectors.
+template <typename T, bool VEC, bool FUSED>
+__global__ void __launch_bounds__(1024) ln_fwd_stream(const LnFwdArgs a) {
+    using E = Elem<T>;
+    constexpr int W = E::kPerVec;
+    constexpr int V = VEC ? W : 1;
+    __shared__ float slots[2][2][32];
+    const int nchunk = a.N / V;
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const float n_f = static_cast<float>(a.N);
+
+    auto load_r = [&](int64_t base, int c, float (&f)[W]) {
+        if constexpr (VEC) {
+            const int64_t vi = base / W + c;
+            E::unpack(__ldcg(static_cast<const uint4 *>(a.x) + vi), f);
+            if constexpr (FUSED) {
+                float bb[W];
+                E::unpack(__ldcg(static_cast<const uint4 *>(a.res) + vi), bb);
+#pragma unroll
+                for (int k = 0; k < W; ++k) f[k] += bb[k];
+            }
+        } else {
+            f[0] = E::load1(a.x, base + c);
+            if constexpr (FUSED) f[0] += E::load1(a.res, base + c);
+        }
+    };
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
+        const int64_t base = row * static_cast<int64_t>(a.N);
+        auto each = [&](auto fn) {
+            for (int c = tid; c < nchunk; c += nthr) {
+                float f[W];
+                load_r(base, c, f);
+#pragma unroll
+                for (int k = 0; k < V; ++k) fn(f[k]);
+            }
+        };
+        const float2 st = ln_stats(each, n_f, a.eps, slots, parity);
+        for (int c = tid; c < nchunk; c += nthr) {
+            float f[W], wf[W], bf[W], o[W];
+            load_r(base, c, f);
+            if constexpr (VEC) {
+                E::unpack(ld_keep(static_cast<const uint4 *>(a.w) + c), wf);
+                if (a.b) E::unpack(ld_keep(static_cast<const uint4 *>(a.b) + c), bf);
+            } else {
+                wf[0] = E::load1(a.w, c);
+                if (a.b) bf[0] = E::load1(a.b, c);
+            }
+            if (!a.b)
+#pragma unroll
+                for (int k = 0; k < V; ++k) bf[k] = 0.f;
+#pragma unroll
+            for (int k = 0; k < V; ++k) o[k] = fmaf((f[k] - st.x) * st.y, wf[k], bf[k]);
+            if constexpr (VEC) {
+                if constexpr (FUSED) st_stream(static_cast<uint4 *>(a.res_out) + base / W + c, E::pack(f));
+                st_stream(static_cast<uint4 *>(a.y) + base / W + c, E::pack(o));
+            } else {
+                if constexpr (FUSED) E::store1(a.res_out, base + c, f[0]);
+                E::store1(a.y, base + c, o[0]);
+            }
+        }
+        if (tid == 0) {
+            if (a.mean) a.mean[row] = st.x;
+            if (a.rstd) a.rstd[row] = st.y;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------ backward
+// Stage 1, rows in registers: CTA p owns rows [p * R, (p + 1) * R); dw and db partials stay in
+// registers and go to rows p of the two [P, N] workspace halves.
+template <typename T, int VPT, bool ADDG>
+__global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_cta(const LnBwdArgs a) {
+    using E = Elem<T>;
+    constexpr int V = E::kPerVec;
+    __shared__ float slots[2][2][32];
+    const int nvec = a.N / V;
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const float n_f = static_cast<float>(a.N);
+
+    uint4 wv[VPT];
+    float dw[VPT][V], db[VPT][V];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * nthr + tid;
+        if (c < nvec) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
+#pragma unroll
+        for (int k = 0; k < V; ++k) dw[v][k] = db[v][k] = 0.f;
+    }
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta;
+    const int64_t row1 = min(a.M, row0 + a.rows_per_cta);
+    int parity = 0;
+    for (int64_t row = row0; row < row1; ++row) {
+        const int64_t base = row * nvec;
+        uint4 xv[VPT], dyv[VPT], gv[VPT];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * nthr + tid;
+            if (c < nvec) {
+                xv[v] = ld_stream(static_cast<const uint4 *>(a.x) + base + c);
+                dyv[v] = ld_stream(static_cast<const uint4 *>(a.dy) + base + c);
+                if constexpr (ADDG) gv[v] = ld_stream(static_cast<const uint4 *>(a.d_ro) + base + c);
+            }
+        }
+        const float mu = __ldg(a.mean + row);
+        const float rs = __ldg(a.rstd + row);
+        float sg = 0.f, sgx = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * nthr + tid;
+            if (c < nvec) {
+                float xf[V], d[V], wf[V];
+                E::unpack(xv[v], xf);
+                E::unpack(dyv[v], d);
+                E::unpack(wv[v], wf);
+#pragma unroll
+                for (int k = 0; k < V; ++k) {
+                    const float xh = (xf[k] - mu) * rs;
+                    const float g = d[k] * wf[k];
+                    sg += g;
+                    sgx = fmaf(g, xh, sgx);
+                    dw[v][k] = fmaf(d[k], xh, dw[v][k]);
+                    db[v][k] += d[k];
+                }
+            }
+        }
+        const float2 t = cta_sum2(sg, sgx, slots[parity]);
+        parity ^= 1;
+        const float mg = t.x / n_f, mgx = t.y / n_f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * nthr + tid;
+            if (c < nvec) {
+                float xf[V], d[V], wf[V], o[V];
+                E::unpack(xv[v], xf);
+                E::unpack(dyv[v], d);
+                E::unpack(wv[v], wf);
+#pragma unroll
+                for (int k = 0; k < V; ++k) o[k] = rs * (d[k] * wf[k] - mg - ((xf[k] - mu) * rs) * mgx);
+                if constexpr (ADDG) {
+                    float gg[V];
+                    E::unpack(gv[v], gg);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) o[k] += gg[k];
+                }
+                st_stream(static_cast<uint4 *>(a.dx) + base + c, E::pack(o));
+            }
+        }
+    }
+    float *pw = a.partial + static_cast<int64_t>(blockIdx.x) * a.N;
+    float *pb = a.partial + (static_cast<int64_t>(gridDim.x) + blockIdx.x) * a.N;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * nthr + tid;
+        if (c < nvec) {
+#pragma unroll
+            for (int q = 0; q < V / 4; ++q) {
+                reinterpret_cast<float4 *>(pw + static_cast<int64_t>(c) * V)[q] =
+                    make_float4(dw[v][4 * q], dw[v][4 * q + 1], dw[v][4 * q + 2], dw[v][4 * q + 3]);
+                reinterpret_cast<float4 *>(pb + static_cast<int64_t>(c) * V)[q] =
+                    make_float4(db[v][4 * q], db[v][4 * q + 1], db[v][4 * q + 2], db[v][4 * q + 3]);
+            }
+        }
+    }
+}
+
+// Stage 1 for any N and alignment: two passes over each row; the partials accumulate in the
+// CTA's own workspace rows (each element owned by one thread).
+template <typename T, bool VEC, bool ADDG>
+__global__ void __launch_bounds__(1024) ln_bwd_stream(const LnBwdArgs a) {
+    using E = Elem<T>;
+    constexpr int W = E::kPerVec;
+    constexpr int V = VEC ? W : 1;
+    __shared__ float slots[2][2][32];
+    const int nchunk = a.N / V;
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const float n_f = static_cast<float>(a.N);
+    float *pw = a.partial + static_cast<int64_t>(blockIdx.x) * a.N;
+    float *pb = a.partial + (static_cast<int64_t>(gridDim.x) + blockIdx.x) * a.N;
+
+    auto load = [&](int64_t base, int c, float (&xf)[W], float (&df)[W], float (&wf)[W]) {
+        if constexpr (VEC) {
+            const int64_t vi = base / W + c;
+            E::unpack(__ldcg(static_cast<const uint4 *>(a.x) + vi), xf);
+            E::unpack(__ldcg(static_cast<const uint4 *>(a.dy) + vi), df);
+            E::unpack(ld_keep(static_cast<const uint4 *>(a.w) + c), wf);
+        } else {
+            xf[0] = E::load1(a.x, base + c);
+            df[0] = E::load1(a.dy, base + c);
+            wf[0] = E::load1(a.w, c);
+        }
+    };
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta;
+    const int64_t row1 = min(a.M, row0 + a.rows_per_cta);
+    int parity = 0;
+    for (int64_t row = row0; row < row1; ++row) {
+        const int64_t base = row * static_cast<int64_t>(a.N);
+        const float mu = __ldg(a.mean + row);
+        const float rs = __ldg(a.rstd + row);
+        float sg = 0.f, sgx = 0.f;
+        for (int c = tid; c < nchunk; c += nthr) {
+            float xf[W], df[W], wf[W];
+            load(base, c, xf, df, wf);
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                const float g = df[k] * wf[k];
+                sg += g;
+                sgx = fmaf(g, (xf[k] - mu) * rs, sgx);
+            }
+        }
+        const float2 t = cta_sum2(sg, sgx, slots[parity]);
+        parity ^= 1;
+        const float mg = t.x / n_f, mgx = t.y / n_f;
+        const bool first = (row == row0);
+        for (int c = tid; c < nchunk; c += nthr) {
+            float xf[W], df[W], wf[W], o[W];
+            load(base, c, xf, df, wf);
+            float gf[W];
+            if constexpr (ADDG) {
+                if constexpr (VEC) {
+                    E::unpack(ld_stream(static_cast<const uint4 *>(a.d_ro) + base / W + c), gf);
+                } else {
+                    gf[0] = E::load1(a.d_ro, base + c);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                const float xh = (xf[k] - mu) * rs;
+                o[k] = rs * (df[k] * wf[k] - mg - xh * mgx);
+                if constexpr (ADDG) o[k] += gf[k];
+                const int64_t j = static_cast<int64_t>(c) * V + k;
+                pw[j] = first ? df[k] * xh : fmaf(df[k], xh, pw[j]);
+                pb[j] = first ? df[k] : pb[j] + df[k];
+            }
+            if constexpr (VEC) {
+                st_stream(static_cast<uint4 *>(a.dx) + base / W + c, E::pack(o));
+            } else {
+                E::store1(a.dx, base + c, o[0]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------ dispatch
+template <typename T, bool FUSED>
+const void *ln_fwd_kernel_ptr(const Launch &l) {
+    switch (l.variant) {
+        case RRN_VARIANT_ROW_CTA:
+            switch (l.vpt) {
+                case 1: return reinterpret_cast<const void *>(&ln_fwd_row_cta<T, 1, FUSED>);
+                case 2: return reinterpret_cast<const void *>(&ln_fwd_row_cta<T, 2, FUSED>);
+                case 4: return reinterpret_cast<const void *>(&ln_fwd_row_cta<T, 4, FUSED>);
+                case 8: return reinterpret_cast<const void *>(&ln_fwd_row_cta<T, 8, FUSED>);
+                default: return nullptr;
+            }
+        case RRN_VARIANT_STREAM:
+            return l.vec ? reinterpret_cast<const void *>(&ln_fwd_stream<T, true, FUSED>)
+                         : reinterpret_cast<const void *>(&ln_fwd_stream<T, false, FUSED>);
+        default: return nullptr;
+    }
+}
+
+template <typename T, bool ADDG>
+const void *ln_bwd_kernel_ptr(const Launch &l) {
+    switch (l.variant) {
+        case RRN_VARIANT_ROW_CTA:
+            switch (l.vpt) {
+                case 1: return reinterpret_cast<const void *>(&ln_bwd_row_cta<T, 1, ADDG>);
+                case 2: return reinterpret_cast<const void *>(&ln_bwd_row_cta<T, 2, ADDG>);
+                case 4: return reinterpret_cast<const void *>(&ln_bwd_row_cta<T, 4, ADDG>);
+                default: return nullptr;
+            }
+        case RRN_VARIANT_STREAM:
+            return l.vec ? reinterpret_cast<const void *>(&ln_bwd_stream<T, true, ADDG>)
+                         : reinterpret_cast<const void *>(&ln_bwd_stream<T, false, ADDG>);
+        default: return nullptr;
+    }
+}
+
+template <typename T>
+cudaError_t launch_ln_fwd(const LnFwdArgs &a, const Launch &l, cudaStream_t stream) {
+    const void *k = a.res ? ln_fwd_kernel_ptr<T, true>(l) : ln_fwd_kernel_ptr<T, false>(l);
+    if (!k) return cudaErrorInvalidConfiguration;
+    LnFwdArgs args = a;
+    void *params[] = {&args};
+    return cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, 0, stream);
+}
+
+// Stage 1, then stage 2 twice (dw from the first workspace half, db from the second).
+template <typename T>
+cudaError_t launch_ln_bwd(const LnBwdArgs &a, const Launch &l, cudaStream_t stream) {
+    const void *k = a.d_ro ? ln_bwd_kernel_ptr<T, true>(l) : ln_bwd_kernel_ptr<T, false>(l);
+    if (!k) return cudaErrorInvalidConfiguration;
+    LnBwdArgs args = a;
+    void *params[] = {&args};
+    cudaError_t e = cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, 0, stream);
+    if (e != cudaSuccess) return e;
+    const int blocks = (a.N + 31) / 32;
+    bwd_dw_reduce<kReduceThreads><<<blocks, kReduceThreads, 0, stream>>>(a.partial, a.dw, l.ctas, a.N);
+    if (a.db)
+        bwd_dw_reduce<kReduceThreads><<<blocks, kReduceThreads, 0, stream>>>(
+            a.partial + static_cast<int64_t>(l.ctas) * a.N, a.db, l.ctas, a.N);
+    return cudaGetLastError();
+}
+
+template <typename T>
+int occupancy_ln_t(bool bwd, bool flag, const Launch &l) {
+    const void *k = bwd ? (flag ? ln_bwd_kernel_ptr<T, true>(l) : ln_bwd_kernel_ptr<T, false>(l))
+                        : (flag ? ln_fwd_kernel_ptr<T, true>(l) : ln_fwd_kernel_ptr<T, false>(l));
+    if (!k) return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, l.threads, 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+}  // namespace rrn

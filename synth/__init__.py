@@ -4,7 +4,7 @@ This module only draws random inputs. It contains none of the normalisation arit
 both the GPU path's tests/benchmark and the CPU oracle can take their inputs from it.
 
 Every workload is drawn on the host with numpy's PCG64 generator, seeded per workload, in a
-fixed order: x, residual, (outlier mask, outlier sign), w, dy, d_ro. Values are drawn in float32
+fixed order: x, residual, (outlier mask, outlier sign), w, b, dy, d_ro. Values are drawn in float32
 and, for bf16 workloads, rounded to bf16 (round to nearest even) by torch's CPU cast. bf16
 tensors are returned as ``uint16`` arrays holding the raw bit patterns; fp32 tensors as
 ``float32`` arrays.
@@ -28,13 +28,15 @@ class Workload:
     """One synthetic problem: op kind, shape, dtype, eps, seed and value distributions."""
 
     name: str
-    op: str                      # "rmsnorm_fwd" | "add_rmsnorm_fwd" | "rmsnorm_bwd" | "add_rmsnorm_bwd"
+    op: str                      # rmsnorm_fwd | add_rmsnorm_fwd | rmsnorm_bwd | add_rmsnorm_bwd |
+                                 # layernorm_fwd | add_layernorm_fwd | layernorm_bwd
     M: int
     N: int
     dtype: str                   # "bf16" | "f32"
     eps: float
     seed: int
-    x_sigma: float = 1.0         # x ~ N(0, x_sigma^2)
+    x_sigma: float = 1.0         # x ~ N(x_mean, x_sigma^2)
+    x_mean: float = 0.0
     res_sigma: float = 1.0       # residual ~ N(0, res_sigma^2)
     outlier_frac: float = 0.0    # fraction of residual entries replaced by +/- outlier_value
     outlier_value: float = 50.0
@@ -71,6 +73,12 @@ _add(Workload("rmsnorm_bwd_16384x4096_bf16", "rmsnorm_bwd", 16384, 4096, BF16, 1
 # The fused backward: x plays the stored residual_out; dy and d_ro are the gradients arriving at
 # y and at residual_out.
 _add(Workload("add_rmsnorm_bwd_16384x4096_bf16", "add_rmsnorm_bwd", 16384, 4096, BF16, 1e-6, 5))
+# LayerNorm (mean-subtracting variant): x ~ N(0.5, 1), bias b ~ 0.1 N(0,1); the backward draws
+# dy and the gradient at residual_out like the fused RMSNorm backward.
+_add(Workload("add_layernorm_fwd_16384x4096_bf16", "add_layernorm_fwd", 16384, 4096, BF16, 1e-5, 6,
+              x_mean=0.5))
+_add(Workload("layernorm_bwd_16384x4096_bf16", "layernorm_bwd", 16384, 4096, BF16, 1e-5, 7,
+              x_mean=0.5))
 
 
 def get(name: str) -> Workload:
@@ -102,9 +110,11 @@ def make(w: Workload) -> Dict[str, np.ndarray]:
     x = rng.standard_normal(shape, dtype=np.float32)
     if w.x_sigma != 1.0:
         x *= np.float32(w.x_sigma)
+    if w.x_mean != 0.0:
+        x += np.float32(w.x_mean)
     out["x"] = _store(x, w.dtype)
     del x
-    if w.op == "add_rmsnorm_fwd":
+    if w.op in ("add_rmsnorm_fwd", "add_layernorm_fwd"):
         res = rng.standard_normal(shape, dtype=np.float32)
         if w.res_sigma != 1.0:
             res *= np.float32(w.res_sigma)
@@ -121,9 +131,11 @@ def make(w: Workload) -> Dict[str, np.ndarray]:
     else:
         wt = (np.float32(1.0) + np.float32(0.1) * rng.standard_normal(w.N, dtype=np.float32))
     out["w"] = _store(wt, w.dtype)
-    if w.op in ("rmsnorm_bwd", "add_rmsnorm_bwd"):
+    if w.op.startswith(("layernorm", "add_layernorm")):
+        out["b"] = _store(np.float32(0.1) * rng.standard_normal(w.N, dtype=np.float32), w.dtype)
+    if w.op in ("rmsnorm_bwd", "add_rmsnorm_bwd", "layernorm_bwd"):
         out["dy"] = _store(rng.standard_normal(shape, dtype=np.float32), w.dtype)
-    if w.op == "add_rmsnorm_bwd":
+    if w.op in ("add_rmsnorm_bwd", "layernorm_bwd"):
         out["d_ro"] = _store(rng.standard_normal(shape, dtype=np.float32), w.dtype)
     return out
 
@@ -135,6 +147,8 @@ def min_bytes(w: Workload) -> int:
     add_rmsnorm_fwd: x, residual, residual_out, y (M*N each), w (N), rstd (M, fp32).
     rmsnorm_bwd: x, dy, dx (M*N each), w (N), rstd (M, fp32), dw (N, fp32).
     add_rmsnorm_bwd: residual_out, dy, d_residual_out, d_r (M*N each), w, rstd, dw.
+    add_layernorm_fwd: x, residual, residual_out, y (M*N each), w, b (N), mean, rstd (M, fp32).
+    layernorm_bwd: x, dy, d_residual_out, dx (M*N each), w (N), mean, rstd (M), dw, db (N, fp32).
     """
     e = w.elem_bytes
     if w.op == "rmsnorm_fwd":
@@ -145,6 +159,10 @@ def min_bytes(w: Workload) -> int:
         return 3 * w.M * w.N * e + w.N * e + 4 * w.M + 4 * w.N
     if w.op == "add_rmsnorm_bwd":
         return 4 * w.M * w.N * e + w.N * e + 4 * w.M + 4 * w.N
+    if w.op == "add_layernorm_fwd":
+        return 4 * w.M * w.N * e + 2 * w.N * e + 8 * w.M
+    if w.op == "layernorm_bwd":
+        return 4 * w.M * w.N * e + w.N * e + 8 * w.M + 8 * w.N
     raise ValueError(w.op)
 
 

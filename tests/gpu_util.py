@@ -5,7 +5,8 @@ Bounds (each compares a GPU output, decoded exactly to fp64, with the oracle's f
   bf16 outputs (y, residual_out, dx): |err| <= 2^-8 * |ref| + 1e-6
   fp32 outputs (y, residual_out):     |err| <= 1e-5 * |ref| + 1e-6
   rstd (fp32):                        |err| <= 1e-5 * |ref|
-  dw (fp32):                          |err| <= 1e-3 * max(|ref|, 1)
+  LayerNorm mean (fp32):              |err| <= 1e-5 * (|ref| + 1 / rstd_ref)   (the row's scale)
+  dw, db (fp32):                      |err| <= 1e-3 * max(|ref|, 1)
 """
 from __future__ import annotations
 
@@ -68,6 +69,14 @@ def check_rstd(got: np.ndarray, ref: np.ndarray, what: str = "rstd") -> float:
     ok = err <= bound
     assert ok.all(), _worst(err, bound, got, ref, what)
     return float(np.max(err / np.where(bound > 0, bound, 1.0))) if err.size else 0.0
+
+
+def check_mean(got: np.ndarray, ref: np.ndarray, rstd_ref: np.ndarray, what: str = "mean") -> float:
+    err = np.abs(got - ref)
+    bound = RSTD_REL * (np.abs(ref) + 1.0 / rstd_ref)
+    ok = err <= bound
+    assert ok.all(), _worst(err, bound, got, ref, what)
+    return float(np.max(err / bound)) if err.size else 0.0
 
 
 def check_dw(got: np.ndarray, ref: np.ndarray, what: str = "dw") -> float:

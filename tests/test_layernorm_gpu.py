@@ -1,0 +1,145 @@
+"""GPU parity of the LayerNorm variant (forward with residual and bias, backward with dw, db)
+against the CPU fp64 oracle, through the C ABI."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import residual_rmsnorm_row_gb300 as rrn
+import synth
+from gpu_util import (bits_of, check_dw, check_mean, check_out, check_rstd, to_dev, to_host,
+                      values)
+
+pytestmark = pytest.mark.gpu
+CHUNK = 2048
+
+
+def ln_fwd(h, dtype, eps, fused, bias, launch=None):
+    x = to_dev(h["x"], dtype)
+    w = to_dev(h["w"], dtype)
+    b = to_dev(h["b"], dtype) if bias else None
+    M = x.shape[0]
+    y = torch.full_like(x, float("nan"))
+    mean = torch.full((M,), float("nan"), device="cuda")
+    rstd = torch.full((M,), float("nan"), device="cuda")
+    res = to_dev(h["residual"], dtype) if fused else None
+    ro = torch.full_like(x, float("nan")) if fused else None
+    rrn.layernorm_fwd(x, w, b, y, mean, rstd, eps, residual=res, residual_out=ro, launch=launch)
+    torch.cuda.synchronize()
+    return y, ro, mean, rstd
+
+
+def compare(h, dtype, eps, fused, bias, y, ro, mean, rstd):
+    M = h["x"].shape[0]
+    for s in range(0, M, CHUNK):
+        idx = np.arange(s, min(M, s + CHUNK))
+        r_ref, y_ref, m_ref, rs_ref = oracle.add_layernorm_fwd(
+            h["x"][idx], h["residual"][idx] if fused else None, h["w"], h["b"] if bias else None, eps)
+        ti = torch.from_numpy(idx).cuda()
+        check_out(values(y.index_select(0, ti)), y_ref, dtype, "LN y")
+        check_rstd(rstd.index_select(0, ti).cpu().numpy().astype(np.float64), rs_ref, "LN rstd")
+        check_mean(mean.index_select(0, ti).cpu().numpy().astype(np.float64), m_ref, rs_ref)
+        if fused:
+            assert np.array_equal(to_host(ro.index_select(0, ti)), bits_of(r_ref.astype(np.float32), dtype))
+
+
+def test_layernorm_forward_full_size():
+    wl = synth.get("add_layernorm_fwd_16384x4096_bf16")
+    h = synth.make(wl)
+    y, ro, mean, rstd = ln_fwd(h, "bf16", wl.eps, True, True)
+    compare(h, "bf16", wl.eps, True, True, y, ro, mean, rstd)
+
+
+def test_layernorm_backward_full_size():
+    wl = synth.get("layernorm_bwd_16384x4096_bf16")
+    h = synth.make(wl)
+    x, w = to_dev(h["x"], "bf16"), to_dev(h["w"], "bf16")
+    _, mean, rstd = rrn.layer_norm(x, w, to_dev(h["b"], "bf16"), wl.eps)
+    dx, dw, db = rrn.layer_norm_backward(to_dev(h["dy"], "bf16"), x, w, mean, rstd, wl.eps,
+                                         d_residual_out=to_dev(h["d_ro"], "bf16"))
+    torch.cuda.synchronize()
+    ref_dx, ref_dw, ref_db = oracle.add_layernorm_bwd(h["dy"], h["d_ro"], h["x"], h["w"], wl.eps)
+    check_out(values(dx), ref_dx, "bf16", "LN dx")
+    check_dw(dw.cpu().numpy().astype(np.float64), ref_dw, "LN dw")
+    check_dw(db.cpu().numpy().astype(np.float64), ref_db, "LN db")
+
+
+def _fwd_launches(dtype, N):
+    V = 8 if dtype == "bf16" else 4
+    out = [None, rrn.Launch(rrn.VARIANT_STREAM, 0, 128, 0), rrn.Launch(rrn.VARIANT_STREAM, 0, 1024, 7)]
+    if N % V == 0:
+        nvec = N // V
+        for vpt in (1, 2, 4, 8):
+            thr = -(-(-(-nvec // vpt)) // 32) * 32
+            if thr <= (256 if vpt == 8 else 512 if vpt == 4 else 1024):
+                out += [rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0), rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 9)]
+    return out
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("N", [1, 7, 1000, 1024, 4095, 4096, 7168, 8192, 20000])
+def test_layernorm_forward_variants(dtype, N):
+    M = 67
+    for fused in (False, True):
+        wl = synth.Workload("ln", "add_layernorm_fwd" if fused else "layernorm_fwd", M, N, dtype,
+                            1e-5, 91, x_mean=0.5)
+        h = synth.make(wl)
+        for bias in (True, False):
+            for launch in _fwd_launches(dtype, N):
+                y, ro, mean, rstd = ln_fwd(h, dtype, wl.eps, fused, bias, launch)
+                compare(h, dtype, wl.eps, fused, bias, y, ro, mean, rstd)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("N", [1, 9, 1000, 1024, 4095, 4096, 7168, 8192])
+def test_layernorm_backward_variants(dtype, N):
+    M = 75
+    wl = synth.Workload("ln-bwd", "layernorm_bwd", M, N, dtype, 1e-5, 92, x_mean=0.5)
+    h = synth.make(wl)
+    x, w = to_dev(h["x"], dtype), to_dev(h["w"], dtype)
+    _, mean, rstd = rrn.layer_norm(x, w, None, wl.eps)
+    V = 8 if dtype == "bf16" else 4
+    launches = [None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0), rrn.Launch(rrn.VARIANT_STREAM, 0, 64, 5)]
+    if N % V == 0:
+        nvec = N // V
+        for vpt in (1, 2, 4):
+            thr = -(-(-(-nvec // vpt)) // 32) * 32
+            if thr <= (256 if vpt == 4 else 512):
+                launches += [rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0), rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 6)]
+    for with_dro in (True, False):
+        ref_dx, ref_dw, ref_db = oracle.add_layernorm_bwd(h["dy"], h["d_ro"] if with_dro else None,
+                                                          h["x"], h["w"], wl.eps)
+        for launch in launches:
+            dx = torch.full_like(x, float("nan"))
+            dw = torch.full((N,), float("nan"), device="cuda")
+            db = torch.full((N,), float("nan"), device="cuda")
+            ws = torch.empty(max(rrn.layernorm_bwd_workspace_bytes(M, N, x.dtype), 8 * x.numel()) // 4,
+                             device="cuda")
+            rrn.layernorm_bwd(to_dev(h["dy"], dtype), to_dev(h["d_ro"], dtype) if with_dro else None,
+                              x, w, mean, rstd, dx, dw, db, ws, wl.eps, launch=launch)
+            torch.cuda.synchronize()
+            check_out(values(dx), ref_dx, dtype, f"LN dx {launch}")
+            check_dw(dw.cpu().numpy().astype(np.float64), ref_dw, f"LN dw {launch}")
+            check_dw(db.cpu().numpy().astype(np.float64), ref_db, f"LN db {launch}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("N", [1024, 4096, 20000])
+def test_layernorm_extreme_rows(dtype, N):
+    rng = np.random.default_rng(93)
+    base = rng.standard_normal((6, N)).astype(np.float32)
+    rows = np.stack([
+        base[0] * 1e36 + 3e36,           # sum and squared deviations overflow fp32
+        np.full(N, 3.0, np.float32),     # constant row: xhat = 0, y = b
+        np.zeros(N, np.float32),
+        base[3] * 1e-30,                 # tiny deviations
+        base[4] + 100.0,                 # large offset relative to the spread
+        base[5],
+    ]).astype(np.float32)
+    h = {"x": bits_of(rows, dtype), "w": bits_of((1 + 0.1 * rng.standard_normal(N)).astype(np.float32), dtype),
+         "b": bits_of((0.1 * rng.standard_normal(N)).astype(np.float32), dtype)}
+    for launch in (None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0)):
+        y, _, mean, rstd = ln_fwd(h, dtype, 1e-5, False, True, launch)
+        compare(h, dtype, 1e-5, False, True, y, None, mean, rstd)

@@ -8,9 +8,10 @@ def test_every_workload_draws_its_tensors():
     for name, w in synth.WORKLOADS.items():
         small = w.with_shape(min(w.M, 64))
         t = synth.make(small)
-        want = {"x", "w"} | ({"residual"} if w.op == "add_rmsnorm_fwd" else set()) | (
-            {"dy"} if w.op in ("rmsnorm_bwd", "add_rmsnorm_bwd") else set()) | (
-            {"d_ro"} if w.op == "add_rmsnorm_bwd" else set())
+        want = {"x", "w"} | ({"residual"} if w.op in ("add_rmsnorm_fwd", "add_layernorm_fwd") else set()) | (
+            {"dy"} if w.op in ("rmsnorm_bwd", "add_rmsnorm_bwd", "layernorm_bwd") else set()) | (
+            {"d_ro"} if w.op in ("add_rmsnorm_bwd", "layernorm_bwd") else set()) | (
+            {"b"} if "layernorm" in w.op else set())
         assert want <= set(t), name
         enc = np.uint16 if w.dtype == synth.BF16 else np.float32
         for k in want:
