@@ -15,6 +15,7 @@ What each function computes, with the passage it follows, is stated in ``oracle.
   rmsnorm_bwd      dx and dw, the exact derivative of rmsnorm_fwd
   add_rmsnorm_bwd  d_r (gradient w.r.t. x + residual) and dw, the derivative of add_rmsnorm_fwd
   add_layernorm_fwd / add_layernorm_bwd   the LayerNorm variant (mean subtracted, bias added)
+  rmsnorm_quant_fp8  RMSNorm (+ residual add) feeding fp8 e4m3 codes with a per-row scale
 """
 from __future__ import annotations
 
@@ -65,6 +66,13 @@ class Oracle:
                                                  _dbl_p, _dbl_p, _dbl_p, _dbl_p]
         lib.oracle_add_layernorm_bwd.argtypes = [vp, i32, vp, i32, vp, i32, vp, i32, i64, i64, dbl,
                                                  _dbl_p, _dbl_p, _dbl_p]
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = dbl
+        lib.oracle_e4m3_encode.argtypes = [dbl]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_rmsnorm_quant_fp8.argtypes = [vp, i32, vp, i32, vp, i32, i64, i64, dbl, _dbl_p,
+                                                 _dbl_p, vp, _dbl_p, _dbl_p]
+        lib.oracle_rmsnorm_quant_fp8.restype = i32
         for name in ("oracle_decode", "oracle_add_rmsnorm_fwd", "oracle_rmsnorm_fwd",
                      "oracle_rmsnorm_bwd", "oracle_add_rmsnorm_bwd", "oracle_add_layernorm_fwd",
                      "oracle_add_layernorm_bwd"):
@@ -200,6 +208,31 @@ class Oracle:
             _code(w), M, N, float(eps), _out(dx), _out(dw), _out(db)), "add_layernorm_bwd")
         return dx, dw, db
 
+    def e4m3_decode(self, code: int) -> float:
+        return float(self.lib.oracle_e4m3_decode(int(code)))
+
+    def e4m3_encode(self, v: float) -> int:
+        return int(self.lib.oracle_e4m3_encode(float(v)))
+
+    def rmsnorm_quant_fp8(self, x: np.ndarray, residual: Optional[np.ndarray], w: np.ndarray,
+                          eps: float):
+        """Return ``(r, v, q, scale, rstd)``: v = y / scale (fp64), q its e4m3 codes (uint8)."""
+        x = np.ascontiguousarray(x)
+        w = np.ascontiguousarray(w)
+        M, N = x.shape
+        if residual is not None:
+            residual = np.ascontiguousarray(residual)
+        r = np.empty((M, N))
+        v = np.empty((M, N))
+        q = np.empty((M, N), dtype=np.uint8)
+        scale = np.empty(M)
+        rstd = np.empty(M)
+        self._check(self.lib.oracle_rmsnorm_quant_fp8(
+            _ptr(x), _code(x), _ptr(residual), 0 if residual is None else _code(residual), _ptr(w),
+            _code(w), M, N, float(eps), _out(r), _out(v), q.ctypes.data_as(ctypes.c_void_p),
+            _out(scale), _out(rstd)), "rmsnorm_quant_fp8")
+        return r, v, q, scale, rstd
+
 
 _DEFAULT: Optional[Oracle] = None
 
@@ -240,11 +273,15 @@ def add_layernorm_bwd(dy, d_residual_out, x, w, eps):
     return default().add_layernorm_bwd(dy, d_residual_out, x, w, eps)
 
 
+def rmsnorm_quant_fp8(x, residual, w, eps):
+    return default().rmsnorm_quant_fp8(x, residual, w, eps)
+
+
 def build(force: bool = False) -> str:
     """Compile ``liboracle.so`` (used by the package's build step)."""
     return _build.build(force)
 
 
 __all__ = ["Oracle", "default", "decode", "add_rmsnorm_fwd", "rmsnorm_fwd", "rmsnorm_bwd",
-           "add_rmsnorm_bwd", "add_layernorm_fwd", "add_layernorm_bwd", "build", "BF16", "F32",
-           "F64"]
+           "add_rmsnorm_bwd", "add_layernorm_fwd", "add_layernorm_bwd", "rmsnorm_quant_fp8",
+           "build", "BF16", "F32", "F64"]

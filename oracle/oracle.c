@@ -291,3 +291,79 @@ int oracle_add_layernorm_bwd(const void *dy, int dy_dt, const void *d_ro, int d_
     free(xr); free(dyr); free(wd); free(xhat); free(g);
     return ORACLE_OK;
 }
+
+/*
+ * FP8 E4M3 (the "e4m3fn" encoding: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits,
+ * no infinities, 0x7F/0xFF are NaN, largest finite 448). Decoding is exact; encoding rounds to
+ * nearest, ties to even, and saturates finite values beyond 448 to +/-448 (the "satfinite"
+ * conversion a quantising kernel uses). Written from the format's definition.
+ */
+double oracle_e4m3_decode(uint8_t code)
+{
+    int s = code >> 7, e = (code >> 3) & 0xF, m = code & 7;
+    if (e == 0xF && m == 7) return NAN;
+    double mag = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+uint8_t oracle_e4m3_encode(double v)
+{
+    if (isnan(v)) return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    if (a >= 448.0) return sign | 0x7E;
+    /* The 127 non-negative finite codes are ordered by value: take the nearest, ties to the
+     * even code (the one whose last mantissa bit is 0). */
+    uint8_t best = 0;
+    for (uint8_t c = 1; c <= 0x7E; ++c) {
+        double dc = oracle_e4m3_decode(c), db = oracle_e4m3_decode(best);
+        double ec = fabs(dc - a), eb = fabs(db - a);
+        if (ec < eb || (ec == eb && (c & 1) == 0)) best = c;
+    }
+    return sign | best;
+}
+
+/*
+ * RMSNorm (fused with the residual add when `res` is not NULL) feeding an FP8 E4M3 output with
+ * one scale per row - the fusion with the neighbouring op that a persistent megakernel would do
+ * (Machete, "Core Ideas": one instruction stream across ops). Per row:
+ *     y = r * rstd * w                         (as oracle_add_rmsnorm_fwd)
+ *     amax = max_j |y_j|;  scale = amax / 448  (scale = 0 for an all-zero y)
+ *     v_j = y_j / scale (0 when scale = 0);    q_j = e4m3(v_j)
+ * Outputs (any may be NULL): r_out, v [M, N] (the real-valued code target, fp64),
+ * q [M, N] (the codes, taking the rounding decision on v), scale [M], rstd [M].
+ */
+int oracle_rmsnorm_quant_fp8(const void *x, int x_dt, const void *res, int res_dt, const void *w,
+                             int w_dt, int64_t M, int64_t N, double eps, double *r_out, double *v,
+                             uint8_t *q, double *scale, double *rstd)
+{
+    if (!x || !w || M < 0 || N < 1) return ORACLE_BAD_ARG;
+    double *y = (double *)malloc((size_t)N * sizeof(double));
+    double *rr = (double *)malloc((size_t)N * sizeof(double));
+    double *s = (double *)malloc(sizeof(double));
+    if (!y || !rr || !s) { free(y); free(rr); free(s); return ORACLE_NO_MEMORY; }
+    int st = ORACLE_OK;
+    for (int64_t i = 0; i < M && st == ORACLE_OK; ++i) {
+        /* one row through the plain definition above */
+        const char *xb = (const char *)x, *rb = (const char *)res;
+        int xs = x_dt == ORACLE_BF16 ? 2 : x_dt == ORACLE_F32 ? 4 : 8;
+        int rs = res_dt == ORACLE_BF16 ? 2 : res_dt == ORACLE_F32 ? 4 : 8;
+        st = oracle_add_rmsnorm_fwd(xb + (size_t)(i * N) * xs, x_dt,
+                                    res ? rb + (size_t)(i * N) * rs : NULL, res_dt, w, w_dt, 1, N,
+                                    eps, rr, y, s);
+        if (st != ORACLE_OK) break;
+        double amax = 0.0;
+        for (int64_t j = 0; j < N; ++j) amax = fmax(amax, fabs(y[j]));
+        double sc = amax / 448.0;
+        if (scale) scale[i] = sc;
+        if (rstd) rstd[i] = *s;
+        for (int64_t j = 0; j < N; ++j) {
+            double vv = sc > 0.0 ? y[j] / sc : 0.0;
+            if (r_out) r_out[i * N + j] = rr[j];
+            if (v) v[i * N + j] = vv;
+            if (q) q[i * N + j] = oracle_e4m3_encode(vv);
+        }
+    }
+    free(y); free(rr); free(s);
+    return st;
+}

@@ -449,6 +449,67 @@ def pin_layernorm_identities(o):
     _close(yl, yr, 1e-12, 1e-14, "zero-mean LayerNorm vs RMSNorm")
 
 
+# --------------------------------------------------------------------------- fp8 e4m3
+def _e4m3_values():
+    import torch
+
+    codes = np.arange(0, 0x7F, dtype=np.uint8)  # non-negative finite codes, ascending values
+    return torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def pin_e4m3_codec_matches_torch(o):
+    """Decoding of all 256 codes, and encoding (round to nearest, ties to even) of every
+    representable value, every midpoint between neighbours and the fp32 values just beside each
+    midpoint, agree with torch's float8_e4m3fn cast; finite values beyond 448 saturate."""
+    import torch
+
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = np.array([o.e4m3_decode(int(c)) for c in codes])
+    assert np.array_equal(np.isnan(got), np.isnan(want)), "e4m3 NaN codes"
+    assert np.array_equal(got[~np.isnan(got)], want[~np.isnan(want)]), "e4m3 decode"
+    vals = _e4m3_values()
+    mids = (vals[:-1] + vals[1:]) / 2
+    probe = np.concatenate([vals, mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+                            np.nextafter(mids.astype(np.float32), np.float32(1e9))]).astype(np.float32)
+    probe = np.concatenate([probe, -probe])
+    ref = torch.from_numpy(probe).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    mine = np.array([o.e4m3_encode(float(v)) for v in probe], dtype=np.uint8)
+    bad = np.nonzero(mine != ref)[0]
+    assert bad.size == 0, f"e4m3 encode of {probe[bad[0]]!r}: {mine[bad[0]]:#x} vs torch {ref[bad[0]]:#x}"
+    for v, c in ((448.0, 0x7E), (449.0, 0x7E), (1e30, 0x7E), (-1000.0, 0xFE), (0.0, 0x00)):
+        assert o.e4m3_encode(v) == c, f"e4m3 saturation of {v}"
+
+
+def pin_rmsnorm_quant_fp8(o):
+    """The fused quantiser: r and rstd as the RMSNorm oracle; scale = max|y| / 448 with y from
+    the RMSNorm oracle; the largest element lands exactly on +/-448; every code is the nearest
+    e4m3 value to y / scale (dequantisation error at most half a code step); an all-zero row gives
+    scale 0 and zero codes."""
+    rng = np.random.default_rng(41)
+    M, N, eps = 5, 96, 1e-6
+    x = rng.standard_normal((M, N))
+    res = 2.0 * rng.standard_normal((M, N))
+    x[4] = -res[4]                                  # an all-zero r row
+    w = 1.0 + 0.1 * rng.standard_normal(N)
+    r, v, q, scale, rstd = o.rmsnorm_quant_fp8(x, res, w, eps)
+    r2, y, rstd2 = o.add_rmsnorm_fwd(x, res, w, eps)
+    assert np.array_equal(r, r2) and np.array_equal(rstd, rstd2), "quant: r / rstd differ"
+    amax = np.max(np.abs(y), axis=1)
+    _close(scale, amax / 448.0, 1e-15, 0.0, "quant scale")
+    vals = _e4m3_values()
+    for i in range(4):
+        j = int(np.argmax(np.abs(y[i])))
+        assert q[i, j] in (0x7E, 0xFE), "argmax element not at +/-448"
+        deq = np.array([o.e4m3_decode(int(c)) for c in q[i]]) * scale[i]
+        a = np.abs(y[i]) / scale[i]
+        k = np.clip(np.searchsorted(vals, a), 1, len(vals) - 1)
+        half = (vals[k] - vals[k - 1]) / 2 * scale[i]
+        assert np.all(np.abs(deq - y[i]) <= half * (1 + 1e-12)), "dequantisation error above half a step"
+        _close(v[i], y[i] / scale[i], 1e-15, 0.0, "quant v")
+    assert scale[4] == 0.0 and np.all(q[4] == 0), "zero row"
+
+
 ALL_PINS = [
     pin_decode_known_bits,
     pin_decode_matches_torch_cast,
@@ -469,4 +530,6 @@ ALL_PINS = [
     pin_layernorm_matches_torch,
     pin_layernorm_finite_differences,
     pin_layernorm_identities,
+    pin_e4m3_codec_matches_torch,
+    pin_rmsnorm_quant_fp8,
 ]

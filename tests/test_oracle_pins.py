@@ -70,6 +70,14 @@ MUTATIONS = [
     ("LN bwd projection sign", "double grad = s * (g[j] - mg - xhat[j] * mgx);",
      "double grad = s * (g[j] - mg + xhat[j] * mgx);"),
     ("LN db not summed", "if (db) db[j] += dyr[j];", "if (db) db[j] = dyr[j];"),
+    ("e4m3 ties away from zero", "if (ec < eb || (ec == eb && (c & 1) == 0)) best = c;",
+     "if (ec < eb || (ec == eb && c > best)) best = c;"),
+    ("e4m3 overflow to NaN", "if (a >= 448.0) return sign | 0x7E;", "if (a >= 448.0) return sign | 0x7F;"),
+    ("e4m3 subnormal exponent", "ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
+    ("e4m3 exponent bias", "ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    ("quant scale for e5m2 range", "double sc = amax / 448.0;", "double sc = amax / 240.0;"),
+    ("quant amax from the sum", "for (int64_t j = 0; j < N; ++j) amax = fmax(amax, fabs(y[j]));",
+     "for (int64_t j = 0; j < N; ++j) amax += fabs(y[j]);"),
     ("LN dw from x, not xhat", "if (dw) dw[j] += dyr[j] * xhat[j];\n            if (db)",
      "if (dw) dw[j] += dyr[j] * xr[j];\n            if (db)"),
 ]
