@@ -194,6 +194,25 @@ RRN_API int layernorm_bwd(const void *dy, const void *d_residual_out, const void
                           float *dw, float *db, void *workspace, size_t workspace_bytes,
                           int64_t M, int64_t N, float eps, int dtype, rrn_stream_t stream);
 
+/*
+ * rmsnorm_fwd_fp8 - RMSNorm (fused with the residual add when `residual` is not NULL) feeding an
+ * FP8 E4M3 output with one fp32 scale per row, for a following FP8 GEMM - the norm fused with
+ * its neighbouring op in one pass, as a persistent megakernel would do (Machete page, "Core
+ * Ideas"). Per row, in fp32: y = r * rstd * w as rmsnorm_fwd computes it;
+ * amax = max_j |y_j|; scale = amax / 448; q_j = e4m3(y_j * (448 / amax)), rounded to nearest
+ * even with saturation to +/-448 (scale = 0 and q = 0 when y is all zero). Dequantised,
+ * q_j * scale approximates y_j within half an e4m3 step.
+ *   x, residual, residual_out, w, rstd   as for add_rmsnorm_fwd (residual may be NULL: plain op;
+ *                                        residual_out is then ignored).
+ *   q      [M, N] bytes (e4m3 codes, 0x7F/0xFF never produced), written.
+ *   scale  [M] fp32, written.
+ * Returns an rrn_status. rmsnorm_fwd_fp8_ex (declared with the launch-control calls below)
+ * takes an explicit launch configuration (RRN_VARIANT_ROW_CTA or RRN_VARIANT_STREAM).
+ */
+RRN_API int rmsnorm_fwd_fp8(const void *x, const void *residual, void *residual_out,
+                            const void *w, void *q, float *scale, float *rstd, int64_t M,
+                            int64_t N, float eps, int dtype, rrn_stream_t stream);
+
 /* rrn_status_string - static, NUL-terminated description of a status code. */
 RRN_API const char *rrn_status_string(int status);
 
@@ -267,6 +286,12 @@ RRN_API int rrn_plan_bwd(const void *dy, const void *x, const void *w, const voi
 RRN_API int add_rmsnorm_fwd_ex(const void *x, const void *residual, void *residual_out,
                                const void *w, void *y, float *rstd, int64_t M, int64_t N,
                                float eps, int dtype, const rrn_launch *cfg, rrn_stream_t stream);
+
+/* rmsnorm_fwd_fp8 with an explicit launch configuration (row-per-CTA or two-pass). */
+RRN_API int rmsnorm_fwd_fp8_ex(const void *x, const void *residual, void *residual_out,
+                               const void *w, void *q, float *scale, float *rstd, int64_t M,
+                               int64_t N, float eps, int dtype, const rrn_launch *cfg,
+                               rrn_stream_t stream);
 
 /* LayerNorm with an explicit launch configuration (row-per-CTA or two-pass variants). */
 RRN_API int add_layernorm_fwd_ex(const void *x, const void *residual, void *residual_out,

@@ -43,6 +43,7 @@ from ._binding import (  # noqa: F401  (re-exported API)
     rmsnorm_bwd_ex,
     rmsnorm_bwd_workspace_bytes,
     rmsnorm_fwd,
+    rmsnorm_fwd_fp8,
     selftest_wait_timeout,
 )
 
@@ -132,6 +133,18 @@ def layer_norm_backward(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, mean
     return dx, dw, db
 
 
+def rms_norm_fp8(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6,
+                 residual: Optional[torch.Tensor] = None, stream=None):
+    """Return ``(q, scale)`` (q as torch.float8_e4m3fn) or, with ``residual``,
+    ``(q, scale, residual_out)``: RMSNorm(x (+ residual)) * w quantised per row."""
+    M = x.numel() // x.shape[-1]
+    q = torch.empty(x.shape, device=x.device, dtype=torch.float8_e4m3fn)
+    scale = torch.empty(M, device=x.device, dtype=torch.float32)
+    ro = torch.empty_like(x) if residual is not None else None
+    rmsnorm_fwd_fp8(x, residual, ro, w, q, scale, None, eps, stream=stream)
+    return (q, scale) if residual is None else (q, scale, ro)
+
+
 class RMSNormFunction(torch.autograd.Function):
     """y = RMSNorm(x) * w with the library's forward and backward kernels."""
 
@@ -196,5 +209,5 @@ __all__ = [
     "load_library", "rms_norm", "add_rms_norm", "rms_norm_backward", "device_faults",
     "add_rmsnorm_bwd", "add_rms_norm_backward", "RMSNormFunction", "AddRMSNormFunction", "RMSNorm",
     "layernorm_fwd", "layernorm_bwd", "layernorm_bwd_workspace_bytes", "layer_norm",
-    "layer_norm_backward",
+    "layer_norm_backward", "rmsnorm_fwd_fp8", "rms_norm_fp8",
 ]

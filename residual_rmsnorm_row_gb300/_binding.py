@@ -96,6 +96,9 @@ _SIGNATURES = {
                               ctypes.POINTER(rrn_launch), _vp]),
     "add_rmsnorm_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _f32, _i32,
                                _vp]),
+    "rmsnorm_fwd_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32, _vp]),
+    "rmsnorm_fwd_fp8_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32,
+                                  ctypes.POINTER(rrn_launch), _vp]),
     "layernorm_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32, _vp]),
     "add_layernorm_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32,
                                  _vp]),
@@ -329,6 +332,32 @@ def layernorm_fwd(x: torch.Tensor, w: torch.Tensor, b: Optional[torch.Tensor], y
                                      pw, pb, py, pm, pr, M, N, float(eps), _dtype(x), _stream(stream)))
     else:
         _check(lib.layernorm_fwd(px, pw, pb, py, pm, pr, M, N, float(eps), _dtype(x), _stream(stream)))
+
+
+def rmsnorm_fwd_fp8(x: torch.Tensor, residual: Optional[torch.Tensor],
+                    residual_out: Optional[torch.Tensor], w: torch.Tensor, q: torch.Tensor,
+                    scale: torch.Tensor, rstd: Optional[torch.Tensor], eps: float,
+                    launch: Optional[Launch] = None, stream=None) -> None:
+    """C ``rmsnorm_fwd_fp8`` (``_ex`` with ``launch``): e4m3 codes ``q`` (uint8 or
+    float8_e4m3fn, [M, N]) and per-row ``scale`` of RMSNorm(x (+ residual)) * w."""
+    M, N = _rows(x)
+    if residual is not None:
+        _same(x, residual, "residual")
+        _same(x, residual_out, "residual_out")
+    if q.shape != x.shape or q.element_size() != 1:
+        raise ValueError("q must be a one-byte tensor of the shape of x")
+    if w.shape != (N,) or w.dtype != x.dtype:
+        raise ValueError("w must have shape (N,) and the dtype of x")
+    if scale.numel() != M or (rstd is not None and rstd.numel() != M):
+        raise ValueError("scale and rstd must hold M values")
+    args = [_mat(x, "x", N), _opt(residual, "residual"), _opt(residual_out, "residual_out"),
+            _mat(w, "w"), _mat(q, "q"), _vec(scale, "scale"), _vec(rstd, "rstd"), M, N,
+            float(eps), _dtype(x)]
+    lib = load_library()
+    if launch is None:
+        _check(lib.rmsnorm_fwd_fp8(*args, _stream(stream)))
+    else:
+        _check(lib.rmsnorm_fwd_fp8_ex(*args, ctypes.byref(launch.to_c()), _stream(stream)))
 
 
 def layernorm_bwd_workspace_bytes(M: int, N: int, dtype: torch.dtype) -> int:

@@ -623,6 +623,51 @@ int run_ln_bwd(const void *dy, const void *d_ro, const void *x, const void *w, c
     return RRN_OK;
 }
 
+// ---------------------------------------------------------------- RMSNorm -> fp8
+int run_quant(const void *x, const void *res, void *res_out, const void *w, void *q, float *scale,
+              float *rstd, int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,
+              cudaStream_t stream) {
+    int st = check_fwd(x, res, res_out, w, x, rstd, M, N, eps, dtype);
+    if (st != RRN_OK) return st;
+    if (!q || !scale) return RRN_ERR_NULL;
+    if (!aligned(scale, 4)) return RRN_ERR_ALIGN;
+    if (M == 0) return RRN_OK;
+    int sms = 0;
+    st = current_sm_count(&sms);
+    if (st != RRN_OK) return st;
+    const bool vec_ok = vec_path_ok({x, res, res_out, w, q}, N, dtype);
+    const int64_t nvec = N / (16 / elem_size(dtype));
+    const bool fused = res != nullptr;
+    Launch l{};
+    l.variant = cfg && cfg->variant ? cfg->variant : RRN_VARIANT_AUTO;
+    if (l.variant == RRN_VARIANT_AUTO)
+        l.variant = vec_ok && nvec <= kRowCtaMaxVec ? RRN_VARIANT_ROW_CTA : RRN_VARIANT_STREAM;
+    l.vec = l.variant == RRN_VARIANT_ROW_CTA;
+    if (l.variant == RRN_VARIANT_ROW_CTA) {
+        if (!vec_ok) return RRN_ERR_CONFIG;
+        st = pick_row_layout(nvec, M, sms, cfg, kMaxVpt, fwd_threads_limit, &l);
+        if (st != RRN_OK) return st;
+        l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid(M);
+    } else if (l.variant == RRN_VARIANT_STREAM) {
+        l.vpt = 1;
+        l.threads = cfg && cfg->threads ? cfg->threads : (N >= 512 ? 512 : round_up32(N));
+        if (l.threads < 32 || l.threads % 32 || l.threads > 1024) return RRN_ERR_CONFIG;
+        if (cfg && cfg->ctas) {
+            l.ctas = cfg->ctas;
+        } else {
+            const int occ = dtype == RRN_BF16 ? occupancy_quant_bf16(fused, l) : occupancy_quant_f32(fused, l);
+            const int64_t cap = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
+            l.ctas = clamp_grid(M < cap ? M : cap);
+        }
+    } else {
+        return RRN_ERR_CONFIG;
+    }
+    QuantArgs a{x, res, fused ? res_out : nullptr, w, q, scale, rstd, M, static_cast<int>(N), eps};
+    cudaError_t e = dtype == RRN_BF16 ? launch_quant_bf16(a, l, stream) : launch_quant_f32(a, l, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return RRN_OK;
+}
+
 void to_public(const Launch &l, rrn_launch *out) {
     out->variant = l.variant;
     out->vpt = l.vpt;
@@ -821,6 +866,21 @@ RRN_API int layernorm_bwd_ex(const void *dy, const void *d_residual_out, const v
                              rrn_stream_t stream) {
     return run_ln_bwd(dy, d_residual_out, x, w, mean, rstd, dx, dw, db, workspace, workspace_bytes,
                       M, N, eps, dtype, cfg, reinterpret_cast<cudaStream_t>(stream));
+}
+
+RRN_API int rmsnorm_fwd_fp8(const void *x, const void *residual, void *residual_out,
+                            const void *w, void *q, float *scale, float *rstd, int64_t M,
+                            int64_t N, float eps, int dtype, rrn_stream_t stream) {
+    return run_quant(x, residual, residual_out, w, q, scale, rstd, M, N, eps, dtype, nullptr,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+RRN_API int rmsnorm_fwd_fp8_ex(const void *x, const void *residual, void *residual_out,
+                               const void *w, void *q, float *scale, float *rstd, int64_t M,
+                               int64_t N, float eps, int dtype, const rrn_launch *cfg,
+                               rrn_stream_t stream) {
+    return run_quant(x, residual, residual_out, w, q, scale, rstd, M, N, eps, dtype, cfg,
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 RRN_API const char *rrn_status_string(int status) {

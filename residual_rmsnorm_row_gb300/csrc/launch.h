@@ -75,6 +75,20 @@ struct LnBwdArgs {
     int64_t rows_per_cta;
 };
 
+// Arguments of one RMSNorm -> fp8 e4m3 call (fused when res != nullptr).
+struct QuantArgs {
+    const void *x;
+    const void *res;
+    void *res_out;
+    const void *w;
+    void *q;        // [M, N] e4m3 codes
+    float *scale;   // [M]
+    float *rstd;    // may be nullptr
+    int64_t M;
+    int N;
+    float eps;
+};
+
 // A resolved launch (all fields set).
 struct Launch {
     int variant;  // rrn_variant, never AUTO here
@@ -115,6 +129,11 @@ cudaError_t launch_ln_bwd_f32(const LnBwdArgs &a, const Launch &l, cudaStream_t 
 // LayerNorm occupancy: bwd selects the kernel family, flag is FUSED (fwd) or ADDG (bwd).
 int occupancy_ln_bf16(bool bwd, bool flag, const Launch &l);
 int occupancy_ln_f32(bool bwd, bool flag, const Launch &l);
+
+cudaError_t launch_quant_bf16(const QuantArgs &a, const Launch &l, cudaStream_t stream);
+cudaError_t launch_quant_f32(const QuantArgs &a, const Launch &l, cudaStream_t stream);
+int occupancy_quant_bf16(bool fused, const Launch &l);
+int occupancy_quant_f32(bool fused, const Launch &l);
 
 // Occupancy (resident CTAs per SM) of the kernel a launch would run, with l.smem bytes of
 // dynamic shared memory; 0 on error.

@@ -1,0 +1,225 @@
+// RMSNorm (fused with the residual add when a residual is given) feeding an FP8 E4M3 output with
+// one fp32 scale per row - the norm fused with the neighbouring quantisation a following FP8
+// GEMM needs (the kind of cross-op fusion a persistent megakernel performs: Machete, "Core
+// Ideas"). Per row, in fp32:
+//   r = x (+ residual);  rstd = rsqrt(sum(r^2) / N + eps);  y = r * rstd * w
+//   amax = max |y|;  scale = amax / 448;  q = e4m3_satfinite_rn(y * (448 / amax))
+// (q = 0 and scale = 0 for a row whose y is all zero). residual_out = RN(r) as in the plain op.
+// The codes come from CUDA's paired fp32 -> e4m3 conversion with saturation to the finite range.
+#pragma once
+
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace rrn {
+
+// rstd from the CTA-wide sum of squares, with the rare rescaled path (see rstd_rescaled).
+template <typename Each>
+__device__ __forceinline__ float rms_rstd(Each each, float ss, float n_f, float eps,
+                                          float (&slots)[2][32], int &parity) {
+    if (!needs_rescale(ss)) return rstd_plain(ss, n_f, eps);
+    float am = 0.f;
+    each([&](float v) { am = fmaxf(am, fabsf(v)); });
+    am = cta_max(am, slots[parity]);
+    parity ^= 1;
+    const int e = rescale_exponent(am);
+    float s2 = 0.f;
+    each([&](float v) {
+        const float t = ldexpf(v, -e);
+        s2 = fmaf(t, t, s2);
+    });
+    s2 = cta_sum(s2, slots[parity]);
+    parity ^= 1;
+    return rstd_rescaled(s2, n_f, eps, e);
+}
+
+__device__ __forceinline__ uint16_t e4m3x2(float a, float b) {
+    return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+template <typename T, int VPT, bool FUSED>
+__global__ void __launch_bounds__(fwd_max_threads(VPT)) quant_row_cta(const QuantArgs a) {
+    using E = Elem<T>;
+    constexpr int V = E::kPerVec;  // 8 (bf16) or 4 (fp32) codes per vector: 8 or 4 bytes
+    __shared__ float slots[2][32];
+    const int nvec = a.N / V;
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const float n_f = static_cast<float>(a.N);
+
+    uint4 wv[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * nthr + tid;
+        if (c < nvec) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
+    }
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
+        const int64_t base = row * nvec;
+        uint4 xv[VPT], rv[VPT];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * nthr + tid;
+            if (c < nvec) {
+                xv[v] = ld_stream(static_cast<const uint4 *>(a.x) + base + c);
+                if (FUSED) rv[v] = ld_stream(static_cast<const uint4 *>(a.res) + base + c);
+            }
+        }
+        float ss = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * nthr + tid;
+            if (c < nvec) {
+                float f[V];
+                r_of<T, FUSED>(xv[v], rv[v], f);
+                if (FUSED) st_stream(static_cast<uint4 *>(a.res_out) + base + c, E::pack(f));
+#pragma unroll
+                for (int k = 0; k < V; ++k) ss = fmaf(f[k], f[k], ss);
+            }
+        }
+        ss = cta_sum(ss, slots[parity]);
+        parity ^= 1;
+        auto each = [&](auto fn) {
+#pragma unroll
+            for (int v = 0; v < VPT; ++v)
+                if (v * nthr + tid < nvec) {
+                    float f[V];
+                    r_of<T, FUSED>(xv[v], rv[v], f);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) fn(f[k]);
+                }
+        };
+        const float rs = rms_rstd(each, ss, n_f, a.eps, slots, parity);
+        // y = r * rstd * w, evaluated identically in both passes below
+        auto y_of = [&](int v, float (&o)[V]) {
+            float f[V], wf[V];
+            r_of<T, FUSED>(xv[v], rv[v], f);
+            E::unpack(wv[v], wf);
+#pragma unroll
+            for (int k = 0; k < V; ++k) o[k] = f[k] * rs * wf[k];
+        };
+        float am = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v)
+            if (v * nthr + tid < nvec) {
+                float o[V];
+                y_of(v, o);
+#pragma unroll
+                for (int k = 0; k < V; ++k) am = fmaxf(am, fabsf(o[k]));
+            }
+        am = cta_max(am, slots[parity]);
+        parity ^= 1;
+        const float inv = am > 0.f ? 448.f / am : 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * nthr + tid;
+            if (c < nvec) {
+                float o[V];
+                y_of(v, o);
+                uint16_t h[V / 2];
+#pragma unroll
+                for (int k = 0; k < V / 2; ++k) h[k] = e4m3x2(o[2 * k] * inv, o[2 * k + 1] * inv);
+                uint8_t *dst = static_cast<uint8_t *>(a.q) + (base + c) * V;
+                if constexpr (V == 8) {
+                    *reinterpret_cast<uint2 *>(dst) =
+                        make_uint2(h[0] | (static_cast<uint32_t>(h[1]) << 16),
+                                   h[2] | (static_cast<uint32_t>(h[3]) << 16));
+                } else {
+                    *reinterpret_cast<uint32_t *>(dst) = h[0] | (static_cast<uint32_t>(h[1]) << 16);
+                }
+            }
+        }
+        if (tid == 0) {
+            a.scale[row] = am / 448.f;
+            if (a.rstd) a.rstd[row] = rs;
+        }
+    }
+}
+
+// Any N and alignment: passes over global memory (sum of squares, amax, codes), one element at
+// a time. For odd widths and unaligned buffers; not a fast path.
+template <typename T, bool FUSED>
+__global__ void __launch_bounds__(1024) quant_stream(const QuantArgs a) {
+    using E = Elem<T>;
+    __shared__ float slots[2][32];
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const float n_f = static_cast<float>(a.N);
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
+        const int64_t base = row * static_cast<int64_t>(a.N);
+        auto r_at = [&](int j) {
+            float f = E::load1(a.x, base + j);
+            if constexpr (FUSED) f += E::load1(a.res, base + j);
+            return f;
+        };
+        auto each = [&](auto fn) {
+            for (int j = tid; j < a.N; j += nthr) fn(r_at(j));
+        };
+        float ss = 0.f;
+        for (int j = tid; j < a.N; j += nthr) {
+            const float f = r_at(j);
+            ss = fmaf(f, f, ss);
+        }
+        ss = cta_sum(ss, slots[parity]);
+        parity ^= 1;
+        const float rs = rms_rstd(each, ss, n_f, a.eps, slots, parity);
+        float am = 0.f;
+        for (int j = tid; j < a.N; j += nthr) am = fmaxf(am, fabsf(r_at(j) * rs * E::load1(a.w, j)));
+        am = cta_max(am, slots[parity]);
+        parity ^= 1;
+        const float inv = am > 0.f ? 448.f / am : 0.f;
+        for (int j = tid; j < a.N; j += nthr) {
+            const float f = r_at(j);
+            if constexpr (FUSED) E::store1(a.res_out, base + j, f);
+            const float y = f * rs * E::load1(a.w, j);
+            static_cast<uint8_t *>(a.q)[base + j] = static_cast<uint8_t>(e4m3x2(y * inv, 0.f) & 0xff);
+        }
+        if (tid == 0) {
+            a.scale[row] = am / 448.f;
+            if (a.rstd) a.rstd[row] = rs;
+        }
+    }
+}
+
+template <typename T, bool FUSED>
+const void *quant_kernel_ptr(const Launch &l) {
+    switch (l.variant) {
+        case RRN_VARIANT_ROW_CTA:
+            switch (l.vpt) {
+                case 1: return reinterpret_cast<const void *>(&quant_row_cta<T, 1, FUSED>);
+                case 2: return reinterpret_cast<const void *>(&quant_row_cta<T, 2, FUSED>);
+                case 4: return reinterpret_cast<const void *>(&quant_row_cta<T, 4, FUSED>);
+                case 8: return reinterpret_cast<const void *>(&quant_row_cta<T, 8, FUSED>);
+                default: return nullptr;
+            }
+        case RRN_VARIANT_STREAM:
+            return reinterpret_cast<const void *>(&quant_stream<T, FUSED>);
+        default: return nullptr;
+    }
+}
+
+template <typename T>
+cudaError_t launch_quant(const QuantArgs &a, const Launch &l, cudaStream_t stream) {
+    const void *k = a.res ? quant_kernel_ptr<T, true>(l) : quant_kernel_ptr<T, false>(l);
+    if (!k) return cudaErrorInvalidConfiguration;
+    QuantArgs args = a;
+    void *params[] = {&args};
+    return cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, 0, stream);
+}
+
+template <typename T>
+int occupancy_quant_t(bool fused, const Launch &l) {
+    const void *k = fused ? quant_kernel_ptr<T, true>(l) : quant_kernel_ptr<T, false>(l);
+    if (!k) return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, l.threads, 0) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+}  // namespace rrn

@@ -1,0 +1,121 @@
+"""GPU parity of RMSNorm (+ residual add) feeding fp8 e4m3 codes with a per-row scale.
+
+The codes are integers decided by rounding: where the exact target y / scale is farther than
+a small relative margin from every e4m3 rounding midpoint, the GPU code must equal the oracle's;
+within that margin (fp32 arithmetic can land on either side) either neighbouring code is valid,
+and the dequantised value must still be within half a step. scale and rstd are checked with the
+rstd bound; residual_out bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import residual_rmsnorm_row_gb300 as rrn
+import synth
+from gpu_util import bits_of, check_rstd, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+# relative distance to a midpoint below which both neighbouring codes are accepted: well above
+# the fp32 error of y * (448 / amax) (a few ulps, ~1e-6)
+MARGIN = 1e-5
+
+
+def e4m3_table():
+    codes = np.arange(256, dtype=np.uint8)
+    return torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def check_codes(q_gpu: np.ndarray, v_ref: np.ndarray, q_ref: np.ndarray, what: str):
+    table = e4m3_table()
+    pos = np.sort(table[:0x7F])                      # non-negative finite values
+    mids = (pos[:-1] + pos[1:]) / 2
+    a = np.abs(v_ref)
+    k = np.clip(np.searchsorted(mids, a), 0, len(mids) - 1)
+    near = np.minimum(np.abs(a - mids[k]), np.abs(a - mids[np.clip(k - 1, 0, len(mids) - 1)]))
+    ambiguous = near <= MARGIN * np.maximum(a, 2.0 ** -9)
+    exact_ok = (q_gpu == q_ref) | ambiguous
+    assert exact_ok.all(), (f"{what}: {int((~exact_ok).sum())} codes differ away from a midpoint; "
+                            f"first at {np.argwhere(~exact_ok)[0].tolist()}")
+    # ambiguous ones: a neighbour of the same sign, within half a step of the target
+    gv = table[q_gpu]
+    assert not np.isnan(gv).any(), f"{what}: NaN code"
+    idx = np.argwhere(ambiguous & (q_gpu != q_ref))
+    for i in idx[:1000]:
+        t = v_ref[tuple(i)]
+        j = np.searchsorted(pos, abs(t))
+        step = pos[min(j, len(pos) - 1)] - pos[max(j - 1, 0)]
+        assert abs(gv[tuple(i)] - t) <= step / 2 * (1 + 1e-3), f"{what}: bad code near a midpoint"
+
+
+def run(h, dtype, eps, fused, launch=None):
+    x = to_dev(h["x"], dtype)
+    w = to_dev(h["w"], dtype)
+    M, N = x.shape
+    res = to_dev(h["residual"], dtype) if fused else None
+    ro = torch.full_like(x, float("nan")) if fused else None
+    q = torch.full((M, N), 0x7F, dtype=torch.uint8, device="cuda")
+    scale = torch.full((M,), float("nan"), device="cuda")
+    rstd = torch.full((M,), float("nan"), device="cuda")
+    rrn.rmsnorm_fwd_fp8(x, res, ro, w, q, scale, rstd, eps, launch=launch)
+    torch.cuda.synchronize()
+    return q, scale, rstd, ro
+
+
+def compare(h, dtype, eps, fused, q, scale, rstd, ro, what=""):
+    r_ref, v_ref, q_ref, s_ref, rs_ref = oracle.rmsnorm_quant_fp8(
+        h["x"], h["residual"] if fused else None, h["w"], eps)
+    check_codes(q.cpu().numpy(), v_ref, q_ref, f"codes {what}")
+    check_rstd(rstd.cpu().numpy().astype(np.float64), rs_ref, "rstd")
+    s = scale.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(s - s_ref) <= 1e-5 * s_ref), f"scale {what}"
+    if fused:
+        assert np.array_equal(to_host(ro), bits_of(r_ref.astype(np.float32), dtype))
+
+
+def test_fp8_fused_full_size():
+    wl = synth.get("add_rmsnorm_fwd_16384x4096_bf16")
+    h = synth.make(wl)
+    q, scale, rstd, ro = run(h, "bf16", wl.eps, True)
+    for s in range(0, wl.M, 2048):
+        sl = slice(s, s + 2048)
+        hh = {k: h[k][sl] for k in ("x", "residual")}
+        hh["w"] = h["w"]
+        compare(hh, "bf16", wl.eps, True, q[sl], scale[sl], rstd[sl], ro[sl], f"rows {s}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("N", [1, 7, 1000, 1024, 4095, 4096, 7168, 8192, 20000])
+def test_fp8_variants(dtype, N):
+    M = 61
+    for fused in (False, True):
+        wl = synth.Workload("fp8", "add_rmsnorm_fwd" if fused else "rmsnorm_fwd", M, N, dtype,
+                            1e-6, 101, res_sigma=2.0)
+        h = synth.make(wl)
+        V = 8 if dtype == "bf16" else 4
+        launches = [None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0), rrn.Launch(rrn.VARIANT_STREAM, 0, 64, 5)]
+        if N % V == 0:
+            nvec = N // V
+            for vpt in (1, 2, 4, 8):
+                thr = -(-(-(-nvec // vpt)) // 32) * 32
+                if thr <= (256 if vpt == 8 else 512 if vpt == 4 else 1024):
+                    launches += [rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0),
+                                 rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 7)]
+        for launch in launches:
+            q, scale, rstd, ro = run(h, dtype, wl.eps, fused, launch)
+            compare(h, dtype, wl.eps, fused, q, scale, rstd, ro, str(launch))
+
+
+def test_fp8_zero_and_extreme_rows():
+    N = 4096
+    rng = np.random.default_rng(102)
+    rows = np.stack([np.zeros(N, np.float32), rng.standard_normal(N).astype(np.float32) * 1e30,
+                     np.full(N, 2.0, np.float32), rng.standard_normal(N).astype(np.float32)])
+    h = {"x": bits_of(rows, "bf16"), "w": bits_of(np.ones(N, np.float32), "bf16")}
+    for launch in (None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0)):
+        q, scale, rstd, _ = run(h, "bf16", 1e-6, False, launch)
+        compare(h, "bf16", 1e-6, False, q, scale, rstd, None, str(launch))
+        assert float(scale[0]) == 0.0 and int(q[0].max()) == 0
