@@ -38,7 +38,8 @@
  *   - Aliasing: an output may be the same buffer as an input of the same shape
  *     (residual_out == residual or x; y == x; dx == dy or x; d_r == dy, d_residual_out or
  *     residual_out). Any other overlap is undefined.
- *   - M == 0 is a no-op that returns RRN_OK and launches nothing.
+ *   - M == 0 is a no-op that returns RRN_OK and launches nothing (after dtype, N and eps are
+ *     checked); the pointers are then not examined and may be NULL.
  *   - Work is enqueued on `stream` (NULL: the legacy default stream) and the call returns
  *     without waiting. Argument errors return a nonzero code before anything is launched;
  *     a failed launch returns RRN_ERR_CUDA (rrn_last_cuda_error() gives the cudaError_t);

@@ -223,8 +223,7 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
         if (!vec_ok) l.variant = RRN_VARIANT_STREAM;
         else if (nvec <= 32 * kMaxVpt && M >= 4LL * sms) l.variant = RRN_VARIANT_ROW_WARP;
         else if (nvec <= kRowCtaMaxVec) l.variant = RRN_VARIANT_ROW_CTA;
-        else if (nvec <= static_cast<int64_t>(kMaxCluster) * kRowCtaMaxVec) l.variant = RRN_VARIANT_ROW_CLUSTER;
-        else l.variant = RRN_VARIANT_STREAM;
+        else l.variant = RRN_VARIANT_STREAM;  // measured faster than the cluster split for wide rows
     }
     l.vec = (l.variant == RRN_VARIANT_STREAM) ? vec_ok : true;
     l.stages = 0;
@@ -344,6 +343,7 @@ int check_fwd(const void *x, const void *res, const void *res_out, const void *w
               const float *rstd, int64_t M, int64_t N, float eps, int dtype) {
     int st = check_common(M, N, eps, dtype);
     if (st != RRN_OK) return st;
+    if (M == 0) return RRN_OK;  // nothing is read or written: pointers are not examined
     if (!x || !w || !y || (res && !res_out)) return RRN_ERR_NULL;
     const uintptr_t es = elem_size(dtype);
     if (!aligned(x, es) || !aligned(w, es) || !aligned(y, es) || (res && !aligned(res, es)) ||
@@ -382,10 +382,14 @@ int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
 
     Launch l{};
     l.variant = cfg && cfg->variant ? cfg->variant : RRN_VARIANT_AUTO;
-    if (l.variant == RRN_VARIANT_AUTO)
-        l.variant = (vec_ok && nvec <= static_cast<int64_t>(kBwdMaxVpt) * bwd_max_threads(kBwdMaxVpt))
-                        ? RRN_VARIANT_ROW_CTA
-                        : RRN_VARIANT_STREAM;
+    if (l.variant == RRN_VARIANT_AUTO) {
+        const bool regs = vec_ok && nvec <= static_cast<int64_t>(kBwdMaxVpt) * bwd_max_threads(kBwdMaxVpt);
+        // Three input rows (the fused backward): the TMA ring keeps enough bytes in flight,
+        // measured faster than the register variant; two input rows: the register variant.
+        l.variant = !regs ? RRN_VARIANT_STREAM
+                          : (add_grad && 3 * N * elem_size(dtype) <= kMaxDynSmem / 2 ? RRN_VARIANT_ROW_TMA
+                                                                                     : RRN_VARIANT_ROW_CTA);
+    }
     l.vec = (l.variant == RRN_VARIANT_STREAM) ? vec_ok : true;
     l.stages = 0;
     l.smem = 0;
@@ -398,7 +402,9 @@ int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
             if (cfg && cfg->vpt) {
                 l.vpt = cfg->vpt;
             } else {
-                l.vpt = ceil_pow2_vpt((nvec + kBwdTargetThreads - 1) / kBwdTargetThreads, kBwdMaxVpt);
+                // the TMA ring measured best with narrower CTAs (more of them per SM)
+                const int target = l.variant == RRN_VARIANT_ROW_TMA ? 128 : kBwdTargetThreads;
+                l.vpt = ceil_pow2_vpt((nvec + target - 1) / target, kBwdMaxVpt);
                 while (l.vpt < kBwdMaxVpt && nvec > static_cast<int64_t>(l.vpt) * bwd_max_threads(l.vpt)) l.vpt *= 2;
             }
             if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4) return RRN_ERR_CONFIG;
@@ -451,6 +457,7 @@ int check_bwd(const void *dy, const void *d_ro, const void *x, const void *w, co
               const void *dx, const float *dw, int64_t M, int64_t N, float eps, int dtype) {
     int st = check_common(M, N, eps, dtype);
     if (st != RRN_OK) return st;
+    if (M == 0) return RRN_OK;  // nothing is read or written: pointers are not examined
     if (!dy || !x || !w || !rstd || !dx || !dw) return RRN_ERR_NULL;
     const uintptr_t es = elem_size(dtype);
     if (!aligned(dy, es) || !aligned(x, es) || !aligned(w, es) || !aligned(dx, es) ||
@@ -588,8 +595,8 @@ int run_ln_fwd(const void *x, const void *res, void *res_out, const void *w, con
                const rrn_launch *cfg, cudaStream_t stream) {
     int st = check_fwd(x, res, res_out, w, y, rstd, M, N, eps, dtype);
     if (st != RRN_OK) return st;
-    if ((b && !aligned(b, elem_size(dtype))) || (mean && !aligned(mean, 4))) return RRN_ERR_ALIGN;
     if (M == 0) return RRN_OK;
+    if ((b && !aligned(b, elem_size(dtype))) || (mean && !aligned(mean, 4))) return RRN_ERR_ALIGN;
     Launch l;
     st = plan_ln_fwd(vec_path_ok({x, res, res_out, w, b, y}, N, dtype), res != nullptr, M, N, dtype,
                      cfg, &l);
@@ -606,9 +613,9 @@ int run_ln_bwd(const void *dy, const void *d_ro, const void *x, const void *w, c
                const rrn_launch *cfg, cudaStream_t stream) {
     int st = check_bwd(dy, d_ro, x, w, rstd, dx, dw, M, N, eps, dtype);
     if (st != RRN_OK) return st;
+    if (M == 0) return RRN_OK;
     if (!mean) return RRN_ERR_NULL;
     if (!aligned(mean, 4) || (db && !aligned(db, 4))) return RRN_ERR_ALIGN;
-    if (M == 0) return RRN_OK;
     Launch l;
     int64_t rpc = 0;
     st = plan_ln_bwd(vec_path_ok({dy, d_ro, x, w, dx}, N, dtype), d_ro != nullptr, M, N, dtype, cfg,
@@ -629,9 +636,9 @@ int run_quant(const void *x, const void *res, void *res_out, const void *w, void
               cudaStream_t stream) {
     int st = check_fwd(x, res, res_out, w, x, rstd, M, N, eps, dtype);
     if (st != RRN_OK) return st;
+    if (M == 0) return RRN_OK;
     if (!q || !scale) return RRN_ERR_NULL;
     if (!aligned(scale, 4)) return RRN_ERR_ALIGN;
-    if (M == 0) return RRN_OK;
     int sms = 0;
     st = current_sm_count(&sms);
     if (st != RRN_OK) return st;

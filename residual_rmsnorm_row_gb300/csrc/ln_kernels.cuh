@@ -45,9 +45,19 @@ __device__ __forceinline__ float2 cta_sum2(float a, float b, float (*slots)[32])
 // sum((r - mean)^2) = sum(d^2) - sum(d)^2 / N (the corrected two-pass algorithm), so the
 // rounding error of m0 - which grows with |mean|, not with the spread - cancels out.
 // Reductions alternate between the two slot pairs (parity), as cta_sum callers do.
+// The result keeps m0 and the small correction apart: deviations are formed as
+// (r - m0) - corr, so the fp32 rounding of the mean itself never enters them.
+struct LnStats {
+    float m0;    // first-pass mean
+    float corr;  // mean - m0
+    float rstd;
+    __device__ __forceinline__ float mean() const { return m0 + corr; }
+    __device__ __forceinline__ float dev(float r) const { return (r - m0) - corr; }
+};
+
 template <typename Each>
-__device__ __forceinline__ float2 ln_stats(Each each, float n_f, float eps,
-                                           float (&slots)[2][2][32], int &parity) {
+__device__ __forceinline__ LnStats ln_stats(Each each, float n_f, float eps,
+                                            float (&slots)[2][2][32], int &parity) {
     float s1 = 0.f;
     each([&](float v) { s1 += v; });
     s1 = cta_sum(s1, slots[parity][0]);
@@ -75,27 +85,30 @@ __device__ __forceinline__ float2 ln_stats(Each each, float n_f, float eps,
     });
     const float2 t2 = cta_sum2(d1, d2, slots[parity]);
     parity ^= 1;
-    const float mu = isfinite(t2.x) ? m0 + t2.x / n_f : m0;
+    LnStats st;
+    st.m0 = m0;
+    st.corr = isfinite(t2.x) ? t2.x / n_f : 0.f;
     float rs;
     if (!needs_rescale(t2.y)) {
         const float ssd = fmaxf(t2.y - t2.x * (t2.x / n_f), 0.f);
         rs = rstd_plain(ssd, n_f, eps);
     } else {  // rare: squared deviations out of fp32 range, or a constant row
         float am = 0.f;
-        each([&](float v) { am = fmaxf(am, fabsf(v - mu)); });
+        each([&](float v) { am = fmaxf(am, fabsf(st.dev(v))); });
         am = cta_max(am, slots[parity][0]);
         parity ^= 1;
         const int e = rescale_exponent(am);
         float t = 0.f;
         each([&](float v) {
-            const float d = ldexpf(v - mu, -e);
+            const float d = ldexpf(st.dev(v), -e);
             t = fmaf(d, d, t);
         });
         t = cta_sum(t, slots[parity][0]);
         parity ^= 1;
         rs = rstd_rescaled(t, n_f, eps, e);
     }
-    return make_float2(mu, rs);
+    st.rstd = rs;
+    return st;
 }
 
 template <typename T, int VPT, bool FUSED>
@@ -150,7 +163,7 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT)) ln_fwd_row_cta(const LnF
                     for (int k = 0; k < V; ++k) fn(f[k]);
                 }
         };
-        const float2 st = ln_stats(each, n_f, a.eps, slots, parity);
+        const LnStats st = ln_stats(each, n_f, a.eps, slots, parity);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * nthr + tid;
@@ -160,13 +173,13 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT)) ln_fwd_row_cta(const LnF
                 E::unpack(wv[v], wf);
                 E::unpack(bv[v], bf);
 #pragma unroll
-                for (int k = 0; k < V; ++k) o[k] = fmaf((f[k] - st.x) * st.y, wf[k], bf[k]);
+                for (int k = 0; k < V; ++k) o[k] = fmaf(st.dev(f[k]) * st.rstd, wf[k], bf[k]);
                 st_stream(static_cast<uint4 *>(a.y) + base + c, E::pack(o));
             }
         }
         if (tid == 0) {
-            if (a.mean) a.mean[row] = st.x;
-            if (a.rstd) a.rstd[row] = st.y;
+            if (a.mean) a.mean[row] = st.mean();
+            if (a.rstd) a.rstd[row] = st.rstd;
         }
     }
 }
@@ -209,7 +222,7 @@ __global__ void __launch_bounds__(1024) ln_fwd_stream(const LnFwdArgs a) {
                 for (int k = 0; k < V; ++k) fn(f[k]);
             }
         };
-        const float2 st = ln_stats(each, n_f, a.eps, slots, parity);
+        const LnStats st = ln_stats(each, n_f, a.eps, slots, parity);
         for (int c = tid; c < nchunk; c += nthr) {
             float f[W], wf[W], bf[W], o[W];
             load_r(base, c, f);
@@ -224,7 +237,7 @@ __global__ void __launch_bounds__(1024) ln_fwd_stream(const LnFwdArgs a) {
 #pragma unroll
                 for (int k = 0; k < V; ++k) bf[k] = 0.f;
 #pragma unroll
-            for (int k = 0; k < V; ++k) o[k] = fmaf((f[k] - st.x) * st.y, wf[k], bf[k]);
+            for (int k = 0; k < V; ++k) o[k] = fmaf(st.dev(f[k]) * st.rstd, wf[k], bf[k]);
             if constexpr (VEC) {
                 if constexpr (FUSED) st_stream(static_cast<uint4 *>(a.res_out) + base / W + c, E::pack(f));
                 st_stream(static_cast<uint4 *>(a.y) + base / W + c, E::pack(o));
@@ -234,8 +247,8 @@ __global__ void __launch_bounds__(1024) ln_fwd_stream(const LnFwdArgs a) {
             }
         }
         if (tid == 0) {
-            if (a.mean) a.mean[row] = st.x;
-            if (a.rstd) a.rstd[row] = st.y;
+            if (a.mean) a.mean[row] = st.mean();
+            if (a.rstd) a.rstd[row] = st.rstd;
         }
     }
 }

@@ -13,7 +13,7 @@ import torch
 import oracle
 import residual_rmsnorm_row_gb300 as rrn
 import synth
-from gpu_util import check_dw, check_out, to_dev, values
+from gpu_util import bwd_cond, check_dw, check_out, to_dev, values
 
 pytestmark = pytest.mark.gpu
 
@@ -67,9 +67,12 @@ def test_fused_backward_variants(dtype, N, with_dro):
     h = synth.make(wl)
     ref_dr, ref_dw = oracle.add_rmsnorm_bwd(h["dy"], h["d_ro"] if with_dro else None, h["x"],
                                             h["w"], wl.eps)
+    cond = bwd_cond(h["x"], h["dy"], h["w"], wl.eps)
+    if with_dro:
+        cond = cond + np.abs(oracle.decode(h["d_ro"]))
     for launch in _launches(dtype, N):
         d_r, dw = run_fused_bwd(h, dtype, wl.eps, launch, with_dro)
-        check_out(values(d_r), ref_dr, dtype, f"d_r {launch}")
+        check_out(values(d_r), ref_dr, dtype, f"d_r {launch}", cond)
         check_dw(dw.cpu().numpy().astype(np.float64), ref_dw, f"dw {launch}")
 
 
