@@ -78,7 +78,8 @@ typedef enum {
     RRN_ERR_ALIGN = 5,     /* a pointer is not aligned to its element size */
     RRN_ERR_WORKSPACE = 6, /* backward workspace NULL or smaller than required */
     RRN_ERR_CUDA = 7,      /* a CUDA runtime call or kernel launch failed */
-    RRN_ERR_CONFIG = 8     /* an explicit launch configuration cannot cover the row */
+    RRN_ERR_CONFIG = 8,    /* an explicit launch configuration cannot cover the row */
+    RRN_ERR_SCRATCH = 9    /* the problem needs more than the built-in scratch array holds */
 } rrn_status;
 
 /*
@@ -135,6 +136,26 @@ RRN_API int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t 
 RRN_API int rmsnorm_bwd(const void *dy, const void *x, const void *w, const float *rstd, void *dx,
                         float *dw, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
                         float eps, int dtype, rrn_stream_t stream);
+
+/*
+ * rmsnorm_bwd_noalloc - rmsnorm_bwd without a caller-provided workspace, for callers that
+ * cannot allocate device memory: code running while a CUDA graph is captured, plugins inside an
+ * engine that owns all device allocations, C callers without a caching allocator for whom a
+ * cudaMalloc/cudaFree pair per call would synchronise the device. (The source pages have no
+ * counterpart of this entry point; it is a deployment convenience of this library.)
+ *   Arguments, layout, results and determinism as for rmsnorm_bwd; no workspace arguments.
+ *   The dw partial sums live in one 8 MiB array of fp32 inside the library (a __device__
+ *   variable, held by every GPU that loads the library until the process exits). The stage-1
+ *   CTA count is lowered so that CTAs * N <= 2,097,152; N > 2,097,152 returns RRN_ERR_SCRATCH.
+ *   Nothing in the array needs to start at zero (stage 1 writes all that stage 2 reads).
+ *   All calls on a device share the array: calls whose kernels overlap on the GPU race - order
+ *   them on one stream. The first call on each device looks the array's address up (with that
+ *   device current); make that first call before any stream capture begins.
+ *   No cudaMalloc, cudaFree or other allocation happens. Returns an rrn_status.
+ */
+RRN_API int rmsnorm_bwd_noalloc(const void *dy, const void *x, const void *w, const float *rstd,
+                                void *dx, float *dw, int64_t M, int64_t N, float eps, int dtype,
+                                rrn_stream_t stream);
 
 /*
  * add_rmsnorm_bwd - backward of the fused residual Add + RMSNorm (add_rmsnorm_fwd), in one pass:

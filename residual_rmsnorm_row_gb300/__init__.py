@@ -41,6 +41,7 @@ from ._binding import (  # noqa: F401  (re-exported API)
     plan_fwd,
     rmsnorm_bwd,
     rmsnorm_bwd_ex,
+    rmsnorm_bwd_noalloc,
     rmsnorm_bwd_workspace_bytes,
     rmsnorm_fwd,
     rmsnorm_fwd_fp8,
@@ -209,5 +210,5 @@ __all__ = [
     "load_library", "rms_norm", "add_rms_norm", "rms_norm_backward", "device_faults",
     "add_rmsnorm_bwd", "add_rms_norm_backward", "RMSNormFunction", "AddRMSNormFunction", "RMSNorm",
     "layernorm_fwd", "layernorm_bwd", "layernorm_bwd_workspace_bytes", "layer_norm",
-    "layer_norm_backward", "rmsnorm_fwd_fp8", "rms_norm_fp8",
+    "layer_norm_backward", "rmsnorm_fwd_fp8", "rms_norm_fp8", "rmsnorm_bwd_noalloc",
 ]

@@ -28,7 +28,7 @@ VARIANT_NAMES = {VARIANT_ROW_CTA: "row_cta", VARIANT_ROW_WARP: "row_warp",
 
 STATUS_NAMES = {0: "RRN_OK", 1: "RRN_ERR_NULL", 2: "RRN_ERR_SHAPE", 3: "RRN_ERR_EPS",
                 4: "RRN_ERR_DTYPE", 5: "RRN_ERR_ALIGN", 6: "RRN_ERR_WORKSPACE",
-                7: "RRN_ERR_CUDA", 8: "RRN_ERR_CONFIG"}
+                7: "RRN_ERR_CUDA", 8: "RRN_ERR_CONFIG", 9: "RRN_ERR_SCRATCH"}
 
 
 class RRNError(RuntimeError):
@@ -85,6 +85,7 @@ _SIGNATURES = {
     "rmsnorm_bwd_workspace_bytes": (_i32, [_i64, _i64, _i32, ctypes.POINTER(_sz)]),
     "rmsnorm_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _f32, _i32, _vp]),
     "rrn_status_string": (ctypes.c_char_p, [_i32]),
+    "rmsnorm_bwd_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32, _vp]),
     "rrn_last_cuda_error": (_i32, []),
     "rrn_device_faults": (_i32, [ctypes.POINTER(ctypes.c_uint), _i32]),
     "rrn_selftest_wait_timeout": (_i32, [ctypes.c_uint64, _vp]),
@@ -258,6 +259,23 @@ def rmsnorm_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, rstd: torch.
         _mat(dy, "dy", N), _mat(x, "x"), _mat(w, "w"), _vec(rstd, "rstd"), _mat(dx, "dx"),
         _vec(dw, "dw"), _mat(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         M, N, float(eps), _dtype(x), _stream(stream)))
+
+
+def rmsnorm_bwd_noalloc(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, rstd: torch.Tensor,
+                        dx: torch.Tensor, dw: torch.Tensor, eps: float, stream=None) -> None:
+    """C ``rmsnorm_bwd_noalloc``: ``rmsnorm_bwd`` for callers that cannot allocate device memory
+    (the partial sums live in the library's own fixed 8 MiB device array; calls that overlap on
+    the GPU race on it, so order them on one stream)."""
+    M, N = _rows(x)
+    _same(x, dy, "dy")
+    _same(x, dx, "dx")
+    if w.shape != (N,) or w.dtype != x.dtype:
+        raise ValueError("w must have shape (N,) and the dtype of x")
+    if rstd.numel() != M or dw.numel() != N:
+        raise ValueError("rstd must hold M values and dw N values")
+    _check(load_library().rmsnorm_bwd_noalloc(
+        _mat(dy, "dy", N), _mat(x, "x"), _mat(w, "w"), _vec(rstd, "rstd"), _mat(dx, "dx"),
+        _vec(dw, "dw"), M, N, float(eps), _dtype(x), _stream(stream)))
 
 
 def rmsnorm_bwd_ex(dy, x, w, rstd, dx, dw, workspace, eps, launch: Optional[Launch] = None,

@@ -901,6 +901,7 @@ RRN_API const char *rrn_status_string(int status) {
         case RRN_ERR_WORKSPACE: return "workspace is NULL, unaligned or smaller than required";
         case RRN_ERR_CUDA: return "a CUDA call or kernel launch failed (see rrn_last_cuda_error)";
         case RRN_ERR_CONFIG: return "the launch configuration cannot run this problem";
+        case RRN_ERR_SCRATCH: return "the problem needs more than the built-in scratch array holds";
         default: return "unknown status";
     }
 }
