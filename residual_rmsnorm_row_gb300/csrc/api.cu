@@ -440,15 +440,10 @@ int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
         want = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
     }
     if (want < 1) return RRN_ERR_CONFIG;
-    if (M == 0) {
-        l.ctas = 0;
-        *rows_per_cta = 0;
-    } else {
-        if (want > M) want = M;
-        const int64_t rpc = (M + want - 1) / want;
-        l.ctas = clamp_grid((M + rpc - 1) / rpc);  // every CTA owns at least one row
-        *rows_per_cta = rpc;
-    }
+    // CTA p takes rows p, p + P, ...: with P <= M every CTA owns at least one row (so every
+    // workspace row stage 2 reads is written).
+    l.ctas = M == 0 ? 0 : clamp_grid(want < M ? want : M);
+    *rows_per_cta = M == 0 ? 0 : (M + l.ctas - 1) / l.ctas;
     *out = l;
     return RRN_OK;
 }
@@ -483,7 +478,7 @@ int run_bwd(const void *dy, const void *d_ro, const void *x, const void *w, cons
     st = fault_word(&faults);
     if (st != RRN_OK) return st;
     BwdArgs a{dy, d_ro, x, w, rstd, dx, dw, static_cast<float *>(workspace), M,
-              static_cast<int>(N), rpc, 0, faults};
+              static_cast<int>(N), 0, faults};
     cudaError_t e = dtype == RRN_BF16 ? launch_bwd_bf16(a, l, stream) : launch_bwd_f32(a, l, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return RRN_OK;
@@ -577,15 +572,8 @@ int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, con
         want = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
     }
     if (want < 1) return RRN_ERR_CONFIG;
-    if (M == 0) {
-        l.ctas = 0;
-        *rows_per_cta = 0;
-    } else {
-        if (want > M) want = M;
-        const int64_t rpc = (M + want - 1) / want;
-        l.ctas = clamp_grid((M + rpc - 1) / rpc);
-        *rows_per_cta = rpc;
-    }
+    l.ctas = M == 0 ? 0 : clamp_grid(want < M ? want : M);
+    *rows_per_cta = M == 0 ? 0 : (M + l.ctas - 1) / l.ctas;
     *out = l;
     return RRN_OK;
 }
@@ -624,7 +612,7 @@ int run_ln_bwd(const void *dy, const void *d_ro, const void *x, const void *w, c
     const size_t need = 2 * static_cast<size_t>(l.ctas) * static_cast<size_t>(N) * sizeof(float);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return RRN_ERR_WORKSPACE;
     LnBwdArgs a{dy, d_ro, x, w, mean, rstd, dx, dw, db, static_cast<float *>(workspace), M,
-                static_cast<int>(N), rpc};
+                static_cast<int>(N)};
     cudaError_t e = dtype == RRN_BF16 ? launch_ln_bwd_bf16(a, l, stream) : launch_ln_bwd_f32(a, l, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return RRN_OK;
@@ -717,7 +705,7 @@ RRN_API int rmsnorm_fwd(const void *x, const void *w, void *y, float *rstd, int6
 RRN_API int add_rmsnorm_fwd(const void *x, const void *residual, void *residual_out, const void *w,
                             void *y, float *rstd, int64_t M, int64_t N, float eps, int dtype,
                             rrn_stream_t stream) {
-    if (!residual) return RRN_ERR_NULL;
+    if (!residual && M != 0) return RRN_ERR_NULL;  // (with M == 0 nothing is examined)
     return run_fwd(x, residual, residual_out, w, y, rstd, M, N, eps, dtype, nullptr,
                    reinterpret_cast<cudaStream_t>(stream));
 }
@@ -823,7 +811,7 @@ RRN_API int layernorm_fwd(const void *x, const void *w, const void *b, void *y, 
 RRN_API int add_layernorm_fwd(const void *x, const void *residual, void *residual_out,
                               const void *w, const void *b, void *y, float *mean, float *rstd,
                               int64_t M, int64_t N, float eps, int dtype, rrn_stream_t stream) {
-    if (!residual) return RRN_ERR_NULL;
+    if (!residual && M != 0) return RRN_ERR_NULL;  // (with M == 0 nothing is examined)
     return run_ln_fwd(x, residual, residual_out, w, b, y, mean, rstd, M, N, eps, dtype, nullptr,
                       reinterpret_cast<cudaStream_t>(stream));
 }

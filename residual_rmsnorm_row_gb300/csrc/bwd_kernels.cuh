@@ -3,9 +3,10 @@
 // Per row (xhat = x * rstd, g = dy * w, c = sum(g * xhat) / N):
 //   dx = rstd * (g - xhat * c)
 // and dw = sum over rows of dy * xhat, reduced in two fixed-order stages:
-//   stage 1  CTA p owns a contiguous block of rows; each thread keeps the dw partial sums of
-//            its own columns in registers across those rows and writes them once to row p of
-//            a [P, N] fp32 workspace.
+//   stage 1  CTA p owns rows p, p + P, p + 2P, ... (P CTAs; consecutive CTAs work on adjacent
+//            rows at any moment, so HBM is read as one stream); each thread keeps the dw partial
+//            sums of its own columns in registers across those rows and writes them once to row
+//            p of a [P, N] fp32 workspace.
 //   stage 2  dw[j] = sum over p of workspace[p, j], in a fixed order (rows p = g, g+G, ...
 //            per group g, then the G group sums in order). No atomics anywhere, so dw is
 //            bitwise reproducible for a given (M, N, dtype, device).
@@ -127,10 +128,8 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_cta(const BwdArg
     float dw[VPT][V];
     bwd_prologue<T, VPT>(a, nvec, wv, dw);
 
-    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta;
-    const int64_t row1 = min(a.M, row0 + a.rows_per_cta);
     int parity = 0;
-    for (int64_t row = row0; row < row1; ++row) {
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
         const int64_t base = row * nvec;
         uint4 xv[VPT], dyv[VPT], gv[VPT];
 #pragma unroll
@@ -148,9 +147,9 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_cta(const BwdArg
     bwd_store_partial<T, VPT>(a, nvec, dw);
 }
 
-// Stage 1 fed by the TMA engine: CTA p owns the contiguous rows [p * R, (p + 1) * R) and keeps
-// a.stages of them (x and dy) in flight in a shared-memory ring filled with cp.async.bulk,
-// refilling a slot as soon as the CTA-wide dot product of its row is done.
+// Stage 1 fed by the TMA engine: CTA p owns rows p, p + P, ... and keeps a.stages of them (x,
+// dy and, fused, d_ro) in flight in a shared-memory ring filled with cp.async.bulk, refilling a
+// slot as soon as the CTA-wide dot product of its row is done.
 template <typename T, int VPT, bool ADDG>
 __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArgs a) {
     constexpr int V = Elem<T>::kPerVec;
@@ -165,13 +164,14 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArg
     const int nthr = blockDim.x;
     const uint32_t row_bytes = static_cast<uint32_t>(a.N) * static_cast<uint32_t>(sizeof(T));
     const int S = a.stages;
-    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta;
-    const int64_t nrows = max(static_cast<int64_t>(0), min(a.M, row0 + a.rows_per_cta) - row0);
+    const int64_t first = blockIdx.x;
+    const int64_t stride = gridDim.x;
+    const int64_t nrows = first < a.M ? (a.M - 1 - first) / stride + 1 : 0;
 
     auto slot = [&](int s, int t) { return ring + static_cast<size_t>(s * NT + t) * row_bytes; };
     auto issue = [&](int64_t k) {
         const int s = static_cast<int>(k % S);
-        const int64_t off = (row0 + k) * static_cast<int64_t>(row_bytes);
+        const int64_t off = (first + k * stride) * static_cast<int64_t>(row_bytes);
         mbar_arrive_expect_tx(&full[s], NT * row_bytes);
         bulk_g2s(slot(s, 0), static_cast<const char *>(a.x) + off, row_bytes, &full[s]);
         bulk_g2s(slot(s, 1), static_cast<const char *>(a.dy) + off, row_bytes, &full[s]);
@@ -207,8 +207,8 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArg
                 if constexpr (ADDG) gv[v] = ld_shared_v4(slot(s, 2) + static_cast<size_t>(c) * 16);
             }
         }
-        const bool done = bwd_row_body<T, VPT, ADDG>(a, row0 + k, nvec, xv, dyv, gv, wv, dw, slots,
-                                                     parity, [&] {
+        const bool done = bwd_row_body<T, VPT, ADDG>(a, first + k * stride, nvec, xv, dyv, gv, wv, dw,
+                                                     slots, parity, [&] {
             if (abort_flag) return false;
             if (tid == 0 && k + S < nrows) {
                 fence_proxy_async();
@@ -242,10 +242,8 @@ __global__ void __launch_bounds__(1024) bwd_stream(const BwdArgs a) {
     const float n_f = static_cast<float>(a.N);
     float *prow = a.partial + static_cast<int64_t>(blockIdx.x) * a.N;
 
-    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta;
-    const int64_t row1 = min(a.M, row0 + a.rows_per_cta);
     int parity = 0;
-    for (int64_t row = row0; row < row1; ++row) {
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
         const int64_t base = row * static_cast<int64_t>(a.N);
         const float rs = __ldg(a.rstd + row);
         float dot = 0.f;
@@ -267,7 +265,7 @@ __global__ void __launch_bounds__(1024) bwd_stream(const BwdArgs a) {
         dot = cta_sum(dot, slots[parity]);
         parity ^= 1;
         const float cm = dot / n_f;
-        const bool first = (row == row0);
+        const bool first = (row == blockIdx.x);
         for (int c = tid; c < nchunk; c += nthr) {
             float xf[W], df[W], wf[W], o[W];
             if constexpr (VEC) {
@@ -308,14 +306,15 @@ __global__ void __launch_bounds__(1024) bwd_stream(const BwdArgs a) {
 }
 
 // Stage 2: dw[j] = sum_p partial[p, j]. A CTA covers 32 consecutive columns with
-// G = kReduceThreads / 32 row groups (one warp each); group g adds rows p = g, g + G, g + 2G, ...
-// in that order (eight loads in flight, the additions still in sequence), then one warp adds
-// the G group sums in group order. The order depends only on (P, N), so dw is reproducible.
+// G = THREADS / 32 row groups (one warp each); group g adds rows p = g, g + G, g + 2G, ...
+// in that order - up to U of its loads are issued before the first addition, so a thread waits
+// for memory about once per U rows - then one warp adds the G group sums in group order. The
+// order depends only on (P, N), so dw is reproducible.
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS)
     bwd_dw_reduce(const float *__restrict__ partial, float *__restrict__ dw, int P, int N) {
     constexpr int G = THREADS / 32;
-    constexpr int U = 8;
+    constexpr int U = 48;
     __shared__ float sums[G][33];
     const int lane = threadIdx.x & 31;
     const int grp = threadIdx.x >> 5;
@@ -323,15 +322,17 @@ __global__ void __launch_bounds__(THREADS)
     float acc = 0.f;
     if (col < N) {
         const float *src = partial + col;
-        int p = grp;
-        for (; p + (U - 1) * G < P; p += U * G) {
+        for (int p0 = grp; p0 < P; p0 += U * G) {
             float v[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) v[u] = __ldcg(src + static_cast<int64_t>(p + u * G) * N);
+            for (int u = 0; u < U; ++u) {
+                const int p = p0 + u * G;
+                v[u] = p < P ? src[static_cast<int64_t>(p) * N] : 0.f;
+            }
 #pragma unroll
-            for (int u = 0; u < U; ++u) acc += v[u];
+            for (int u = 0; u < U; ++u)
+                if (p0 + u * G < P) acc += v[u];
         }
-        for (; p < P; p += G) acc += __ldcg(src + static_cast<int64_t>(p) * N);
     }
     sums[grp][lane] = acc;
     __syncthreads();
@@ -372,7 +373,7 @@ const void *bwd_kernel_ptr_any(bool add_grad, const Launch &l) {
     return add_grad ? bwd_kernel_ptr<T, true>(l) : bwd_kernel_ptr<T, false>(l);
 }
 
-// Stage 1 on l.ctas CTAs (each owning a.rows_per_cta rows), then stage 2, on one stream.
+// Stage 1 on l.ctas CTAs (CTA p owning rows p, p + ctas, ...), then stage 2, on one stream.
 template <typename T>
 cudaError_t launch_bwd(const BwdArgs &a, const Launch &l, cudaStream_t stream) {
     const void *k = bwd_kernel_ptr_any<T>(a.d_ro != nullptr, l);

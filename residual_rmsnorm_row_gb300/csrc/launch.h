@@ -24,7 +24,8 @@ struct FwdArgs {
     unsigned int *faults;    // the library's device fault word
 };
 
-// Arguments of one backward call. `partial` is the [P, N] fp32 workspace (P = ctas).
+// Arguments of one backward call. `partial` is the [P, N] fp32 workspace (P = ctas; CTA p
+// handles rows p, p + P, ...).
 // d_ro (nullable) is the gradient arriving at residual_out in the fused op; it is added to dx.
 struct BwdArgs {
     const void *dy;
@@ -37,7 +38,6 @@ struct BwdArgs {
     float *partial;
     int64_t M;
     int N;
-    int64_t rows_per_cta;
     int stages;              // shared-memory ring depth (TMA variant)
     unsigned int *faults;    // the library's device fault word
 };
@@ -72,7 +72,6 @@ struct LnBwdArgs {
     float *partial;
     int64_t M;
     int N;
-    int64_t rows_per_cta;
 };
 
 // Arguments of one RMSNorm -> fp8 e4m3 call (fused when res != nullptr).
@@ -107,7 +106,7 @@ constexpr int kMaxVpt = 8;
 constexpr int fwd_max_threads(int vpt) { return vpt >= 8 ? 256 : vpt >= 4 ? 512 : 1024; }
 constexpr int bwd_max_threads(int vpt) { return vpt >= 4 ? 256 : 512; }
 constexpr int kBwdMaxVpt = 4;
-constexpr int kReduceThreads = 1024; // dw stage-2 CTA size: 32 columns x 32 row groups
+constexpr int kReduceThreads = 512;  // dw stage-2 CTA size: 32 columns x 16 row groups
 constexpr int kMaxStages = 8;        // deepest shared-memory ring of the TMA variants
 constexpr int kMaxCluster = 8;       // largest (portable) thread-block cluster
 

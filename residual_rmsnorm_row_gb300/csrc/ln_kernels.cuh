@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(1024) ln_fwd_stream(const LnFwdArgs a) {
 }
 
 // ------------------------------------------------------------------------------ backward
-// Stage 1, rows in registers: CTA p owns rows [p * R, (p + 1) * R); dw and db partials stay in
+// Stage 1, rows in registers: CTA p owns rows p, p + P, p + 2P, ...; dw and db partials stay in
 // registers and go to rows p of the two [P, N] workspace halves.
 template <typename T, int VPT, bool ADDG>
 __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_cta(const LnBwdArgs a) {
@@ -275,10 +275,8 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_cta(const LnB
 #pragma unroll
         for (int k = 0; k < V; ++k) dw[v][k] = db[v][k] = 0.f;
     }
-    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta;
-    const int64_t row1 = min(a.M, row0 + a.rows_per_cta);
     int parity = 0;
-    for (int64_t row = row0; row < row1; ++row) {
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
         const int64_t base = row * nvec;
         uint4 xv[VPT], dyv[VPT], gv[VPT];
 #pragma unroll
@@ -379,10 +377,8 @@ __global__ void __launch_bounds__(1024) ln_bwd_stream(const LnBwdArgs a) {
             wf[0] = E::load1(a.w, c);
         }
     };
-    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * a.rows_per_cta;
-    const int64_t row1 = min(a.M, row0 + a.rows_per_cta);
     int parity = 0;
-    for (int64_t row = row0; row < row1; ++row) {
+    for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
         const int64_t base = row * static_cast<int64_t>(a.N);
         const float mu = __ldg(a.mean + row);
         const float rs = __ldg(a.rstd + row);
@@ -400,7 +396,7 @@ __global__ void __launch_bounds__(1024) ln_bwd_stream(const LnBwdArgs a) {
         const float2 t = cta_sum2(sg, sgx, slots[parity]);
         parity ^= 1;
         const float mg = t.x / n_f, mgx = t.y / n_f;
-        const bool first = (row == row0);
+        const bool first = (row == blockIdx.x);
         for (int c = tid; c < nchunk; c += nthr) {
             float xf[W], df[W], wf[W], o[W];
             load(base, c, xf, df, wf);
