@@ -458,7 +458,7 @@ def measure_shape(name: str, dev, reps: int):
     if "layernorm" in wl.op:
         plan = "layernorm planner (row_cta or stream)"
     elif wl.op in ("rmsnorm_bwd", "add_rmsnorm_bwd"):
-        plan = rrn.plan_bwd(sets[0]["dy"], sets[0]["x"], w, outs[0]["y"]).name
+        plan = rrn.plan_bwd(sets[0]["dy"], sets[0]["x"], w, outs[0]["y"], sets[0].get("d_ro")).name
     else:
         plan = rrn.plan_fwd(sets[0]["x"], sets[0].get("residual"), outs[0]["ro"], w, outs[0]["y"]).name
     return {"workload": name, "op": wl.op, "M": M, "N": N, "dtype": wl.dtype, "us": round(us, 2),

@@ -284,20 +284,27 @@ typedef struct {
     int threads; /* threads per CTA (a multiple of 32, at most 1024) */
     int ctas;    /* CTAs in the grid; each walks rows with a grid-sized stride */
     int stages;  /* RRN_VARIANT_ROW_TMA: rows in flight per CTA, 1..8 */
-    int cluster; /* RRN_VARIANT_ROW_CLUSTER: CTAs per cluster, 2..8 (ctas: a multiple of it) */
+    int cluster; /* forward RRN_VARIANT_ROW_CLUSTER: CTAs per cluster, 2..8 (ctas a multiple of
+                    it). Backward (ROW_CTA, ROW_TMA): 2, 4 or 8 = add the dw partial sums of
+                    that many stage-1 CTAs through distributed shared memory before stage 2
+                    (used when there are at least twice that many CTAs; the CTA count is
+                    rounded down to a multiple of it), 1 = no clusters, 0 = the planner's
+                    choice (currently no clusters). */
     int vec;     /* output of rrn_plan_*: 1 when the 128-bit vector path is used */
 } rrn_launch;
 
 /*
  * rrn_plan_fwd / rrn_plan_bwd - the configuration the automatic entry points would use for
  * these arguments (the pointers only matter for their alignment; they are not dereferenced).
- * `residual` NULL plans the plain forward. Returns an rrn_status.
+ * `residual` NULL plans the plain forward; `d_residual_out` NULL plans rmsnorm_bwd, non-NULL
+ * add_rmsnorm_bwd (x is then residual_out and dx is d_r). Returns an rrn_status.
  */
 RRN_API int rrn_plan_fwd(const void *x, const void *residual, const void *residual_out,
                          const void *w, const void *y, int64_t M, int64_t N, int dtype,
                          rrn_launch *out);
-RRN_API int rrn_plan_bwd(const void *dy, const void *x, const void *w, const void *dx, int64_t M,
-                         int64_t N, int dtype, rrn_launch *out);
+RRN_API int rrn_plan_bwd(const void *dy, const void *d_residual_out, const void *x,
+                         const void *w, const void *dx, int64_t M, int64_t N, int dtype,
+                         rrn_launch *out);
 
 /*
  * add_rmsnorm_fwd_ex - add_rmsnorm_fwd (residual != NULL) or rmsnorm_fwd (residual == NULL,

@@ -71,7 +71,7 @@ class Launch:
     def name(self) -> str:
         base = VARIANT_NAMES.get(self.variant, "auto")
         st = f",stages={self.stages}" if self.variant == VARIANT_ROW_TMA else ""
-        st += f",cluster={self.cluster}" if self.variant == VARIANT_ROW_CLUSTER else ""
+        st += f",cluster={self.cluster}" if self.cluster > 1 else ""
         return f"{base}(vpt={self.vpt},threads={self.threads},ctas={self.ctas}{st},vec={self.vec})"
 
 
@@ -90,7 +90,7 @@ _SIGNATURES = {
     "rrn_device_faults": (_i32, [ctypes.POINTER(ctypes.c_uint), _i32]),
     "rrn_selftest_wait_timeout": (_i32, [ctypes.c_uint64, _vp]),
     "rrn_plan_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, ctypes.POINTER(rrn_launch)]),
-    "rrn_plan_bwd": (_i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i32, ctypes.POINTER(rrn_launch)]),
+    "rrn_plan_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, ctypes.POINTER(rrn_launch)]),
     "add_rmsnorm_fwd_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32,
                                   ctypes.POINTER(rrn_launch), _vp]),
     "rmsnorm_bwd_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _f32, _i32,
@@ -436,10 +436,13 @@ def selftest_wait_timeout(limit_ns: int = 50_000_000, stream=None) -> None:
     _check(load_library().rrn_selftest_wait_timeout(int(limit_ns), _stream(stream)))
 
 
-def plan_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, dx: torch.Tensor) -> Launch:
-    """C ``rrn_plan_bwd``: the stage-1 launch the automatic backward would use."""
+def plan_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, dx: torch.Tensor,
+             d_residual_out: Optional[torch.Tensor] = None) -> Launch:
+    """C ``rrn_plan_bwd``: the stage-1 launch the automatic backward would use
+    (``d_residual_out`` given: the fused backward's)."""
     M, N = _rows(x)
     out = rrn_launch()
-    _check(load_library().rrn_plan_bwd(dy.data_ptr(), x.data_ptr(), w.data_ptr(), dx.data_ptr(),
-                                       M, N, _dtype(x), ctypes.byref(out)))
+    dro = None if d_residual_out is None else d_residual_out.data_ptr()
+    _check(load_library().rrn_plan_bwd(dy.data_ptr(), dro, x.data_ptr(), w.data_ptr(),
+                                       dx.data_ptr(), M, N, _dtype(x), ctypes.byref(out)))
     return Launch.from_c(out)

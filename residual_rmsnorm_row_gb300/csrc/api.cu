@@ -90,9 +90,10 @@ int fault_word(unsigned int **out) {
     return RRN_OK;
 }
 
-// Occupancy per (device, kernel instance, block size, dynamic shared memory), computed once.
+// Occupancy per (device, kernel instance, block size, dynamic shared memory, cluster size),
+// computed once.
 std::mutex g_occ_mutex;
-std::map<std::tuple<int, int, int, int, int, int, int, int, int>, int> g_occ;
+std::map<std::tuple<int, int, int, int, int, int, int, int, int, int>, int> g_occ;
 
 int occupancy(bool bwd, int dtype, bool fused, const Launch &l) {
     int dev = 0;
@@ -101,7 +102,7 @@ int occupancy(bool bwd, int dtype, bool fused, const Launch &l) {
         return 0;
     }
     const auto key = std::make_tuple(dev, bwd ? 1 : 0, dtype, fused ? 1 : 0, l.variant, l.vpt,
-                                     l.threads, l.vec ? 1 : 0, l.smem);
+                                     l.threads, l.vec ? 1 : 0, l.smem, l.cluster);
     {
         std::lock_guard<std::mutex> g(g_occ_mutex);
         auto it = g_occ.find(key);
@@ -122,7 +123,7 @@ int occupancy_ln(bool bwd, int dtype, bool flag, const Launch &l) {
         return 0;
     }
     const auto key = std::make_tuple(dev, 2 + (bwd ? 1 : 0), dtype, flag ? 1 : 0, l.variant, l.vpt,
-                                     l.threads, l.vec ? 1 : 0, l.smem);
+                                     l.threads, l.vec ? 1 : 0, l.smem, l.cluster);
     {
         std::lock_guard<std::mutex> g(g_occ_mutex);
         auto it = g_occ.find(key);
@@ -160,24 +161,32 @@ int clamp_grid(int64_t v) {
     return v > INT32_MAX ? INT32_MAX : static_cast<int>(v);
 }
 
-// Threads per CTA the row-per-CTA forward aims for on large M: 8 CTAs of 256 threads fill an
-// SM, each with one 128-bit load per tensor per VPT in flight.
-constexpr int kFwdTargetThreads = 256;
+// Threads per CTA the row-per-CTA forward aims for on large M (VPT grows with N): measured best
+// across N = 4096 and 7168 (narrow CTAs with many vectors per thread, several CTAs per SM).
+constexpr int kFwdTargetThreads = 128;
 constexpr int kBwdTargetThreads = 256;
 // Widest row (in 128-bit vectors) one CTA holds in registers: 8 vectors x 256 threads.
 constexpr int kRowCtaMaxVec = 2048;
+// Vectors of a row each CTA of the cluster split takes when the planner chooses the cluster
+// size (measured best: 4 vectors x 128 threads a CTA, several CTAs per SM).
+constexpr int kClusterChunkVec = 512;
+// CTAs per cluster for the backward's distributed-shared-memory pre-reduction of dw when the
+// caller leaves the choice to the planner (0: no clusters).
+constexpr int kBwdCluster = 0;
 
 // Largest dynamic shared memory one CTA may use (sm_100-class parts: 227 KB).
 constexpr int kMaxDynSmem = 227 * 1024;
-// Keep this much of an SM's shared memory free for the static parts and the runtime.
-constexpr int kSmemPerSm = 220 * 1024;
 
-// Pick the ring depth for a TMA variant whose one-row slot takes `slot_bytes`: the depth that
-// keeps the most bytes in flight per SM (resident CTAs x depth x slot), preferring the
-// shallower ring (more CTAs) on ties. Fills l->stages, l->smem; returns CTAs per SM (0: none).
+// Pick the ring depth for a TMA variant whose one-row slot takes `slot_bytes`. Resident CTAs
+// per SM come first (measured on the 16384 x 4096 bf16 backward: 4 CTAs x 2 stages 71.8 us,
+// 2 CTAs x 7 stages 96.8 us); among the depths that keep the most CTAs resident, the shallowest
+// from 2 up that keeps kRingTargetBytes per SM in flight (else the deepest of them). Returns
+// the CTAs per SM (0: no depth fits); sets l->stages and l->smem.
+constexpr int64_t kRingTargetBytes = 64 * 1024;
+
 int plan_ring(bool bwd, int dtype, bool fused, int slot_bytes, int want_stages, Launch *l) {
-    int best_occ = 0, best_s = 0;
-    int64_t best_inflight = -1;
+    int occ_of[kMaxStages + 1] = {};
+    int best_occ = 0;
     for (int S = 1; S <= kMaxStages; ++S) {
         if (want_stages && S != want_stages) continue;
         const int64_t smem = static_cast<int64_t>(S) * slot_bytes;
@@ -185,19 +194,18 @@ int plan_ring(bool bwd, int dtype, bool fused, int slot_bytes, int want_stages, 
         Launch t = *l;
         t.stages = S;
         t.smem = static_cast<int>(smem);
-        const int occ = occupancy(bwd, dtype, fused, t);
-        if (occ < 1) continue;
-        int64_t inflight = static_cast<int64_t>(occ) * S * slot_bytes;
-        if (inflight > kSmemPerSm) inflight = kSmemPerSm;  // beyond this the ring adds nothing
-        if (inflight > best_inflight) {
-            best_inflight = inflight;
-            best_occ = occ;
-            best_s = S;
-        }
+        occ_of[S] = occupancy(bwd, dtype, fused, t);
+        if (occ_of[S] > best_occ) best_occ = occ_of[S];
     }
-    if (!best_occ) return 0;
-    l->stages = best_s;
-    l->smem = best_s * slot_bytes;
+    if (best_occ < 1) return 0;
+    int pick = 0;
+    for (int S = 1; S <= kMaxStages; ++S) {
+        if (occ_of[S] != best_occ) continue;
+        pick = S;
+        if (S >= 2 && static_cast<int64_t>(best_occ) * S * slot_bytes >= kRingTargetBytes) break;
+    }
+    l->stages = pick;
+    l->smem = pick * slot_bytes;
     return best_occ;
 }
 
@@ -220,10 +228,16 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
     Launch l{};
     l.variant = cfg && cfg->variant ? cfg->variant : RRN_VARIANT_AUTO;
     if (l.variant == RRN_VARIANT_AUTO) {
+        // Measured on 16384 x {4096, 7168, 16384}, 8192 x 32768, 4096 x 65536, 1024 x 262144
+        // bf16: one row per CTA while a 128-thread CTA holds the row (8 vectors a thread);
+        // wider rows split over a cluster, at most kClusterChunkVec vectors per CTA; wider
+        // still, the two-pass kernel. Few rows (decode): one CTA per row up to kRowCtaMaxVec.
+        const bool few = M < 2LL * sms;
         if (!vec_ok) l.variant = RRN_VARIANT_STREAM;
         else if (nvec <= 32 * kMaxVpt && M >= 4LL * sms) l.variant = RRN_VARIANT_ROW_WARP;
-        else if (nvec <= kRowCtaMaxVec) l.variant = RRN_VARIANT_ROW_CTA;
-        else l.variant = RRN_VARIANT_STREAM;  // measured faster than the cluster split for wide rows
+        else if (nvec <= (few ? kRowCtaMaxVec : 128 * kMaxVpt)) l.variant = RRN_VARIANT_ROW_CTA;
+        else if (nvec <= static_cast<int64_t>(kMaxCluster) * kClusterChunkVec) l.variant = RRN_VARIANT_ROW_CLUSTER;
+        else l.variant = RRN_VARIANT_STREAM;
     }
     l.vec = (l.variant == RRN_VARIANT_STREAM) ? vec_ok : true;
     l.stages = 0;
@@ -266,7 +280,7 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
                 l.cluster = cfg->cluster;
             } else {
                 l.cluster = 2;
-                while (l.cluster < kMaxCluster && nvec > static_cast<int64_t>(l.cluster) * kRowCtaMaxVec) l.cluster *= 2;
+                while (l.cluster < kMaxCluster && nvec > static_cast<int64_t>(l.cluster) * kClusterChunkVec) l.cluster *= 2;
             }
             if (l.cluster < 2 || l.cluster > kMaxCluster) return RRN_ERR_CONFIG;
             const int64_t chunk = (nvec + l.cluster - 1) / l.cluster;
@@ -284,8 +298,8 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
                 l.ctas = cfg->ctas;
                 if (l.ctas % l.cluster) return RRN_ERR_CONFIG;
             } else {
-                const int occ = occupancy(false, dtype, fused, l);
-                int64_t clusters = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1) / l.cluster;
+                // one wave of clusters: as many as the GPU holds at once
+                int64_t clusters = occupancy(false, dtype, fused, l);
                 if (clusters < 1) clusters = 1;
                 if (clusters > M) clusters = M;
                 if (clusters > INT32_MAX / l.cluster) clusters = INT32_MAX / l.cluster;
@@ -318,8 +332,9 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
         case RRN_VARIANT_STREAM: {
             l.vpt = 1;
             const int64_t chunks = l.vec ? nvec : N;
+            // 1024 threads measured faster from 8192 chunks a row (4096 x 65536, 1024 x 262144)
             l.threads = cfg && cfg->threads ? cfg->threads
-                                            : (chunks >= 512 ? 512 : round_up32(chunks));
+                                            : (chunks >= 8192 ? 1024 : chunks >= 512 ? 512 : round_up32(chunks));
             if (l.threads < 32 || l.threads % 32 || l.threads > 1024) return RRN_ERR_CONFIG;
             if (cfg && cfg->ctas) {
                 l.ctas = cfg->ctas;
@@ -384,11 +399,12 @@ int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
     l.variant = cfg && cfg->variant ? cfg->variant : RRN_VARIANT_AUTO;
     if (l.variant == RRN_VARIANT_AUTO) {
         const bool regs = vec_ok && nvec <= static_cast<int64_t>(kBwdMaxVpt) * bwd_max_threads(kBwdMaxVpt);
-        // Three input rows (the fused backward): the TMA ring keeps enough bytes in flight,
-        // measured faster than the register variant; two input rows: the register variant.
+        // The TMA ring (rows and the next rstd requested ahead) measured faster than the
+        // register variant for two and three input rows; rows whose ring slot would take more
+        // than half the shared memory use the register variant.
+        const int64_t slot = (add_grad ? 3 : 2) * N * elem_size(dtype);
         l.variant = !regs ? RRN_VARIANT_STREAM
-                          : (add_grad && 3 * N * elem_size(dtype) <= kMaxDynSmem / 2 ? RRN_VARIANT_ROW_TMA
-                                                                                     : RRN_VARIANT_ROW_CTA);
+                          : (slot <= kMaxDynSmem / 2 ? RRN_VARIANT_ROW_TMA : RRN_VARIANT_ROW_CTA);
     }
     l.vec = (l.variant == RRN_VARIANT_STREAM) ? vec_ok : true;
     l.stages = 0;
@@ -440,9 +456,30 @@ int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
         want = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
     }
     if (want < 1) return RRN_ERR_CONFIG;
+    // Register and TMA stage 1 may pre-reduce the dw partial sums over clusters of C CTAs
+    // (distributed shared memory), so that stage 2 reads P / C rows. cfg->cluster: 0 = the
+    // planner's choice (kBwdCluster), 1 = no clusters, 2, 4 or 8 = that size.
+    int C = cfg && cfg->cluster ? cfg->cluster : kBwdCluster;
+    if (C != 0 && C != 1 && C != 2 && C != 4 && C != 8) return RRN_ERR_CONFIG;
+    if (C == 1 || (l.variant != RRN_VARIANT_ROW_CTA && l.variant != RRN_VARIANT_ROW_TMA)) C = 0;
+    Launch lc = l;
+    if (C) {
+        lc.cluster = C;
+        if (l.variant == RRN_VARIANT_ROW_CTA) lc.smem = static_cast<int>(N * sizeof(float));
+        if (!(cfg && cfg->ctas)) {
+            // clusters are placed within one GPC: keep P to one wave of them
+            const int clusters = occupancy(true, dtype, add_grad, lc);
+            if (clusters < 1) return RRN_ERR_CONFIG;
+            if (want > static_cast<int64_t>(clusters) * C) want = static_cast<int64_t>(clusters) * C;
+        }
+    }
     // CTA p takes rows p, p + P, ...: with P <= M every CTA owns at least one row (so every
     // workspace row stage 2 reads is written).
     l.ctas = M == 0 ? 0 : clamp_grid(want < M ? want : M);
+    if (C && l.ctas >= 2 * C) {
+        lc.ctas = l.ctas / C * C;  // P a multiple of the cluster size
+        l = lc;
+    }
     *rows_per_cta = M == 0 ? 0 : (M + l.ctas - 1) / l.ctas;
     *out = l;
     return RRN_OK;
@@ -690,6 +727,28 @@ cudaError_t allow_dynamic_smem(const void *kernel, int bytes) {
     return e;
 }
 
+int max_active_clusters(const void *kernel, const Launch &l) {
+    if (l.cluster < 1) return 0;
+    if (l.smem > 0 && allow_dynamic_smem(kernel, l.smem) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(l.cluster));
+    cfg.blockDim = dim3(static_cast<unsigned>(l.threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(l.smem);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(l.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 }  // namespace rrn
 
 using namespace rrn;
@@ -787,15 +846,17 @@ RRN_API int rrn_plan_fwd(const void *x, const void *residual, const void *residu
     return RRN_OK;
 }
 
-RRN_API int rrn_plan_bwd(const void *dy, const void *x, const void *w, const void *dx, int64_t M,
-                         int64_t N, int dtype, rrn_launch *out) {
+RRN_API int rrn_plan_bwd(const void *dy, const void *d_residual_out, const void *x,
+                         const void *w, const void *dx, int64_t M, int64_t N, int dtype,
+                         rrn_launch *out) {
     if (!out) return RRN_ERR_NULL;
     int st = check_common(M, N, 0.f, dtype);
     if (st != RRN_OK) return st;
     if (!dy || !x || !w || !dx) return RRN_ERR_NULL;
     Launch l;
     int64_t rpc = 0;
-    st = plan_bwd_impl(vec_path_ok({dy, x, w, dx}, N, dtype), false, M, N, dtype, nullptr, &l, &rpc);
+    st = plan_bwd_impl(vec_path_ok({dy, d_residual_out, x, w, dx}, N, dtype),
+                       d_residual_out != nullptr, M, N, dtype, nullptr, &l, &rpc);
     if (st != RRN_OK) return st;
     to_public(l, out);
     return RRN_OK;

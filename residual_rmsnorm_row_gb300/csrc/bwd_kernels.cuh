@@ -24,21 +24,20 @@
 namespace rrn {
 
 // dx for one row held in registers (x vectors xv, dy vectors dyv; this thread owns vector
-// c = v * blockDim.x + threadIdx.x), and dy * xhat added into this thread's dw registers.
-// `after_reduce` runs right after the CTA-wide dot product, when every thread has consumed
-// its inputs; when it returns false the row is abandoned.
+// c = v * blockDim.x + threadIdx.x; rs = rstd[row]), and dy * xhat added into this thread's dw
+// registers. `after_reduce` runs right after the CTA-wide dot product, when every thread has
+// consumed its inputs; when it returns false the row is abandoned.
 template <typename T, int VPT, bool ADDG, typename AfterReduce>
 __device__ __forceinline__ bool bwd_row_body(const BwdArgs &a, int64_t row, int nvec,
                                              const uint4 (&xv)[VPT], const uint4 (&dyv)[VPT],
                                              const uint4 (&gv)[VPT], const uint4 (&wv)[VPT],
                                              float (&dw)[VPT][Elem<T>::kPerVec],
-                                             float (&slots)[2][32], int &parity,
+                                             float (&slots)[2][32], int &parity, float rs,
                                              AfterReduce after_reduce) {
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
-    const float rs = __ldg(a.rstd + row);
     float dot = 0.f;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
@@ -95,27 +94,57 @@ __device__ __forceinline__ void bwd_prologue(const BwdArgs &a, int nvec, uint4 (
     }
 }
 
-// This CTA's dw partial sums -> row blockIdx.x of the [P, N] workspace.
-template <typename T, int VPT>
+// This CTA's dw partial sums -> the [P, N] workspace.
+// Without a cluster (CLUSTER == false) CTA p writes row p. With one (the kernel launched in
+// clusters of C CTAs; `red` is N floats of this CTA's shared memory), the C CTAs of cluster k
+// first add their sums through distributed shared memory - CTA q adds column slice q of all C
+// CTAs in rank order - and write row k, so stage 2 reads P / C rows.
+template <typename T, int VPT, bool CLUSTER>
 __device__ __forceinline__ void bwd_store_partial(const BwdArgs &a, int nvec,
-                                                  const float (&dw)[VPT][Elem<T>::kPerVec]) {
+                                                  const float (&dw)[VPT][Elem<T>::kPerVec],
+                                                  float *red) {
     constexpr int V = Elem<T>::kPerVec;
-    float *prow = a.partial + static_cast<int64_t>(blockIdx.x) * a.N;
+    if constexpr (!CLUSTER) {
+        float *prow = a.partial + static_cast<int64_t>(blockIdx.x) * a.N;
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-        const int c = v * blockDim.x + threadIdx.x;
-        if (c < nvec) {
-            float4 *dst = reinterpret_cast<float4 *>(prow + static_cast<int64_t>(c) * V);
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * blockDim.x + threadIdx.x;
+            if (c < nvec) {
+                float4 *dst = reinterpret_cast<float4 *>(prow + static_cast<int64_t>(c) * V);
 #pragma unroll
-            for (int q = 0; q < V / 4; ++q)
-                dst[q] = make_float4(dw[v][4 * q], dw[v][4 * q + 1], dw[v][4 * q + 2], dw[v][4 * q + 3]);
+                for (int q = 0; q < V / 4; ++q)
+                    dst[q] = make_float4(dw[v][4 * q], dw[v][4 * q + 1], dw[v][4 * q + 2], dw[v][4 * q + 3]);
+            }
         }
+    } else {
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * blockDim.x + threadIdx.x;
+            if (c < nvec)
+#pragma unroll
+                for (int k = 0; k < V; ++k) red[c * V + k] = dw[v][k];
+        }
+        cluster_sync();  // every CTA's sums are in its shared memory
+        const int C = static_cast<int>(cluster_nctarank());
+        const int q = static_cast<int>(cluster_ctarank());
+        const int slice = (a.N + C - 1) / C;
+        const int j0 = q * slice;
+        const int j1 = min(a.N, j0 + slice);
+        float *prow = a.partial + static_cast<int64_t>(cluster_id_x()) * a.N;
+        for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+            float t = 0.f;
+            for (int r = 0; r < C; ++r) t += ld_cluster_f32(red + j, static_cast<uint32_t>(r));
+            prow[j] = t;
+        }
+        cluster_sync();  // no CTA leaves while a peer still reads its shared memory
     }
 }
 
-template <typename T, int VPT, bool ADDG>
+template <typename T, int VPT, bool ADDG, bool CLUSTER>
 __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_cta(const BwdArgs a) {
+    pdl_allow_dependents();  // stage 2 may be scheduled now; it waits for our results
     constexpr int V = Elem<T>::kPerVec;
+    extern __shared__ __align__(16) float red[];  // N floats when CLUSTER
     __shared__ float slots[2][32];
     const int nvec = a.N / V;
     const int tid = threadIdx.x;
@@ -141,17 +170,20 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_cta(const BwdArg
                 if constexpr (ADDG) gv[v] = ld_stream(g4 + base + c);
             }
         }
+        // rstd read here, beside the row's loads: prefetching the next row's value costs this
+        // kernel registers (and CTAs per SM) that it cannot spare
         bwd_row_body<T, VPT, ADDG>(a, row, nvec, xv, dyv, gv, wv, dw, slots, parity,
-                                   [] { return true; });
+                                   __ldg(a.rstd + row), [] { return true; });
     }
-    bwd_store_partial<T, VPT>(a, nvec, dw);
+    bwd_store_partial<T, VPT, CLUSTER>(a, nvec, dw, red);
 }
 
 // Stage 1 fed by the TMA engine: CTA p owns rows p, p + P, ... and keeps a.stages of them (x,
 // dy and, fused, d_ro) in flight in a shared-memory ring filled with cp.async.bulk, refilling a
 // slot as soon as the CTA-wide dot product of its row is done.
-template <typename T, int VPT, bool ADDG>
+template <typename T, int VPT, bool ADDG, bool CLUSTER>
 __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArgs a) {
+    pdl_allow_dependents();  // stage 2 may be scheduled now; it waits for our results
     constexpr int V = Elem<T>::kPerVec;
     constexpr int NT = ADDG ? 3 : 2;  // rows per slot: x, dy (, d_ro)
     extern __shared__ __align__(128) unsigned char ring[];
@@ -194,7 +226,12 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArg
 
     int parity = 0;
     int64_t k = 0;
+    // rstd of the next row is requested one row ahead: the row data already waits in the ring,
+    // so a load issued at the top of the row would put one global-memory round trip on every
+    // row's critical path
+    float rs = nrows > 0 ? __ldg(a.rstd + first) : 0.f;
     for (; k < nrows; ++k) {
+        const float rs_next = k + 1 < nrows ? __ldg(a.rstd + first + (k + 1) * stride) : 0.f;
         const int s = static_cast<int>(k % S);
         if (!mbar_wait(&full[s], static_cast<uint32_t>((k / S) & 1), a.faults)) abort_flag = 1;
         uint4 xv[VPT], dyv[VPT], gv[VPT];
@@ -208,7 +245,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArg
             }
         }
         const bool done = bwd_row_body<T, VPT, ADDG>(a, first + k * stride, nvec, xv, dyv, gv, wv, dw,
-                                                     slots, parity, [&] {
+                                                     slots, parity, rs, [&] {
             if (abort_flag) return false;
             if (tid == 0 && k + S < nrows) {
                 fence_proxy_async();
@@ -217,20 +254,26 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArg
             return true;
         });
         if (!done) break;
+        rs = rs_next;
     }
     if (k < nrows) {
         if (tid == 0)
             for (int64_t j = k; j < nrows && j < k + S; ++j)
                 (void)mbar_wait(&full[j % S], static_cast<uint32_t>((j / S) & 1), nullptr, 100000000ull);
-        return;  // the partial row is not written; the fault word reports the failure
+        if constexpr (!CLUSTER) return;  // the partial row is not written; the fault word tells
+        // (in a cluster the peers still wait at the cluster barriers: take part with the sums)
     }
-    bwd_store_partial<T, VPT>(a, nvec, dw);
+    // Every row is consumed, so the ring (at least N floats: stages x (2 or 3) rows of N
+    // elements of >= 2 bytes) is free to hold the cluster reduction's sums.
+    __syncthreads();
+    bwd_store_partial<T, VPT, CLUSTER>(a, nvec, dw, reinterpret_cast<float *>(ring));
 }
 
 // Two passes over each row (any N, any alignment); the dw partials live in the CTA's own
 // workspace row instead of registers. Each workspace element is owned by one thread.
 template <typename T, bool VEC, bool ADDG>
 __global__ void __launch_bounds__(1024) bwd_stream(const BwdArgs a) {
+    pdl_allow_dependents();  // stage 2 may be scheduled now; it waits for our results
     using E = Elem<T>;
     constexpr int W = E::kPerVec;
     constexpr int V = VEC ? W : 1;
@@ -319,6 +362,7 @@ __global__ void __launch_bounds__(THREADS)
     const int lane = threadIdx.x & 31;
     const int grp = threadIdx.x >> 5;
     const int col = blockIdx.x * 32 + lane;
+    pdl_wait();  // stage 1 has finished and its partial sums are visible
     float acc = 0.f;
     if (col < N) {
         const float *src = partial + col;
@@ -348,20 +392,26 @@ template <typename T, bool ADDG>
 const void *bwd_kernel_ptr(const Launch &l) {
     switch (l.variant) {
         case RRN_VARIANT_ROW_CTA:
-            switch (l.vpt) {
-                case 1: return reinterpret_cast<const void *>(&bwd_row_cta<T, 1, ADDG>);
-                case 2: return reinterpret_cast<const void *>(&bwd_row_cta<T, 2, ADDG>);
-                case 4: return reinterpret_cast<const void *>(&bwd_row_cta<T, 4, ADDG>);
+            switch (l.vpt * 2 + (l.cluster ? 1 : 0)) {
+                case 2: return reinterpret_cast<const void *>(&bwd_row_cta<T, 1, ADDG, false>);
+                case 3: return reinterpret_cast<const void *>(&bwd_row_cta<T, 1, ADDG, true>);
+                case 4: return reinterpret_cast<const void *>(&bwd_row_cta<T, 2, ADDG, false>);
+                case 5: return reinterpret_cast<const void *>(&bwd_row_cta<T, 2, ADDG, true>);
+                case 8: return reinterpret_cast<const void *>(&bwd_row_cta<T, 4, ADDG, false>);
+                case 9: return reinterpret_cast<const void *>(&bwd_row_cta<T, 4, ADDG, true>);
                 default: return nullptr;
             }
         case RRN_VARIANT_STREAM:
             return l.vec ? reinterpret_cast<const void *>(&bwd_stream<T, true, ADDG>)
                          : reinterpret_cast<const void *>(&bwd_stream<T, false, ADDG>);
         case RRN_VARIANT_ROW_TMA:
-            switch (l.vpt) {
-                case 1: return reinterpret_cast<const void *>(&bwd_row_tma<T, 1, ADDG>);
-                case 2: return reinterpret_cast<const void *>(&bwd_row_tma<T, 2, ADDG>);
-                case 4: return reinterpret_cast<const void *>(&bwd_row_tma<T, 4, ADDG>);
+            switch (l.vpt * 2 + (l.cluster ? 1 : 0)) {
+                case 2: return reinterpret_cast<const void *>(&bwd_row_tma<T, 1, ADDG, false>);
+                case 3: return reinterpret_cast<const void *>(&bwd_row_tma<T, 1, ADDG, true>);
+                case 4: return reinterpret_cast<const void *>(&bwd_row_tma<T, 2, ADDG, false>);
+                case 5: return reinterpret_cast<const void *>(&bwd_row_tma<T, 2, ADDG, true>);
+                case 8: return reinterpret_cast<const void *>(&bwd_row_tma<T, 4, ADDG, false>);
+                case 9: return reinterpret_cast<const void *>(&bwd_row_tma<T, 4, ADDG, true>);
                 default: return nullptr;
             }
         default: return nullptr;
@@ -371,6 +421,22 @@ const void *bwd_kernel_ptr(const Launch &l) {
 template <typename T>
 const void *bwd_kernel_ptr_any(bool add_grad, const Launch &l) {
     return add_grad ? bwd_kernel_ptr<T, true>(l) : bwd_kernel_ptr<T, false>(l);
+}
+
+// Stage 2 on the stream, launched with programmatic stream serialisation so that it is
+// scheduled while stage 1 drains (it waits for stage 1 inside the kernel).
+inline cudaError_t launch_dw_reduce(const float *partial, float *out, int P, int N,
+                                    cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((N + 31) / 32);
+    cfg.blockDim = dim3(kReduceThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, bwd_dw_reduce<kReduceThreads>, partial, out, P, N);
 }
 
 // Stage 1 on l.ctas CTAs (CTA p owning rows p, p + ctas, ...), then stage 2, on one stream.
@@ -385,18 +451,34 @@ cudaError_t launch_bwd(const BwdArgs &a, const Launch &l, cudaStream_t stream) {
     BwdArgs args = a;
     args.stages = l.stages;
     void *params[] = {&args};
-    cudaError_t e = cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params,
-                                     static_cast<size_t>(l.smem), stream);
+    cudaError_t e;
+    if (l.cluster) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(l.ctas);
+        cfg.blockDim = dim3(l.threads);
+        cfg.dynamicSmemBytes = static_cast<size_t>(l.smem);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(l.cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelExC(&cfg, k, params);
+    } else {
+        e = cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, static_cast<size_t>(l.smem),
+                             stream);
+    }
     if (e != cudaSuccess) return e;
-    const int blocks = (a.N + 31) / 32;
-    bwd_dw_reduce<kReduceThreads><<<blocks, kReduceThreads, 0, stream>>>(a.partial, a.dw, l.ctas, a.N);
-    return cudaGetLastError();
+    return launch_dw_reduce(a.partial, a.dw, l.cluster ? l.ctas / l.cluster : l.ctas, a.N, stream);
 }
 
 template <typename T>
 int occupancy_bwd_t(bool add_grad, const Launch &l) {
     const void *k = bwd_kernel_ptr_any<T>(add_grad, l);
     if (!k) return 0;
+    if (l.cluster > 0) return max_active_clusters(k, l);
     if (l.smem > 0 && allow_dynamic_smem(k, l.smem) != cudaSuccess) return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, l.threads, static_cast<size_t>(l.smem)) !=

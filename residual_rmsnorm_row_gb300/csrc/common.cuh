@@ -97,6 +97,22 @@ __device__ __forceinline__ void r_of(const uint4 &xv, const uint4 &rv,
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) { __stcs(p, v); }
 __device__ __forceinline__ uint4 ld_keep(const uint4 *p) { return __ldg(p); }
+// Pull a line into L1 ahead of its use, without holding a register for it.
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
+// ----------------------------------------------------------------------------------------
+// Programmatic dependent launch. A kernel calls pdl_allow_dependents() to let the next kernel
+// on the stream - when that one was launched with programmatic stream serialisation - be
+// scheduled before this one finishes; the dependent kernel calls pdl_wait() before it reads
+// anything the first one writes (it returns once the first grid has completed and its memory
+// is visible). Without such a launch both are no-ops.
+// ----------------------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ----------------------------------------------------------------------------------------
 // Reductions: butterfly over the warp with shfl_xor (every lane ends with the total), then

@@ -24,14 +24,16 @@ namespace rrn {
 
 // The per-row work of the row-per-CTA variants, on a row already in registers: this thread
 // owns the 128-bit vectors c = v * blockDim.x + threadIdx.x (v < VPT, c < nvec) of x (xv) and
-// residual (rv), and the matching weight vectors (wv). Writes residual_out (fused), y and rstd.
+// residual (rv). The weight vectors are read where they are used, from L1 (the kernels prefetch
+// them there), rather than held in registers across rows: fewer registers per thread means
+// more CTAs - more rows in flight - per SM. Writes residual_out (fused), y and rstd.
 // `after_reduce` runs right after the CTA-wide sum of squares, when every thread has consumed
 // its inputs; when it returns false the row is abandoned (nothing more is written).
 template <typename T, int VPT, bool FUSED, typename AfterReduce>
 __device__ __forceinline__ bool row_cta_body(const FwdArgs &a, int64_t row, int nvec,
                                              const uint4 (&xv)[VPT], const uint4 (&rv)[VPT],
-                                             const uint4 (&wv)[VPT], float (&slots)[2][32],
-                                             int &parity, AfterReduce after_reduce) {
+                                             float (&slots)[2][32], int &parity,
+                                             AfterReduce after_reduce) {
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
     const int tid = threadIdx.x;
@@ -91,7 +93,7 @@ __device__ __forceinline__ bool row_cta_body(const FwdArgs &a, int64_t row, int 
         if (c < nvec) {
             float f[V], wf[V], o[V];
             r_of<T, FUSED>(xv[v], rv[v], f);
-            E::unpack(wv[v], wf);
+            E::unpack(ld_keep(static_cast<const uint4 *>(a.w) + c), wf);
 #pragma unroll
             for (int k = 0; k < V; ++k) o[k] = f[k] * rs * wf[k];
             st_stream(static_cast<uint4 *>(a.y) + base + c, E::pack(o));
@@ -101,18 +103,23 @@ __device__ __forceinline__ bool row_cta_body(const FwdArgs &a, int64_t row, int 
     return true;
 }
 
-template <typename T, int VPT>
-__device__ __forceinline__ void load_w(const FwdArgs &a, int nvec, uint4 (&wv)[VPT]) {
+// Start pulling this thread's weight vectors into L1 (they are read after the reduction).
+template <int VPT>
+__device__ __forceinline__ void prefetch_w(const FwdArgs &a, int nvec) {
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int c = v * blockDim.x + threadIdx.x;
-        if (c < nvec) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
+        if (c < nvec) prefetch_l1(static_cast<const uint4 *>(a.w) + c);
     }
 }
 
+// Registers per thread the row-per-CTA forward kernels may use: with VPT vectors per thread they
+// launch with at most fwd_max_threads(VPT) threads, and the cap keeps that many resident
+// (VPT <= 2: 48 x 1024, VPT 4: 96 x 512, VPT 8: 192 x 256 - all at most 48K of the SM's 64K).
+constexpr int fwd_max_regs(int vpt) { return vpt <= 2 ? 48 : vpt == 4 ? 96 : 192; }
+
 template <typename T, int VPT, bool FUSED>
-__global__ void __launch_bounds__(fwd_max_threads(VPT))
-    fwd_row_cta(const FwdArgs a) {
+__global__ void __maxnreg__(fwd_max_regs(VPT)) fwd_row_cta(const FwdArgs a) {
     constexpr int V = Elem<T>::kPerVec;
     __shared__ float slots[2][32];
     const int nvec = a.N / V;
@@ -120,10 +127,7 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT))
     const int nthr = blockDim.x;
     const uint4 *x4 = static_cast<const uint4 *>(a.x);
     const uint4 *r4 = static_cast<const uint4 *>(a.res);
-
-    // The weight row stays in registers for every row this CTA handles.
-    uint4 wv[VPT];
-    load_w<T, VPT>(a, nvec, wv);
+    prefetch_w<VPT>(a, nvec);
 
     int parity = 0;
     for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
@@ -137,7 +141,7 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT))
                 if (FUSED) rv[v] = ld_stream(r4 + base + c);
             }
         }
-        row_cta_body<T, VPT, FUSED>(a, row, nvec, xv, rv, wv, slots, parity, [] { return true; });
+        row_cta_body<T, VPT, FUSED>(a, row, nvec, xv, rv, slots, parity, [] { return true; });
     }
 }
 
@@ -185,8 +189,7 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT))
     if (tid == 0)
         for (int64_t k = 0; k < nrows && k < S; ++k) issue(k);
 
-    uint4 wv[VPT];
-    load_w<T, VPT>(a, nvec, wv);
+    prefetch_w<VPT>(a, nvec);
 
     int parity = 0;
     int64_t k = 0;
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT))
             }
         }
         const bool done = row_cta_body<T, VPT, FUSED>(
-            a, first + k * stride, nvec, xv, rv, wv, slots, parity, [&] {
+            a, first + k * stride, nvec, xv, rv, slots, parity, [&] {
                 if (abort_flag) return false;  // written before the barrier: uniform
                 if (tid == 0 && k + S < nrows) {
                     fence_proxy_async();       // our generic reads of the slot come first
@@ -620,6 +623,7 @@ template <typename T>
 int occupancy_fwd_t(bool fused, const Launch &l) {
     const void *k = fwd_kernel_ptr_any<T>(fused, l);
     if (!k) return 0;
+    if (l.cluster > 0) return max_active_clusters(k, l);
     if (l.smem > 0 && allow_dynamic_smem(k, l.smem) != cudaSuccess) return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, l.threads, static_cast<size_t>(l.smem)) !=

@@ -97,7 +97,8 @@ struct Launch {
     bool vec;     // 128-bit vectors (else element-wise)
     int stages;   // TMA variant: rows in flight per CTA (shared-memory ring depth)
     int smem;     // dynamic shared memory bytes per CTA
-    int cluster;  // cluster variant: CTAs per cluster (one row split across them)
+    int cluster;  // CTAs per thread-block cluster (0: no cluster). Forward cluster variant: one
+                  // row split across them; backward: dw partial sums pre-reduced across them.
 };
 
 // Largest vectors-per-thread the register variants are compiled for, and the thread limit
@@ -113,6 +114,11 @@ constexpr int kMaxCluster = 8;       // largest (portable) thread-block cluster
 // Raise a kernel's dynamic shared-memory limit to `bytes` on the current device (done once
 // per kernel, device and size; defined in api.cu).
 cudaError_t allow_dynamic_smem(const void *kernel, int bytes);
+
+// Clusters of l.cluster CTAs (l.threads threads, l.smem bytes of dynamic shared memory each) of
+// `kernel` that the whole GPU holds at once; 0 on error (defined in api.cu). Clusters are placed
+// within one GPC, so this can be below SMs x CTAs-per-SM / l.cluster.
+int max_active_clusters(const void *kernel, const Launch &l);
 
 // Kernel launchers, one per dtype (defined in fwd_bf16.cu, fwd_f32.cu and bwd.cu). They
 // enqueue on `stream` and return the cudaError_t of the launch.
@@ -135,7 +141,8 @@ int occupancy_quant_bf16(bool fused, const Launch &l);
 int occupancy_quant_f32(bool fused, const Launch &l);
 
 // Occupancy (resident CTAs per SM) of the kernel a launch would run, with l.smem bytes of
-// dynamic shared memory; 0 on error.
+// dynamic shared memory; for a cluster launch (l.cluster > 0) the clusters resident on the
+// whole GPU instead. 0 on error.
 int occupancy_fwd_bf16(bool fused, const Launch &l);
 int occupancy_fwd_f32(bool fused, const Launch &l);
 int occupancy_bwd_bf16(bool add_grad, const Launch &l);

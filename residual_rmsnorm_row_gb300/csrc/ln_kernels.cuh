@@ -258,6 +258,7 @@ __global__ void __launch_bounds__(1024) ln_fwd_stream(const LnFwdArgs a) {
 // registers and go to rows p of the two [P, N] workspace halves.
 template <typename T, int VPT, bool ADDG>
 __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_cta(const LnBwdArgs a) {
+    pdl_allow_dependents();  // the stage-2 reductions may be scheduled now
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
     __shared__ float slots[2][2][32];
@@ -354,6 +355,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_cta(const LnB
 // CTA's own workspace rows (each element owned by one thread).
 template <typename T, bool VEC, bool ADDG>
 __global__ void __launch_bounds__(1024) ln_bwd_stream(const LnBwdArgs a) {
+    pdl_allow_dependents();  // the stage-2 reductions may be scheduled now
     using E = Elem<T>;
     constexpr int W = E::kPerVec;
     constexpr int V = VEC ? W : 1;
@@ -480,12 +482,11 @@ cudaError_t launch_ln_bwd(const LnBwdArgs &a, const Launch &l, cudaStream_t stre
     void *params[] = {&args};
     cudaError_t e = cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, 0, stream);
     if (e != cudaSuccess) return e;
-    const int blocks = (a.N + 31) / 32;
-    bwd_dw_reduce<kReduceThreads><<<blocks, kReduceThreads, 0, stream>>>(a.partial, a.dw, l.ctas, a.N);
-    if (a.db)
-        bwd_dw_reduce<kReduceThreads><<<blocks, kReduceThreads, 0, stream>>>(
-            a.partial + static_cast<int64_t>(l.ctas) * a.N, a.db, l.ctas, a.N);
-    return cudaGetLastError();
+    e = launch_dw_reduce(a.partial, a.dw, l.ctas, a.N, stream);
+    if (e != cudaSuccess || !a.db) return e;
+    // launched the same way: its wait returns once the dw reduction has finished, which in turn
+    // started reading only after stage 1 had finished
+    return launch_dw_reduce(a.partial + static_cast<int64_t>(l.ctas) * a.N, a.db, l.ctas, a.N, stream);
 }
 
 template <typename T>

@@ -71,7 +71,7 @@ extern "C" RRN_API int rmsnorm_bwd_noalloc(const void *dy, const void *x, const 
     // The regular plan, with the number of stage-1 CTAs (one row of partial sums each) lowered
     // until the partial sums fit the array.
     rrn_launch cfg{};
-    int st = rrn_plan_bwd(dy, x, w, dx, M, N, dtype, &cfg);
+    int st = rrn_plan_bwd(dy, nullptr, x, w, dx, M, N, dtype, &cfg);
     if (st != RRN_OK) return st;
     const int64_t fit = kScratchFloats / N;
     if (cfg.ctas > fit) cfg.ctas = static_cast<int>(fit);

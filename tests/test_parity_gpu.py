@@ -319,10 +319,18 @@ def test_backward_shapes(dtype, N):
         for vpt in (1, 2, 4):
             thr = -(-(-(-nvec // vpt)) // 32) * 32
             if thr <= (256 if vpt == 4 else 512):
+                # (ctas, stages, cluster): cluster > 1 adds the dw partial sums of that many
+                # CTAs in distributed shared memory; 37 -> 36 CTAs in clusters of 4, 13 -> 12
+                # in clusters of 2
                 launches += [rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0),
+                             rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0, 0, 8),
                              rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 13),
+                             rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 37),
+                             rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 37, 0, 4),
                              rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 0, 0),
+                             rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 0, 2, 8),
                              rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 13, 1),
+                             rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 13, 1, 2),
                              rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 7, 3)]
     for launch in launches:
         dx, dw = _bwd_case(h, dtype, wl.eps, launch)
