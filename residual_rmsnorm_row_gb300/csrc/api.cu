@@ -165,6 +165,11 @@ int clamp_grid(int64_t v) {
 // across N = 4096 and 7168 (narrow CTAs with many vectors per thread, several CTAs per SM).
 constexpr int kFwdTargetThreads = 128;
 constexpr int kBwdTargetThreads = 256;
+// LayerNorm backward (the dw and db sums in registers): both the register and the TMA ring
+// variants measured best with 256-thread CTAs on 16384 x 4096 bf16 (ring: 114.9 us at 256
+// threads, 127.1 us at 128).
+constexpr int kLnBwdTargetThreads = 256;
+constexpr int kLnBwdTmaTargetThreads = 256;
 // Widest row (in 128-bit vectors) one CTA holds in registers: 8 vectors x 256 threads.
 constexpr int kRowCtaMaxVec = 2048;
 // Vectors of a row each CTA of the cluster split takes when the planner chooses the cluster
@@ -184,7 +189,9 @@ constexpr int kMaxDynSmem = 227 * 1024;
 // the CTAs per SM (0: no depth fits); sets l->stages and l->smem.
 constexpr int64_t kRingTargetBytes = 64 * 1024;
 
-int plan_ring(bool bwd, int dtype, bool fused, int slot_bytes, int want_stages, Launch *l) {
+// occ(t): resident CTAs per SM of launch t.
+template <typename Occ>
+int plan_ring(Occ occ, int slot_bytes, int want_stages, Launch *l) {
     int occ_of[kMaxStages + 1] = {};
     int best_occ = 0;
     for (int S = 1; S <= kMaxStages; ++S) {
@@ -194,7 +201,7 @@ int plan_ring(bool bwd, int dtype, bool fused, int slot_bytes, int want_stages, 
         Launch t = *l;
         t.stages = S;
         t.smem = static_cast<int>(smem);
-        occ_of[S] = occupancy(bwd, dtype, fused, t);
+        occ_of[S] = occ(t);
         if (occ_of[S] > best_occ) best_occ = occ_of[S];
     }
     if (best_occ < 1) return 0;
@@ -323,7 +330,8 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
             if (want < 0 || want > kMaxStages) return RRN_ERR_CONFIG;
             const int64_t slot = (fused ? 2 : 1) * N * elem_size(dtype);
             if (slot > kMaxDynSmem) return RRN_ERR_CONFIG;
-            const int occ = plan_ring(false, dtype, fused, static_cast<int>(slot), want, &l);
+            const int occ = plan_ring([&](const Launch &t) { return occupancy(false, dtype, fused, t); },
+                                      static_cast<int>(slot), want, &l);
             if (occ < 1) return RRN_ERR_CONFIG;
             l.ctas = cfg && cfg->ctas ? cfg->ctas
                                       : clamp_grid(M < static_cast<int64_t>(sms) * occ ? M : static_cast<int64_t>(sms) * occ);
@@ -432,7 +440,8 @@ int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
                 if (want < 0 || want > kMaxStages) return RRN_ERR_CONFIG;
                 const int64_t slot = (add_grad ? 3 : 2) * N * elem_size(dtype);
                 if (slot > kMaxDynSmem) return RRN_ERR_CONFIG;
-                ring_occ = plan_ring(true, dtype, add_grad, static_cast<int>(slot), want, &l);
+                ring_occ = plan_ring([&](const Launch &t) { return occupancy(true, dtype, add_grad, t); },
+                                     static_cast<int>(slot), want, &l);
                 if (ring_occ < 1) return RRN_ERR_CONFIG;
             }
             break;
@@ -525,11 +534,11 @@ int run_bwd(const void *dy, const void *d_ro, const void *x, const void *w, cons
 // Register layout (vpt, threads) for a row of nvec vectors, as the RMSNorm planners choose it:
 // the widest CTA for few rows, about kFwdTargetThreads threads otherwise.
 int pick_row_layout(int64_t nvec, int64_t M, int sms, const rrn_launch *cfg, int max_vpt,
-                    int (*max_threads)(int), Launch *l) {
+                    int (*max_threads)(int), int target_threads, Launch *l) {
     if (cfg && cfg->vpt) {
         l->vpt = cfg->vpt;
     } else {
-        l->vpt = M < 2LL * sms ? 1 : ceil_pow2_vpt((nvec + kFwdTargetThreads - 1) / kFwdTargetThreads, max_vpt);
+        l->vpt = M < 2LL * sms ? 1 : ceil_pow2_vpt((nvec + target_threads - 1) / target_threads, max_vpt);
         while (l->vpt < max_vpt && nvec > static_cast<int64_t>(l->vpt) * max_threads(l->vpt)) l->vpt *= 2;
     }
     if (l->vpt < 1 || l->vpt > max_vpt || (l->vpt & (l->vpt - 1))) return RRN_ERR_CONFIG;
@@ -555,7 +564,7 @@ int plan_ln_fwd(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const 
     l.vec = l.variant == RRN_VARIANT_STREAM ? vec_ok : true;
     if (l.variant == RRN_VARIANT_ROW_CTA) {
         if (!vec_ok) return RRN_ERR_CONFIG;
-        st = pick_row_layout(nvec, M, sms, cfg, kMaxVpt, fwd_threads_limit, &l);
+        st = pick_row_layout(nvec, M, sms, cfg, kMaxVpt, fwd_threads_limit, kFwdTargetThreads, &l);
         if (st != RRN_OK) return st;
         l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid(M);
     } else if (l.variant == RRN_VARIANT_STREAM) {
@@ -586,15 +595,26 @@ int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, con
     if (st != RRN_OK) return st;
     Launch l{};
     l.variant = cfg && cfg->variant ? cfg->variant : RRN_VARIANT_AUTO;
-    if (l.variant == RRN_VARIANT_AUTO)
-        l.variant = vec_ok && nvec <= static_cast<int64_t>(kBwdMaxVpt) * bwd_max_threads(kBwdMaxVpt)
-                        ? RRN_VARIANT_ROW_CTA
-                        : RRN_VARIANT_STREAM;
+    const int64_t slot = (add_grad ? 3 : 2) * N * elem_size(dtype);
+    if (l.variant == RRN_VARIANT_AUTO) {
+        const bool regs = vec_ok && nvec <= static_cast<int64_t>(kBwdMaxVpt) * bwd_max_threads(kBwdMaxVpt);
+        l.variant = !regs ? RRN_VARIANT_STREAM
+                          : (slot <= kMaxDynSmem / 2 ? RRN_VARIANT_ROW_TMA : RRN_VARIANT_ROW_CTA);
+    }
     l.vec = l.variant == RRN_VARIANT_STREAM ? vec_ok : true;
-    if (l.variant == RRN_VARIANT_ROW_CTA) {
+    int ring_occ = 0;
+    if (l.variant == RRN_VARIANT_ROW_CTA || l.variant == RRN_VARIANT_ROW_TMA) {
         if (!vec_ok) return RRN_ERR_CONFIG;
-        st = pick_row_layout(nvec, 1LL << 40, sms, cfg, kBwdMaxVpt, bwd_threads_limit, &l);
+        const int target = l.variant == RRN_VARIANT_ROW_TMA ? kLnBwdTmaTargetThreads : kLnBwdTargetThreads;
+        st = pick_row_layout(nvec, 1LL << 40, sms, cfg, kBwdMaxVpt, bwd_threads_limit, target, &l);
         if (st != RRN_OK) return st;
+        if (l.variant == RRN_VARIANT_ROW_TMA) {
+            const int want = cfg ? cfg->stages : 0;
+            if (want < 0 || want > kMaxStages || slot > kMaxDynSmem) return RRN_ERR_CONFIG;
+            ring_occ = plan_ring([&](const Launch &t) { return occupancy_ln(true, dtype, add_grad, t); },
+                                 static_cast<int>(slot), want, &l);
+            if (ring_occ < 1) return RRN_ERR_CONFIG;
+        }
     } else if (l.variant == RRN_VARIANT_STREAM) {
         l.vpt = 1;
         const int64_t chunks = l.vec ? nvec : N;
@@ -605,7 +625,7 @@ int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, con
     }
     int64_t want = cfg && cfg->ctas ? cfg->ctas : 0;
     if (!want) {
-        const int occ = occupancy_ln(true, dtype, add_grad, l);
+        const int occ = ring_occ ? ring_occ : occupancy_ln(true, dtype, add_grad, l);
         want = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
     }
     if (want < 1) return RRN_ERR_CONFIG;
@@ -648,8 +668,11 @@ int run_ln_bwd(const void *dy, const void *d_ro, const void *x, const void *w, c
     if (st != RRN_OK) return st;
     const size_t need = 2 * static_cast<size_t>(l.ctas) * static_cast<size_t>(N) * sizeof(float);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return RRN_ERR_WORKSPACE;
+    unsigned int *faults = nullptr;
+    st = fault_word(&faults);
+    if (st != RRN_OK) return st;
     LnBwdArgs a{dy, d_ro, x, w, mean, rstd, dx, dw, db, static_cast<float *>(workspace), M,
-                static_cast<int>(N)};
+                static_cast<int>(N), 0, faults};
     cudaError_t e = dtype == RRN_BF16 ? launch_ln_bwd_bf16(a, l, stream) : launch_ln_bwd_f32(a, l, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return RRN_OK;
@@ -677,7 +700,7 @@ int run_quant(const void *x, const void *res, void *res_out, const void *w, void
     l.vec = l.variant == RRN_VARIANT_ROW_CTA;
     if (l.variant == RRN_VARIANT_ROW_CTA) {
         if (!vec_ok) return RRN_ERR_CONFIG;
-        st = pick_row_layout(nvec, M, sms, cfg, kMaxVpt, fwd_threads_limit, &l);
+        st = pick_row_layout(nvec, M, sms, cfg, kMaxVpt, fwd_threads_limit, kFwdTargetThreads, &l);
         if (st != RRN_OK) return st;
         l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid(M);
     } else if (l.variant == RRN_VARIANT_STREAM) {

@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArg
     pdl_allow_dependents();  // stage 2 may be scheduled now; it waits for our results
     constexpr int V = Elem<T>::kPerVec;
     constexpr int NT = ADDG ? 3 : 2;  // rows per slot: x, dy (, d_ro)
-    extern __shared__ __align__(128) unsigned char ring[];
+    extern __shared__ __align__(128) unsigned char ring_buf[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
     __shared__ float slots[2][32];
     __shared__ int abort_flag;
@@ -194,31 +194,24 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArg
     const int nvec = a.N / V;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
-    const uint32_t row_bytes = static_cast<uint32_t>(a.N) * static_cast<uint32_t>(sizeof(T));
-    const int S = a.stages;
-    const int64_t first = blockIdx.x;
-    const int64_t stride = gridDim.x;
-    const int64_t nrows = first < a.M ? (a.M - 1 - first) / stride + 1 : 0;
-
-    auto slot = [&](int s, int t) { return ring + static_cast<size_t>(s * NT + t) * row_bytes; };
-    auto issue = [&](int64_t k) {
-        const int s = static_cast<int>(k % S);
-        const int64_t off = (first + k * stride) * static_cast<int64_t>(row_bytes);
-        mbar_arrive_expect_tx(&full[s], NT * row_bytes);
-        bulk_g2s(slot(s, 0), static_cast<const char *>(a.x) + off, row_bytes, &full[s]);
-        bulk_g2s(slot(s, 1), static_cast<const char *>(a.dy) + off, row_bytes, &full[s]);
-        if (ADDG) bulk_g2s(slot(s, 2), static_cast<const char *>(a.d_ro) + off, row_bytes, &full[s]);
-    };
+    RowRing<NT> ring;
+    ring.buf = ring_buf;
+    ring.full = full;
+    ring.src[0] = static_cast<const char *>(a.x);
+    ring.src[1] = static_cast<const char *>(a.dy);
+    if constexpr (ADDG) ring.src[NT - 1] = static_cast<const char *>(a.d_ro);
+    ring.row_bytes = static_cast<uint32_t>(a.N) * static_cast<uint32_t>(sizeof(T));
+    ring.S = a.stages;
+    ring.first = blockIdx.x;
+    ring.stride = gridDim.x;
+    ring.nrows = ring.first < a.M ? (a.M - 1 - ring.first) / ring.stride + 1 : 0;
 
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        ring.init();
         abort_flag = 0;
-        fence_mbarrier_init();
-        fence_proxy_async();
     }
     __syncthreads();
-    if (tid == 0)
-        for (int64_t k = 0; k < nrows && k < S; ++k) issue(k);
+    if (tid == 0) ring.prime();
 
     uint4 wv[VPT];
     float dw[VPT][V];
@@ -229,44 +222,41 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArg
     // rstd of the next row is requested one row ahead: the row data already waits in the ring,
     // so a load issued at the top of the row would put one global-memory round trip on every
     // row's critical path
-    float rs = nrows > 0 ? __ldg(a.rstd + first) : 0.f;
-    for (; k < nrows; ++k) {
-        const float rs_next = k + 1 < nrows ? __ldg(a.rstd + first + (k + 1) * stride) : 0.f;
-        const int s = static_cast<int>(k % S);
-        if (!mbar_wait(&full[s], static_cast<uint32_t>((k / S) & 1), a.faults)) abort_flag = 1;
+    float rs = ring.nrows > 0 ? __ldg(a.rstd + ring.first) : 0.f;
+    for (; k < ring.nrows; ++k) {
+        const float rs_next = k + 1 < ring.nrows ? __ldg(a.rstd + ring.first + (k + 1) * ring.stride) : 0.f;
+        if (!ring.wait(k, a.faults)) abort_flag = 1;
         uint4 xv[VPT], dyv[VPT], gv[VPT];
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * nthr + tid;
             if (c < nvec) {
-                xv[v] = ld_shared_v4(slot(s, 0) + static_cast<size_t>(c) * 16);
-                dyv[v] = ld_shared_v4(slot(s, 1) + static_cast<size_t>(c) * 16);
-                if constexpr (ADDG) gv[v] = ld_shared_v4(slot(s, 2) + static_cast<size_t>(c) * 16);
+                xv[v] = ld_shared_v4(ring.slot(k, 0) + static_cast<size_t>(c) * 16);
+                dyv[v] = ld_shared_v4(ring.slot(k, 1) + static_cast<size_t>(c) * 16);
+                if constexpr (ADDG) gv[v] = ld_shared_v4(ring.slot(k, NT - 1) + static_cast<size_t>(c) * 16);
             }
         }
-        const bool done = bwd_row_body<T, VPT, ADDG>(a, first + k * stride, nvec, xv, dyv, gv, wv, dw,
-                                                     slots, parity, rs, [&] {
+        const bool done = bwd_row_body<T, VPT, ADDG>(a, ring.first + k * ring.stride, nvec, xv, dyv, gv,
+                                                     wv, dw, slots, parity, rs, [&] {
             if (abort_flag) return false;
-            if (tid == 0 && k + S < nrows) {
+            if (tid == 0 && k + ring.S < ring.nrows) {
                 fence_proxy_async();
-                issue(k + S);
+                ring.issue(k + ring.S);
             }
             return true;
         });
         if (!done) break;
         rs = rs_next;
     }
-    if (k < nrows) {
-        if (tid == 0)
-            for (int64_t j = k; j < nrows && j < k + S; ++j)
-                (void)mbar_wait(&full[j % S], static_cast<uint32_t>((j / S) & 1), nullptr, 100000000ull);
+    if (k < ring.nrows) {
+        if (tid == 0) ring.drain(k);
         if constexpr (!CLUSTER) return;  // the partial row is not written; the fault word tells
         // (in a cluster the peers still wait at the cluster barriers: take part with the sums)
     }
     // Every row is consumed, so the ring (at least N floats: stages x (2 or 3) rows of N
     // elements of >= 2 bytes) is free to hold the cluster reduction's sums.
     __syncthreads();
-    bwd_store_partial<T, VPT, CLUSTER>(a, nvec, dw, reinterpret_cast<float *>(ring));
+    bwd_store_partial<T, VPT, CLUSTER>(a, nvec, dw, reinterpret_cast<float *>(ring_buf));
 }
 
 // Two passes over each row (any N, any alignment); the dw partials live in the CTA's own
@@ -353,19 +343,23 @@ __global__ void __launch_bounds__(1024) bwd_stream(const BwdArgs a) {
 // in that order - up to U of its loads are issued before the first addition, so a thread waits
 // for memory about once per U rows - then one warp adds the G group sums in group order. The
 // order depends only on (P, N), so dw is reproducible.
+// blockIdx.y selects one of two [P, N] blocks of partial sums (the second, reduced into out1,
+// follows the first), so that LayerNorm's dw and db reductions run in one launch.
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS)
-    bwd_dw_reduce(const float *__restrict__ partial, float *__restrict__ dw, int P, int N) {
+    bwd_dw_reduce(const float *__restrict__ partial, float *__restrict__ out0,
+                  float *__restrict__ out1, int P, int N) {
     constexpr int G = THREADS / 32;
     constexpr int U = 48;
     __shared__ float sums[G][33];
     const int lane = threadIdx.x & 31;
     const int grp = threadIdx.x >> 5;
     const int col = blockIdx.x * 32 + lane;
+    float *dw = blockIdx.y ? out1 : out0;
     pdl_wait();  // stage 1 has finished and its partial sums are visible
     float acc = 0.f;
     if (col < N) {
-        const float *src = partial + col;
+        const float *src = partial + static_cast<int64_t>(blockIdx.y) * P * N + col;
         for (int p0 = grp; p0 < P; p0 += U * G) {
             float v[U];
 #pragma unroll
@@ -424,11 +418,12 @@ const void *bwd_kernel_ptr_any(bool add_grad, const Launch &l) {
 }
 
 // Stage 2 on the stream, launched with programmatic stream serialisation so that it is
-// scheduled while stage 1 drains (it waits for stage 1 inside the kernel).
-inline cudaError_t launch_dw_reduce(const float *partial, float *out, int P, int N,
+// scheduled while stage 1 drains (it waits for stage 1 inside the kernel). out1 non-NULL: a
+// second [P, N] block after the first is reduced into it by the same launch.
+inline cudaError_t launch_dw_reduce(const float *partial, float *out0, float *out1, int P, int N,
                                     cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((N + 31) / 32);
+    cfg.gridDim = dim3((N + 31) / 32, out1 ? 2 : 1);
     cfg.blockDim = dim3(kReduceThreads);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -436,7 +431,7 @@ inline cudaError_t launch_dw_reduce(const float *partial, float *out, int P, int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, bwd_dw_reduce<kReduceThreads>, partial, out, P, N);
+    return cudaLaunchKernelEx(&cfg, bwd_dw_reduce<kReduceThreads>, partial, out0, out1, P, N);
 }
 
 // Stage 1 on l.ctas CTAs (CTA p owning rows p, p + ctas, ...), then stage 2, on one stream.
@@ -471,7 +466,8 @@ cudaError_t launch_bwd(const BwdArgs &a, const Launch &l, cudaStream_t stream) {
                              stream);
     }
     if (e != cudaSuccess) return e;
-    return launch_dw_reduce(a.partial, a.dw, l.cluster ? l.ctas / l.cluster : l.ctas, a.N, stream);
+    return launch_dw_reduce(a.partial, a.dw, nullptr, l.cluster ? l.ctas / l.cluster : l.ctas, a.N,
+                            stream);
 }
 
 template <typename T>

@@ -113,11 +113,6 @@ __device__ __forceinline__ void prefetch_w(const FwdArgs &a, int nvec) {
     }
 }
 
-// Registers per thread the row-per-CTA forward kernels may use: with VPT vectors per thread they
-// launch with at most fwd_max_threads(VPT) threads, and the cap keeps that many resident
-// (VPT <= 2: 48 x 1024, VPT 4: 96 x 512, VPT 8: 192 x 256 - all at most 48K of the SM's 64K).
-constexpr int fwd_max_regs(int vpt) { return vpt <= 2 ? 48 : vpt == 4 ? 96 : 192; }
-
 template <typename T, int VPT, bool FUSED>
 __global__ void __maxnreg__(fwd_max_regs(VPT)) fwd_row_cta(const FwdArgs a) {
     constexpr int V = Elem<T>::kPerVec;
@@ -156,7 +151,7 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT))
     fwd_row_tma(const FwdArgs a) {
     constexpr int V = Elem<T>::kPerVec;
     constexpr int NT = FUSED ? 2 : 1;
-    extern __shared__ __align__(128) unsigned char ring[];
+    extern __shared__ __align__(128) unsigned char ring_buf[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
     __shared__ float slots[2][32];
     __shared__ int abort_flag;
@@ -164,64 +159,53 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT))
     const int nvec = a.N / V;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
-    const uint32_t row_bytes = static_cast<uint32_t>(a.N) * static_cast<uint32_t>(sizeof(T));
-    const int S = a.stages;
-    const int64_t first = blockIdx.x;
-    const int64_t stride = gridDim.x;
-    const int64_t nrows = first < a.M ? (a.M - 1 - first) / stride + 1 : 0;
-
-    auto slot = [&](int s, int t) { return ring + static_cast<size_t>(s * NT + t) * row_bytes; };
-    auto issue = [&](int64_t k) {  // one thread: fetch the k-th row of this CTA into its slot
-        const int s = static_cast<int>(k % S);
-        const int64_t off = (first + k * stride) * static_cast<int64_t>(row_bytes);
-        mbar_arrive_expect_tx(&full[s], NT * row_bytes);
-        bulk_g2s(slot(s, 0), static_cast<const char *>(a.x) + off, row_bytes, &full[s]);
-        if (FUSED) bulk_g2s(slot(s, 1), static_cast<const char *>(a.res) + off, row_bytes, &full[s]);
-    };
+    RowRing<NT> ring;
+    ring.buf = ring_buf;
+    ring.full = full;
+    ring.src[0] = static_cast<const char *>(a.x);
+    if constexpr (FUSED) ring.src[NT - 1] = static_cast<const char *>(a.res);
+    ring.row_bytes = static_cast<uint32_t>(a.N) * static_cast<uint32_t>(sizeof(T));
+    ring.S = a.stages;
+    ring.first = blockIdx.x;
+    ring.stride = gridDim.x;
+    ring.nrows = ring.first < a.M ? (a.M - 1 - ring.first) / ring.stride + 1 : 0;
 
     if (tid == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        ring.init();
         abort_flag = 0;
-        fence_mbarrier_init();
-        fence_proxy_async();
     }
     __syncthreads();
-    if (tid == 0)
-        for (int64_t k = 0; k < nrows && k < S; ++k) issue(k);
+    if (tid == 0) ring.prime();
 
     prefetch_w<VPT>(a, nvec);
 
     int parity = 0;
     int64_t k = 0;
-    for (; k < nrows; ++k) {
-        const int s = static_cast<int>(k % S);
-        if (!mbar_wait(&full[s], static_cast<uint32_t>((k / S) & 1), a.faults)) abort_flag = 1;
+    for (; k < ring.nrows; ++k) {
+        if (!ring.wait(k, a.faults)) abort_flag = 1;
         uint4 xv[VPT], rv[VPT];
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * nthr + tid;
             if (c < nvec) {
-                xv[v] = ld_shared_v4(slot(s, 0) + static_cast<size_t>(c) * 16);
-                if (FUSED) rv[v] = ld_shared_v4(slot(s, 1) + static_cast<size_t>(c) * 16);
+                xv[v] = ld_shared_v4(ring.slot(k, 0) + static_cast<size_t>(c) * 16);
+                if (FUSED) rv[v] = ld_shared_v4(ring.slot(k, NT - 1) + static_cast<size_t>(c) * 16);
             }
         }
         const bool done = row_cta_body<T, VPT, FUSED>(
-            a, first + k * stride, nvec, xv, rv, slots, parity, [&] {
+            a, ring.first + k * ring.stride, nvec, xv, rv, slots, parity, [&] {
                 if (abort_flag) return false;  // written before the barrier: uniform
-                if (tid == 0 && k + S < nrows) {
+                if (tid == 0 && k + ring.S < ring.nrows) {
                     fence_proxy_async();       // our generic reads of the slot come first
-                    issue(k + S);
+                    ring.issue(k + ring.S);
                 }
                 return true;
             });
         if (!done) break;
     }
-    if (k < nrows && tid == 0) {
-        // A wait ran out: let the copies already issued land before the CTA's shared memory is
-        // released (each wait bounded again), then leave; the fault word tells the host.
-        for (int64_t j = k; j < nrows && j < k + S; ++j)
-            (void)mbar_wait(&full[j % S], static_cast<uint32_t>((j / S) & 1), nullptr, 100000000ull);
-    }
+    // A wait ran out: let the copies already issued land before the CTA's shared memory is
+    // released, then leave; the fault word tells the host.
+    if (k < ring.nrows && tid == 0) ring.drain(k);
 }
 
 // One row split across the C CTAs of a thread-block cluster (C = 2..8): CTA rank q owns the

@@ -72,6 +72,8 @@ struct LnBwdArgs {
     float *partial;
     int64_t M;
     int N;
+    int stages;             // TMA variant: ring depth
+    unsigned int *faults;   // device fault word (TMA variant's bounded waits)
 };
 
 // Arguments of one RMSNorm -> fp8 e4m3 call (fused when res != nullptr).
@@ -105,6 +107,11 @@ struct Launch {
 // each VPT is compiled with (__launch_bounds__), which bounds registers per thread.
 constexpr int kMaxVpt = 8;
 constexpr int fwd_max_threads(int vpt) { return vpt >= 8 ? 256 : vpt >= 4 ? 512 : 1024; }
+// Registers per thread the row-per-CTA forward kernels may use (__maxnreg__): with VPT vectors
+// per thread they launch with at most fwd_max_threads(VPT) threads, and the cap keeps that many
+// resident (VPT <= 2: 48 x 1024, VPT 4: 96 x 512, VPT 8: 192 x 256 - all at most 48K of the
+// SM's 64K).
+constexpr int fwd_max_regs(int vpt) { return vpt <= 2 ? 48 : vpt == 4 ? 96 : 192; }
 constexpr int bwd_max_threads(int vpt) { return vpt >= 4 ? 256 : 512; }
 constexpr int kBwdMaxVpt = 4;
 constexpr int kReduceThreads = 512;  // dw stage-2 CTA size: 32 columns x 16 row groups

@@ -111,8 +111,11 @@ __device__ __forceinline__ LnStats ln_stats(Each each, float n_f, float eps,
     return st;
 }
 
+// Row per CTA (rows in registers). w and b are read where they are used, from L1 (prefetched
+// there at the start), rather than held in registers: with the register cap that keeps more
+// CTAs - more rows in flight - per SM, as in the RMSNorm forward.
 template <typename T, int VPT, bool FUSED>
-__global__ void __launch_bounds__(fwd_max_threads(VPT)) ln_fwd_row_cta(const LnFwdArgs a) {
+__global__ void __maxnreg__(fwd_max_regs(VPT)) ln_fwd_row_cta(const LnFwdArgs a) {
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
     __shared__ float slots[2][2][32];
@@ -120,14 +123,15 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT)) ln_fwd_row_cta(const LnF
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
     const float n_f = static_cast<float>(a.N);
+    const uint4 *w4 = static_cast<const uint4 *>(a.w);
+    const uint4 *b4 = static_cast<const uint4 *>(a.b);
 
-    uint4 wv[VPT], bv[VPT];
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int c = v * nthr + tid;
         if (c < nvec) {
-            wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
-            bv[v] = a.b ? ld_keep(static_cast<const uint4 *>(a.b) + c) : make_uint4(0, 0, 0, 0);
+            prefetch_l1(w4 + c);
+            if (b4) prefetch_l1(b4 + c);
         }
     }
     int parity = 0;
@@ -170,8 +174,13 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT)) ln_fwd_row_cta(const LnF
             if (c < nvec) {
                 float f[V], wf[V], bf[V], o[V];
                 r_of<T, FUSED>(xv[v], rv[v], f);
-                E::unpack(wv[v], wf);
-                E::unpack(bv[v], bf);
+                E::unpack(ld_keep(w4 + c), wf);
+                if (b4) {
+                    E::unpack(ld_keep(b4 + c), bf);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < V; ++k) bf[k] = 0.f;
+                }
 #pragma unroll
                 for (int k = 0; k < V; ++k) o[k] = fmaf(st.dev(f[k]) * st.rstd, wf[k], bf[k]);
                 st_stream(static_cast<uint4 *>(a.y) + base + c, E::pack(o));
@@ -254,25 +263,112 @@ __global__ void __launch_bounds__(1024) ln_fwd_stream(const LnFwdArgs a) {
 }
 
 // ------------------------------------------------------------------------------ backward
+// One row of the backward with its x, dy (and d_ro) vectors in registers (this thread owns
+// vectors c = v * blockDim.x + threadIdx.x; mu, rs the row's mean and rstd): dx written, and
+// dy * xhat and dy added into this thread's dw and db registers. w is read where it is used,
+// from L1, rather than held in registers: this kernel's registers go to the dw and db sums.
+// `after_reduce` runs right after the CTA-wide sums, when every thread has consumed its inputs;
+// when it returns false the row is abandoned.
+template <typename T, int VPT, bool ADDG, typename AfterReduce>
+__device__ __forceinline__ bool ln_bwd_row_body(const LnBwdArgs &a, int64_t row, int nvec,
+                                                const uint4 (&xv)[VPT], const uint4 (&dyv)[VPT],
+                                                const uint4 (&gv)[VPT],
+                                                float (&dw)[VPT][Elem<T>::kPerVec],
+                                                float (&db)[VPT][Elem<T>::kPerVec],
+                                                float (&slots)[2][2][32], int &parity, float mu,
+                                                float rs, AfterReduce after_reduce) {
+    using E = Elem<T>;
+    constexpr int V = E::kPerVec;
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const float n_f = static_cast<float>(a.N);
+    const uint4 *w4 = static_cast<const uint4 *>(a.w);
+    float sg = 0.f, sgx = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * nthr + tid;
+        if (c < nvec) {
+            float xf[V], d[V], wf[V];
+            E::unpack(xv[v], xf);
+            E::unpack(dyv[v], d);
+            E::unpack(ld_keep(w4 + c), wf);
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                const float xh = (xf[k] - mu) * rs;
+                const float g = d[k] * wf[k];
+                sg += g;
+                sgx = fmaf(g, xh, sgx);
+                dw[v][k] = fmaf(d[k], xh, dw[v][k]);
+                db[v][k] += d[k];
+            }
+        }
+    }
+    const float2 t = cta_sum2(sg, sgx, slots[parity]);
+    parity ^= 1;
+    if (!after_reduce()) return false;
+    const float mg = t.x / n_f, mgx = t.y / n_f;
+    const int64_t base = row * nvec;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * nthr + tid;
+        if (c < nvec) {
+            float xf[V], d[V], wf[V], o[V];
+            E::unpack(xv[v], xf);
+            E::unpack(dyv[v], d);
+            E::unpack(ld_keep(w4 + c), wf);
+#pragma unroll
+            for (int k = 0; k < V; ++k) o[k] = rs * (d[k] * wf[k] - mg - ((xf[k] - mu) * rs) * mgx);
+            if constexpr (ADDG) {
+                float gg[V];
+                E::unpack(gv[v], gg);
+#pragma unroll
+                for (int k = 0; k < V; ++k) o[k] += gg[k];
+            }
+            st_stream(static_cast<uint4 *>(a.dx) + base + c, E::pack(o));
+        }
+    }
+    return true;
+}
+
+// This CTA's dw and db partial sums -> row blockIdx.x of the two [P, N] workspace halves.
+template <typename T, int VPT>
+__device__ __forceinline__ void ln_bwd_store_partial(const LnBwdArgs &a, int nvec,
+                                                     const float (&dw)[VPT][Elem<T>::kPerVec],
+                                                     const float (&db)[VPT][Elem<T>::kPerVec]) {
+    constexpr int V = Elem<T>::kPerVec;
+    float *pw = a.partial + static_cast<int64_t>(blockIdx.x) * a.N;
+    float *pb = a.partial + (static_cast<int64_t>(gridDim.x) + blockIdx.x) * a.N;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * blockDim.x + threadIdx.x;
+        if (c < nvec) {
+#pragma unroll
+            for (int q = 0; q < V / 4; ++q) {
+                reinterpret_cast<float4 *>(pw + static_cast<int64_t>(c) * V)[q] =
+                    make_float4(dw[v][4 * q], dw[v][4 * q + 1], dw[v][4 * q + 2], dw[v][4 * q + 3]);
+                reinterpret_cast<float4 *>(pb + static_cast<int64_t>(c) * V)[q] =
+                    make_float4(db[v][4 * q], db[v][4 * q + 1], db[v][4 * q + 2], db[v][4 * q + 3]);
+            }
+        }
+    }
+}
+
 // Stage 1, rows in registers: CTA p owns rows p, p + P, p + 2P, ...; dw and db partials stay in
 // registers and go to rows p of the two [P, N] workspace halves.
 template <typename T, int VPT, bool ADDG>
 __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_cta(const LnBwdArgs a) {
-    pdl_allow_dependents();  // the stage-2 reductions may be scheduled now
-    using E = Elem<T>;
-    constexpr int V = E::kPerVec;
+    pdl_allow_dependents();  // the stage-2 reduction may be scheduled now
+    constexpr int V = Elem<T>::kPerVec;
     __shared__ float slots[2][2][32];
     const int nvec = a.N / V;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
-    const float n_f = static_cast<float>(a.N);
 
-    uint4 wv[VPT];
     float dw[VPT][V], db[VPT][V];
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int c = v * nthr + tid;
-        if (c < nvec) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
+        if (c < nvec) prefetch_l1(static_cast<const uint4 *>(a.w) + c);
 #pragma unroll
         for (int k = 0; k < V; ++k) dw[v][k] = db[v][k] = 0.f;
     }
@@ -289,66 +385,99 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_cta(const LnB
                 if constexpr (ADDG) gv[v] = ld_stream(static_cast<const uint4 *>(a.d_ro) + base + c);
             }
         }
-        const float mu = __ldg(a.mean + row);
-        const float rs = __ldg(a.rstd + row);
-        float sg = 0.f, sgx = 0.f;
-#pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const int c = v * nthr + tid;
-            if (c < nvec) {
-                float xf[V], d[V], wf[V];
-                E::unpack(xv[v], xf);
-                E::unpack(dyv[v], d);
-                E::unpack(wv[v], wf);
-#pragma unroll
-                for (int k = 0; k < V; ++k) {
-                    const float xh = (xf[k] - mu) * rs;
-                    const float g = d[k] * wf[k];
-                    sg += g;
-                    sgx = fmaf(g, xh, sgx);
-                    dw[v][k] = fmaf(d[k], xh, dw[v][k]);
-                    db[v][k] += d[k];
-                }
-            }
-        }
-        const float2 t = cta_sum2(sg, sgx, slots[parity]);
-        parity ^= 1;
-        const float mg = t.x / n_f, mgx = t.y / n_f;
-#pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const int c = v * nthr + tid;
-            if (c < nvec) {
-                float xf[V], d[V], wf[V], o[V];
-                E::unpack(xv[v], xf);
-                E::unpack(dyv[v], d);
-                E::unpack(wv[v], wf);
-#pragma unroll
-                for (int k = 0; k < V; ++k) o[k] = rs * (d[k] * wf[k] - mg - ((xf[k] - mu) * rs) * mgx);
-                if constexpr (ADDG) {
-                    float gg[V];
-                    E::unpack(gv[v], gg);
-#pragma unroll
-                    for (int k = 0; k < V; ++k) o[k] += gg[k];
-                }
-                st_stream(static_cast<uint4 *>(a.dx) + base + c, E::pack(o));
-            }
-        }
+        ln_bwd_row_body<T, VPT, ADDG>(a, row, nvec, xv, dyv, gv, dw, db, slots, parity,
+                                      __ldg(a.mean + row), __ldg(a.rstd + row), [] { return true; });
     }
-    float *pw = a.partial + static_cast<int64_t>(blockIdx.x) * a.N;
-    float *pb = a.partial + (static_cast<int64_t>(gridDim.x) + blockIdx.x) * a.N;
+    ln_bwd_store_partial<T, VPT>(a, nvec, dw, db);
+}
+
+// Stage 1 fed by the TMA engine, as the RMSNorm backward's: CTA p owns rows p, p + P, ...,
+// keeps a.stages of them (x, dy and, fused, d_ro) in a shared-memory ring filled with
+// cp.async.bulk and refills a slot once the row's CTA-wide sums are done; the next row's mean
+// and rstd are requested one row ahead.
+template <typename T, int VPT, bool ADDG>
+__global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_tma(const LnBwdArgs a) {
+    pdl_allow_dependents();  // the stage-2 reduction may be scheduled now
+    constexpr int V = Elem<T>::kPerVec;
+    constexpr int NT = ADDG ? 3 : 2;
+    extern __shared__ __align__(128) unsigned char ring_buf[];
+    __shared__ __align__(8) uint64_t full[kMaxStages];
+    __shared__ float slots[2][2][32];
+    __shared__ int abort_flag;
+
+    const int nvec = a.N / V;
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    RowRing<NT> ring;
+    ring.buf = ring_buf;
+    ring.full = full;
+    ring.src[0] = static_cast<const char *>(a.x);
+    ring.src[1] = static_cast<const char *>(a.dy);
+    if constexpr (ADDG) ring.src[NT - 1] = static_cast<const char *>(a.d_ro);
+    ring.row_bytes = static_cast<uint32_t>(a.N) * static_cast<uint32_t>(sizeof(T));
+    ring.S = a.stages;
+    ring.first = blockIdx.x;
+    ring.stride = gridDim.x;
+    ring.nrows = ring.first < a.M ? (a.M - 1 - ring.first) / ring.stride + 1 : 0;
+
+    if (tid == 0) {
+        ring.init();
+        abort_flag = 0;
+    }
+    __syncthreads();
+    if (tid == 0) ring.prime();
+
+    float dw[VPT][V], db[VPT][V];
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int c = v * nthr + tid;
-        if (c < nvec) {
+        if (c < nvec) prefetch_l1(static_cast<const uint4 *>(a.w) + c);
 #pragma unroll
-            for (int q = 0; q < V / 4; ++q) {
-                reinterpret_cast<float4 *>(pw + static_cast<int64_t>(c) * V)[q] =
-                    make_float4(dw[v][4 * q], dw[v][4 * q + 1], dw[v][4 * q + 2], dw[v][4 * q + 3]);
-                reinterpret_cast<float4 *>(pb + static_cast<int64_t>(c) * V)[q] =
-                    make_float4(db[v][4 * q], db[v][4 * q + 1], db[v][4 * q + 2], db[v][4 * q + 3]);
+        for (int k = 0; k < V; ++k) dw[v][k] = db[v][k] = 0.f;
+    }
+    int parity = 0;
+    int64_t k = 0;
+    float mu = 0.f, rs = 0.f;
+    if (ring.nrows > 0) {
+        mu = __ldg(a.mean + ring.first);
+        rs = __ldg(a.rstd + ring.first);
+    }
+    for (; k < ring.nrows; ++k) {
+        float mu_next = 0.f, rs_next = 0.f;
+        if (k + 1 < ring.nrows) {
+            const int64_t nxt = ring.first + (k + 1) * ring.stride;
+            mu_next = __ldg(a.mean + nxt);
+            rs_next = __ldg(a.rstd + nxt);
+        }
+        if (!ring.wait(k, a.faults)) abort_flag = 1;
+        uint4 xv[VPT], dyv[VPT], gv[VPT];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * nthr + tid;
+            if (c < nvec) {
+                xv[v] = ld_shared_v4(ring.slot(k, 0) + static_cast<size_t>(c) * 16);
+                dyv[v] = ld_shared_v4(ring.slot(k, 1) + static_cast<size_t>(c) * 16);
+                if constexpr (ADDG) gv[v] = ld_shared_v4(ring.slot(k, NT - 1) + static_cast<size_t>(c) * 16);
             }
         }
+        const bool done = ln_bwd_row_body<T, VPT, ADDG>(
+            a, ring.first + k * ring.stride, nvec, xv, dyv, gv, dw, db, slots, parity, mu, rs, [&] {
+                if (abort_flag) return false;  // written before the barrier: uniform
+                if (tid == 0 && k + ring.S < ring.nrows) {
+                    fence_proxy_async();
+                    ring.issue(k + ring.S);
+                }
+                return true;
+            });
+        if (!done) break;
+        mu = mu_next;
+        rs = rs_next;
     }
+    if (k < ring.nrows) {  // a wait ran out: the partial rows are not written; the fault word tells
+        if (tid == 0) ring.drain(k);
+        return;
+    }
+    ln_bwd_store_partial<T, VPT>(a, nvec, dw, db);
 }
 
 // Stage 1 for any N and alignment: two passes over each row; the partials accumulate in the
@@ -457,6 +586,13 @@ const void *ln_bwd_kernel_ptr(const Launch &l) {
                 case 4: return reinterpret_cast<const void *>(&ln_bwd_row_cta<T, 4, ADDG>);
                 default: return nullptr;
             }
+        case RRN_VARIANT_ROW_TMA:
+            switch (l.vpt) {
+                case 1: return reinterpret_cast<const void *>(&ln_bwd_row_tma<T, 1, ADDG>);
+                case 2: return reinterpret_cast<const void *>(&ln_bwd_row_tma<T, 2, ADDG>);
+                case 4: return reinterpret_cast<const void *>(&ln_bwd_row_tma<T, 4, ADDG>);
+                default: return nullptr;
+            }
         case RRN_VARIANT_STREAM:
             return l.vec ? reinterpret_cast<const void *>(&ln_bwd_stream<T, true, ADDG>)
                          : reinterpret_cast<const void *>(&ln_bwd_stream<T, false, ADDG>);
@@ -478,15 +614,17 @@ template <typename T>
 cudaError_t launch_ln_bwd(const LnBwdArgs &a, const Launch &l, cudaStream_t stream) {
     const void *k = a.d_ro ? ln_bwd_kernel_ptr<T, true>(l) : ln_bwd_kernel_ptr<T, false>(l);
     if (!k) return cudaErrorInvalidConfiguration;
+    if (l.smem > 0) {
+        cudaError_t e = allow_dynamic_smem(k, l.smem);
+        if (e != cudaSuccess) return e;
+    }
     LnBwdArgs args = a;
+    args.stages = l.stages;
     void *params[] = {&args};
-    cudaError_t e = cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, 0, stream);
+    cudaError_t e = cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params,
+                                     static_cast<size_t>(l.smem), stream);
     if (e != cudaSuccess) return e;
-    e = launch_dw_reduce(a.partial, a.dw, l.ctas, a.N, stream);
-    if (e != cudaSuccess || !a.db) return e;
-    // launched the same way: its wait returns once the dw reduction has finished, which in turn
-    // started reading only after stage 1 had finished
-    return launch_dw_reduce(a.partial + static_cast<int64_t>(l.ctas) * a.N, a.db, l.ctas, a.N, stream);
+    return launch_dw_reduce(a.partial, a.dw, a.db, l.ctas, a.N, stream);  // dw and db together
 }
 
 template <typename T>
@@ -494,8 +632,10 @@ int occupancy_ln_t(bool bwd, bool flag, const Launch &l) {
     const void *k = bwd ? (flag ? ln_bwd_kernel_ptr<T, true>(l) : ln_bwd_kernel_ptr<T, false>(l))
                         : (flag ? ln_fwd_kernel_ptr<T, true>(l) : ln_fwd_kernel_ptr<T, false>(l));
     if (!k) return 0;
+    if (l.smem > 0 && allow_dynamic_smem(k, l.smem) != cudaSuccess) return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, l.threads, 0) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, l.threads, static_cast<size_t>(l.smem)) !=
+        cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }

@@ -145,6 +145,53 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// A CTA's ring of S shared-memory slots fed by bulk copies. Slot k % S holds row k of the CTA
+// (global row first + k * stride, k < nrows) of NT tensors - src[t] + row * row_bytes - and
+// completes on the mbarrier full[k % S]. One thread initialises the barriers and issues the
+// copies; every thread waits. A slot may be refilled once every thread is done reading it.
+template <int NT>
+struct RowRing {
+    unsigned char *buf;  // S * NT * row_bytes bytes of dynamic shared memory
+    uint64_t *full;      // S mbarriers
+    const char *src[NT];
+    uint32_t row_bytes;
+    int S;
+    int64_t first, stride, nrows;
+
+    __device__ __forceinline__ unsigned char *slot(int64_t k, int t) const {
+        return buf + static_cast<size_t>(static_cast<int>(k % S) * NT + t) * row_bytes;
+    }
+    // One thread, before the CTA barrier that precedes any use.
+    __device__ __forceinline__ void init() const {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        fence_mbarrier_init();
+        fence_proxy_async();
+    }
+    // One thread: request row k of every tensor into its slot. The caller has ordered its own
+    // earlier reads of that slot (fence_proxy_async) when the slot is being refilled.
+    __device__ __forceinline__ void issue(int64_t k) const {
+        uint64_t *bar = &full[k % S];
+        const int64_t off = (first + k * stride) * static_cast<int64_t>(row_bytes);
+        mbar_arrive_expect_tx(bar, NT * row_bytes);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) bulk_g2s(slot(k, t), src[t] + off, row_bytes, bar);
+    }
+    // One thread: fill the ring with the first rows.
+    __device__ __forceinline__ void prime() const {
+        for (int64_t k = 0; k < nrows && k < S; ++k) issue(k);
+    }
+    // Every thread: wait (bounded) until row k has landed; false after a timeout.
+    __device__ __forceinline__ bool wait(int64_t k, unsigned int *faults) const {
+        return mbar_wait(&full[k % S], static_cast<uint32_t>((k / S) & 1), faults);
+    }
+    // One thread, after the CTA gave up at row k: let the copies already issued land before the
+    // shared memory is released (each wait bounded again).
+    __device__ __forceinline__ void drain(int64_t k) const {
+        for (int64_t j = k; j < nrows && j < k + S; ++j)
+            (void)mbar_wait(&full[j % S], static_cast<uint32_t>((j / S) & 1), nullptr, 100000000ull);
+    }
+};
+
 // Load one float from the shared memory of CTA `rank` of this cluster, at the address `local`
 // has in this CTA.
 __device__ __forceinline__ float ld_cluster_f32(const float *local, uint32_t rank) {

@@ -107,7 +107,10 @@ def test_layernorm_backward_variants(dtype, N):
         for vpt in (1, 2, 4):
             thr = -(-(-(-nvec // vpt)) // 32) * 32
             if thr <= (256 if vpt == 4 else 512):
-                launches += [rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0), rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 6)]
+                launches += [rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0), rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 6),
+                             rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 0, 0),     # ring depth planned
+                             rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 7, 1),     # one row in flight
+                             rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 0, 3)]
     cond0 = bwd_cond(h["x"], h["dy"], h["w"], wl.eps, layernorm=True)
     for with_dro in (True, False):
         ref_dx, ref_dw, ref_db = oracle.add_layernorm_bwd(h["dy"], h["d_ro"] if with_dro else None,
