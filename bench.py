@@ -41,10 +41,10 @@ CSRC = os.path.join(ROOT, "residual_rmsnorm_row_gb300", "csrc")
 # The sources the timed forward kernel (fwd_row_cta, fused, bf16) is built from; the ncu DRAM
 # traffic below holds only while their hash matches (else `traffic` is reported as null).
 FWD_SOURCES = ("common.cuh", "launch.h", "fwd_kernels.cuh", "fwd_bf16.cu", "tma.cuh")
-# dram__bytes_read.sum + dram__bytes_write.sum of one fwd_row_cta<bf16, 2, fused> launch on the
-# 16384 x 4096 workload (ncu --set full, summarised under profiles/) and the source hash it was
-# taken at.
-NCU_FWD_TRAFFIC = {"bytes": None, "sources_sha": None}
+# dram__bytes_read.sum + dram__bytes_write.sum of one fwd_row_cta<bf16, 4, fused> launch on the
+# 16384 x 4096 workload (ncu --set full, summarised under profiles/: 268,476,160 read +
+# 214,852,096 written) and the source hash it was taken at.
+NCU_FWD_TRAFFIC = {"bytes": 483328256, "sources_sha": "5edda1d3154277f8"}
 
 
 # ------------------------------------------------------------------ helpers
