@@ -361,6 +361,8 @@ BY_SHAPE = [
     "rmsnorm_fwd_32x8192_f32", "rmsnorm_fwd_64x8192_f32", "rmsnorm_fwd_65536x2048_bf16",
     "rmsnorm_fwd_65536x2048_f32", "rmsnorm_bwd_16384x4096_bf16", "add_rmsnorm_bwd_16384x4096_bf16",
     "add_layernorm_fwd_16384x4096_bf16", "layernorm_bwd_16384x4096_bf16",
+    "add_rmsnorm_fp8_16384x4096_bf16", "add_rmsnorm_fwd_16384x16384_bf16",
+    "add_rmsnorm_fwd_4096x65536_bf16",
 ]
 L2_BYTES = 129 * 2 ** 20
 SMALL_BYTES = 8 * 2 ** 20     # below this a launch takes a few microseconds: time it in a graph
@@ -393,11 +395,17 @@ def measure_shape(name: str, dev, reps: int):
         t = {key: dev_tensor(h[key], dev).roll(k, 0).contiguous()
              for key in ("x", "residual", "dy", "d_ro") if key in h}
         sets.append(t)
+    bwd = wl.op in ("rmsnorm_bwd", "add_rmsnorm_bwd", "layernorm_bwd")
     ws = torch.empty(max(rrn.rmsnorm_bwd_workspace_bytes(M, N, w.dtype),
-                         rrn.layernorm_bwd_workspace_bytes(M, N, w.dtype), 16) // 4, device=dev)
+                         rrn.layernorm_bwd_workspace_bytes(M, N, w.dtype), 16) // 4 if bwd else 4,
+                     device=dev)
     f32 = lambda n: torch.empty(n, device=dev)  # noqa: E731
     outs = [dict(y=torch.empty_like(s["x"]), ro=torch.empty_like(s["x"]), rstd=f32(M), mean=f32(M),
                  dw=f32(N), db=f32(N)) for s in sets]
+    if wl.op == "add_rmsnorm_fp8":
+        for o in outs:
+            o["q"] = torch.empty(M, N, dtype=torch.uint8, device=dev)
+            o["scale"] = f32(M)
     if wl.op in ("rmsnorm_bwd", "add_rmsnorm_bwd", "layernorm_bwd"):
         for s in sets:   # the forward statistics the backward consumes
             if wl.op == "layernorm_bwd":
@@ -421,6 +429,8 @@ def measure_shape(name: str, dev, reps: int):
         elif wl.op == "layernorm_bwd":
             rrn.layernorm_bwd(s["dy"], s["d_ro"], s["x"], w, s["mean"], s["rstd"], o["y"], o["dw"],
                               o["db"], ws, wl.eps)
+        elif wl.op == "add_rmsnorm_fp8":
+            rrn.rmsnorm_fwd_fp8(s["x"], s["residual"], o["ro"], w, o["q"], o["scale"], None, wl.eps)
 
     for i in range(3):
         run(i)
@@ -457,6 +467,8 @@ def measure_shape(name: str, dev, reps: int):
     gbs = nbytes / (us * 1e-6) / 1e9
     if "layernorm" in wl.op:
         plan = "layernorm planner (row_cta or stream)"
+    elif wl.op == "add_rmsnorm_fp8":
+        plan = "fp8 planner (row_cta or stream)"
     elif wl.op in ("rmsnorm_bwd", "add_rmsnorm_bwd"):
         plan = rrn.plan_bwd(sets[0]["dy"], sets[0]["x"], w, outs[0]["y"], sets[0].get("d_ro")).name
     else:

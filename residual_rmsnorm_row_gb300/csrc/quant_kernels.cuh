@@ -39,23 +39,47 @@ __device__ __forceinline__ uint16_t e4m3x2(float a, float b) {
     return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
+// Sum of one float and maximum of another over the CTA, with one barrier (fixed order).
+__device__ __forceinline__ float2 cta_sum_max(float s, float m, float (*slots)[32]) {
+    s = warp_sum(s);
+    m = warp_max(m);
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) {
+        slots[0][warp] = s;
+        slots[1][warp] = m;
+    }
+    __syncthreads();
+    const int nwarps = blockDim.x >> 5;
+    float2 t = make_float2(0.f, 0.f);
+    for (int i = 0; i < nwarps; ++i) {
+        t.x += slots[0][i];
+        t.y = fmaxf(t.y, slots[1][i]);
+    }
+    return t;
+}
+
+// Row per CTA (rows in registers; w read through L1, prefetched at the start, under the
+// forward's register cap). One CTA-wide step per row gives both sum(r^2) and max|r * w|: as
+// rstd > 0 multiplies every y, amax = rstd * max|r * w| (within a rounding or two of the amax
+// over the fp32 y values, far inside the scale's tolerance; saturation keeps every code finite).
 template <typename T, int VPT, bool FUSED>
-__global__ void __launch_bounds__(fwd_max_threads(VPT)) quant_row_cta(const QuantArgs a) {
+__global__ void __maxnreg__(fwd_max_regs(VPT)) quant_row_cta(const QuantArgs a) {
     using E = Elem<T>;
     constexpr int V = E::kPerVec;  // 8 (bf16) or 4 (fp32) codes per vector: 8 or 4 bytes
-    __shared__ float slots[2][32];
+    __shared__ float slots[2][2][32];
+    __shared__ float rescue_slots[2][32];  // the rare rescaled-rstd path's own reductions
     const int nvec = a.N / V;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
     const float n_f = static_cast<float>(a.N);
+    const uint4 *w4 = static_cast<const uint4 *>(a.w);
 
-    uint4 wv[VPT];
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int c = v * nthr + tid;
-        if (c < nvec) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
+        if (c < nvec) prefetch_l1(w4 + c);
     }
-    int parity = 0;
+    int parity = 0, rescue_parity = 0;
     for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
         const int64_t base = row * nvec;
         uint4 xv[VPT], rv[VPT];
@@ -67,19 +91,23 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT)) quant_row_cta(const Quan
                 if (FUSED) rv[v] = ld_stream(static_cast<const uint4 *>(a.res) + base + c);
             }
         }
-        float ss = 0.f;
+        float ss = 0.f, mw = 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * nthr + tid;
             if (c < nvec) {
-                float f[V];
+                float f[V], wf[V];
                 r_of<T, FUSED>(xv[v], rv[v], f);
                 if (FUSED) st_stream(static_cast<uint4 *>(a.res_out) + base + c, E::pack(f));
+                E::unpack(ld_keep(w4 + c), wf);
 #pragma unroll
-                for (int k = 0; k < V; ++k) ss = fmaf(f[k], f[k], ss);
+                for (int k = 0; k < V; ++k) {
+                    ss = fmaf(f[k], f[k], ss);
+                    mw = fmaxf(mw, fabsf(f[k] * wf[k]));
+                }
             }
         }
-        ss = cta_sum(ss, slots[parity]);
+        const float2 t = cta_sum_max(ss, mw, slots[parity]);
         parity ^= 1;
         auto each = [&](auto fn) {
 #pragma unroll
@@ -91,36 +119,20 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT)) quant_row_cta(const Quan
                     for (int k = 0; k < V; ++k) fn(f[k]);
                 }
         };
-        const float rs = rms_rstd(each, ss, n_f, a.eps, slots, parity);
-        // y = r * rstd * w, evaluated identically in both passes below
-        auto y_of = [&](int v, float (&o)[V]) {
-            float f[V], wf[V];
-            r_of<T, FUSED>(xv[v], rv[v], f);
-            E::unpack(wv[v], wf);
-#pragma unroll
-            for (int k = 0; k < V; ++k) o[k] = f[k] * rs * wf[k];
-        };
-        float am = 0.f;
-#pragma unroll
-        for (int v = 0; v < VPT; ++v)
-            if (v * nthr + tid < nvec) {
-                float o[V];
-                y_of(v, o);
-#pragma unroll
-                for (int k = 0; k < V; ++k) am = fmaxf(am, fabsf(o[k]));
-            }
-        am = cta_max(am, slots[parity]);
-        parity ^= 1;
+        const float rs = rms_rstd(each, t.x, n_f, a.eps, rescue_slots, rescue_parity);
+        const float am = rs * t.y;
         const float inv = am > 0.f ? 448.f / am : 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * nthr + tid;
             if (c < nvec) {
-                float o[V];
-                y_of(v, o);
+                float f[V], wf[V];
+                r_of<T, FUSED>(xv[v], rv[v], f);
+                E::unpack(ld_keep(w4 + c), wf);
                 uint16_t h[V / 2];
 #pragma unroll
-                for (int k = 0; k < V / 2; ++k) h[k] = e4m3x2(o[2 * k] * inv, o[2 * k + 1] * inv);
+                for (int k = 0; k < V / 2; ++k)
+                    h[k] = e4m3x2(f[2 * k] * rs * wf[2 * k] * inv, f[2 * k + 1] * rs * wf[2 * k + 1] * inv);
                 uint8_t *dst = static_cast<uint8_t *>(a.q) + (base + c) * V;
                 if constexpr (V == 8) {
                     *reinterpret_cast<uint2 *>(dst) =

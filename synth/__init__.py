@@ -29,7 +29,8 @@ class Workload:
 
     name: str
     op: str                      # rmsnorm_fwd | add_rmsnorm_fwd | rmsnorm_bwd | add_rmsnorm_bwd |
-                                 # layernorm_fwd | add_layernorm_fwd | layernorm_bwd
+                                 # layernorm_fwd | add_layernorm_fwd | layernorm_bwd |
+                                 # add_rmsnorm_fp8
     M: int
     N: int
     dtype: str                   # "bf16" | "f32"
@@ -79,6 +80,12 @@ _add(Workload("add_layernorm_fwd_16384x4096_bf16", "add_layernorm_fwd", 16384, 4
               x_mean=0.5))
 _add(Workload("layernorm_bwd_16384x4096_bf16", "layernorm_bwd", 16384, 4096, BF16, 1e-5, 7,
               x_mean=0.5))
+# The fused Add+RMSNorm feeding fp8 e4m3 codes with a per-row scale (inputs as the fused forward).
+_add(Workload("add_rmsnorm_fp8_16384x4096_bf16", "add_rmsnorm_fp8", 16384, 4096, BF16, 1e-6, 8))
+# Rows wider than one CTA holds in registers: split over a thread-block cluster (16384 wide) or
+# the two-pass kernel (65536 wide).
+_add(Workload("add_rmsnorm_fwd_16384x16384_bf16", "add_rmsnorm_fwd", 16384, 16384, BF16, 1e-6, 9))
+_add(Workload("add_rmsnorm_fwd_4096x65536_bf16", "add_rmsnorm_fwd", 4096, 65536, BF16, 1e-6, 9))
 
 
 def get(name: str) -> Workload:
@@ -114,7 +121,7 @@ def make(w: Workload) -> Dict[str, np.ndarray]:
         x += np.float32(w.x_mean)
     out["x"] = _store(x, w.dtype)
     del x
-    if w.op in ("add_rmsnorm_fwd", "add_layernorm_fwd"):
+    if w.op in ("add_rmsnorm_fwd", "add_layernorm_fwd", "add_rmsnorm_fp8"):
         res = rng.standard_normal(shape, dtype=np.float32)
         if w.res_sigma != 1.0:
             res *= np.float32(w.res_sigma)
@@ -149,6 +156,8 @@ def min_bytes(w: Workload) -> int:
     add_rmsnorm_bwd: residual_out, dy, d_residual_out, d_r (M*N each), w, rstd, dw.
     add_layernorm_fwd: x, residual, residual_out, y (M*N each), w, b (N), mean, rstd (M, fp32).
     layernorm_bwd: x, dy, d_residual_out, dx (M*N each), w (N), mean, rstd (M), dw, db (N, fp32).
+    add_rmsnorm_fp8: x, residual, residual_out (M*N each), the codes (M*N bytes), w (N),
+    scale (M, fp32).
     """
     e = w.elem_bytes
     if w.op == "rmsnorm_fwd":
@@ -163,6 +172,8 @@ def min_bytes(w: Workload) -> int:
         return 4 * w.M * w.N * e + 2 * w.N * e + 8 * w.M
     if w.op == "layernorm_bwd":
         return 4 * w.M * w.N * e + w.N * e + 8 * w.M + 8 * w.N
+    if w.op == "add_rmsnorm_fp8":
+        return 3 * w.M * w.N * e + w.M * w.N + w.N * e + 4 * w.M
     raise ValueError(w.op)
 
 

@@ -8,7 +8,8 @@ def test_every_workload_draws_its_tensors():
     for name, w in synth.WORKLOADS.items():
         small = w.with_shape(min(w.M, 64))
         t = synth.make(small)
-        want = {"x", "w"} | ({"residual"} if w.op in ("add_rmsnorm_fwd", "add_layernorm_fwd") else set()) | (
+        want = {"x", "w"} | ({"residual"} if w.op in ("add_rmsnorm_fwd", "add_layernorm_fwd",
+                                                       "add_rmsnorm_fp8") else set()) | (
             {"dy"} if w.op in ("rmsnorm_bwd", "add_rmsnorm_bwd", "layernorm_bwd") else set()) | (
             {"d_ro"} if w.op in ("add_rmsnorm_bwd", "layernorm_bwd") else set()) | (
             {"b"} if "layernorm" in w.op else set())
@@ -54,3 +55,6 @@ def test_min_bytes_matches_tensor_sizes():
     assert synth.min_bytes(synth.get("add_rmsnorm_fwd_16384x7168_bf16")) == 939_603_968
     assert synth.min_bytes(synth.get("rmsnorm_bwd_16384x4096_bf16")) == 402_743_296
     assert synth.min_bytes(synth.get("rmsnorm_fwd_65536x2048_f32")) == 1_074_012_160
+    # 16384 x 4096: x, residual, residual_out (bf16) + codes (1 byte) + w + scale
+    assert synth.min_bytes(synth.get("add_rmsnorm_fp8_16384x4096_bf16")) == \
+        3 * 16384 * 4096 * 2 + 16384 * 4096 + 4096 * 2 + 4 * 16384
