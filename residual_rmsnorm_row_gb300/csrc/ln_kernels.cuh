@@ -55,9 +55,10 @@ struct LnStats {
     __device__ __forceinline__ float dev(float r) const { return (r - m0) - corr; }
 };
 
+// The corrected two-pass statistics (the fallback of ln_stats).
 template <typename Each>
-__device__ __forceinline__ LnStats ln_stats(Each each, float n_f, float eps,
-                                            float (&slots)[2][2][32], int &parity) {
+__device__ __forceinline__ LnStats ln_stats_two_pass(Each each, float n_f, float eps,
+                                                  float (&slots)[2][2][32], int &parity) {
     float s1 = 0.f;
     each([&](float v) { s1 += v; });
     s1 = cta_sum(s1, slots[parity][0]);
@@ -111,6 +112,48 @@ __device__ __forceinline__ LnStats ln_stats(Each each, float n_f, float eps,
     return st;
 }
 
+// One CTA-wide step in the common case: with K the row's first value (every thread reads it;
+// it is one of the row's own values, so it lies within the row's range), sum d = r - K and d^2
+// together; then mean = K + sum(d) / N and sum((r - mean)^2) = sum(d^2) - sum(d)^2 / N. The
+// subtraction loses precision only when K sits far from the mean compared with the spread: the
+// result is kept when sum((r - mean)^2) >= sum(d^2) / 16 (so at most four bits of cancellation)
+// and the sums are in range; otherwise - a constant row, K an outlier, overflow - the row gets
+// the corrected two-pass statistics (ln_stats_two_pass). As there, m0 (= K) and the
+// correction stay apart.
+// ln_stats_shifted takes this thread's sums d1 = sum(r - K), d2 = sum((r - K)^2), which a kernel
+// may have formed in a pass of its own (the row-per-CTA forward forms them while it stores
+// residual_out); ln_stats forms them itself.
+template <typename Each>
+__device__ __forceinline__ LnStats ln_stats_shifted(Each each, float K, float d1, float d2, float n_f,
+                                                    float eps, float (&slots)[2][2][32], int &parity) {
+    const float2 t = cta_sum2(d1, d2, slots[parity]);
+    parity ^= 1;
+    if (isfinite(t.x) && !needs_rescale(t.y)) {
+        const float corr = t.x / n_f;
+        const float ssd = t.y - t.x * corr;
+        if (ssd >= 0.0625f * t.y) {
+            LnStats st;
+            st.m0 = K;
+            st.corr = corr;
+            st.rstd = rstd_plain(ssd, n_f, eps);
+            return st;
+        }
+    }
+    return ln_stats_two_pass(each, n_f, eps, slots, parity);
+}
+
+template <typename Each>
+__device__ __forceinline__ LnStats ln_stats(Each each, float K, float n_f, float eps,
+                                            float (&slots)[2][2][32], int &parity) {
+    float d1 = 0.f, d2 = 0.f;
+    each([&](float v) {
+        const float d = v - K;
+        d1 += d;
+        d2 = fmaf(d, d, d2);
+    });
+    return ln_stats_shifted(each, K, d1, d2, n_f, eps, slots, parity);
+}
+
 // Row per CTA (rows in registers). w and b are read where they are used, from L1 (prefetched
 // there at the start), rather than held in registers: with the register cap that keeps more
 // CTAs - more rows in flight - per SM, as in the RMSNorm forward.
@@ -146,14 +189,22 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) ln_fwd_row_cta(const LnFwdArgs a)
                 if (FUSED) rv[v] = ld_stream(static_cast<const uint4 *>(a.res) + base + c);
             }
         }
-        if (FUSED) {
+        // the row's first value, formed exactly as r_of forms it (the shift of the statistics)
+        float K = E::load1(a.x, row * static_cast<int64_t>(a.N));
+        if constexpr (FUSED) K += E::load1(a.res, row * static_cast<int64_t>(a.N));
+        float d1 = 0.f, d2 = 0.f;  // residual_out is stored in the same pass
 #pragma unroll
-            for (int v = 0; v < VPT; ++v) {
-                const int c = v * nthr + tid;
-                if (c < nvec) {
-                    float f[V];
-                    r_of<T, FUSED>(xv[v], rv[v], f);
-                    st_stream(static_cast<uint4 *>(a.res_out) + base + c, E::pack(f));
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * nthr + tid;
+            if (c < nvec) {
+                float f[V];
+                r_of<T, FUSED>(xv[v], rv[v], f);
+                if (FUSED) st_stream(static_cast<uint4 *>(a.res_out) + base + c, E::pack(f));
+#pragma unroll
+                for (int k = 0; k < V; ++k) {
+                    const float d = f[k] - K;
+                    d1 += d;
+                    d2 = fmaf(d, d, d2);
                 }
             }
         }
@@ -167,7 +218,8 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) ln_fwd_row_cta(const LnFwdArgs a)
                     for (int k = 0; k < V; ++k) fn(f[k]);
                 }
         };
-        const LnStats st = ln_stats(each, n_f, a.eps, slots, parity);
+        const LnStats st = ln_stats_shifted(each, K, d1, d2, n_f, a.eps, slots, parity);
+        const float ncr = -st.corr * st.rstd;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * nthr + tid;
@@ -181,8 +233,9 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) ln_fwd_row_cta(const LnFwdArgs a)
 #pragma unroll
                     for (int k = 0; k < V; ++k) bf[k] = 0.f;
                 }
+                // (r - m0 - corr) * rstd with one operation fewer: (r - m0) * rstd - corr * rstd
 #pragma unroll
-                for (int k = 0; k < V; ++k) o[k] = fmaf(st.dev(f[k]) * st.rstd, wf[k], bf[k]);
+                for (int k = 0; k < V; ++k) o[k] = fmaf(fmaf(f[k] - st.m0, st.rstd, ncr), wf[k], bf[k]);
                 st_stream(static_cast<uint4 *>(a.y) + base + c, E::pack(o));
             }
         }
@@ -231,7 +284,9 @@ __global__ void __launch_bounds__(1024) ln_fwd_stream(const LnFwdArgs a) {
                 for (int k = 0; k < V; ++k) fn(f[k]);
             }
         };
-        const LnStats st = ln_stats(each, n_f, a.eps, slots, parity);
+        float K = E::load1(a.x, base);  // the row's first value: the shift of ln_stats
+        if constexpr (FUSED) K += E::load1(a.res, base);
+        const LnStats st = ln_stats(each, K, n_f, a.eps, slots, parity);
         for (int c = tid; c < nchunk; c += nthr) {
             float f[W], wf[W], bf[W], o[W];
             load_r(base, c, f);

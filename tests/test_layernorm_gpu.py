@@ -135,6 +135,13 @@ def test_layernorm_backward_variants(dtype, N):
 def test_layernorm_extreme_rows(dtype, N):
     rng = np.random.default_rng(93)
     base = rng.standard_normal((6, N)).astype(np.float32)
+    # The statistics are taken relative to the row's first value; a first value far from the
+    # mean compared with the spread sends the row to the two-pass path, one 3.5 sigma away
+    # stays on the one-step path with about four bits of cancellation.
+    first_outlier = base[1].copy()
+    first_outlier[0] = 50.0
+    first_far = base[2].copy()
+    first_far[0] = 3.5
     rows = np.stack([
         base[0] * 1e36 + 3e36,           # sum and squared deviations overflow fp32
         np.full(N, 3.0, np.float32),     # constant row: xhat = 0, y = b
@@ -142,6 +149,9 @@ def test_layernorm_extreme_rows(dtype, N):
         base[3] * 1e-30,                 # tiny deviations
         base[4] + 100.0,                 # large offset relative to the spread
         base[5],
+        first_outlier,
+        first_far,
+        base[5] * 0.01 + 1e4,            # offset a million times the spread
     ]).astype(np.float32)
     h = {"x": bits_of(rows, dtype), "w": bits_of((1 + 0.1 * rng.standard_normal(N)).astype(np.float32), dtype),
          "b": bits_of((0.1 * rng.standard_normal(N)).astype(np.float32), dtype)}
