@@ -566,9 +566,19 @@ def main():
     ap.add_argument("--no-by-shape", action="store_true",
                     help="skip the per-shape table (every named workload timed alone)")
     ap.add_argument("--by-shape-reps", type=int, default=50)
+    ap.add_argument("--shape", choices=BY_SHAPE, default=None,
+                    help="time one workload of the per-shape table alone and print its entry "
+                         "(3 untimed launches, then --by-shape-reps timed ones; for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.shape:
+        import residual_rmsnorm_row_gb300 as rrn
+
+        rrn.load_library()
+        print(json.dumps(measure_shape(args.shape, torch.device("cuda", 0), args.by_shape_reps)),
+              flush=True)
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         out = run_reference(args, world, rank)
