@@ -121,7 +121,8 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) quant_row_cta(const QuantArgs a) 
         };
         const float rs = rms_rstd(each, t.x, n_f, a.eps, rescue_slots, rescue_parity);
         const float am = rs * t.y;
-        const float inv = am > 0.f ? 448.f / am : 0.f;
+        // code k = e4m3(r * w * (rstd * 448 / amax)): one per-row factor
+        const float qs = am > 0.f ? rs * (448.f / am) : 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * nthr + tid;
@@ -132,7 +133,7 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) quant_row_cta(const QuantArgs a) 
                 uint16_t h[V / 2];
 #pragma unroll
                 for (int k = 0; k < V / 2; ++k)
-                    h[k] = e4m3x2(f[2 * k] * rs * wf[2 * k] * inv, f[2 * k + 1] * rs * wf[2 * k + 1] * inv);
+                    h[k] = e4m3x2(f[2 * k] * wf[2 * k] * qs, f[2 * k + 1] * wf[2 * k + 1] * qs);
                 uint8_t *dst = static_cast<uint8_t *>(a.q) + (base + c) * V;
                 if constexpr (V == 8) {
                     *reinterpret_cast<uint2 *>(dst) =
