@@ -535,7 +535,7 @@ int run_bwd(const void *dy, const void *d_ro, const void *x, const void *w, cons
 
 // ---------------------------------------------------------------- LayerNorm
 // Register layout (vpt, threads) for a row of nvec vectors, as the RMSNorm planners choose it:
-// the widest CTA for few rows, about kFwdTargetThreads threads otherwise.
+// about kDecodeTargetThreads threads for few rows, about target_threads otherwise.
 int pick_row_layout(int64_t nvec, int64_t M, int sms, const rrn_launch *cfg, int max_vpt,
                     int (*max_threads)(int), int target_threads, Launch *l) {
     if (cfg && cfg->vpt) {

@@ -8,12 +8,15 @@
 // KernelAgent-Oink's RMSNorm and fused Add + RMSNorm - and, for the reduction, the
 // warp-shuffle-then-shared-memory pattern of the CuTe DSL skill page; the kernels are this
 // library's own design for sm_103a):
-//   fwd_row_cta   one row per CTA, the row held in registers as 128-bit vectors; the grid
-//                 walks rows with a grid-sized stride (persistent when the grid is smaller
-//                 than M, one row per CTA when it is not). Used for N up to 16K (bf16).
-//   fwd_row_warp  one row per warp, no barrier at all; for short rows (bf16 N <= 2048).
-//   fwd_stream    one row per CTA in two passes over global memory (sum of squares, then
-//                 normalise, re-reading the row from L2): any N and any alignment.
+//   fwd_row_cta     one row per CTA, the row held in registers as 128-bit vectors; the grid
+//                   walks rows with a grid-sized stride (persistent when the grid is smaller
+//                   than M, one row per CTA when it is not). Rows up to 1024 vectors (bf16
+//                   N <= 8192), up to 2048 when there are few rows.
+//   fwd_row_warp    one row per warp, no barrier at all; for short rows (bf16 N <= 2048).
+//   fwd_row_cluster one row split over the CTAs of a thread-block cluster (wider rows).
+//   fwd_row_tma     row per CTA fed through a shared-memory ring by bulk copies (on request).
+//   fwd_stream      one row per CTA in two passes over global memory (sum of squares, then
+//                   normalise, re-reading the row from L2): any N and any alignment.
 #pragma once
 
 #include "common.cuh"

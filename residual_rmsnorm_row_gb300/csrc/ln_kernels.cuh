@@ -39,16 +39,17 @@ __device__ __forceinline__ float2 cta_sum2(float a, float b, float (*slots)[32])
 
 // ------------------------------------------------------------------------------ forward
 // The row statistics from per-thread access to the row values: `each(fn)` calls fn(v) for
-// every fp32 value of the row this thread owns. Returns (mean, rstd).
-// Pass 1 gives a first mean m0 = sum(r) / N. Pass 2 sums d = r - m0 and d^2 together (one
-// barrier) and corrects both: mean = m0 + sum(d) / N and
+// every fp32 value of the row this thread owns. Returns (mean, rstd) as a reference value m0,
+// a small correction corr (mean = m0 + corr) and rstd: deviations are formed as
+// (r - m0) - corr, so the fp32 rounding of the mean itself never enters them. Reductions
+// alternate between the two slot pairs (parity), as cta_sum callers do.
+// ln_stats_two_pass: pass 1 gives a first mean m0 = sum(r) / N; pass 2 sums d = r - m0 and d^2
+// together (one barrier) and corrects both: corr = sum(d) / N and
 // sum((r - mean)^2) = sum(d^2) - sum(d)^2 / N (the corrected two-pass algorithm), so the
 // rounding error of m0 - which grows with |mean|, not with the spread - cancels out.
-// Reductions alternate between the two slot pairs (parity), as cta_sum callers do.
-// The result keeps m0 and the small correction apart: deviations are formed as
-// (r - m0) - corr, so the fp32 rounding of the mean itself never enters them.
+// ln_stats (below) does the same in one step with m0 = the row's first value when that is safe.
 struct LnStats {
-    float m0;    // first-pass mean
+    float m0;    // reference value: the first-pass mean or the row's first value
     float corr;  // mean - m0
     float rstd;
     __device__ __forceinline__ float mean() const { return m0 + corr; }
