@@ -501,7 +501,8 @@ def oracle_sample(target_s: float, rows_cap: int = 16384):
     bytes_done = n * rows * (fb + bb) / fw.M
     return {"value": round(bytes_done / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{n} x {rows} of {fw.M} rows (fused fwd + bwd, N={fw.N}, bf16 in, fp64 "
-                      f"arithmetic), single-threaded C, {el:.1f} s wall"}
+                      f"arithmetic), single-threaded C, {el:.1f} s wall, on a host with "
+                      f"{os.cpu_count()} cores"}
 
 
 def run_reference(args, world, rank):

@@ -92,6 +92,9 @@ def check_dw(got: np.ndarray, ref: np.ndarray, what: str = "dw") -> float:
     bound = DW_REL * np.maximum(np.abs(ref), 1.0)
     ok = err <= bound
     assert ok.all(), _worst(err, bound, got, ref, what)
+    big = np.abs(ref) >= 1.0  # the pure relative error where it is well conditioned, reported
+    if big.any():
+        print(f"{what}: max relative error over |ref| >= 1: {float(np.max(err[big] / np.abs(ref[big]))):.2e}")
     return float(np.max(err / bound)) if err.size else 0.0
 
 
