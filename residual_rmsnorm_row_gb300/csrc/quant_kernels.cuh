@@ -62,6 +62,7 @@ __device__ __forceinline__ float2 cta_sum_max(float s, float m, float (*slots)[3
 // forward's register cap). One CTA-wide step per row gives both sum(r^2) and max|r * w|: as
 // rstd > 0 multiplies every y, amax = rstd * max|r * w| (within a rounding or two of the amax
 // over the fp32 y values, far inside the scale's tolerance; saturation keeps every code finite).
+// Only when some |r * w| overflows fp32 does the row take a second step, for the amax of y.
 template <typename T, int VPT, bool FUSED>
 __global__ void __maxnreg__(fwd_max_regs(VPT)) quant_row_cta(const QuantArgs a) {
     using E = Elem<T>;
@@ -120,9 +121,26 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) quant_row_cta(const QuantArgs a) 
                 }
         };
         const float rs = rms_rstd(each, t.x, n_f, a.eps, rescue_slots, rescue_parity);
-        const float am = rs * t.y;
-        // code k = e4m3(r * w * (rstd * 448 / amax)): one per-row factor
-        const float qs = am > 0.f ? rs * (448.f / am) : 0.f;
+        float am = rs * t.y;
+        if (!isfinite(t.y)) {
+            // rare: some |r * w| beyond the fp32 range while y = r * rstd * w is not - the amax
+            // over the y values themselves (a uniform decision: t is the same in every thread)
+            float m = 0.f;
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int c = v * nthr + tid;
+                if (c < nvec) {
+                    float f[V], wf[V];
+                    r_of<T, FUSED>(xv[v], rv[v], f);
+                    E::unpack(ld_keep(w4 + c), wf);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) m = fmaxf(m, fabsf(f[k] * rs * wf[k]));
+                }
+            }
+            am = cta_max(m, rescue_slots[rescue_parity]);
+            rescue_parity ^= 1;
+        }
+        const float inv = am > 0.f ? 448.f / am : 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * nthr + tid;
@@ -133,7 +151,7 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) quant_row_cta(const QuantArgs a) 
                 uint16_t h[V / 2];
 #pragma unroll
                 for (int k = 0; k < V / 2; ++k)
-                    h[k] = e4m3x2(f[2 * k] * wf[2 * k] * qs, f[2 * k + 1] * wf[2 * k + 1] * qs);
+                    h[k] = e4m3x2(f[2 * k] * rs * wf[2 * k] * inv, f[2 * k + 1] * rs * wf[2 * k + 1] * inv);
                 uint8_t *dst = static_cast<uint8_t *>(a.q) + (base + c) * V;
                 if constexpr (V == 8) {
                     *reinterpret_cast<uint2 *>(dst) =

@@ -119,3 +119,15 @@ def test_fp8_zero_and_extreme_rows():
         q, scale, rstd, _ = run(h, "bf16", 1e-6, False, launch)
         compare(h, "bf16", 1e-6, False, q, scale, rstd, None, str(launch))
         assert float(scale[0]) == 0.0 and int(q[0].max()) == 0
+
+
+def test_fp8_row_whose_r_times_w_overflows():
+    # |r| near 1e38 with w = 8: r * w is beyond fp32 although y = r * rstd * w is about 8
+    N = 4096
+    rng = np.random.default_rng(103)
+    z = np.clip(rng.standard_normal(N), -3.0, 3.0).astype(np.float32)  # |r| <= 3e38 stays finite
+    rows = np.stack([z * np.float32(1e38), rng.standard_normal(N).astype(np.float32)])
+    h = {"x": bits_of(rows, "bf16"), "w": bits_of(np.full(N, 8.0, np.float32), "bf16")}
+    for launch in (None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0)):
+        q, scale, rstd, _ = run(h, "bf16", 1e-6, False, launch)
+        compare(h, "bf16", 1e-6, False, q, scale, rstd, None, str(launch))
