@@ -150,6 +150,41 @@ def test_edge_shapes_forward(dtype, N, M):
         compare_fwd(h["x"], h.get("residual"), h["w"], dtype, wl.eps, y, ro, rstd)
 
 
+# The automatic plan for wide rows when rows are not few (M >= 2 x SMs): one row per CTA up to
+# 1024 vectors, a cluster split of at most 512 vectors per CTA up to 4096 vectors, the two-pass
+# kernel beyond (1024 threads from 8192 vectors) and for unaligned rows.
+WIDE_PLANS = [  # (dtype, N, variant, cluster size or threads)
+    ("bf16", 8192, rrn.VARIANT_ROW_CTA, None),
+    ("bf16", 16384, rrn.VARIANT_ROW_CLUSTER, 4),
+    ("bf16", 24576, rrn.VARIANT_ROW_CLUSTER, 8),
+    ("bf16", 32768, rrn.VARIANT_ROW_CLUSTER, 8),
+    ("bf16", 40000, rrn.VARIANT_STREAM, 512),
+    ("bf16", 65536, rrn.VARIANT_STREAM, 1024),
+    ("bf16", 9001, rrn.VARIANT_STREAM, 1024),   # unaligned rows: element-wise two-pass
+    ("f32", 16384, rrn.VARIANT_ROW_CLUSTER, 8),
+    ("f32", 32768, rrn.VARIANT_STREAM, 1024),
+]
+
+
+@pytest.mark.parametrize("dtype,N,variant,extra", WIDE_PLANS)
+def test_wide_rows_automatic_plan(dtype, N, variant, extra):
+    M = 400
+    for fused in (False, True):
+        wl = synth.Workload("wide-plan", "add_rmsnorm_fwd" if fused else "rmsnorm_fwd", M, N, dtype,
+                            1e-6, 200 + N, res_sigma=2.0)
+        h = synth.make(wl)
+        x, w = to_dev(h["x"], dtype), to_dev(h["w"], dtype)
+        res = to_dev(h["residual"], dtype) if fused else None
+        plan = rrn.plan_fwd(x, res, torch.empty_like(x) if fused else None, w, torch.empty_like(x))
+        assert plan.variant == variant, plan.name
+        if variant == rrn.VARIANT_ROW_CLUSTER:
+            assert plan.cluster == extra and plan.ctas % extra == 0, plan.name
+        if variant == rrn.VARIANT_STREAM:
+            assert plan.threads == extra, plan.name
+        y, ro, rstd = fwd_case(h["x"], h.get("residual"), h["w"], dtype, wl.eps)
+        compare_fwd(h["x"], h.get("residual"), h["w"], dtype, wl.eps, y, ro, rstd)
+
+
 def test_empty_matrix_writes_nothing():
     x = torch.zeros(0, 4096, dtype=torch.bfloat16, device="cuda")
     w = torch.ones(4096, dtype=torch.bfloat16, device="cuda")
