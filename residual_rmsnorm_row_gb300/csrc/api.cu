@@ -167,11 +167,13 @@ constexpr int kFwdTargetThreads = 128;
 constexpr int kBwdTargetThreads = 256;
 // Threads per CTA for few-row (decode) problems: one CTA per row, as wide as this.
 constexpr int kDecodeTargetThreads = 512;
-// LayerNorm backward (the dw and db sums in registers): both the register and the TMA ring
-// variants measured best with 256-thread CTAs on 16384 x 4096 bf16 (ring: 114.9 us at 256
-// threads, 127.1 us at 128).
+// LayerNorm backward (the dw and db sums in registers), measured on 16384 x 4096 bf16: the
+// register variant best with 256-thread CTAs; the TMA ring with 256 threads when the gradient at
+// residual_out is a third input row (115.1 us vs 129.4 at 128) and 128 without it (104.4 vs
+// 107.5 at 256).
 constexpr int kLnBwdTargetThreads = 256;
-constexpr int kLnBwdTmaTargetThreads = 256;
+constexpr int kLnBwdTmaTargetThreadsFused = 256;
+constexpr int kLnBwdTmaTargetThreadsPlain = 128;
 // Widest row (in 128-bit vectors) one CTA holds in registers: 8 vectors x 256 threads.
 constexpr int kRowCtaMaxVec = 2048;
 // Vectors of a row each CTA of the cluster split takes when the planner chooses the cluster
@@ -609,7 +611,9 @@ int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, con
     int ring_occ = 0;
     if (l.variant == RRN_VARIANT_ROW_CTA || l.variant == RRN_VARIANT_ROW_TMA) {
         if (!vec_ok) return RRN_ERR_CONFIG;
-        const int target = l.variant == RRN_VARIANT_ROW_TMA ? kLnBwdTmaTargetThreads : kLnBwdTargetThreads;
+        const int target = l.variant != RRN_VARIANT_ROW_TMA ? kLnBwdTargetThreads
+                           : add_grad                         ? kLnBwdTmaTargetThreadsFused
+                                                              : kLnBwdTmaTargetThreadsPlain;
         st = pick_row_layout(nvec, 1LL << 40, sms, cfg, kBwdMaxVpt, bwd_threads_limit, target, &l);
         if (st != RRN_OK) return st;
         if (l.variant == RRN_VARIANT_ROW_TMA) {
