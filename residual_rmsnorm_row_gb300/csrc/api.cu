@@ -177,8 +177,13 @@ constexpr int kLnBwdTmaTargetThreadsPlain = 128;
 // Widest row (in 128-bit vectors) one CTA holds in registers: 8 vectors x 256 threads.
 constexpr int kRowCtaMaxVec = 2048;
 // Vectors of a row each CTA of the cluster split takes when the planner chooses the cluster
-// size (measured best: 4 vectors x 128 threads a CTA, several CTAs per SM).
+// size, for the fused forward (two input rows): measured best at 4 vectors x 128 threads a CTA.
+// The plain forward (one input row) keeps the same bytes in flight per thread with twice as
+// many vectors: measured best at 8 x 128.
 constexpr int kClusterChunkVec = 512;
+
+// Vectors per CTA of the forward's row split for a fused or plain forward.
+int cluster_chunk_vec(bool fused) { return fused ? kClusterChunkVec : 2 * kClusterChunkVec; }
 // CTAs per cluster for the backward's distributed-shared-memory pre-reduction of dw when the
 // caller leaves the choice to the planner (0: no clusters).
 constexpr int kBwdCluster = 0;
@@ -239,15 +244,17 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
     Launch l{};
     l.variant = cfg && cfg->variant ? cfg->variant : RRN_VARIANT_AUTO;
     if (l.variant == RRN_VARIANT_AUTO) {
-        // Measured on 16384 x {4096, 7168, 16384}, 8192 x 32768, 4096 x 65536, 1024 x 262144
-        // bf16: one row per CTA while a 128-thread CTA holds the row (8 vectors a thread);
-        // wider rows split over a cluster, at most kClusterChunkVec vectors per CTA; wider
-        // still, the two-pass kernel. Few rows (decode): one CTA per row up to kRowCtaMaxVec.
+        // Measured on bf16 rows of 4096 to 262144 columns, fused and plain: one row per CTA
+        // while the CTA holds the row - fused up to 1024 vectors (8 a thread x 128 threads),
+        // plain up to kRowCtaMaxVec (8 x 256: the same bytes in flight per thread); wider rows
+        // split over a cluster, cluster_chunk_vec vectors per CTA; wider still, the two-pass
+        // kernel. Few rows (decode): one CTA per row up to kRowCtaMaxVec.
         const bool few = M < 2LL * sms;
+        const int64_t cta_max = few || !fused ? kRowCtaMaxVec : 128 * kMaxVpt;
         if (!vec_ok) l.variant = RRN_VARIANT_STREAM;
         else if (nvec <= 32 * kMaxVpt && M >= 4LL * sms) l.variant = RRN_VARIANT_ROW_WARP;
-        else if (nvec <= (few ? kRowCtaMaxVec : 128 * kMaxVpt)) l.variant = RRN_VARIANT_ROW_CTA;
-        else if (nvec <= static_cast<int64_t>(kMaxCluster) * kClusterChunkVec) l.variant = RRN_VARIANT_ROW_CLUSTER;
+        else if (nvec <= cta_max) l.variant = RRN_VARIANT_ROW_CTA;
+        else if (nvec <= static_cast<int64_t>(kMaxCluster) * cluster_chunk_vec(fused)) l.variant = RRN_VARIANT_ROW_CLUSTER;
         else l.variant = RRN_VARIANT_STREAM;
     }
     l.vec = (l.variant == RRN_VARIANT_STREAM) ? vec_ok : true;
@@ -292,7 +299,7 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
                 l.cluster = cfg->cluster;
             } else {
                 l.cluster = 2;
-                while (l.cluster < kMaxCluster && nvec > static_cast<int64_t>(l.cluster) * kClusterChunkVec) l.cluster *= 2;
+                while (l.cluster < kMaxCluster && nvec > static_cast<int64_t>(l.cluster) * cluster_chunk_vec(fused)) l.cluster *= 2;
             }
             if (l.cluster < 2 || l.cluster > kMaxCluster) return RRN_ERR_CONFIG;
             const int64_t chunk = (nvec + l.cluster - 1) / l.cluster;

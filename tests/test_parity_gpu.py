@@ -150,39 +150,42 @@ def test_edge_shapes_forward(dtype, N, M):
         compare_fwd(h["x"], h.get("residual"), h["w"], dtype, wl.eps, y, ro, rstd)
 
 
-# The automatic plan for wide rows when rows are not few (M >= 2 x SMs): one row per CTA up to
-# 1024 vectors, a cluster split of at most 512 vectors per CTA up to 4096 vectors, the two-pass
-# kernel beyond (1024 threads from 8192 vectors) and for unaligned rows.
-WIDE_PLANS = [  # (dtype, N, variant, cluster size or threads)
-    ("bf16", 8192, rrn.VARIANT_ROW_CTA, None),
-    ("bf16", 16384, rrn.VARIANT_ROW_CLUSTER, 4),
-    ("bf16", 24576, rrn.VARIANT_ROW_CLUSTER, 8),
-    ("bf16", 32768, rrn.VARIANT_ROW_CLUSTER, 8),
-    ("bf16", 40000, rrn.VARIANT_STREAM, 512),
-    ("bf16", 65536, rrn.VARIANT_STREAM, 1024),
-    ("bf16", 9001, rrn.VARIANT_STREAM, 1024),   # unaligned rows: element-wise two-pass
-    ("f32", 16384, rrn.VARIANT_ROW_CLUSTER, 8),
-    ("f32", 32768, rrn.VARIANT_STREAM, 1024),
+# The automatic plan for wide rows when rows are not few (M >= 2 x SMs). Fused (two input
+# rows): one row per CTA up to 1024 vectors, a cluster split of at most 512 vectors per CTA up
+# to 4096 vectors. Plain (one input row, so twice the vectors for the same bytes in flight):
+# one row per CTA up to 2048 vectors, cluster chunks of at most 1024 up to 8192. Wider: the
+# two-pass kernel (1024 threads from 8192 vectors or elements), as for unaligned rows.
+R, C, S = rrn.VARIANT_ROW_CTA, rrn.VARIANT_ROW_CLUSTER, rrn.VARIANT_STREAM
+WIDE_PLANS = [  # (dtype, N, fused, variant, cluster size or threads)
+    ("bf16", 8192, True, R, None), ("bf16", 8192, False, R, None),
+    ("bf16", 16384, True, C, 4), ("bf16", 16384, False, R, None),
+    ("bf16", 24576, True, C, 8), ("bf16", 24576, False, C, 4),
+    ("bf16", 32768, True, C, 8), ("bf16", 32768, False, C, 4),
+    ("bf16", 40000, True, S, 512), ("bf16", 40000, False, C, 8),
+    ("bf16", 65536, True, S, 1024), ("bf16", 65536, False, C, 8),
+    ("bf16", 80000, False, S, 1024),
+    ("bf16", 9001, True, S, 1024), ("bf16", 9001, False, S, 1024),   # unaligned: element-wise
+    ("f32", 16384, True, C, 8), ("f32", 16384, False, C, 4),
+    ("f32", 32768, True, S, 1024), ("f32", 32768, False, C, 8),
 ]
 
 
-@pytest.mark.parametrize("dtype,N,variant,extra", WIDE_PLANS)
-def test_wide_rows_automatic_plan(dtype, N, variant, extra):
+@pytest.mark.parametrize("dtype,N,fused,variant,extra", WIDE_PLANS)
+def test_wide_rows_automatic_plan(dtype, N, fused, variant, extra):
     M = 400
-    for fused in (False, True):
-        wl = synth.Workload("wide-plan", "add_rmsnorm_fwd" if fused else "rmsnorm_fwd", M, N, dtype,
-                            1e-6, 200 + N, res_sigma=2.0)
-        h = synth.make(wl)
-        x, w = to_dev(h["x"], dtype), to_dev(h["w"], dtype)
-        res = to_dev(h["residual"], dtype) if fused else None
-        plan = rrn.plan_fwd(x, res, torch.empty_like(x) if fused else None, w, torch.empty_like(x))
-        assert plan.variant == variant, plan.name
-        if variant == rrn.VARIANT_ROW_CLUSTER:
-            assert plan.cluster == extra and plan.ctas % extra == 0, plan.name
-        if variant == rrn.VARIANT_STREAM:
-            assert plan.threads == extra, plan.name
-        y, ro, rstd = fwd_case(h["x"], h.get("residual"), h["w"], dtype, wl.eps)
-        compare_fwd(h["x"], h.get("residual"), h["w"], dtype, wl.eps, y, ro, rstd)
+    wl = synth.Workload("wide-plan", "add_rmsnorm_fwd" if fused else "rmsnorm_fwd", M, N, dtype,
+                        1e-6, 200 + N, res_sigma=2.0)
+    h = synth.make(wl)
+    x, w = to_dev(h["x"], dtype), to_dev(h["w"], dtype)
+    res = to_dev(h["residual"], dtype) if fused else None
+    plan = rrn.plan_fwd(x, res, torch.empty_like(x) if fused else None, w, torch.empty_like(x))
+    assert plan.variant == variant, plan.name
+    if variant == rrn.VARIANT_ROW_CLUSTER:
+        assert plan.cluster == extra and plan.ctas % extra == 0, plan.name
+    if variant == rrn.VARIANT_STREAM:
+        assert plan.threads == extra, plan.name
+    y, ro, rstd = fwd_case(h["x"], h.get("residual"), h["w"], dtype, wl.eps)
+    compare_fwd(h["x"], h.get("residual"), h["w"], dtype, wl.eps, y, ro, rstd)
 
 
 def test_empty_matrix_writes_nothing():
