@@ -274,7 +274,8 @@ typedef enum {
                                 into a shared-memory ring of `stages` rows, 128-bit vectors */
     RRN_VARIANT_ROW_CLUSTER = 5 /* one row split across the `cluster` CTAs of a thread-block
                                    cluster; partial sums exchanged in distributed shared memory.
-                                   Forward only. */
+                                   Forward and RMSNorm backward (the backward's workspace then
+                                   needs one row per cluster). */
 } rrn_variant;
 
 /* A launch configuration. Zero fields mean "choose automatically". */
@@ -284,8 +285,8 @@ typedef struct {
     int threads; /* threads per CTA (a multiple of 32, at most 1024) */
     int ctas;    /* CTAs in the grid; each walks rows with a grid-sized stride */
     int stages;  /* RRN_VARIANT_ROW_TMA: rows in flight per CTA, 1..8 */
-    int cluster; /* forward RRN_VARIANT_ROW_CLUSTER: CTAs per cluster, 2..8 (ctas a multiple of
-                    it). Backward (ROW_CTA, ROW_TMA): 2, 4 or 8 = add the dw partial sums of
+    int cluster; /* RRN_VARIANT_ROW_CLUSTER: CTAs per cluster, 2..8 (ctas a multiple of it).
+                    Backward ROW_CTA, ROW_TMA: 2, 4 or 8 = add the dw partial sums of
                     that many stage-1 CTAs through distributed shared memory before stage 2
                     (used when there are at least twice that many CTAs; the CTA count is
                     rounded down to a multiple of it), 1 = no clusters, 0 = the planner's
@@ -334,8 +335,9 @@ RRN_API int layernorm_bwd_ex(const void *dy, const void *d_residual_out, const v
                              rrn_stream_t stream);
 
 /* rmsnorm_bwd_ex / add_rmsnorm_bwd_ex - the backward calls with an explicit stage-1 launch
- * configuration (see above). The workspace must hold cfg->ctas * N fp32 values (at most M * N;
- * rrn_plan_bwd reports the default). */
+ * configuration (see above). The workspace must hold one row of N fp32 values per stage-1 CTA,
+ * or per cluster when the CTAs work in clusters (cfg->ctas / cfg->cluster rows); rrn_plan_bwd
+ * reports the default configuration. */
 RRN_API int rmsnorm_bwd_ex(const void *dy, const void *x, const void *w, const float *rstd,
                            void *dx, float *dw, void *workspace, size_t workspace_bytes,
                            int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,

@@ -407,6 +407,10 @@ int run_fwd(const void *x, const void *res, void *res_out, const void *w, void *
 
 // ---------------------------------------------------------------- backward planning
 // add_grad: the fused backward (a third input row, the gradient at residual_out).
+// Rows of partial sums the RMSNorm backward's stage 1 writes (and its workspace must hold): one
+// per CTA, or one per cluster when the CTAs work in clusters.
+int bwd_partial_rows(const Launch &l) { return l.cluster ? l.ctas / l.cluster : l.ctas; }
+
 int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
                   const rrn_launch *cfg, Launch *out, int64_t *rows_per_cta) {
     const int V = 16 / elem_size(dtype);
@@ -422,9 +426,13 @@ int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
         // The TMA ring (rows and the next rstd requested ahead) measured faster than the
         // register variant for two and three input rows; rows whose ring slot would take more
         // than half the shared memory use the register variant.
+        // Rows too wide for that: split over a thread-block cluster up to kMaxCluster chunks of
+        // kClusterChunkVec vectors (4 a thread x 128 threads, as the ring's CTAs), else the
+        // two-pass kernel.
         const int64_t slot = (add_grad ? 3 : 2) * N * elem_size(dtype);
-        l.variant = !regs ? RRN_VARIANT_STREAM
-                          : (slot <= kMaxDynSmem / 2 ? RRN_VARIANT_ROW_TMA : RRN_VARIANT_ROW_CTA);
+        l.variant = regs ? (slot <= kMaxDynSmem / 2 ? RRN_VARIANT_ROW_TMA : RRN_VARIANT_ROW_CTA)
+                  : vec_ok && nvec <= static_cast<int64_t>(kMaxCluster) * kClusterChunkVec ? RRN_VARIANT_ROW_CLUSTER
+                                                                                           : RRN_VARIANT_STREAM;
     }
     l.vec = (l.variant == RRN_VARIANT_STREAM) ? vec_ok : true;
     l.stages = 0;
@@ -432,6 +440,42 @@ int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
     l.cluster = 0;
     int ring_occ = 0;
     switch (l.variant) {
+        case RRN_VARIANT_ROW_CLUSTER: {
+            // Each row split across l.cluster CTAs; the grid is the clusters resident at once
+            // (at most M), cluster k walking rows k, k + K, ...; the workspace gets K rows.
+            if (!vec_ok) return RRN_ERR_CONFIG;
+            if (cfg && cfg->cluster) {
+                l.cluster = cfg->cluster;
+            } else {
+                l.cluster = 2;
+                while (l.cluster < kMaxCluster && nvec > static_cast<int64_t>(l.cluster) * kClusterChunkVec) l.cluster *= 2;
+            }
+            if (l.cluster < 2 || l.cluster > kMaxCluster) return RRN_ERR_CONFIG;
+            const int64_t chunk = (nvec + l.cluster - 1) / l.cluster;
+            if (cfg && cfg->vpt) {
+                l.vpt = cfg->vpt;
+            } else {
+                l.vpt = ceil_pow2_vpt((chunk + 127) / 128, kBwdMaxVpt);
+                while (l.vpt < kBwdMaxVpt && chunk > static_cast<int64_t>(l.vpt) * bwd_max_threads(l.vpt)) l.vpt *= 2;
+            }
+            if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4) return RRN_ERR_CONFIG;
+            l.threads = cfg && cfg->threads ? cfg->threads : round_up32((chunk + l.vpt - 1) / l.vpt);
+            if (l.threads < 32 || l.threads % 32 || l.threads > bwd_max_threads(l.vpt)) return RRN_ERR_CONFIG;
+            if (static_cast<int64_t>(l.vpt) * l.threads < chunk) return RRN_ERR_CONFIG;
+            if (cfg && cfg->ctas) {
+                l.ctas = cfg->ctas;
+                if (l.ctas % l.cluster) return RRN_ERR_CONFIG;
+            } else {
+                int64_t clusters = occupancy(true, dtype, add_grad, l);
+                if (clusters < 1) clusters = 1;
+                if (clusters > M) clusters = M;
+                if (clusters > INT32_MAX / l.cluster) clusters = INT32_MAX / l.cluster;
+                l.ctas = M == 0 ? 0 : static_cast<int>(clusters) * l.cluster;
+            }
+            *rows_per_cta = M == 0 ? 0 : (M + l.ctas / l.cluster - 1) / (l.ctas / l.cluster);
+            *out = l;
+            return RRN_OK;
+        }
         case RRN_VARIANT_ROW_TMA:
         case RRN_VARIANT_ROW_CTA: {
             if (!vec_ok) return RRN_ERR_CONFIG;
@@ -530,7 +574,7 @@ int run_bwd(const void *dy, const void *d_ro, const void *x, const void *w, cons
     st = plan_bwd_impl(vec_path_ok({dy, d_ro, x, w, dx}, N, dtype), d_ro != nullptr, M, N, dtype,
                        cfg, &l, &rpc);
     if (st != RRN_OK) return st;
-    const size_t need = static_cast<size_t>(l.ctas) * static_cast<size_t>(N) * sizeof(float);
+    const size_t need = static_cast<size_t>(bwd_partial_rows(l)) * static_cast<size_t>(N) * sizeof(float);
     if (!workspace || workspace_bytes < need || !aligned(workspace, 16)) return RRN_ERR_WORKSPACE;
     unsigned int *faults = nullptr;
     st = fault_word(&faults);
@@ -824,7 +868,7 @@ RRN_API int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t 
     }
     // The caller's buffers are not known here: size for the 128-bit vector plan and the
     // element-wise plan (unaligned buffers), plain and fused, and return the largest.
-    int ctas = 0;
+    int rows = 0;
     const bool vec_possible = N % (16 / elem_size(dtype)) == 0;
     for (int vec = 0; vec < (vec_possible ? 2 : 1); ++vec)
         for (int add = 0; add < 2; ++add) {
@@ -832,9 +876,9 @@ RRN_API int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t 
             int64_t rpc = 0;
             st = plan_bwd_impl(vec != 0, add != 0, M, N, dtype, nullptr, &l, &rpc);
             if (st != RRN_OK) return st;
-            if (l.ctas > ctas) ctas = l.ctas;
+            if (bwd_partial_rows(l) > rows) rows = bwd_partial_rows(l);
         }
-    *bytes = static_cast<size_t>(ctas) * static_cast<size_t>(N) * sizeof(float);
+    *bytes = static_cast<size_t>(rows) * static_cast<size_t>(N) * sizeof(float);
     return RRN_OK;
 }
 

@@ -259,6 +259,120 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArg
     bwd_store_partial<T, VPT, CLUSTER>(a, nvec, dw, reinterpret_cast<float *>(ring_buf));
 }
 
+// Stage 1 for rows too wide for one CTA's registers, each row split across the C CTAs of a
+// thread-block cluster (C = 2..8): CTA rank q owns the vectors [q * chunk, (q + 1) * chunk) of
+// every row its cluster handles (chunk = ceil(nvec / C)), holds that slice of x, dy (, d_ro) in
+// registers and keeps the dw partial sums of its columns across rows. A row's dot product
+// sum(g * xhat) is the sum of the C CTAs' parts, exchanged through distributed shared memory as
+// the split forward exchanges its sums of squares (each CTA writes its part into slot q of every
+// peer, one cluster barrier, every CTA adds the C slots in rank order: the same bits
+// everywhere). Cluster k owns rows k, k + K, ... (K clusters) and writes its dw partial sums -
+// each CTA its column slice - to row k of the [K, N] workspace.
+template <typename T, int VPT, bool ADDG>
+__global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_split(const BwdArgs a) {
+    pdl_allow_dependents();  // stage 2 may be scheduled now; it waits for our results
+    using E = Elem<T>;
+    constexpr int V = E::kPerVec;
+    __shared__ float slots[2][32];
+    __shared__ float part[2][kMaxCluster];  // one buffer per exchange, alternating
+
+    const int nvec = a.N / V;
+    const int C = static_cast<int>(cluster_nctarank());
+    const int q = static_cast<int>(cluster_ctarank());
+    const int chunk = (nvec + C - 1) / C;
+    const int c0 = q * chunk;
+    const int c1 = min(nvec, c0 + chunk);
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const float n_f = static_cast<float>(a.N);
+    const uint4 *x4 = static_cast<const uint4 *>(a.x);
+    const uint4 *dy4 = static_cast<const uint4 *>(a.dy);
+    const uint4 *g4 = static_cast<const uint4 *>(a.d_ro);
+
+    uint4 wv[VPT];
+    float dw[VPT][V];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = c0 + v * nthr + tid;
+        if (c < c1) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
+#pragma unroll
+        for (int k = 0; k < V; ++k) dw[v][k] = 0.f;
+    }
+    int parity = 0, pbuf = 0;
+    const int64_t first = cluster_id_x();
+    const int64_t ncl = cluster_nclusters_x();
+    float rs_next = first < a.M ? __ldg(a.rstd + first) : 0.f;
+    for (int64_t row = first; row < a.M; row += ncl) {
+        const float rs = rs_next;  // requested a row ahead
+        if (row + ncl < a.M) rs_next = __ldg(a.rstd + row + ncl);
+        const int64_t base = row * nvec;
+        uint4 xv[VPT], dyv[VPT], gv[VPT];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = c0 + v * nthr + tid;
+            if (c < c1) {
+                xv[v] = ld_stream(x4 + base + c);
+                dyv[v] = ld_stream(dy4 + base + c);
+                if constexpr (ADDG) gv[v] = ld_stream(g4 + base + c);
+            }
+        }
+        float dot = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            if (c0 + v * nthr + tid < c1) {
+                float xf[V], d[V], wf[V];
+                E::unpack(xv[v], xf);
+                E::unpack(dyv[v], d);
+                E::unpack(wv[v], wf);
+#pragma unroll
+                for (int k = 0; k < V; ++k) {
+                    const float xh = xf[k] * rs;
+                    dot = fmaf(d[k] * wf[k], xh, dot);
+                    dw[v][k] = fmaf(d[k], xh, dw[v][k]);
+                }
+            }
+        }
+        dot = cta_sum(dot, slots[parity]);
+        parity ^= 1;
+        if (tid < C) st_cluster_f32(&part[pbuf][q], static_cast<uint32_t>(tid), dot);
+        cluster_sync();
+        float t = 0.f;
+        for (int i = 0; i < C; ++i) t += part[pbuf][i];
+        pbuf ^= 1;
+        const float cm = t / n_f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = c0 + v * nthr + tid;
+            if (c < c1) {
+                float xf[V], d[V], wf[V], o[V];
+                E::unpack(xv[v], xf);
+                E::unpack(dyv[v], d);
+                E::unpack(wv[v], wf);
+#pragma unroll
+                for (int k = 0; k < V; ++k) o[k] = rs * (d[k] * wf[k] - (xf[k] * rs) * cm);
+                if constexpr (ADDG) {
+                    float g[V];
+                    E::unpack(gv[v], g);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) o[k] += g[k];
+                }
+                st_stream(static_cast<uint4 *>(a.dx) + base + c, E::pack(o));
+            }
+        }
+    }
+    float *prow = a.partial + first * a.N;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = c0 + v * nthr + tid;
+        if (c < c1) {
+            float4 *dst = reinterpret_cast<float4 *>(prow + static_cast<int64_t>(c) * V);
+#pragma unroll
+            for (int k = 0; k < V / 4; ++k)
+                dst[k] = make_float4(dw[v][4 * k], dw[v][4 * k + 1], dw[v][4 * k + 2], dw[v][4 * k + 3]);
+        }
+    }
+}
+
 // Two passes over each row (any N, any alignment); the dw partials live in the CTA's own
 // workspace row instead of registers. Each workspace element is owned by one thread.
 template <typename T, bool VEC, bool ADDG>
@@ -398,6 +512,13 @@ const void *bwd_kernel_ptr(const Launch &l) {
         case RRN_VARIANT_STREAM:
             return l.vec ? reinterpret_cast<const void *>(&bwd_stream<T, true, ADDG>)
                          : reinterpret_cast<const void *>(&bwd_stream<T, false, ADDG>);
+        case RRN_VARIANT_ROW_CLUSTER:
+            switch (l.vpt) {
+                case 1: return reinterpret_cast<const void *>(&bwd_row_split<T, 1, ADDG>);
+                case 2: return reinterpret_cast<const void *>(&bwd_row_split<T, 2, ADDG>);
+                case 4: return reinterpret_cast<const void *>(&bwd_row_split<T, 4, ADDG>);
+                default: return nullptr;
+            }
         case RRN_VARIANT_ROW_TMA:
             switch (l.vpt * 2 + (l.cluster ? 1 : 0)) {
                 case 2: return reinterpret_cast<const void *>(&bwd_row_tma<T, 1, ADDG, false>);
@@ -434,7 +555,8 @@ inline cudaError_t launch_dw_reduce(const float *partial, float *out0, float *ou
     return cudaLaunchKernelEx(&cfg, bwd_dw_reduce<kReduceThreads>, partial, out0, out1, P, N);
 }
 
-// Stage 1 on l.ctas CTAs (CTA p owning rows p, p + ctas, ...), then stage 2, on one stream.
+// Stage 1 on l.ctas CTAs (in clusters of l.cluster when set), then stage 2 over the workspace
+// rows stage 1 wrote (one per CTA, or one per cluster), on one stream.
 template <typename T>
 cudaError_t launch_bwd(const BwdArgs &a, const Launch &l, cudaStream_t stream) {
     const void *k = bwd_kernel_ptr_any<T>(a.d_ro != nullptr, l);

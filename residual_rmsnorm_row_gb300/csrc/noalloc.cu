@@ -74,7 +74,11 @@ extern "C" RRN_API int rmsnorm_bwd_noalloc(const void *dy, const void *x, const 
     int st = rrn_plan_bwd(dy, nullptr, x, w, dx, M, N, dtype, &cfg);
     if (st != RRN_OK) return st;
     const int64_t fit = kScratchFloats / N;
-    if (cfg.ctas > fit) cfg.ctas = static_cast<int>(fit);
+    if (cfg.ctas > fit) {
+        cfg.ctas = static_cast<int>(fit);
+        // a row split over clusters needs whole clusters (it then writes a row per cluster)
+        if (cfg.variant == RRN_VARIANT_ROW_CLUSTER) cfg.ctas -= cfg.ctas % cfg.cluster;
+    }
     float *scratch = nullptr;
     st = scratch_address(&scratch);
     if (st != RRN_OK) return st;

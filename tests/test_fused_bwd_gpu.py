@@ -54,6 +54,7 @@ def _launches(dtype, N):
             if thr <= (256 if vpt == 4 else 512):
                 out += [rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0),
                         rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0, 0, 8),   # dw over clusters
+                        rrn.Launch(rrn.VARIANT_ROW_CLUSTER, vpt, 0, 0, 0, 2),  # rows split
                         rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 0, 0),
                         rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 0, 2, 4),
                         rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 11, 2)]

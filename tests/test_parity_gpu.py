@@ -370,10 +370,36 @@ def test_backward_shapes(dtype, N):
                              rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 13, 1),
                              rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 13, 1, 2),
                              rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 7, 3)]
+    if N % V == 0 and N // V >= 512:
+        # each row split over a cluster (CTA q owning a column slice); 3 x C CTAs: ragged rows
+        for C in (2, 4, 8):
+            if -(-(N // V) // C) <= 1024:
+                launches += [rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 0, 0, C),
+                             rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 3 * C, 0, C)]
     for launch in launches:
         dx, dw = _bwd_case(h, dtype, wl.eps, launch)
         check_out(values(dx), dx_ref, dtype, f"dx {launch}", cond)
         check_dw(dw.cpu().numpy().astype(np.float64), dw_ref, f"dw {launch}")
+
+
+# Backward of wide rows with many rows: split over a cluster (at most 512 vectors per CTA) up to
+# 4096 vectors, the two-pass kernel beyond.
+@pytest.mark.parametrize("dtype,N,variant,cluster", [
+    ("bf16", 16384, rrn.VARIANT_ROW_CLUSTER, 4), ("bf16", 24576, rrn.VARIANT_ROW_CLUSTER, 8),
+    ("bf16", 32768, rrn.VARIANT_ROW_CLUSTER, 8), ("bf16", 40000, rrn.VARIANT_STREAM, 0),
+    ("f32", 16384, rrn.VARIANT_ROW_CLUSTER, 8)])
+def test_wide_rows_backward_automatic_plan(dtype, N, variant, cluster):
+    M = 400
+    wl = synth.Workload("wide-bwd", "rmsnorm_bwd", M, N, dtype, 1e-6, 300 + N)
+    h = synth.make(wl)
+    x, w, dy = to_dev(h["x"], dtype), to_dev(h["w"], dtype), to_dev(h["dy"], dtype)
+    plan = rrn.plan_bwd(dy, x, w, torch.empty_like(x))
+    assert plan.variant == variant and plan.cluster == cluster, plan.name
+    dx_ref, dw_ref = oracle.rmsnorm_bwd(h["dy"], h["x"], h["w"], wl.eps)
+    cond = bwd_cond(h["x"], h["dy"], h["w"], wl.eps)
+    dx, dw = _bwd_case(h, dtype, wl.eps)
+    check_out(values(dx), dx_ref, dtype, "dx", cond)
+    check_dw(dw.cpu().numpy().astype(np.float64), dw_ref, "dw")
 
 
 def test_backward_is_deterministic():

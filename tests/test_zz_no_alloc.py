@@ -67,6 +67,12 @@ def test_noalloc_matches_the_regular_backward_on_calls_in_a_row():
         _agree(*_both(M, N, dtype, seed))
 
 
+def test_noalloc_wide_rows_split_over_clusters():
+    # rows of 24576 columns: each row is split over a cluster of 8 CTAs, and the array holds
+    # partial sums for 85 CTAs - lowered to 80, whole clusters
+    _agree(*_both(400, 24576, "bf16", 6))
+
+
 def test_noalloc_rejects_rows_wider_than_its_array_and_allows_empty():
     lib = rrn.load_library()
     n_too_wide = (1 << 21) + 8
