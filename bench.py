@@ -362,7 +362,7 @@ BY_SHAPE = [
     "rmsnorm_fwd_65536x2048_f32", "rmsnorm_bwd_16384x4096_bf16", "add_rmsnorm_bwd_16384x4096_bf16",
     "add_layernorm_fwd_16384x4096_bf16", "layernorm_bwd_16384x4096_bf16",
     "add_rmsnorm_fp8_16384x4096_bf16", "add_rmsnorm_fwd_16384x16384_bf16",
-    "add_rmsnorm_fwd_4096x65536_bf16",
+    "add_rmsnorm_fwd_4096x65536_bf16", "rmsnorm_bwd_8192x16384_bf16",
 ]
 L2_BYTES = 129 * 2 ** 20
 SMALL_BYTES = 8 * 2 ** 20     # below this a launch takes a few microseconds: time it in a graph
