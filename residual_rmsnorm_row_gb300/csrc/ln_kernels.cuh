@@ -47,14 +47,32 @@ __device__ __forceinline__ float2 cta_sum2(float a, float b, float (*slots)[32])
 // together (one barrier) and corrects both: corr = sum(d) / N and
 // sum((r - mean)^2) = sum(d^2) - sum(d)^2 / N (the corrected two-pass algorithm), so the
 // rounding error of m0 - which grows with |mean|, not with the spread - cancels out.
-// ln_stats (below) does the same in one step with m0 = the row's first value when that is safe.
+// ln_stats (below) does the same in one step, relative to a shift from the row's first values,
+// when that is safe.
 struct LnStats {
-    float m0;    // reference value: the first-pass mean or the row's first value
+    float m0;    // reference value: the first-pass mean or the shift of the one-step statistics
     float corr;  // mean - m0
     float rstd;
     __device__ __forceinline__ float mean() const { return m0 + corr; }
     __device__ __forceinline__ float dev(float r) const { return (r - m0) - corr; }
 };
+
+// The shift of the one-step statistics: the mean of the row's first min(N, 8) values r (formed
+// as r_of forms them), which every thread computes from the same loads - the same bits
+// everywhere - and which lies within a few sigma / sqrt(8) of the row mean in typical rows, so
+// that the one-step statistics lose next to nothing to cancellation.
+template <typename T, bool FUSED>
+__device__ __forceinline__ float ln_shift(const void *x, const void *res, int64_t base, int N) {
+    using E = Elem<T>;
+    const int n = N < 8 ? N : 8;
+    float s = 0.f;
+    for (int k = 0; k < n; ++k) {
+        float r = E::load1(x, base + k);
+        if constexpr (FUSED) r += E::load1(res, base + k);
+        s += r;
+    }
+    return s / static_cast<float>(n);
+}
 
 // The corrected two-pass statistics (the fallback of ln_stats).
 template <typename Each>
@@ -113,14 +131,15 @@ __device__ __forceinline__ LnStats ln_stats_two_pass(Each each, float n_f, float
     return st;
 }
 
-// One CTA-wide step in the common case: with K the row's first value (every thread reads it;
-// it is one of the row's own values, so it lies within the row's range), sum d = r - K and d^2
-// together; then mean = K + sum(d) / N and sum((r - mean)^2) = sum(d^2) - sum(d)^2 / N. The
-// subtraction loses precision only when K sits far from the mean compared with the spread: the
-// result is kept when sum((r - mean)^2) >= sum(d^2) / 16 (so at most four bits of cancellation)
-// and the sums are in range; otherwise - a constant row, K an outlier, overflow - the row gets
-// the corrected two-pass statistics (ln_stats_two_pass). As there, m0 (= K) and the
-// correction stay apart.
+// One CTA-wide step in the common case: with K the mean of the row's first values (ln_shift),
+// sum d = r - K and d^2 together; then mean = K + sum(d) / N and
+// sum((r - mean)^2) = sum(d^2) - sum(d)^2 / N. The subtraction loses precision only when K sits
+// far from the mean compared with the spread: the result is kept when
+// sum((r - mean)^2) >= sum(d^2) / 16 (at most four bits of cancellation - and in typical rows
+// well under one, as K is within about sigma / sqrt(8) of the mean) and the sums are in range;
+// otherwise - a constant row, outliers among the first values, overflow - the row gets the
+// corrected two-pass statistics (ln_stats_two_pass). As there, m0 (= K) and the correction stay
+// apart.
 // ln_stats_shifted takes this thread's sums d1 = sum(r - K), d2 = sum((r - K)^2), which a kernel
 // may have formed in a pass of its own (the row-per-CTA forward forms them while it stores
 // residual_out); ln_stats forms them itself.
@@ -190,9 +209,7 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) ln_fwd_row_cta(const LnFwdArgs a)
                 if (FUSED) rv[v] = ld_stream(static_cast<const uint4 *>(a.res) + base + c);
             }
         }
-        // the row's first value, formed exactly as r_of forms it (the shift of the statistics)
-        float K = E::load1(a.x, row * static_cast<int64_t>(a.N));
-        if constexpr (FUSED) K += E::load1(a.res, row * static_cast<int64_t>(a.N));
+        const float K = ln_shift<T, FUSED>(a.x, a.res, row * static_cast<int64_t>(a.N), a.N);
         float d1 = 0.f, d2 = 0.f;  // residual_out is stored in the same pass
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
@@ -285,8 +302,7 @@ __global__ void __launch_bounds__(1024) ln_fwd_stream(const LnFwdArgs a) {
                 for (int k = 0; k < V; ++k) fn(f[k]);
             }
         };
-        float K = E::load1(a.x, base);  // the row's first value: the shift of ln_stats
-        if constexpr (FUSED) K += E::load1(a.res, base);
+        const float K = ln_shift<T, FUSED>(a.x, a.res, base, a.N);
         const LnStats st = ln_stats(each, K, n_f, a.eps, slots, parity);
         for (int c = tid; c < nchunk; c += nthr) {
             float f[W], wf[W], bf[W], o[W];
@@ -536,6 +552,129 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_tma(const LnB
     ln_bwd_store_partial<T, VPT>(a, nvec, dw, db);
 }
 
+// Stage 1 for rows too wide for one CTA's dw and db registers, each row split across the C CTAs
+// of a thread-block cluster (as the RMSNorm backward's bwd_row_split): CTA rank q owns the
+// vectors [q * chunk, (q + 1) * chunk) of every row its cluster handles and keeps the dw and db
+// partial sums of those columns; the row's two sums (of g and of g * xhat) are the sums of the C
+// CTAs' parts, exchanged through distributed shared memory (each CTA writes its pair into slot q
+// of every peer, one cluster barrier, every CTA adds the C pairs in rank order). Cluster k owns
+// rows k, k + K, ... (K clusters) and writes its dw sums to row k and its db sums to row K + k
+// of the workspace.
+template <typename T, int VPT, bool ADDG>
+__global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_split(const LnBwdArgs a) {
+    pdl_allow_dependents();  // the stage-2 reduction may be scheduled now
+    using E = Elem<T>;
+    constexpr int V = E::kPerVec;
+    __shared__ float slots[2][2][32];
+    __shared__ float part[2][2][kMaxCluster];  // [exchange buffer][sum][rank]
+
+    const int nvec = a.N / V;
+    const int C = static_cast<int>(cluster_nctarank());
+    const int q = static_cast<int>(cluster_ctarank());
+    const int chunk = (nvec + C - 1) / C;
+    const int c0 = min(nvec, q * chunk);
+    const int c1 = min(nvec, c0 + chunk);
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const float n_f = static_cast<float>(a.N);
+    const uint4 *w4 = static_cast<const uint4 *>(a.w);
+
+    float dw[VPT][V], db[VPT][V];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = c0 + v * nthr + tid;
+        if (c < c1) prefetch_l1(w4 + c);
+#pragma unroll
+        for (int k = 0; k < V; ++k) dw[v][k] = db[v][k] = 0.f;
+    }
+    int parity = 0, pbuf = 0;
+    const int64_t first = cluster_id_x();
+    const int64_t ncl = cluster_nclusters_x();
+    for (int64_t row = first; row < a.M; row += ncl) {
+        const float mu = __ldg(a.mean + row);
+        const float rs = __ldg(a.rstd + row);
+        const int64_t base = row * nvec;
+        uint4 xv[VPT], dyv[VPT], gv[VPT];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = c0 + v * nthr + tid;
+            if (c < c1) {
+                xv[v] = ld_stream(static_cast<const uint4 *>(a.x) + base + c);
+                dyv[v] = ld_stream(static_cast<const uint4 *>(a.dy) + base + c);
+                if constexpr (ADDG) gv[v] = ld_stream(static_cast<const uint4 *>(a.d_ro) + base + c);
+            }
+        }
+        float sg = 0.f, sgx = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = c0 + v * nthr + tid;
+            if (c < c1) {
+                float xf[V], d[V], wf[V];
+                E::unpack(xv[v], xf);
+                E::unpack(dyv[v], d);
+                E::unpack(ld_keep(w4 + c), wf);
+#pragma unroll
+                for (int k = 0; k < V; ++k) {
+                    const float xh = (xf[k] - mu) * rs;
+                    const float g = d[k] * wf[k];
+                    sg += g;
+                    sgx = fmaf(g, xh, sgx);
+                    dw[v][k] = fmaf(d[k], xh, dw[v][k]);
+                    db[v][k] += d[k];
+                }
+            }
+        }
+        const float2 t = cta_sum2(sg, sgx, slots[parity]);
+        parity ^= 1;
+        if (tid < C) {
+            st_cluster_f32(&part[pbuf][0][q], static_cast<uint32_t>(tid), t.x);
+            st_cluster_f32(&part[pbuf][1][q], static_cast<uint32_t>(tid), t.y);
+        }
+        cluster_sync();
+        float tg = 0.f, tgx = 0.f;
+        for (int i = 0; i < C; ++i) {
+            tg += part[pbuf][0][i];
+            tgx += part[pbuf][1][i];
+        }
+        pbuf ^= 1;
+        const float mg = tg / n_f, mgx = tgx / n_f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = c0 + v * nthr + tid;
+            if (c < c1) {
+                float xf[V], d[V], wf[V], o[V];
+                E::unpack(xv[v], xf);
+                E::unpack(dyv[v], d);
+                E::unpack(ld_keep(w4 + c), wf);
+#pragma unroll
+                for (int k = 0; k < V; ++k) o[k] = rs * (d[k] * wf[k] - mg - ((xf[k] - mu) * rs) * mgx);
+                if constexpr (ADDG) {
+                    float gg[V];
+                    E::unpack(gv[v], gg);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) o[k] += gg[k];
+                }
+                st_stream(static_cast<uint4 *>(a.dx) + base + c, E::pack(o));
+            }
+        }
+    }
+    float *pw = a.partial + first * a.N;
+    float *pb = a.partial + (ncl + first) * a.N;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = c0 + v * nthr + tid;
+        if (c < c1) {
+#pragma unroll
+            for (int i = 0; i < V / 4; ++i) {
+                reinterpret_cast<float4 *>(pw + static_cast<int64_t>(c) * V)[i] =
+                    make_float4(dw[v][4 * i], dw[v][4 * i + 1], dw[v][4 * i + 2], dw[v][4 * i + 3]);
+                reinterpret_cast<float4 *>(pb + static_cast<int64_t>(c) * V)[i] =
+                    make_float4(db[v][4 * i], db[v][4 * i + 1], db[v][4 * i + 2], db[v][4 * i + 3]);
+            }
+        }
+    }
+}
+
 // Stage 1 for any N and alignment: two passes over each row; the partials accumulate in the
 // CTA's own workspace rows (each element owned by one thread).
 template <typename T, bool VEC, bool ADDG>
@@ -642,6 +781,13 @@ const void *ln_bwd_kernel_ptr(const Launch &l) {
                 case 4: return reinterpret_cast<const void *>(&ln_bwd_row_cta<T, 4, ADDG>);
                 default: return nullptr;
             }
+        case RRN_VARIANT_ROW_CLUSTER:
+            switch (l.vpt) {
+                case 1: return reinterpret_cast<const void *>(&ln_bwd_row_split<T, 1, ADDG>);
+                case 2: return reinterpret_cast<const void *>(&ln_bwd_row_split<T, 2, ADDG>);
+                case 4: return reinterpret_cast<const void *>(&ln_bwd_row_split<T, 4, ADDG>);
+                default: return nullptr;
+            }
         case RRN_VARIANT_ROW_TMA:
             switch (l.vpt) {
                 case 1: return reinterpret_cast<const void *>(&ln_bwd_row_tma<T, 1, ADDG>);
@@ -677,10 +823,29 @@ cudaError_t launch_ln_bwd(const LnBwdArgs &a, const Launch &l, cudaStream_t stre
     LnBwdArgs args = a;
     args.stages = l.stages;
     void *params[] = {&args};
-    cudaError_t e = cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params,
-                                     static_cast<size_t>(l.smem), stream);
+    cudaError_t e;
+    if (l.cluster) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(l.ctas);
+        cfg.blockDim = dim3(l.threads);
+        cfg.dynamicSmemBytes = static_cast<size_t>(l.smem);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(l.cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelExC(&cfg, k, params);
+    } else {
+        e = cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, static_cast<size_t>(l.smem),
+                             stream);
+    }
     if (e != cudaSuccess) return e;
-    return launch_dw_reduce(a.partial, a.dw, a.db, l.ctas, a.N, stream);  // dw and db together
+    // dw and db together, from the rows stage 1 wrote: one per CTA, or one per cluster
+    const int rows = l.cluster ? l.ctas / l.cluster : l.ctas;
+    return launch_dw_reduce(a.partial, a.dw, a.db, rows, a.N, stream);
 }
 
 template <typename T>
@@ -688,6 +853,7 @@ int occupancy_ln_t(bool bwd, bool flag, const Launch &l) {
     const void *k = bwd ? (flag ? ln_bwd_kernel_ptr<T, true>(l) : ln_bwd_kernel_ptr<T, false>(l))
                         : (flag ? ln_fwd_kernel_ptr<T, true>(l) : ln_fwd_kernel_ptr<T, false>(l));
     if (!k) return 0;
+    if (l.cluster > 0) return max_active_clusters(k, l);
     if (l.smem > 0 && allow_dynamic_smem(k, l.smem) != cudaSuccess) return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, l.threads, static_cast<size_t>(l.smem)) !=

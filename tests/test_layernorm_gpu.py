@@ -111,6 +111,12 @@ def test_layernorm_backward_variants(dtype, N):
                              rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 0, 0),     # ring depth planned
                              rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 7, 1),     # one row in flight
                              rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 0, 3)]
+    if N % V == 0 and N // V >= 512:
+        # each row split over a cluster (CTA q owning a column slice); 3 x C CTAs: ragged rows
+        for C in (2, 4, 8):
+            if -(-(N // V) // C) <= 1024:
+                launches += [rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 0, 0, C),
+                             rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 3 * C, 0, C)]
     cond0 = bwd_cond(h["x"], h["dy"], h["w"], wl.eps, layernorm=True)
     for with_dro in (True, False):
         ref_dx, ref_dw, ref_db = oracle.add_layernorm_bwd(h["dy"], h["d_ro"] if with_dro else None,
@@ -135,13 +141,13 @@ def test_layernorm_backward_variants(dtype, N):
 def test_layernorm_extreme_rows(dtype, N):
     rng = np.random.default_rng(93)
     base = rng.standard_normal((6, N)).astype(np.float32)
-    # The statistics are taken relative to the row's first value; a first value far from the
-    # mean compared with the spread sends the row to the two-pass path, one 3.5 sigma away
-    # stays on the one-step path with about four bits of cancellation.
+    # The statistics are taken relative to the mean of the row's first 8 values; first values
+    # far from the mean compared with the spread send the row to the two-pass path, first
+    # values 3.5 sigma away keep it on the one-step path with about four bits of cancellation.
     first_outlier = base[1].copy()
-    first_outlier[0] = 50.0
+    first_outlier[:8] = 50.0
     first_far = base[2].copy()
-    first_far[0] = 3.5
+    first_far[:8] = 3.5
     rows = np.stack([
         base[0] * 1e36 + 3e36,           # sum and squared deviations overflow fp32
         np.full(N, 3.0, np.float32),     # constant row: xhat = 0, y = b
@@ -158,3 +164,29 @@ def test_layernorm_extreme_rows(dtype, N):
     for launch in (None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0)):
         y, _, mean, rstd = ln_fwd(h, dtype, 1e-5, False, True, launch)
         compare(h, dtype, 1e-5, False, True, y, None, mean, rstd)
+
+
+@pytest.mark.parametrize("dtype,N", [("bf16", 16384), ("bf16", 32768), ("f32", 16384)])
+def test_layernorm_backward_wide_rows(dtype, N):
+    # rows too wide for one CTA's dw and db registers: the automatic plan splits each row over
+    # a thread-block cluster
+    M = 300
+    wl = synth.Workload("ln-bwd-wide", "layernorm_bwd", M, N, dtype, 1e-5, 400 + N, x_mean=0.5)
+    h = synth.make(wl)
+    x, w = to_dev(h["x"], dtype), to_dev(h["w"], dtype)
+    _, mean, rstd = rrn.layer_norm(x, w, None, wl.eps)
+    cond0 = bwd_cond(h["x"], h["dy"], h["w"], wl.eps, layernorm=True)
+    for with_dro in (True, False):
+        ref_dx, ref_dw, ref_db = oracle.add_layernorm_bwd(h["dy"], h["d_ro"] if with_dro else None,
+                                                          h["x"], h["w"], wl.eps)
+        cond = cond0 + (np.abs(oracle.decode(h["d_ro"])) if with_dro else 0.0)
+        dx = torch.full_like(x, float("nan"))
+        dw = torch.full((N,), float("nan"), device="cuda")
+        db = torch.full((N,), float("nan"), device="cuda")
+        ws = torch.empty(rrn.layernorm_bwd_workspace_bytes(M, N, x.dtype) // 4, device="cuda")
+        rrn.layernorm_bwd(to_dev(h["dy"], dtype), to_dev(h["d_ro"], dtype) if with_dro else None,
+                          x, w, mean, rstd, dx, dw, db, ws, wl.eps)
+        torch.cuda.synchronize()
+        check_out(values(dx), ref_dx, dtype, "LN dx", cond)
+        check_dw(dw.cpu().numpy().astype(np.float64), ref_dw, "LN dw")
+        check_dw(db.cpu().numpy().astype(np.float64), ref_db, "LN db")
