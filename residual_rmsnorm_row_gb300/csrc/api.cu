@@ -167,13 +167,14 @@ constexpr int kFwdTargetThreads = 128;
 constexpr int kBwdTargetThreads = 256;
 // Threads per CTA for few-row (decode) problems: one CTA per row, as wide as this.
 constexpr int kDecodeTargetThreads = 512;
-// LayerNorm backward (the dw and db sums in registers), measured on 16384 x 4096 bf16: the
-// register variant best with 256-thread CTAs; the TMA ring with 256 threads when the gradient at
-// residual_out is a third input row (115.1 us vs 129.4 at 128) and 128 without it (104.4 vs
-// 107.5 at 256).
-constexpr int kLnBwdTargetThreads = 256;
+// LayerNorm backward of rows split over a cluster: 256-thread CTAs when the gradient at
+// residual_out is a third input row, 128 without it (8192 x 16384 bf16: 353 us fused, 271 us
+// plain vs 338 at 256 threads). Rows held by one CTA: see ln_bwd_vpt.
 constexpr int kLnBwdTmaTargetThreadsFused = 256;
 constexpr int kLnBwdTmaTargetThreadsPlain = 128;
+// Narrowest CTA the LayerNorm backward feeds through the TMA ring; narrower ones hold their rows
+// in registers (65536 x 1024 bf16 fused: 106 us for 64 threads without the ring, 111 with it).
+constexpr int kLnBwdMinRingThreads = 128;
 // Widest row (in 128-bit vectors) one CTA holds in registers: 8 vectors x 256 threads.
 constexpr int kRowCtaMaxVec = 2048;
 // Vectors of a row each CTA of the cluster split takes when the planner chooses the cluster
@@ -644,6 +645,17 @@ int plan_ln_fwd(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const 
     return RRN_OK;
 }
 
+// Vectors per thread of the LayerNorm backward with whole rows in one CTA, chosen by
+// measurement over 1024-8192 bf16 columns (128 MB per input matrix): 2 when the gradient at
+// residual_out is a third input row (the dw and db sums of 16 columns and three rows' vectors
+// leave 2 CTAs of up to 512 threads per SM; 4 vectors measured 13-28 % slower), and without it
+// 2 below 512 vectors a row and 4 from there (within 2-4 % of the best layout at every width).
+int ln_bwd_vpt(int64_t nvec, bool add_grad) {
+    int vpt = add_grad || nvec < 512 ? 2 : 4;
+    while (vpt < kBwdMaxVpt && nvec > static_cast<int64_t>(vpt) * bwd_max_threads(vpt)) vpt *= 2;
+    return vpt;
+}
+
 int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, const rrn_launch *cfg,
                 Launch *out, int64_t *rows_per_cta) {
     const int64_t nvec = N / (16 / elem_size(dtype));
@@ -657,7 +669,9 @@ int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, con
         // wider rows than one CTA's dw and db registers hold: split over a cluster, as the
         // RMSNorm backward (measured 0.9 TB/s for the two-pass kernel on 8192 x 16384)
         const bool regs = vec_ok && nvec <= static_cast<int64_t>(kBwdMaxVpt) * bwd_max_threads(kBwdMaxVpt);
-        l.variant = regs ? (slot <= kMaxDynSmem / 2 ? RRN_VARIANT_ROW_TMA : RRN_VARIANT_ROW_CTA)
+        const int vpt = ln_bwd_vpt(nvec, add_grad);
+        const bool ring = slot <= kMaxDynSmem / 2 && round_up32((nvec + vpt - 1) / vpt) >= kLnBwdMinRingThreads;
+        l.variant = regs ? (ring ? RRN_VARIANT_ROW_TMA : RRN_VARIANT_ROW_CTA)
                   : vec_ok && nvec <= static_cast<int64_t>(kMaxCluster) * kClusterChunkVec ? RRN_VARIANT_ROW_CLUSTER
                                                                                            : RRN_VARIANT_STREAM;
     }
@@ -694,10 +708,11 @@ int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, con
     }
     if (l.variant == RRN_VARIANT_ROW_CTA || l.variant == RRN_VARIANT_ROW_TMA) {
         if (!vec_ok) return RRN_ERR_CONFIG;
-        const int target = l.variant != RRN_VARIANT_ROW_TMA ? kLnBwdTargetThreads
-                           : add_grad                         ? kLnBwdTmaTargetThreadsFused
-                                                              : kLnBwdTmaTargetThreadsPlain;
-        st = pick_row_layout(nvec, 1LL << 40, sms, cfg, kBwdMaxVpt, bwd_threads_limit, target, &l);
+        rrn_launch pick = cfg ? *cfg : rrn_launch{};
+        if (!pick.vpt && !pick.threads) pick.vpt = ln_bwd_vpt(nvec, add_grad);
+        // (given only the threads, the vectors per thread are fitted to them)
+        st = pick_row_layout(nvec, 1LL << 40, sms, &pick, kBwdMaxVpt, bwd_threads_limit,
+                             pick.threads ? pick.threads : bwd_max_threads(1), &l);
         if (st != RRN_OK) return st;
         if (l.variant == RRN_VARIANT_ROW_TMA) {
             const int want = cfg ? cfg->stages : 0;

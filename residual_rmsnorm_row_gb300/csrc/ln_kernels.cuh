@@ -74,6 +74,29 @@ __device__ __forceinline__ float ln_shift(const void *x, const void *res, int64_
     return s / static_cast<float>(n);
 }
 
+// ln_shift for the 128-bit vector kernels: the same values summed in the same order, read as
+// the one or two vectors that hold them (vbase = the row's first vector).
+template <typename T, bool FUSED>
+__device__ __forceinline__ float ln_shift_vec(const void *x, const void *res, int64_t vbase, int N) {
+    using E = Elem<T>;
+    constexpr int V = E::kPerVec;
+    const int n = N < 8 ? N : 8;
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < (8 + V - 1) / V; ++c) {
+        if (c * V >= n) break;
+        const uint4 xv = __ldca(static_cast<const uint4 *>(x) + vbase + c);
+        uint4 rv{};
+        if constexpr (FUSED) rv = __ldca(static_cast<const uint4 *>(res) + vbase + c);
+        float f[V];
+        r_of<T, FUSED>(xv, rv, f);
+#pragma unroll
+        for (int k = 0; k < V; ++k)
+            if (c * V + k < n) s += f[k];
+    }
+    return s / static_cast<float>(n);
+}
+
 // The corrected two-pass statistics (the fallback of ln_stats).
 template <typename Each>
 __device__ __forceinline__ LnStats ln_stats_two_pass(Each each, float n_f, float eps,
@@ -174,6 +197,67 @@ __device__ __forceinline__ LnStats ln_stats(Each each, float K, float n_f, float
     return ln_stats_shifted(each, K, d1, d2, n_f, eps, slots, parity);
 }
 
+// The forward's per-vector arithmetic, in packed fp32 pairs (PACKED) or one value at a time;
+// both give the same values, except that the pairs keep two partial sums where one value at a
+// time keeps one. Packed pairs issue half the floating-point instructions but hold more
+// registers: the row-per-CTA forward uses them from 4 vectors per thread up, where its register
+// cap leaves room (at 2 they made it spill).
+// r = x (+ residual):
+template <typename T, bool FUSED, bool PACKED>
+__device__ __forceinline__ void ln_r_of(const uint4 &xv, const uint4 &rv, float (&f)[Elem<T>::kPerVec]) {
+    using E = Elem<T>;
+    constexpr int V = E::kPerVec;
+    if constexpr (!PACKED) {
+        r_of<T, FUSED>(xv, rv, f);
+    } else {
+        E::unpack(xv, f);
+        if constexpr (FUSED) {
+            float rf[V];
+            E::unpack(rv, rf);
+#pragma unroll
+            for (int k = 0; k < V; k += 2) {
+                const float2 t = add2(pair(f[k], f[k + 1]), pair(rf[k], rf[k + 1]));
+                f[k] = t.x;
+                f[k + 1] = t.y;
+            }
+        }
+    }
+}
+
+// d1 += sum(r - K), d2 += sum((r - K)^2) over the vector (one value at a time: in d1.x, d2.x):
+template <int V, bool PACKED>
+__device__ __forceinline__ void ln_moments(const float (&f)[V], float K, float2 &d1, float2 &d2) {
+#pragma unroll
+    for (int k = 0; k < V; k += PACKED ? 2 : 1) {
+        if constexpr (PACKED) {
+            const float2 d = add2(pair(f[k], f[k + 1]), splat(-K));
+            d1 = add2(d1, d);
+            d2 = fma2(d, d, d2);
+        } else {
+            const float d = f[k] - K;
+            d1.x += d;
+            d2.x = fmaf(d, d, d2.x);
+        }
+    }
+}
+
+// y = ((r - m0) * rstd + ncr) * w + b, where ncr = -corr * rstd:
+template <int V, bool PACKED>
+__device__ __forceinline__ void ln_out(const float (&f)[V], const float (&wf)[V], const float (&bf)[V],
+                                       float m0, float rstd, float ncr, float (&o)[V]) {
+#pragma unroll
+    for (int k = 0; k < V; k += PACKED ? 2 : 1) {
+        if constexpr (PACKED) {
+            const float2 t = fma2(add2(pair(f[k], f[k + 1]), splat(-m0)), splat(rstd), splat(ncr));
+            const float2 u = fma2(t, pair(wf[k], wf[k + 1]), pair(bf[k], bf[k + 1]));
+            o[k] = u.x;
+            o[k + 1] = u.y;
+        } else {
+            o[k] = fmaf(fmaf(f[k] - m0, rstd, ncr), wf[k], bf[k]);
+        }
+    }
+}
+
 // Row per CTA (rows in registers). w and b are read where they are used, from L1 (prefetched
 // there at the start), rather than held in registers: with the register cap that keeps more
 // CTAs - more rows in flight - per SM, as in the RMSNorm forward.
@@ -181,6 +265,7 @@ template <typename T, int VPT, bool FUSED>
 __global__ void __maxnreg__(fwd_max_regs(VPT)) ln_fwd_row_cta(const LnFwdArgs a) {
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
+    constexpr bool P = VPT >= 4;  // packed fp32 pairs
     __shared__ float slots[2][2][32];
     const int nvec = a.N / V;
     const int tid = threadIdx.x;
@@ -209,21 +294,19 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) ln_fwd_row_cta(const LnFwdArgs a)
                 if (FUSED) rv[v] = ld_stream(static_cast<const uint4 *>(a.res) + base + c);
             }
         }
-        const float K = ln_shift<T, FUSED>(a.x, a.res, row * static_cast<int64_t>(a.N), a.N);
-        float d1 = 0.f, d2 = 0.f;  // residual_out is stored in the same pass
+        const float K = ln_shift_vec<T, FUSED>(a.x, a.res, base, a.N);
+        // residual_out is stored in the same pass, except the vectors that hold the values K is
+        // formed from: residual_out may be the buffer of x or residual, and other warps may not
+        // have read them yet; those are stored after the CTA-wide sums (a barrier) below
+        float2 d1 = splat(0.f), d2 = splat(0.f);  // sums of d = r - K and d^2
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * nthr + tid;
             if (c < nvec) {
                 float f[V];
-                r_of<T, FUSED>(xv[v], rv[v], f);
-                if (FUSED) st_stream(static_cast<uint4 *>(a.res_out) + base + c, E::pack(f));
-#pragma unroll
-                for (int k = 0; k < V; ++k) {
-                    const float d = f[k] - K;
-                    d1 += d;
-                    d2 = fmaf(d, d, d2);
-                }
+                ln_r_of<T, FUSED, P>(xv[v], rv[v], f);
+                if (FUSED && c * V >= 8) st_stream(static_cast<uint4 *>(a.res_out) + base + c, E::pack(f));
+                ln_moments<V, P>(f, K, d1, d2);
             }
         }
         auto each = [&](auto fn) {
@@ -236,14 +319,14 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) ln_fwd_row_cta(const LnFwdArgs a)
                     for (int k = 0; k < V; ++k) fn(f[k]);
                 }
         };
-        const LnStats st = ln_stats_shifted(each, K, d1, d2, n_f, a.eps, slots, parity);
+        const LnStats st = ln_stats_shifted(each, K, d1.x + d1.y, d2.x + d2.y, n_f, a.eps, slots, parity);
         const float ncr = -st.corr * st.rstd;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * nthr + tid;
             if (c < nvec) {
                 float f[V], wf[V], bf[V], o[V];
-                r_of<T, FUSED>(xv[v], rv[v], f);
+                ln_r_of<T, FUSED, P>(xv[v], rv[v], f);
                 E::unpack(ld_keep(w4 + c), wf);
                 if (b4) {
                     E::unpack(ld_keep(b4 + c), bf);
@@ -252,8 +335,8 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) ln_fwd_row_cta(const LnFwdArgs a)
                     for (int k = 0; k < V; ++k) bf[k] = 0.f;
                 }
                 // (r - m0 - corr) * rstd with one operation fewer: (r - m0) * rstd - corr * rstd
-#pragma unroll
-                for (int k = 0; k < V; ++k) o[k] = fmaf(fmaf(f[k] - st.m0, st.rstd, ncr), wf[k], bf[k]);
+                ln_out<V, P>(f, wf, bf, st.m0, st.rstd, ncr, o);
+                if (FUSED && c * V < 8) st_stream(static_cast<uint4 *>(a.res_out) + base + c, E::pack(f));
                 st_stream(static_cast<uint4 *>(a.y) + base + c, E::pack(o));
             }
         }
@@ -341,6 +424,46 @@ __global__ void __launch_bounds__(1024) ln_fwd_stream(const LnFwdArgs a) {
 // from L1, rather than held in registers: this kernel's registers go to the dw and db sums.
 // `after_reduce` runs right after the CTA-wide sums, when every thread has consumed its inputs;
 // when it returns false the row is abandoned.
+// One vector (V values, V even) of a row in the backward, in packed fp32 pairs: with
+// xhat = (x - mean) * rstd and g = dy * w, adds dy * xhat into dw, dy into db, and g and
+// g * xhat into the row's two running sums (kept as pairs, added up once per row).
+template <int V>
+__device__ __forceinline__ void ln_bwd_accumulate(const float (&xf)[V], const float (&d)[V],
+                                                  const float (&wf)[V], float mu, float rs,
+                                                  float (&dw)[V], float (&db)[V], float2 &sg,
+                                                  float2 &sgx) {
+#pragma unroll
+    for (int k = 0; k < V; k += 2) {
+        const float2 d2 = pair(d[k], d[k + 1]);
+        const float2 xh = mul2(add2(pair(xf[k], xf[k + 1]), splat(-mu)), splat(rs));
+        const float2 g = mul2(d2, pair(wf[k], wf[k + 1]));
+        sg = add2(sg, g);
+        sgx = fma2(g, xh, sgx);
+        const float2 w2 = fma2(d2, xh, pair(dw[k], dw[k + 1]));
+        const float2 b2 = add2(pair(db[k], db[k + 1]), d2);
+        dw[k] = w2.x;
+        dw[k + 1] = w2.y;
+        db[k] = b2.x;
+        db[k + 1] = b2.y;
+    }
+}
+
+// dx for one vector: rstd * (g - mean(g) - xhat * mean(g * xhat)), evaluated as
+// g * rstd + (xhat * cx + c) with cx = -rstd * mean(g * xhat), c = -rstd * mean(g).
+template <int V>
+__device__ __forceinline__ void ln_bwd_dx(const float (&xf)[V], const float (&d)[V],
+                                          const float (&wf)[V], float mu, float rs, float cx,
+                                          float c, float (&o)[V]) {
+#pragma unroll
+    for (int k = 0; k < V; k += 2) {
+        const float2 xh = mul2(add2(pair(xf[k], xf[k + 1]), splat(-mu)), splat(rs));
+        const float2 g = mul2(pair(d[k], d[k + 1]), pair(wf[k], wf[k + 1]));
+        const float2 r = fma2(g, splat(rs), fma2(xh, splat(cx), splat(c)));
+        o[k] = r.x;
+        o[k + 1] = r.y;
+    }
+}
+
 template <typename T, int VPT, bool ADDG, typename AfterReduce>
 __device__ __forceinline__ bool ln_bwd_row_body(const LnBwdArgs &a, int64_t row, int nvec,
                                                 const uint4 (&xv)[VPT], const uint4 (&dyv)[VPT],
@@ -355,7 +478,7 @@ __device__ __forceinline__ bool ln_bwd_row_body(const LnBwdArgs &a, int64_t row,
     const int nthr = blockDim.x;
     const float n_f = static_cast<float>(a.N);
     const uint4 *w4 = static_cast<const uint4 *>(a.w);
-    float sg = 0.f, sgx = 0.f;
+    float2 sg = splat(0.f), sgx = splat(0.f);
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int c = v * nthr + tid;
@@ -364,21 +487,13 @@ __device__ __forceinline__ bool ln_bwd_row_body(const LnBwdArgs &a, int64_t row,
             E::unpack(xv[v], xf);
             E::unpack(dyv[v], d);
             E::unpack(ld_keep(w4 + c), wf);
-#pragma unroll
-            for (int k = 0; k < V; ++k) {
-                const float xh = (xf[k] - mu) * rs;
-                const float g = d[k] * wf[k];
-                sg += g;
-                sgx = fmaf(g, xh, sgx);
-                dw[v][k] = fmaf(d[k], xh, dw[v][k]);
-                db[v][k] += d[k];
-            }
+            ln_bwd_accumulate<V>(xf, d, wf, mu, rs, dw[v], db[v], sg, sgx);
         }
     }
-    const float2 t = cta_sum2(sg, sgx, slots[parity]);
+    const float2 t = cta_sum2(sg.x + sg.y, sgx.x + sgx.y, slots[parity]);
     parity ^= 1;
     if (!after_reduce()) return false;
-    const float mg = t.x / n_f, mgx = t.y / n_f;
+    const float cx = -rs * (t.y / n_f), cc = -rs * (t.x / n_f);
     const int64_t base = row * nvec;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
@@ -388,8 +503,7 @@ __device__ __forceinline__ bool ln_bwd_row_body(const LnBwdArgs &a, int64_t row,
             E::unpack(xv[v], xf);
             E::unpack(dyv[v], d);
             E::unpack(ld_keep(w4 + c), wf);
-#pragma unroll
-            for (int k = 0; k < V; ++k) o[k] = rs * (d[k] * wf[k] - mg - ((xf[k] - mu) * rs) * mgx);
+            ln_bwd_dx<V>(xf, d, wf, mu, rs, cx, cc, o);
             if constexpr (ADDG) {
                 float gg[V];
                 E::unpack(gv[v], gg);
@@ -604,7 +718,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_split(const L
                 if constexpr (ADDG) gv[v] = ld_stream(static_cast<const uint4 *>(a.d_ro) + base + c);
             }
         }
-        float sg = 0.f, sgx = 0.f;
+        float2 sg = splat(0.f), sgx = splat(0.f);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = c0 + v * nthr + tid;
@@ -613,18 +727,10 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_split(const L
                 E::unpack(xv[v], xf);
                 E::unpack(dyv[v], d);
                 E::unpack(ld_keep(w4 + c), wf);
-#pragma unroll
-                for (int k = 0; k < V; ++k) {
-                    const float xh = (xf[k] - mu) * rs;
-                    const float g = d[k] * wf[k];
-                    sg += g;
-                    sgx = fmaf(g, xh, sgx);
-                    dw[v][k] = fmaf(d[k], xh, dw[v][k]);
-                    db[v][k] += d[k];
-                }
+                ln_bwd_accumulate<V>(xf, d, wf, mu, rs, dw[v], db[v], sg, sgx);
             }
         }
-        const float2 t = cta_sum2(sg, sgx, slots[parity]);
+        const float2 t = cta_sum2(sg.x + sg.y, sgx.x + sgx.y, slots[parity]);
         parity ^= 1;
         if (tid < C) {
             st_cluster_f32(&part[pbuf][0][q], static_cast<uint32_t>(tid), t.x);
@@ -637,7 +743,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_split(const L
             tgx += part[pbuf][1][i];
         }
         pbuf ^= 1;
-        const float mg = tg / n_f, mgx = tgx / n_f;
+        const float cx = -rs * (tgx / n_f), cc = -rs * (tg / n_f);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = c0 + v * nthr + tid;
@@ -646,8 +752,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_split(const L
                 E::unpack(xv[v], xf);
                 E::unpack(dyv[v], d);
                 E::unpack(ld_keep(w4 + c), wf);
-#pragma unroll
-                for (int k = 0; k < V; ++k) o[k] = rs * (d[k] * wf[k] - mg - ((xf[k] - mu) * rs) * mgx);
+                ln_bwd_dx<V>(xf, d, wf, mu, rs, cx, cc, o);
                 if constexpr (ADDG) {
                     float gg[V];
                     E::unpack(gv[v], gg);

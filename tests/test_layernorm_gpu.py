@@ -93,6 +93,36 @@ def test_layernorm_forward_variants(dtype, N):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("N", [4, 8, 1000, 4096, 8192])
+def test_layernorm_forward_in_place(dtype, N):
+    """residual_out written over residual, and over x; y written over x (the plain op)."""
+    M = 300
+    wl = synth.Workload("ln-alias", "add_layernorm_fwd", M, N, dtype, 1e-5, 93, x_mean=0.5)
+    h = synth.make(wl)
+    r_ref, y_ref, m_ref, rs_ref = oracle.add_layernorm_fwd(h["x"], h["residual"], h["w"], h["b"], wl.eps)
+    y2_ref = oracle.add_layernorm_fwd(h["x"], None, h["w"], h["b"], wl.eps)[1]
+    w, b = to_dev(h["w"], dtype), to_dev(h["b"], dtype)
+    r_bits = bits_of(r_ref.astype(np.float32), dtype)
+    for launch in _fwd_launches(dtype, N):
+        for target in ("residual", "x"):
+            x, res = to_dev(h["x"], dtype), to_dev(h["residual"], dtype)
+            y = torch.empty_like(x)
+            mean, rstd = torch.empty(M, device="cuda"), torch.empty(M, device="cuda")
+            ro = res if target == "residual" else x
+            rrn.layernorm_fwd(x, w, b, y, mean, rstd, wl.eps, residual=res, residual_out=ro, launch=launch)
+            torch.cuda.synchronize()
+            assert np.array_equal(to_host(ro), r_bits), f"residual_out over {target}, {launch}"
+            check_out(values(y), y_ref, dtype, f"LN y (residual_out over {target}), {launch}")
+            check_rstd(rstd.cpu().numpy().astype(np.float64), rs_ref, "LN rstd")
+            check_mean(mean.cpu().numpy().astype(np.float64), m_ref, rs_ref)
+        x = to_dev(h["x"], dtype)
+        mean, rstd = torch.empty(M, device="cuda"), torch.empty(M, device="cuda")
+        rrn.layernorm_fwd(x, w, b, x, mean, rstd, wl.eps, launch=launch)
+        torch.cuda.synchronize()
+        check_out(values(x), y2_ref, dtype, f"LN y over x, {launch}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("N", [1, 9, 1000, 1024, 4095, 4096, 7168, 8192])
 def test_layernorm_backward_variants(dtype, N):
     M = 75
