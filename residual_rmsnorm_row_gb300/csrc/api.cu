@@ -234,6 +234,43 @@ bool vec_path_ok(std::initializer_list<const void *> ptrs, int64_t N, int dtype)
     return N % (16 / elem_size(dtype)) == 0;
 }
 
+// The layout of a forward-type kernel with each row split over a cluster (fwd_row_cluster,
+// quant_row_cluster): the cluster size from cluster_chunk_vec unless given, the vectors per thread
+// as the row-per-CTA forward picks them for one CTA's chunk, and - unless given - one wave of
+// clusters: as many as the GPU holds at once (`occ` gives that number for a layout).
+template <typename Occ>
+int fwd_cluster_layout(int64_t nvec, int64_t M, bool fused, const rrn_launch *cfg, Occ occ, Launch *l) {
+    if (cfg && cfg->cluster) {
+        l->cluster = cfg->cluster;
+    } else {
+        l->cluster = 2;
+        while (l->cluster < kMaxCluster && nvec > static_cast<int64_t>(l->cluster) * cluster_chunk_vec(fused)) l->cluster *= 2;
+    }
+    if (l->cluster < 2 || l->cluster > kMaxCluster) return RRN_ERR_CONFIG;
+    const int64_t chunk = (nvec + l->cluster - 1) / l->cluster;
+    if (cfg && cfg->vpt) {
+        l->vpt = cfg->vpt;
+    } else {
+        l->vpt = ceil_pow2_vpt((chunk + kFwdTargetThreads - 1) / kFwdTargetThreads, kMaxVpt);
+        while (l->vpt < kMaxVpt && chunk > static_cast<int64_t>(l->vpt) * fwd_max_threads(l->vpt)) l->vpt *= 2;
+    }
+    l->threads = cfg && cfg->threads ? cfg->threads : round_up32((chunk + l->vpt - 1) / l->vpt);
+    if (l->vpt != 1 && l->vpt != 2 && l->vpt != 4 && l->vpt != 8) return RRN_ERR_CONFIG;
+    if (l->threads < 32 || l->threads % 32 || l->threads > fwd_max_threads(l->vpt)) return RRN_ERR_CONFIG;
+    if (static_cast<int64_t>(l->vpt) * l->threads < chunk) return RRN_ERR_CONFIG;
+    if (cfg && cfg->ctas) {
+        l->ctas = cfg->ctas;
+        if (l->ctas % l->cluster) return RRN_ERR_CONFIG;
+    } else {
+        int64_t clusters = occ(*l);
+        if (clusters < 1) clusters = 1;
+        if (clusters > M) clusters = M;
+        if (clusters > INT32_MAX / l->cluster) clusters = INT32_MAX / l->cluster;
+        l->ctas = static_cast<int>(clusters) * l->cluster;
+    }
+    return RRN_OK;
+}
+
 int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const rrn_launch *cfg,
                   Launch *out) {
     const int V = 16 / elem_size(dtype);
@@ -296,35 +333,9 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
         }
         case RRN_VARIANT_ROW_CLUSTER: {
             if (!vec_ok) return RRN_ERR_CONFIG;
-            if (cfg && cfg->cluster) {
-                l.cluster = cfg->cluster;
-            } else {
-                l.cluster = 2;
-                while (l.cluster < kMaxCluster && nvec > static_cast<int64_t>(l.cluster) * cluster_chunk_vec(fused)) l.cluster *= 2;
-            }
-            if (l.cluster < 2 || l.cluster > kMaxCluster) return RRN_ERR_CONFIG;
-            const int64_t chunk = (nvec + l.cluster - 1) / l.cluster;
-            if (cfg && cfg->vpt) {
-                l.vpt = cfg->vpt;
-            } else {
-                l.vpt = ceil_pow2_vpt((chunk + kFwdTargetThreads - 1) / kFwdTargetThreads, kMaxVpt);
-                while (l.vpt < kMaxVpt && chunk > static_cast<int64_t>(l.vpt) * fwd_max_threads(l.vpt)) l.vpt *= 2;
-            }
-            l.threads = cfg && cfg->threads ? cfg->threads : round_up32((chunk + l.vpt - 1) / l.vpt);
-            if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4 && l.vpt != 8) return RRN_ERR_CONFIG;
-            if (l.threads < 32 || l.threads % 32 || l.threads > fwd_max_threads(l.vpt)) return RRN_ERR_CONFIG;
-            if (static_cast<int64_t>(l.vpt) * l.threads < chunk) return RRN_ERR_CONFIG;
-            if (cfg && cfg->ctas) {
-                l.ctas = cfg->ctas;
-                if (l.ctas % l.cluster) return RRN_ERR_CONFIG;
-            } else {
-                // one wave of clusters: as many as the GPU holds at once
-                int64_t clusters = occupancy(false, dtype, fused, l);
-                if (clusters < 1) clusters = 1;
-                if (clusters > M) clusters = M;
-                if (clusters > INT32_MAX / l.cluster) clusters = INT32_MAX / l.cluster;
-                l.ctas = static_cast<int>(clusters) * l.cluster;
-            }
+            st = fwd_cluster_layout(nvec, M, fused, cfg, [&](const Launch &t) { return occupancy(false, dtype, fused, t); },
+                                    &l);
+            if (st != RRN_OK) return st;
             break;
         }
         case RRN_VARIANT_ROW_TMA: {
@@ -801,23 +812,41 @@ int run_quant(const void *x, const void *res, void *res_out, const void *w, void
     const bool fused = res != nullptr;
     Launch l{};
     l.variant = cfg && cfg->variant ? cfg->variant : RRN_VARIANT_AUTO;
-    if (l.variant == RRN_VARIANT_AUTO)
-        l.variant = vec_ok && nvec <= kRowCtaMaxVec ? RRN_VARIANT_ROW_CTA : RRN_VARIANT_STREAM;
-    l.vec = l.variant == RRN_VARIANT_ROW_CTA;
+    if (l.variant == RRN_VARIANT_AUTO) {
+        // as the forward: one row per CTA while the CTA holds it, wider rows split over a
+        // cluster, wider still the two-pass kernel
+        const int64_t cta_max = M < 2LL * sms || !fused ? kRowCtaMaxVec : 128 * kMaxVpt;
+        l.variant = !vec_ok          ? RRN_VARIANT_STREAM
+                    : nvec <= cta_max ? RRN_VARIANT_ROW_CTA
+                    : nvec <= static_cast<int64_t>(kMaxCluster) * cluster_chunk_vec(fused) ? RRN_VARIANT_ROW_CLUSTER
+                                                                                            : RRN_VARIANT_STREAM;
+    }
+    l.vec = l.variant == RRN_VARIANT_STREAM ? vec_ok : true;
+    auto occ = [&](const Launch &t) {
+        return dtype == RRN_BF16 ? occupancy_quant_bf16(fused, t) : occupancy_quant_f32(fused, t);
+    };
     if (l.variant == RRN_VARIANT_ROW_CTA) {
         if (!vec_ok) return RRN_ERR_CONFIG;
         st = pick_row_layout(nvec, M, sms, cfg, kMaxVpt, fwd_threads_limit, kFwdTargetThreads, &l);
         if (st != RRN_OK) return st;
         l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid(M);
+    } else if (l.variant == RRN_VARIANT_ROW_CLUSTER) {
+        if (!vec_ok) return RRN_ERR_CONFIG;
+        st = fwd_cluster_layout(nvec, M, fused, cfg, occ, &l);
+        if (st != RRN_OK) return st;
     } else if (l.variant == RRN_VARIANT_STREAM) {
         l.vpt = 1;
-        l.threads = cfg && cfg->threads ? cfg->threads : (N >= 512 ? 512 : round_up32(N));
+        const int64_t chunks = l.vec ? nvec : N;
+        // as the forward's two-pass kernel: 1024 threads from 8192 chunks a row (4096 x 65536
+        // bf16 with a residual: 395 us vs 446 at 512)
+        l.threads = cfg && cfg->threads ? cfg->threads
+                                        : (chunks >= 8192 ? 1024 : chunks >= 512 ? 512 : round_up32(chunks));
         if (l.threads < 32 || l.threads % 32 || l.threads > 1024) return RRN_ERR_CONFIG;
         if (cfg && cfg->ctas) {
             l.ctas = cfg->ctas;
         } else {
-            const int occ = dtype == RRN_BF16 ? occupancy_quant_bf16(fused, l) : occupancy_quant_f32(fused, l);
-            const int64_t cap = static_cast<int64_t>(sms) * (occ > 0 ? occ : 1);
+            const int n = occ(l);
+            const int64_t cap = static_cast<int64_t>(sms) * (n > 0 ? n : 1);
             l.ctas = clamp_grid(M < cap ? M : cap);
         }
     } else {

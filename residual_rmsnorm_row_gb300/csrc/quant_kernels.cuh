@@ -12,6 +12,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tma.cuh"
 
 namespace rrn {
 
@@ -56,6 +57,22 @@ __device__ __forceinline__ float2 cta_sum_max(float s, float m, float (*slots)[3
         t.y = fmaxf(t.y, slots[1][i]);
     }
     return t;
+}
+
+// The V codes of one vector, q = e4m3(r * rstd * w * inv), written as one 8- or 4-byte store.
+template <int V>
+__device__ __forceinline__ void store_codes(uint8_t *dst, const float (&f)[V], const float (&wf)[V],
+                                            float rs, float inv) {
+    uint16_t h[V / 2];
+#pragma unroll
+    for (int k = 0; k < V / 2; ++k)
+        h[k] = e4m3x2(f[2 * k] * rs * wf[2 * k] * inv, f[2 * k + 1] * rs * wf[2 * k + 1] * inv);
+    if constexpr (V == 8) {
+        *reinterpret_cast<uint2 *>(dst) =
+            make_uint2(h[0] | (static_cast<uint32_t>(h[1]) << 16), h[2] | (static_cast<uint32_t>(h[3]) << 16));
+    } else {
+        *reinterpret_cast<uint32_t *>(dst) = h[0] | (static_cast<uint32_t>(h[1]) << 16);
+    }
 }
 
 // Row per CTA (rows in registers; w read through L1, prefetched at the start, under the
@@ -148,18 +165,7 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) quant_row_cta(const QuantArgs a) 
                 float f[V], wf[V];
                 r_of<T, FUSED>(xv[v], rv[v], f);
                 E::unpack(ld_keep(w4 + c), wf);
-                uint16_t h[V / 2];
-#pragma unroll
-                for (int k = 0; k < V / 2; ++k)
-                    h[k] = e4m3x2(f[2 * k] * rs * wf[2 * k] * inv, f[2 * k + 1] * rs * wf[2 * k + 1] * inv);
-                uint8_t *dst = static_cast<uint8_t *>(a.q) + (base + c) * V;
-                if constexpr (V == 8) {
-                    *reinterpret_cast<uint2 *>(dst) =
-                        make_uint2(h[0] | (static_cast<uint32_t>(h[1]) << 16),
-                                   h[2] | (static_cast<uint32_t>(h[3]) << 16));
-                } else {
-                    *reinterpret_cast<uint32_t *>(dst) = h[0] | (static_cast<uint32_t>(h[1]) << 16);
-                }
+                store_codes<V>(static_cast<uint8_t *>(a.q) + (base + c) * V, f, wf, rs, inv);
             }
         }
         if (tid == 0) {
@@ -169,44 +175,237 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) quant_row_cta(const QuantArgs a) 
     }
 }
 
-// Any N and alignment: passes over global memory (sum of squares, amax, codes), one element at
-// a time. For odd widths and unaligned buffers; not a fast path.
-template <typename T, bool FUSED>
-__global__ void __launch_bounds__(1024) quant_stream(const QuantArgs a) {
+// Rows too wide for one CTA's registers, split over the C CTAs of a thread-block cluster as the
+// plain forward's fwd_row_cluster splits them: CTA rank q holds the vectors
+// [q * chunk, (q + 1) * chunk) of every row its cluster handles, w in registers. Each CTA's
+// sum(r^2) and max|r * w| are exchanged through distributed shared memory (each CTA writes its
+// pair into slot q of every peer, one cluster barrier, every CTA combines the C pairs in rank
+// order: the same bits everywhere); the rare paths (rescaled rstd, the amax of y itself when some
+// |r * w| overflows) exchange one more value each, as the row-per-CTA kernel reduces one more.
+template <typename T, int VPT, bool FUSED>
+__global__ void __launch_bounds__(fwd_max_threads(VPT)) quant_row_cluster(const QuantArgs a) {
     using E = Elem<T>;
-    __shared__ float slots[2][32];
+    constexpr int V = E::kPerVec;
+    __shared__ float slots[2][2][32];
+    __shared__ float part[2][2][kMaxCluster];  // [exchange buffer][value][rank]
+
+    const int nvec = a.N / V;
+    const int C = static_cast<int>(cluster_nctarank());
+    const int q = static_cast<int>(cluster_ctarank());
+    const int chunk = (nvec + C - 1) / C;
+    const int c0 = min(nvec, q * chunk);
+    const int c1 = min(nvec, c0 + chunk);
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
     const float n_f = static_cast<float>(a.N);
-    int parity = 0;
+
+    uint4 wv[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = c0 + v * nthr + tid;
+        if (c < c1) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
+    }
+    int parity = 0, pbuf = 0;
+    // cluster-wide (sum of the first values, max of the second values)
+    auto exchange = [&](float s, float m) {
+        if (tid < C) {
+            st_cluster_f32(&part[pbuf][0][q], static_cast<uint32_t>(tid), s);
+            st_cluster_f32(&part[pbuf][1][q], static_cast<uint32_t>(tid), m);
+        }
+        cluster_sync();
+        float2 t = make_float2(0.f, 0.f);
+        for (int i = 0; i < C; ++i) {
+            t.x += part[pbuf][0][i];
+            t.y = fmaxf(t.y, part[pbuf][1][i]);
+        }
+        pbuf ^= 1;
+        return t;
+    };
+
+    const int64_t ncl = cluster_nclusters_x();
+    for (int64_t row = cluster_id_x(); row < a.M; row += ncl) {
+        const int64_t base = row * nvec;
+        uint4 xv[VPT], rv[VPT];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = c0 + v * nthr + tid;
+            if (c < c1) {
+                xv[v] = ld_stream(static_cast<const uint4 *>(a.x) + base + c);
+                if (FUSED) rv[v] = ld_stream(static_cast<const uint4 *>(a.res) + base + c);
+            }
+        }
+        float ss = 0.f, mw = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = c0 + v * nthr + tid;
+            if (c < c1) {
+                float f[V], wf[V];
+                r_of<T, FUSED>(xv[v], rv[v], f);
+                if (FUSED) st_stream(static_cast<uint4 *>(a.res_out) + base + c, E::pack(f));
+                E::unpack(wv[v], wf);
+#pragma unroll
+                for (int k = 0; k < V; ++k) {
+                    ss = fmaf(f[k], f[k], ss);
+                    mw = fmaxf(mw, fabsf(f[k] * wf[k]));
+                }
+            }
+        }
+        float2 t = cta_sum_max(ss, mw, slots[parity]);
+        parity ^= 1;
+        t = exchange(t.x, t.y);
+        float rs;
+        if (!needs_rescale(t.x)) {
+            rs = rstd_plain(t.x, n_f, a.eps);
+        } else {  // rare: sum of squares out of fp32 range, or an all-zero row
+            float am = 0.f;
+#pragma unroll
+            for (int v = 0; v < VPT; ++v)
+                if (c0 + v * nthr + tid < c1) {
+                    float f[V];
+                    r_of<T, FUSED>(xv[v], rv[v], f);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) am = fmaxf(am, fabsf(f[k]));
+                }
+            am = cta_max(am, slots[parity][0]);
+            parity ^= 1;
+            const int e = rescale_exponent(exchange(0.f, am).y);
+            float s2 = 0.f;
+#pragma unroll
+            for (int v = 0; v < VPT; ++v)
+                if (c0 + v * nthr + tid < c1) {
+                    float f[V];
+                    r_of<T, FUSED>(xv[v], rv[v], f);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) {
+                        const float u = ldexpf(f[k], -e);
+                        s2 = fmaf(u, u, s2);
+                    }
+                }
+            s2 = cta_sum(s2, slots[parity][0]);
+            parity ^= 1;
+            rs = rstd_rescaled(exchange(s2, 0.f).x, n_f, a.eps, e);
+        }
+        float am = rs * t.y;
+        if (!isfinite(t.y)) {  // rare: some |r * w| beyond fp32 while y is not (see quant_row_cta)
+            float m = 0.f;
+#pragma unroll
+            for (int v = 0; v < VPT; ++v)
+                if (c0 + v * nthr + tid < c1) {
+                    float f[V], wf[V];
+                    r_of<T, FUSED>(xv[v], rv[v], f);
+                    E::unpack(wv[v], wf);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) m = fmaxf(m, fabsf(f[k] * rs * wf[k]));
+                }
+            m = cta_max(m, slots[parity][0]);
+            parity ^= 1;
+            am = exchange(0.f, m).y;
+        }
+        const float inv = am > 0.f ? 448.f / am : 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = c0 + v * nthr + tid;
+            if (c < c1) {
+                float f[V], wf[V];
+                r_of<T, FUSED>(xv[v], rv[v], f);
+                E::unpack(wv[v], wf);
+                store_codes<V>(static_cast<uint8_t *>(a.q) + (base + c) * V, f, wf, rs, inv);
+            }
+        }
+        if (q == 0 && tid == 0) {
+            a.scale[row] = am / 448.f;
+            if (a.rstd) a.rstd[row] = rs;
+        }
+    }
+    cluster_sync();  // no CTA exits while a peer may still write into its shared memory
+}
+
+// Any N and alignment: passes over global memory (sum of squares with max|r * w|, then the
+// codes; the rare paths one more each), the row re-read from L2. VEC: 128-bit vectors (rows
+// too wide for the cluster split); otherwise one element at a time (odd widths, unaligned
+// buffers).
+template <typename T, bool VEC, bool FUSED>
+__global__ void __launch_bounds__(1024) quant_stream(const QuantArgs a) {
+    using E = Elem<T>;
+    constexpr int W = E::kPerVec;
+    constexpr int V = VEC ? W : 1;  // values per chunk
+    __shared__ float slots[2][2][32];
+    __shared__ float rescue_slots[2][32];
+    const int nchunk = a.N / V;
+    const int tid = threadIdx.x;
+    const int nthr = blockDim.x;
+    const float n_f = static_cast<float>(a.N);
+
+    auto load_r = [&](int64_t base, int c, float (&f)[W]) {
+        if constexpr (VEC) {
+            const int64_t vi = base / W + c;
+            E::unpack(__ldcg(static_cast<const uint4 *>(a.x) + vi), f);
+            if constexpr (FUSED) {
+                float b[W];
+                E::unpack(__ldcg(static_cast<const uint4 *>(a.res) + vi), b);
+#pragma unroll
+                for (int k = 0; k < W; ++k) f[k] += b[k];
+            }
+        } else {
+            f[0] = E::load1(a.x, base + c);
+            if constexpr (FUSED) f[0] += E::load1(a.res, base + c);
+        }
+    };
+    auto load_w = [&](int c, float (&wf)[W]) {
+        if constexpr (VEC) E::unpack(ld_keep(static_cast<const uint4 *>(a.w) + c), wf);
+        else wf[0] = E::load1(a.w, c);
+    };
+    int parity = 0, rescue_parity = 0;
     for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x) {
         const int64_t base = row * static_cast<int64_t>(a.N);
-        auto r_at = [&](int j) {
-            float f = E::load1(a.x, base + j);
-            if constexpr (FUSED) f += E::load1(a.res, base + j);
-            return f;
-        };
         auto each = [&](auto fn) {
-            for (int j = tid; j < a.N; j += nthr) fn(r_at(j));
+            for (int c = tid; c < nchunk; c += nthr) {
+                float f[W];
+                load_r(base, c, f);
+#pragma unroll
+                for (int k = 0; k < V; ++k) fn(f[k]);
+            }
         };
-        float ss = 0.f;
-        for (int j = tid; j < a.N; j += nthr) {
-            const float f = r_at(j);
-            ss = fmaf(f, f, ss);
+        float ss = 0.f, mw = 0.f;
+        for (int c = tid; c < nchunk; c += nthr) {
+            float f[W], wf[W];
+            load_r(base, c, f);
+            load_w(c, wf);
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                ss = fmaf(f[k], f[k], ss);
+                mw = fmaxf(mw, fabsf(f[k] * wf[k]));
+            }
         }
-        ss = cta_sum(ss, slots[parity]);
+        const float2 t = cta_sum_max(ss, mw, slots[parity]);
         parity ^= 1;
-        const float rs = rms_rstd(each, ss, n_f, a.eps, slots, parity);
-        float am = 0.f;
-        for (int j = tid; j < a.N; j += nthr) am = fmaxf(am, fabsf(r_at(j) * rs * E::load1(a.w, j)));
-        am = cta_max(am, slots[parity]);
-        parity ^= 1;
+        const float rs = rms_rstd(each, t.x, n_f, a.eps, rescue_slots, rescue_parity);
+        float am = rs * t.y;
+        if (!isfinite(t.y)) {  // rare: as in quant_row_cta
+            float m = 0.f;
+            for (int c = tid; c < nchunk; c += nthr) {
+                float f[W], wf[W];
+                load_r(base, c, f);
+                load_w(c, wf);
+#pragma unroll
+                for (int k = 0; k < V; ++k) m = fmaxf(m, fabsf(f[k] * rs * wf[k]));
+            }
+            am = cta_max(m, rescue_slots[rescue_parity]);
+            rescue_parity ^= 1;
+        }
         const float inv = am > 0.f ? 448.f / am : 0.f;
-        for (int j = tid; j < a.N; j += nthr) {
-            const float f = r_at(j);
-            if constexpr (FUSED) E::store1(a.res_out, base + j, f);
-            const float y = f * rs * E::load1(a.w, j);
-            static_cast<uint8_t *>(a.q)[base + j] = static_cast<uint8_t>(e4m3x2(y * inv, 0.f) & 0xff);
+        for (int c = tid; c < nchunk; c += nthr) {
+            float f[W], wf[W];
+            load_r(base, c, f);
+            load_w(c, wf);
+            if constexpr (VEC) {
+                if constexpr (FUSED) st_stream(static_cast<uint4 *>(a.res_out) + base / W + c, E::pack(f));
+                store_codes<W>(static_cast<uint8_t *>(a.q) + base + static_cast<int64_t>(c) * W, f, wf, rs, inv);
+            } else {
+                if constexpr (FUSED) E::store1(a.res_out, base + c, f[0]);
+                static_cast<uint8_t *>(a.q)[base + c] =
+                    static_cast<uint8_t>(e4m3x2(f[0] * rs * wf[0] * inv, 0.f) & 0xff);
+            }
         }
         if (tid == 0) {
             a.scale[row] = am / 448.f;
@@ -226,8 +425,17 @@ const void *quant_kernel_ptr(const Launch &l) {
                 case 8: return reinterpret_cast<const void *>(&quant_row_cta<T, 8, FUSED>);
                 default: return nullptr;
             }
+        case RRN_VARIANT_ROW_CLUSTER:
+            switch (l.vpt) {
+                case 1: return reinterpret_cast<const void *>(&quant_row_cluster<T, 1, FUSED>);
+                case 2: return reinterpret_cast<const void *>(&quant_row_cluster<T, 2, FUSED>);
+                case 4: return reinterpret_cast<const void *>(&quant_row_cluster<T, 4, FUSED>);
+                case 8: return reinterpret_cast<const void *>(&quant_row_cluster<T, 8, FUSED>);
+                default: return nullptr;
+            }
         case RRN_VARIANT_STREAM:
-            return reinterpret_cast<const void *>(&quant_stream<T, FUSED>);
+            return l.vec ? reinterpret_cast<const void *>(&quant_stream<T, true, FUSED>)
+                         : reinterpret_cast<const void *>(&quant_stream<T, false, FUSED>);
         default: return nullptr;
     }
 }
@@ -238,6 +446,20 @@ cudaError_t launch_quant(const QuantArgs &a, const Launch &l, cudaStream_t strea
     if (!k) return cudaErrorInvalidConfiguration;
     QuantArgs args = a;
     void *params[] = {&args};
+    if (l.variant == RRN_VARIANT_ROW_CLUSTER) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(l.ctas);
+        cfg.blockDim = dim3(l.threads);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(l.cluster);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelExC(&cfg, k, params);
+    }
     return cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, 0, stream);
 }
 
@@ -245,6 +467,7 @@ template <typename T>
 int occupancy_quant_t(bool fused, const Launch &l) {
     const void *k = fused ? quant_kernel_ptr<T, true>(l) : quant_kernel_ptr<T, false>(l);
     if (!k) return 0;
+    if (l.cluster > 0) return max_active_clusters(k, l);
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, l.threads, 0) != cudaSuccess) {
         (void)cudaGetLastError();

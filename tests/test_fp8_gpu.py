@@ -104,6 +104,13 @@ def test_fp8_variants(dtype, N):
                 if thr <= (256 if vpt == 8 else 512 if vpt == 4 else 1024):
                     launches += [rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0),
                                  rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 7)]
+            # rows split over clusters (a CTA's slice may be empty; at most 8 x 256 vectors a CTA)
+            if 2 <= nvec <= 2 * 2048:
+                launches += [rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 0, 0, 2)]
+                if -(-nvec // 2) <= 1024:
+                    launches += [rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 1, 0, 6, 0, 2)]
+            if 8 <= nvec <= 8 * 2048:
+                launches += [rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 0, 0, 8)]
         for launch in launches:
             q, scale, rstd, ro = run(h, dtype, wl.eps, fused, launch)
             compare(h, dtype, wl.eps, fused, q, scale, rstd, ro, str(launch))
@@ -115,7 +122,7 @@ def test_fp8_zero_and_extreme_rows():
     rows = np.stack([np.zeros(N, np.float32), rng.standard_normal(N).astype(np.float32) * 1e30,
                      np.full(N, 2.0, np.float32), rng.standard_normal(N).astype(np.float32)])
     h = {"x": bits_of(rows, "bf16"), "w": bits_of(np.ones(N, np.float32), "bf16")}
-    for launch in (None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0)):
+    for launch in (None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0), rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 0, 0, 4)):
         q, scale, rstd, _ = run(h, "bf16", 1e-6, False, launch)
         compare(h, "bf16", 1e-6, False, q, scale, rstd, None, str(launch))
         assert float(scale[0]) == 0.0 and int(q[0].max()) == 0
@@ -128,6 +135,21 @@ def test_fp8_row_whose_r_times_w_overflows():
     z = np.clip(rng.standard_normal(N), -3.0, 3.0).astype(np.float32)  # |r| <= 3e38 stays finite
     rows = np.stack([z * np.float32(1e38), rng.standard_normal(N).astype(np.float32)])
     h = {"x": bits_of(rows, "bf16"), "w": bits_of(np.full(N, 8.0, np.float32), "bf16")}
-    for launch in (None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0)):
+    for launch in (None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0), rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 0, 0, 4)):
         q, scale, rstd, _ = run(h, "bf16", 1e-6, False, launch)
         compare(h, "bf16", 1e-6, False, q, scale, rstd, None, str(launch))
+
+
+@pytest.mark.parametrize("dtype,N", [("bf16", 16384), ("bf16", 32768), ("bf16", 65536), ("f32", 16384)])
+def test_fp8_wide_rows(dtype, N):
+    """Rows wider than one CTA holds: split over clusters (automatic up to 8 CTAs of 512 vectors
+    with a residual, 1024 without), the 128-bit two-pass kernel beyond."""
+    M = 40
+    for fused in (False, True):
+        wl = synth.Workload("fp8-wide", "add_rmsnorm_fwd" if fused else "rmsnorm_fwd", M, N, dtype,
+                            1e-6, 104, res_sigma=2.0)
+        h = synth.make(wl)
+        for launch in (None, rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 0, 0, 8),
+                       rrn.Launch(rrn.VARIANT_STREAM, 0, 1024, 0)):
+            q, scale, rstd, ro = run(h, dtype, wl.eps, fused, launch)
+            compare(h, dtype, wl.eps, fused, q, scale, rstd, ro, f"{N} {launch}")
