@@ -362,7 +362,8 @@ BY_SHAPE = [
     "rmsnorm_fwd_65536x2048_f32", "rmsnorm_bwd_16384x4096_bf16", "add_rmsnorm_bwd_16384x4096_bf16",
     "add_layernorm_fwd_16384x4096_bf16", "layernorm_bwd_16384x4096_bf16",
     "add_rmsnorm_fp8_16384x4096_bf16", "add_rmsnorm_fwd_16384x16384_bf16",
-    "add_rmsnorm_fwd_4096x65536_bf16", "rmsnorm_bwd_8192x16384_bf16",
+    "add_rmsnorm_fwd_4096x65536_bf16", "rmsnorm_bwd_8192x16384_bf16", "add_rmsnorm_bwd_8192x16384_bf16",
+    "layernorm_bwd_8192x16384_bf16", "add_rmsnorm_fp8_16384x16384_bf16",
 ]
 L2_BYTES = 129 * 2 ** 20
 SMALL_BYTES = 8 * 2 ** 20     # below this a launch takes a few microseconds: time it in a graph
@@ -466,9 +467,9 @@ def measure_shape(name: str, dev, reps: int):
     peak, _ = hbm_peak()
     gbs = nbytes / (us * 1e-6) / 1e9
     if "layernorm" in wl.op:
-        plan = "layernorm planner (row_cta or stream)"
+        plan = "layernorm planner"
     elif wl.op == "add_rmsnorm_fp8":
-        plan = "fp8 planner (row_cta or stream)"
+        plan = "fp8 planner"
     elif wl.op in ("rmsnorm_bwd", "add_rmsnorm_bwd"):
         plan = rrn.plan_bwd(sets[0]["dy"], sets[0]["x"], w, outs[0]["y"], sets[0].get("d_ro")).name
     else:

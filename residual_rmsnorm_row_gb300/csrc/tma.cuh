@@ -202,4 +202,10 @@ __device__ __forceinline__ float ld_cluster_f32(const float *local, uint32_t ran
     return v;
 }
 
+// A hint to bring [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple of 16): no
+// completion to wait for, no effect on any value.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 }  // namespace rrn

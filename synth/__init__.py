@@ -88,6 +88,11 @@ _add(Workload("add_rmsnorm_fwd_16384x16384_bf16", "add_rmsnorm_fwd", 16384, 1638
 _add(Workload("add_rmsnorm_fwd_4096x65536_bf16", "add_rmsnorm_fwd", 4096, 65536, BF16, 1e-6, 9))
 # The backward of rows too wide for one CTA's registers (each row split over a cluster).
 _add(Workload("rmsnorm_bwd_8192x16384_bf16", "rmsnorm_bwd", 8192, 16384, BF16, 1e-6, 10))
+_add(Workload("add_rmsnorm_bwd_8192x16384_bf16", "add_rmsnorm_bwd", 8192, 16384, BF16, 1e-6, 11))
+_add(Workload("layernorm_bwd_8192x16384_bf16", "layernorm_bwd", 8192, 16384, BF16, 1e-5, 12,
+              x_mean=0.5))
+# The fp8 output of wide rows (split over a cluster).
+_add(Workload("add_rmsnorm_fp8_16384x16384_bf16", "add_rmsnorm_fp8", 16384, 16384, BF16, 1e-6, 13))
 
 
 def get(name: str) -> Workload:
