@@ -229,7 +229,8 @@ RRN_API int layernorm_bwd(const void *dy, const void *d_residual_out, const void
  *   q      [M, N] bytes (e4m3 codes, 0x7F/0xFF never produced), written.
  *   scale  [M] fp32, written.
  * Returns an rrn_status. rmsnorm_fwd_fp8_ex (declared with the launch-control calls below)
- * takes an explicit launch configuration (RRN_VARIANT_ROW_CTA or RRN_VARIANT_STREAM).
+ * takes an explicit launch configuration (RRN_VARIANT_ROW_CTA, RRN_VARIANT_ROW_CLUSTER or
+ * RRN_VARIANT_STREAM).
  */
 RRN_API int rmsnorm_fwd_fp8(const void *x, const void *residual, void *residual_out,
                             const void *w, void *q, float *scale, float *rstd, int64_t M,
@@ -274,8 +275,9 @@ typedef enum {
                                 into a shared-memory ring of `stages` rows, 128-bit vectors */
     RRN_VARIANT_ROW_CLUSTER = 5 /* one row split across the `cluster` CTAs of a thread-block
                                    cluster; partial sums exchanged in distributed shared memory.
-                                   Forward and RMSNorm backward (the backward's workspace then
-                                   needs one row per cluster). */
+                                   RMSNorm forward and backward, the fp8 forward and the
+                                   LayerNorm backward (a backward's workspace then needs one
+                                   row per cluster, two for LayerNorm). */
 } rrn_variant;
 
 /* A launch configuration. Zero fields mean "choose automatically". */
@@ -317,13 +319,16 @@ RRN_API int add_rmsnorm_fwd_ex(const void *x, const void *residual, void *residu
                                const void *w, void *y, float *rstd, int64_t M, int64_t N,
                                float eps, int dtype, const rrn_launch *cfg, rrn_stream_t stream);
 
-/* rmsnorm_fwd_fp8 with an explicit launch configuration (row-per-CTA or two-pass). */
+/* rmsnorm_fwd_fp8 with an explicit launch configuration (row-per-CTA, cluster split or
+ * two-pass). */
 RRN_API int rmsnorm_fwd_fp8_ex(const void *x, const void *residual, void *residual_out,
                                const void *w, void *q, float *scale, float *rstd, int64_t M,
                                int64_t N, float eps, int dtype, const rrn_launch *cfg,
                                rrn_stream_t stream);
 
-/* LayerNorm with an explicit launch configuration (row-per-CTA or two-pass variants). */
+/* LayerNorm with an explicit launch configuration: the forward row-per-CTA or two-pass; the
+ * backward also the TMA ring (ROW_TMA) and the cluster split (ROW_CLUSTER; workspace: one dw and
+ * one db row per cluster). */
 RRN_API int add_layernorm_fwd_ex(const void *x, const void *residual, void *residual_out,
                                  const void *w, const void *b, void *y, float *mean, float *rstd,
                                  int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,

@@ -153,3 +153,34 @@ def test_fp8_wide_rows(dtype, N):
                        rrn.Launch(rrn.VARIANT_STREAM, 0, 1024, 0)):
             q, scale, rstd, ro = run(h, dtype, wl.eps, fused, launch)
             compare(h, dtype, wl.eps, fused, q, scale, rstd, ro, f"{N} {launch}")
+
+
+@pytest.mark.parametrize("dtype,N", [("bf16", 4096), ("f32", 4096), ("bf16", 4095), ("bf16", 32768)])
+def test_fp8_in_place(dtype, N):
+    """residual_out written over residual, and over x."""
+    M = 96
+    wl = synth.Workload("fp8-alias", "add_rmsnorm_fwd", M, N, dtype, 1e-6, 105, res_sigma=2.0)
+    h = synth.make(wl)
+    r_ref, v_ref, q_ref, s_ref, rs_ref = oracle.rmsnorm_quant_fp8(h["x"], h["residual"], h["w"], wl.eps)
+    r_bits = bits_of(r_ref.astype(np.float32), dtype)
+    w = to_dev(h["w"], dtype)
+    V = 8 if dtype == "bf16" else 4
+    launches = [None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0)]
+    if N % V == 0:
+        launches += [rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 0, 0, 4)]
+        if N // V <= 1024:
+            launches += [rrn.Launch(rrn.VARIANT_ROW_CTA, 0, 0, 0)]
+    for launch in launches:
+        for target in ("residual", "x"):
+            x, res = to_dev(h["x"], dtype), to_dev(h["residual"], dtype)
+            ro = res if target == "residual" else x
+            q = torch.full((M, N), 0x7F, dtype=torch.uint8, device="cuda")
+            scale = torch.full((M,), float("nan"), device="cuda")
+            rstd = torch.full((M,), float("nan"), device="cuda")
+            rrn.rmsnorm_fwd_fp8(x, res, ro, w, q, scale, rstd, wl.eps, launch=launch)
+            torch.cuda.synchronize()
+            assert np.array_equal(to_host(ro), r_bits), f"residual_out over {target}, {launch}"
+            check_codes(q.cpu().numpy(), v_ref, q_ref, f"codes (residual_out over {target}), {launch}")
+            check_rstd(rstd.cpu().numpy().astype(np.float64), rs_ref, "rstd")
+            s = scale.cpu().numpy().astype(np.float64)
+            assert np.all(np.abs(s - s_ref) <= 1e-5 * s_ref), f"scale {launch}"
