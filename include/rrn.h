@@ -286,7 +286,8 @@ typedef struct {
     int vpt;     /* 128-bit vectors per thread for the register variants: 1, 2, 4 or 8 */
     int threads; /* threads per CTA (a multiple of 32, at most 1024) */
     int ctas;    /* CTAs in the grid; each walks rows with a grid-sized stride */
-    int stages;  /* RRN_VARIANT_ROW_TMA: rows in flight per CTA, 1..8 */
+    int stages;  /* RRN_VARIANT_ROW_TMA: rows in flight per CTA, 1..8 (the LayerNorm
+                    backward: ring slots, 2..8, holding S - 1 rows in flight) */
     int cluster; /* RRN_VARIANT_ROW_CLUSTER: CTAs per cluster, 2..8 (ctas a multiple of it).
                     Backward ROW_CTA, ROW_TMA: 2, 4 or 8 = add the dw partial sums of
                     that many stage-1 CTAs through distributed shared memory before stage 2

@@ -172,8 +172,10 @@ constexpr int kDecodeTargetThreads = 512;
 // plain vs 338 at 256 threads). Rows held by one CTA: see ln_bwd_vpt.
 constexpr int kLnBwdTmaTargetThreadsFused = 256;
 constexpr int kLnBwdTmaTargetThreadsPlain = 128;
-// Narrowest CTA the LayerNorm backward feeds through the TMA ring; narrower ones hold their rows
-// in registers (65536 x 1024 bf16 fused: 106 us for 64 threads without the ring, 111 with it).
+// Narrowest CTA the LayerNorm backward feeds through the TMA ring at 2 vectors per thread;
+// narrower ones hold their rows in registers (65536 x 1024 bf16 plain: 96.6 us at 64 threads
+// without the ring, 105 with it). At 4 vectors per thread the ring wins at any width
+// (32768 x 2048 plain, 64 threads: 92.5 us vs 117).
 constexpr int kLnBwdMinRingThreads = 128;
 // Widest row (in 128-bit vectors) one CTA holds in registers: 8 vectors x 256 threads.
 constexpr int kRowCtaMaxVec = 2048;
@@ -657,12 +659,13 @@ int plan_ln_fwd(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const 
 }
 
 // Vectors per thread of the LayerNorm backward with whole rows in one CTA, chosen by
-// measurement over 1024-8192 bf16 columns (128 MB per input matrix): 2 when the gradient at
-// residual_out is a third input row (the dw and db sums of 16 columns and three rows' vectors
-// leave 2 CTAs of up to 512 threads per SM; 4 vectors measured 13-28 % slower), and without it
-// 2 below 512 vectors a row and 4 from there (within 2-4 % of the best layout at every width).
+// measurement over 1024-8192 bf16 columns (128 MB per input matrix; ln_bwd_row_tma reading rows
+// twice from its ring): with the gradient at residual_out (a third input row) 2 up to 512
+// vectors a row and 4 above (8192 columns: 113 us vs 127 at 2), without it 2 below 256 vectors
+// and 4 from there (2048 columns: 92.5 us vs 98.8 at 2) - within 2 % of the best layout measured
+// at every width.
 int ln_bwd_vpt(int64_t nvec, bool add_grad) {
-    int vpt = add_grad || nvec < 512 ? 2 : 4;
+    int vpt = (add_grad ? nvec <= 512 : nvec < 256) ? 2 : 4;
     while (vpt < kBwdMaxVpt && nvec > static_cast<int64_t>(vpt) * bwd_max_threads(vpt)) vpt *= 2;
     return vpt;
 }
@@ -681,7 +684,8 @@ int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, con
         // RMSNorm backward (measured 0.9 TB/s for the two-pass kernel on 8192 x 16384)
         const bool regs = vec_ok && nvec <= static_cast<int64_t>(kBwdMaxVpt) * bwd_max_threads(kBwdMaxVpt);
         const int vpt = ln_bwd_vpt(nvec, add_grad);
-        const bool ring = slot <= kMaxDynSmem / 2 && round_up32((nvec + vpt - 1) / vpt) >= kLnBwdMinRingThreads;
+        const bool ring = slot <= kMaxDynSmem / 2 &&
+                          (vpt >= 4 || round_up32((nvec + vpt - 1) / vpt) >= kLnBwdMinRingThreads);
         l.variant = regs ? (ring ? RRN_VARIANT_ROW_TMA : RRN_VARIANT_ROW_CTA)
                   : vec_ok && nvec <= static_cast<int64_t>(kMaxCluster) * kClusterChunkVec ? RRN_VARIANT_ROW_CLUSTER
                                                                                            : RRN_VARIANT_STREAM;
@@ -726,11 +730,27 @@ int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, con
                              pick.threads ? pick.threads : bwd_max_threads(1), &l);
         if (st != RRN_OK) return st;
         if (l.variant == RRN_VARIANT_ROW_TMA) {
+            // The ring refills a slot one row late (ln_bwd_row_tma), so it needs 2 stages or
+            // more: S - 1 rows in flight. Measured on 16384 x 4096 bf16: 3 stages with the
+            // gradient at residual_out (102.6 us vs 108.7 at 2), 2 without (90.8 vs 94.4 at 3);
+            // fewer when more would cost CTAs per SM.
             const int want = cfg ? cfg->stages : 0;
-            if (want < 0 || want > kMaxStages || slot > kMaxDynSmem) return RRN_ERR_CONFIG;
-            ring_occ = plan_ring([&](const Launch &t) { return occupancy_ln(true, dtype, add_grad, t); },
-                                 static_cast<int>(slot), want, &l);
+            if (want < 0 || want == 1 || want > kMaxStages || 2 * slot > kMaxDynSmem) return RRN_ERR_CONFIG;
+            auto occ_at = [&](int S) {
+                Launch t = l;
+                t.stages = S;
+                t.smem = static_cast<int>(S * slot);
+                return S * slot <= kMaxDynSmem ? occupancy_ln(true, dtype, add_grad, t) : 0;
+            };
+            int S = want ? want : add_grad ? 3 : 2;
+            ring_occ = occ_at(S);
+            if (!want && ring_occ < occ_at(2)) {
+                S = 2;
+                ring_occ = occ_at(2);
+            }
             if (ring_occ < 1) return RRN_ERR_CONFIG;
+            l.stages = S;
+            l.smem = static_cast<int>(S * slot);
         }
     } else if (l.variant == RRN_VARIANT_STREAM) {
         l.vpt = 1;

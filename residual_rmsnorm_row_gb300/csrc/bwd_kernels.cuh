@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArg
         rs = rs_next;
     }
     if (k < ring.nrows) {
-        if (tid == 0) ring.drain(k);
+        if (tid == 0) ring.drain(k, ring.S);
         if constexpr (!CLUSTER) return;  // the partial row is not written; the fault word tells
         // (in a cluster the peers still wait at the cluster barriers: take part with the sums)
     }

@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT))
     }
     // A wait ran out: let the copies already issued land before the CTA's shared memory is
     // released, then leave; the fault word tells the host.
-    if (k < ring.nrows && tid == 0) ring.drain(k);
+    if (k < ring.nrows && tid == 0) ring.drain(k, ring.S);
 }
 
 // One row split across the C CTAs of a thread-block cluster (C = 2..8): CTA rank q owns the

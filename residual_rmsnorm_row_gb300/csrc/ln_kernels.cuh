@@ -577,14 +577,21 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_cta(const LnB
     ln_bwd_store_partial<T, VPT>(a, nvec, dw, db);
 }
 
-// Stage 1 fed by the TMA engine, as the RMSNorm backward's: CTA p owns rows p, p + P, ...,
-// keeps a.stages of them (x, dy and, fused, d_ro) in a shared-memory ring filled with
-// cp.async.bulk and refills a slot once the row's CTA-wide sums are done; the next row's mean
-// and rstd are requested one row ahead.
+// Stage 1 fed by the TMA engine: CTA p owns rows p, p + P, ..., keeps a.stages (>= 2) of them
+// (x, dy and, fused, d_ro) in a shared-memory ring filled with cp.async.bulk, and reads each row
+// from the ring twice - for the sums, and again for dx - instead of holding it in registers
+// across the CTA-wide sums (the dw and db sums already take most of the registers: without the
+// row, 2 vectors a thread fit in 80 registers, 3 CTAs of 256 threads per SM). So a slot is free
+// only after the row's second pass: slot k % S is refilled (with row k - 1 + S) at the barrier
+// of row k + 1, which every thread reaches after row k's second pass, and S - 1 rows are in
+// flight while a row is worked on. The next row's mean and rstd are requested one row ahead.
+constexpr int ln_bwd_ring_max_regs(int vpt) { return vpt == 2 ? 80 : vpt >= 4 ? 255 : 128; }
 template <typename T, int VPT, bool ADDG>
-__global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_tma(const LnBwdArgs a) {
+__global__ void __launch_bounds__(bwd_max_threads(VPT)) __maxnreg__(ln_bwd_ring_max_regs(VPT))
+    ln_bwd_row_tma(const LnBwdArgs a) {
     pdl_allow_dependents();  // the stage-2 reduction may be scheduled now
-    constexpr int V = Elem<T>::kPerVec;
+    using E = Elem<T>;
+    constexpr int V = E::kPerVec;
     constexpr int NT = ADDG ? 3 : 2;
     extern __shared__ __align__(128) unsigned char ring_buf[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
@@ -594,6 +601,8 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_tma(const LnB
     const int nvec = a.N / V;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
+    const float n_f = static_cast<float>(a.N);
+    const uint4 *w4 = static_cast<const uint4 *>(a.w);
     RowRing<NT> ring;
     ring.buf = ring_buf;
     ring.full = full;
@@ -617,10 +626,13 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_tma(const LnB
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int c = v * nthr + tid;
-        if (c < nvec) prefetch_l1(static_cast<const uint4 *>(a.w) + c);
+        if (c < nvec) prefetch_l1(w4 + c);
 #pragma unroll
         for (int k = 0; k < V; ++k) dw[v][k] = db[v][k] = 0.f;
     }
+    auto vec = [&](int64_t k, int t, int c) {  // vector c of tensor t of row k, from the ring
+        return ld_shared_v4(ring.slot(k, t) + static_cast<size_t>(c) * 16);
+    };
     int parity = 0;
     int64_t k = 0;
     float mu = 0.f, rs = 0.f;
@@ -636,31 +648,51 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_tma(const LnB
             rs_next = __ldg(a.rstd + nxt);
         }
         if (!ring.wait(k, a.faults)) abort_flag = 1;
-        uint4 xv[VPT], dyv[VPT], gv[VPT];
+        float2 sg = splat(0.f), sgx = splat(0.f);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * nthr + tid;
             if (c < nvec) {
-                xv[v] = ld_shared_v4(ring.slot(k, 0) + static_cast<size_t>(c) * 16);
-                dyv[v] = ld_shared_v4(ring.slot(k, 1) + static_cast<size_t>(c) * 16);
-                if constexpr (ADDG) gv[v] = ld_shared_v4(ring.slot(k, NT - 1) + static_cast<size_t>(c) * 16);
+                float xf[V], d[V], wf[V];
+                E::unpack(vec(k, 0, c), xf);
+                E::unpack(vec(k, 1, c), d);
+                E::unpack(ld_keep(w4 + c), wf);
+                ln_bwd_accumulate<V>(xf, d, wf, mu, rs, dw[v], db[v], sg, sgx);
             }
         }
-        const bool done = ln_bwd_row_body<T, VPT, ADDG>(
-            a, ring.first + k * ring.stride, nvec, xv, dyv, gv, dw, db, slots, parity, mu, rs, [&] {
-                if (abort_flag) return false;  // written before the barrier: uniform
-                if (tid == 0 && k + ring.S < ring.nrows) {
-                    fence_proxy_async();
-                    ring.issue(k + ring.S);
+        // past this barrier every thread is done with row k's first pass and row k - 1's second
+        const float2 t = cta_sum2(sg.x + sg.y, sgx.x + sgx.y, slots[parity]);
+        parity ^= 1;
+        if (abort_flag) break;  // written before the barrier: uniform
+        if (tid == 0 && k >= 1 && k - 1 + ring.S < ring.nrows) {
+            fence_proxy_async();
+            ring.issue(k - 1 + ring.S);
+        }
+        const float cx = -rs * (t.y / n_f), cc = -rs * (t.x / n_f);
+        const int64_t base = (ring.first + k * ring.stride) * nvec;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * nthr + tid;
+            if (c < nvec) {
+                float xf[V], d[V], wf[V], o[V];
+                E::unpack(vec(k, 0, c), xf);
+                E::unpack(vec(k, 1, c), d);
+                E::unpack(ld_keep(w4 + c), wf);
+                ln_bwd_dx<V>(xf, d, wf, mu, rs, cx, cc, o);
+                if constexpr (ADDG) {
+                    float gg[V];
+                    E::unpack(vec(k, NT - 1, c), gg);
+#pragma unroll
+                    for (int j = 0; j < V; ++j) o[j] += gg[j];
                 }
-                return true;
-            });
-        if (!done) break;
+                st_stream(static_cast<uint4 *>(a.dx) + base + c, E::pack(o));
+            }
+        }
         mu = mu_next;
         rs = rs_next;
     }
     if (k < ring.nrows) {  // a wait ran out: the partial rows are not written; the fault word tells
-        if (tid == 0) ring.drain(k);
+        if (tid == 0) ring.drain(k, ring.S - 1);  // rows k .. k + S - 2 are in flight
         return;
     }
     ln_bwd_store_partial<T, VPT>(a, nvec, dw, db);

@@ -184,10 +184,10 @@ struct RowRing {
     __device__ __forceinline__ bool wait(int64_t k, unsigned int *faults) const {
         return mbar_wait(&full[k % S], static_cast<uint32_t>((k / S) & 1), faults);
     }
-    // One thread, after the CTA gave up at row k: let the copies already issued land before the
-    // shared memory is released (each wait bounded again).
-    __device__ __forceinline__ void drain(int64_t k) const {
-        for (int64_t j = k; j < nrows && j < k + S; ++j)
+    // One thread, after the CTA gave up at row k: let the copies already issued - rows k to
+    // k + ahead - 1 - land before the shared memory is released (each wait bounded again).
+    __device__ __forceinline__ void drain(int64_t k, int ahead) const {
+        for (int64_t j = k; j < nrows && j < k + ahead; ++j)
             (void)mbar_wait(&full[j % S], static_cast<uint32_t>((j / S) & 1), nullptr, 100000000ull);
     }
 };

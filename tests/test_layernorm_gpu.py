@@ -139,7 +139,8 @@ def test_layernorm_backward_variants(dtype, N):
             if thr <= (256 if vpt == 4 else 512):
                 launches += [rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0), rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 6),
                              rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 0, 0),     # ring depth planned
-                             rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 7, 1),     # one row in flight
+                             rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 7, 2),     # one row in flight,
+                             rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 5, 4),     # 10-15 rows a CTA
                              rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 0, 3)]
     if N % V == 0 and N // V >= 512:
         # each row split over a cluster (CTA q owning a column slice); 3 x C CTAs: ragged rows
@@ -164,6 +165,25 @@ def test_layernorm_backward_variants(dtype, N):
             check_out(values(dx), ref_dx, dtype, f"LN dx {launch}", cond)
             check_dw(dw.cpu().numpy().astype(np.float64), ref_dw, f"LN dw {launch}")
             check_dw(db.cpu().numpy().astype(np.float64), ref_db, f"LN db {launch}")
+
+
+def test_layernorm_backward_ring_needs_two_stages():
+    """The backward's ring refills a slot one row late: one stage is refused before any launch."""
+    M, N = 64, 4096
+    x = torch.zeros(M, N, device="cuda", dtype=torch.bfloat16)
+    w = torch.ones(N, device="cuda", dtype=torch.bfloat16)
+    mean, rstd = torch.zeros(M, device="cuda"), torch.ones(M, device="cuda")
+    dx, dw, db = torch.empty_like(x), torch.empty(N, device="cuda"), torch.empty(N, device="cuda")
+    ws = torch.empty(rrn.layernorm_bwd_workspace_bytes(M, N, x.dtype) // 4, device="cuda")
+    with pytest.raises(rrn.RRNError):
+        rrn.layernorm_bwd(x, None, x, w, mean, rstd, dx, dw, db, ws, 1e-5,
+                          launch=rrn.Launch(rrn.VARIANT_ROW_TMA, 2, 256, 0, 1))
+    # the rows of a CTA fewer than the stages, and a single CTA walking every row
+    for launch in (rrn.Launch(rrn.VARIANT_ROW_TMA, 2, 256, 0, 4), rrn.Launch(rrn.VARIANT_ROW_TMA, 4, 128, 1, 3)):
+        rrn.layernorm_bwd(x, x, x, w, mean, rstd, dx, dw, db, ws, 1e-5, launch=launch)
+        torch.cuda.synchronize()
+        assert torch.equal(dx, x) and float(dw.abs().max()) == 0.0 and float(db.abs().max()) == 0.0
+    assert rrn.device_faults() == 0
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
