@@ -170,8 +170,8 @@ constexpr int kDecodeTargetThreads = 512;
 // LayerNorm backward of rows split over a cluster: 256-thread CTAs when the gradient at
 // residual_out is a third input row, 128 without it (8192 x 16384 bf16: 353 us fused, 271 us
 // plain vs 338 at 256 threads). Rows held by one CTA: see ln_bwd_vpt.
-constexpr int kLnBwdTmaTargetThreadsFused = 256;
-constexpr int kLnBwdTmaTargetThreadsPlain = 128;
+constexpr int kLnBwdSplitThreadsFused = 256;
+constexpr int kLnBwdSplitThreadsPlain = 128;
 // Narrowest CTA the LayerNorm backward feeds through the TMA ring at 2 vectors per thread;
 // narrower ones hold their rows in registers (65536 x 1024 bf16 plain: 96.6 us at 64 threads
 // without the ring, 105 with it). At 4 vectors per thread the ring wins at any width
@@ -702,10 +702,10 @@ int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, con
         }
         if (l.cluster < 2 || l.cluster > kMaxCluster) return RRN_ERR_CONFIG;
         const int64_t chunk = (nvec + l.cluster - 1) / l.cluster;
-        // as the ring: 256-thread CTAs with the gradient at residual_out, 128 without (measured
-        // on 8192 x 16384 bf16: 353 us fused, 271 us plain vs 338 at 256 threads)
+        // kLnBwdSplitThreads*: CTAs of 256 threads with the gradient at residual_out, 128
+        // without
         st = pick_row_layout(chunk, 1LL << 40, sms, cfg, kBwdMaxVpt, bwd_threads_limit,
-                             add_grad ? kLnBwdTmaTargetThreadsFused : kLnBwdTmaTargetThreadsPlain, &l);
+                             add_grad ? kLnBwdSplitThreadsFused : kLnBwdSplitThreadsPlain, &l);
         if (st != RRN_OK) return st;
         if (cfg && cfg->ctas) {
             l.ctas = cfg->ctas;

@@ -3,9 +3,10 @@
 // "Workflow 0" example index; the kernels here are this library's own design).
 //
 // Forward, per row of r = x (+ residual) in fp32:
-//   mean = sum(r) / N;  var = sum((r - mean)^2) / N  (corrected two-pass: no cancellation-prone
-//   sum of squares, and the first pass's rounding error in the mean is corrected);
-//   rstd = rsqrt(var + eps)
+//   mean = sum(r) / N;  var = sum((r - mean)^2) / N;  rstd = rsqrt(var + eps)
+//   (sums of deviations from a shift K near the mean, in one CTA-wide step, or the corrected
+//   two-pass algorithm where K is far from the mean: never the cancellation-prone
+//   sum(r^2) / N - mean^2; see ln_stats)
 //   y = RN((r - mean) * rstd * w + b);  residual_out = RN(r);  mean, rstd stored as fp32
 // Backward, with xhat = (x - mean) * rstd and g = dy * w:
 //   dx = rstd * (g - mean(g) - xhat * mean(g * xhat))  (+ d_ro, fused)
