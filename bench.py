@@ -466,10 +466,12 @@ def measure_shape(name: str, dev, reps: int):
         l2_note = "flushed" if flush else "%d rotating sets" % nsets
     peak, _ = hbm_peak()
     gbs = nbytes / (us * 1e-6) / 1e9
-    if "layernorm" in wl.op:
-        plan = "layernorm planner"
+    if wl.op == "add_layernorm_fwd":
+        plan = rrn.plan_layernorm_fwd(sets[0]["x"], w, outs[0]["y"], b, sets[0]["residual"], outs[0]["ro"]).name
+    elif wl.op == "layernorm_bwd":
+        plan = rrn.plan_layernorm_bwd(sets[0]["dy"], sets[0]["x"], w, outs[0]["y"], sets[0].get("d_ro")).name
     elif wl.op == "add_rmsnorm_fp8":
-        plan = "fp8 planner"
+        plan = rrn.plan_fwd_fp8(sets[0]["x"], w, outs[0]["q"], sets[0]["residual"], outs[0]["ro"]).name
     elif wl.op in ("rmsnorm_bwd", "add_rmsnorm_bwd"):
         plan = rrn.plan_bwd(sets[0]["dy"], sets[0]["x"], w, outs[0]["y"], sets[0].get("d_ro")).name
     else:

@@ -309,6 +309,21 @@ RRN_API int rrn_plan_fwd(const void *x, const void *residual, const void *residu
 RRN_API int rrn_plan_bwd(const void *dy, const void *d_residual_out, const void *x,
                          const void *w, const void *dx, int64_t M, int64_t N, int dtype,
                          rrn_launch *out);
+/*
+ * rrn_plan_layernorm_fwd / rrn_plan_layernorm_bwd / rrn_plan_fwd_fp8 - the same for
+ * add_layernorm_fwd (`residual` NULL: layernorm_fwd; b may be NULL), layernorm_bwd
+ * (`d_residual_out` NULL: the plain backward; the stage-1 launch) and rmsnorm_fwd_fp8 (q: the
+ * codes). Returns an rrn_status.
+ */
+RRN_API int rrn_plan_layernorm_fwd(const void *x, const void *residual, const void *residual_out,
+                                   const void *w, const void *b, const void *y, int64_t M, int64_t N,
+                                   int dtype, rrn_launch *out);
+RRN_API int rrn_plan_layernorm_bwd(const void *dy, const void *d_residual_out, const void *x,
+                                   const void *w, const void *dx, int64_t M, int64_t N, int dtype,
+                                   rrn_launch *out);
+RRN_API int rrn_plan_fwd_fp8(const void *x, const void *residual, const void *residual_out,
+                             const void *w, const void *q, int64_t M, int64_t N, int dtype,
+                             rrn_launch *out);
 
 /*
  * add_rmsnorm_fwd_ex - add_rmsnorm_fwd (residual != NULL) or rmsnorm_fwd (residual == NULL,

@@ -39,6 +39,9 @@ from ._binding import (  # noqa: F401  (re-exported API)
     load_library,
     plan_bwd,
     plan_fwd,
+    plan_fwd_fp8,
+    plan_layernorm_bwd,
+    plan_layernorm_fwd,
     rmsnorm_bwd,
     rmsnorm_bwd_ex,
     rmsnorm_bwd_noalloc,
@@ -211,4 +214,5 @@ __all__ = [
     "add_rmsnorm_bwd", "add_rms_norm_backward", "RMSNormFunction", "AddRMSNormFunction", "RMSNorm",
     "layernorm_fwd", "layernorm_bwd", "layernorm_bwd_workspace_bytes", "layer_norm",
     "layer_norm_backward", "rmsnorm_fwd_fp8", "rms_norm_fp8", "rmsnorm_bwd_noalloc",
+    "plan_layernorm_fwd", "plan_layernorm_bwd", "plan_fwd_fp8",
 ]

@@ -91,6 +91,10 @@ _SIGNATURES = {
     "rrn_selftest_wait_timeout": (_i32, [ctypes.c_uint64, _vp]),
     "rrn_plan_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, ctypes.POINTER(rrn_launch)]),
     "rrn_plan_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, ctypes.POINTER(rrn_launch)]),
+    "rrn_plan_layernorm_fwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32,
+                                      ctypes.POINTER(rrn_launch)]),
+    "rrn_plan_layernorm_bwd": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, ctypes.POINTER(rrn_launch)]),
+    "rrn_plan_fwd_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i32, ctypes.POINTER(rrn_launch)]),
     "add_rmsnorm_fwd_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _f32, _i32,
                                   ctypes.POINTER(rrn_launch), _vp]),
     "rmsnorm_bwd_ex": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _f32, _i32,
@@ -421,6 +425,40 @@ def plan_fwd(x: torch.Tensor, residual: Optional[torch.Tensor] = None,
     _check(load_library().rrn_plan_fwd(ptr(x), ptr(residual), ptr(residual_out),
                                        ptr(w if w is not None else x), ptr(y if y is not None else x),
                                        M, N, _dtype(x), ctypes.byref(out)))
+    return Launch.from_c(out)
+
+
+def plan_layernorm_fwd(x: torch.Tensor, w: torch.Tensor, y: torch.Tensor, b: Optional[torch.Tensor] = None,
+                       residual: Optional[torch.Tensor] = None,
+                       residual_out: Optional[torch.Tensor] = None) -> Launch:
+    """C ``rrn_plan_layernorm_fwd``: the launch the automatic LayerNorm forward would use."""
+    M, N = _rows(x)
+    out = rrn_launch()
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    _check(load_library().rrn_plan_layernorm_fwd(ptr(x), ptr(residual), ptr(residual_out), ptr(w), ptr(b),
+                                                 ptr(y), M, N, _dtype(x), ctypes.byref(out)))
+    return Launch.from_c(out)
+
+
+def plan_layernorm_bwd(dy: torch.Tensor, x: torch.Tensor, w: torch.Tensor, dx: torch.Tensor,
+                       d_residual_out: Optional[torch.Tensor] = None) -> Launch:
+    """C ``rrn_plan_layernorm_bwd``: the stage-1 launch the automatic LayerNorm backward would use."""
+    M, N = _rows(x)
+    out = rrn_launch()
+    dro = None if d_residual_out is None else d_residual_out.data_ptr()
+    _check(load_library().rrn_plan_layernorm_bwd(dy.data_ptr(), dro, x.data_ptr(), w.data_ptr(),
+                                                 dx.data_ptr(), M, N, _dtype(x), ctypes.byref(out)))
+    return Launch.from_c(out)
+
+
+def plan_fwd_fp8(x: torch.Tensor, w: torch.Tensor, q: torch.Tensor, residual: Optional[torch.Tensor] = None,
+                 residual_out: Optional[torch.Tensor] = None) -> Launch:
+    """C ``rrn_plan_fwd_fp8``: the launch the automatic fp8 forward would use."""
+    M, N = _rows(x)
+    out = rrn_launch()
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    _check(load_library().rrn_plan_fwd_fp8(ptr(x), ptr(residual), ptr(residual_out), ptr(w), ptr(q),
+                                           M, N, _dtype(x), ctypes.byref(out)))
     return Launch.from_c(out)
 
 

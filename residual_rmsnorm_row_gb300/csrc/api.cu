@@ -816,20 +816,13 @@ int run_ln_bwd(const void *dy, const void *d_ro, const void *x, const void *w, c
 }
 
 // ---------------------------------------------------------------- RMSNorm -> fp8
-int run_quant(const void *x, const void *res, void *res_out, const void *w, void *q, float *scale,
-              float *rstd, int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,
-              cudaStream_t stream) {
-    int st = check_fwd(x, res, res_out, w, x, rstd, M, N, eps, dtype);
-    if (st != RRN_OK) return st;
-    if (M == 0) return RRN_OK;
-    if (!q || !scale) return RRN_ERR_NULL;
-    if (!aligned(scale, 4)) return RRN_ERR_ALIGN;
-    int sms = 0;
-    st = current_sm_count(&sms);
-    if (st != RRN_OK) return st;
-    const bool vec_ok = vec_path_ok({x, res, res_out, w, q}, N, dtype);
+// The launch of the RMSNorm -> fp8 forward (rmsnorm_fwd_fp8): as the forward's planner.
+int plan_quant(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const rrn_launch *cfg,
+               Launch *out) {
     const int64_t nvec = N / (16 / elem_size(dtype));
-    const bool fused = res != nullptr;
+    int sms = 0;
+    int st = current_sm_count(&sms);
+    if (st != RRN_OK) return st;
     Launch l{};
     l.variant = cfg && cfg->variant ? cfg->variant : RRN_VARIANT_AUTO;
     if (l.variant == RRN_VARIANT_AUTO) {
@@ -872,6 +865,22 @@ int run_quant(const void *x, const void *res, void *res_out, const void *w, void
     } else {
         return RRN_ERR_CONFIG;
     }
+    *out = l;
+    return RRN_OK;
+}
+
+int run_quant(const void *x, const void *res, void *res_out, const void *w, void *q, float *scale,
+              float *rstd, int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,
+              cudaStream_t stream) {
+    int st = check_fwd(x, res, res_out, w, x, rstd, M, N, eps, dtype);
+    if (st != RRN_OK) return st;
+    if (M == 0) return RRN_OK;
+    if (!q || !scale) return RRN_ERR_NULL;
+    if (!aligned(scale, 4)) return RRN_ERR_ALIGN;
+    const bool fused = res != nullptr;
+    Launch l{};
+    st = plan_quant(vec_path_ok({x, res, res_out, w, q}, N, dtype), fused, M, N, dtype, cfg, &l);
+    if (st != RRN_OK) return st;
     QuantArgs a{x, res, fused ? res_out : nullptr, w, q, scale, rstd, M, static_cast<int>(N), eps};
     cudaError_t e = dtype == RRN_BF16 ? launch_quant_bf16(a, l, stream) : launch_quant_f32(a, l, stream);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -1035,6 +1044,51 @@ RRN_API int rrn_plan_bwd(const void *dy, const void *d_residual_out, const void 
     int64_t rpc = 0;
     st = plan_bwd_impl(vec_path_ok({dy, d_residual_out, x, w, dx}, N, dtype),
                        d_residual_out != nullptr, M, N, dtype, nullptr, &l, &rpc);
+    if (st != RRN_OK) return st;
+    to_public(l, out);
+    return RRN_OK;
+}
+
+RRN_API int rrn_plan_layernorm_fwd(const void *x, const void *residual, const void *residual_out,
+                                   const void *w, const void *b, const void *y, int64_t M, int64_t N,
+                                   int dtype, rrn_launch *out) {
+    if (!out) return RRN_ERR_NULL;
+    int st = check_fwd(x, residual, residual_out, w, y, nullptr, M, N, 0.f, dtype);
+    if (st != RRN_OK) return st;
+    Launch l;
+    st = plan_ln_fwd(vec_path_ok({x, residual, residual_out, w, b, y}, N, dtype), residual != nullptr, M,
+                     N, dtype, nullptr, &l);
+    if (st != RRN_OK) return st;
+    to_public(l, out);
+    return RRN_OK;
+}
+
+RRN_API int rrn_plan_layernorm_bwd(const void *dy, const void *d_residual_out, const void *x,
+                                   const void *w, const void *dx, int64_t M, int64_t N, int dtype,
+                                   rrn_launch *out) {
+    if (!out) return RRN_ERR_NULL;
+    int st = check_common(M, N, 0.f, dtype);
+    if (st != RRN_OK) return st;
+    if (!dy || !x || !w || !dx) return RRN_ERR_NULL;
+    Launch l;
+    int64_t rpc = 0;
+    st = plan_ln_bwd(vec_path_ok({dy, d_residual_out, x, w, dx}, N, dtype), d_residual_out != nullptr, M,
+                     N, dtype, nullptr, &l, &rpc);
+    if (st != RRN_OK) return st;
+    to_public(l, out);
+    return RRN_OK;
+}
+
+RRN_API int rrn_plan_fwd_fp8(const void *x, const void *residual, const void *residual_out,
+                             const void *w, const void *q, int64_t M, int64_t N, int dtype,
+                             rrn_launch *out) {
+    if (!out) return RRN_ERR_NULL;
+    int st = check_fwd(x, residual, residual_out, w, x, nullptr, M, N, 0.f, dtype);
+    if (st != RRN_OK) return st;
+    if (!q) return RRN_ERR_NULL;
+    Launch l;
+    st = plan_quant(vec_path_ok({x, residual, residual_out, w, q}, N, dtype), residual != nullptr, M, N,
+                    dtype, nullptr, &l);
     if (st != RRN_OK) return st;
     to_public(l, out);
     return RRN_OK;

@@ -184,3 +184,24 @@ def test_fp8_in_place(dtype, N):
             check_rstd(rstd.cpu().numpy().astype(np.float64), rs_ref, "rstd")
             s = scale.cpu().numpy().astype(np.float64)
             assert np.all(np.abs(s - s_ref) <= 1e-5 * s_ref), f"scale {launch}"
+
+
+def test_fp8_plans():
+    """The forward's layouts: one row per CTA, cluster split for wide rows with a residual (and
+    beyond 2048 vectors without one), the 128-bit two-pass kernel beyond 8 chunks."""
+    def plan(M, N, fused):
+        x = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+        w = torch.empty(N, device="cuda", dtype=torch.bfloat16)
+        q = torch.empty(M, N, device="cuda", dtype=torch.uint8)
+        return rrn.plan_fwd_fp8(x, w, q, x if fused else None, x if fused else None)
+
+    p = plan(16384, 4096, True)
+    assert (p.variant, p.vpt, p.threads) == (rrn.VARIANT_ROW_CTA, 4, 128), p
+    p = plan(16384, 16384, True)
+    assert (p.variant, p.cluster) == (rrn.VARIANT_ROW_CLUSTER, 4), p
+    p = plan(16384, 16384, False)
+    assert (p.variant, p.vpt) == (rrn.VARIANT_ROW_CTA, 8), p
+    p = plan(4096, 65536, True)
+    assert (p.variant, p.threads, p.vec) == (rrn.VARIANT_STREAM, 1024, 1), p
+    p = plan(64, 4095, False)
+    assert p.variant == rrn.VARIANT_STREAM and p.vec == 0, p

@@ -240,3 +240,31 @@ def test_layernorm_backward_wide_rows(dtype, N):
         check_out(values(dx), ref_dx, dtype, "LN dx", cond)
         check_dw(dw.cpu().numpy().astype(np.float64), ref_dw, "LN dw")
         check_dw(db.cpu().numpy().astype(np.float64), ref_db, "LN db")
+
+
+def test_layernorm_plans():
+    """The automatic layouts the measurements chose (vectors per thread, ring or registers, ring
+    slots, cluster split), through the C plan queries (tensors never read)."""
+    def bwd(M, N, fused):
+        x = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+        w = torch.empty(N, device="cuda", dtype=torch.bfloat16)
+        return rrn.plan_layernorm_bwd(x, x, w, x, x if fused else None)
+
+    p = bwd(16384, 4096, True)
+    assert (p.variant, p.vpt, p.threads, p.stages) == (rrn.VARIANT_ROW_TMA, 2, 256, 3), p
+    p = bwd(16384, 4096, False)
+    assert (p.variant, p.vpt, p.threads, p.stages) == (rrn.VARIANT_ROW_TMA, 4, 128, 2), p
+    p = bwd(32768, 2048, False)
+    assert (p.variant, p.vpt, p.threads) == (rrn.VARIANT_ROW_TMA, 4, 64), p
+    p = bwd(65536, 1024, False)
+    assert (p.variant, p.vpt, p.threads) == (rrn.VARIANT_ROW_CTA, 2, 64), p
+    p = bwd(8192, 8192, True)
+    assert (p.variant, p.vpt, p.threads) == (rrn.VARIANT_ROW_TMA, 4, 256) and p.stages >= 2, p
+    p = bwd(8192, 16384, True)
+    assert p.variant == rrn.VARIANT_ROW_CLUSTER and 2 <= p.cluster <= 8, p
+    p = bwd(64, 4095, False)
+    assert p.variant == rrn.VARIANT_STREAM and p.vec == 0, p
+    x = torch.empty(16384, 4096, device="cuda", dtype=torch.bfloat16)
+    w = torch.empty(4096, device="cuda", dtype=torch.bfloat16)
+    p = rrn.plan_layernorm_fwd(x, w, x, w, x, x)
+    assert (p.variant, p.vpt, p.threads) == (rrn.VARIANT_ROW_CTA, 4, 128), p
