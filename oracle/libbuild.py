@@ -1,7 +1,8 @@
 """Compile the CPU oracle (``oracle.c``) into ``liboracle.so`` with the host C compiler.
 
 Test infrastructure: the oracle is built beside the GPU library so the tests, the smoke check
-and the benchmark's CPU-baseline leg can load it; building the checker is not using it.
+and the benchmark's CPU-baseline leg can load it; compiling it does not run it, and nothing on the
+GPU path links or calls it.
 """
 from __future__ import annotations
 
