@@ -419,12 +419,6 @@ __global__ void __launch_bounds__(1024) ln_fwd_stream(const LnFwdArgs a) {
 }
 
 // ------------------------------------------------------------------------------ backward
-// One row of the backward with its x, dy (and d_ro) vectors in registers (this thread owns
-// vectors c = v * blockDim.x + threadIdx.x; mu, rs the row's mean and rstd): dx written, and
-// dy * xhat and dy added into this thread's dw and db registers. w is read where it is used,
-// from L1, rather than held in registers: this kernel's registers go to the dw and db sums.
-// `after_reduce` runs right after the CTA-wide sums, when every thread has consumed its inputs;
-// when it returns false the row is abandoned.
 // One vector (V values, V even) of a row in the backward, in packed fp32 pairs: with
 // xhat = (x - mean) * rstd and g = dy * w, adds dy * xhat into dw, dy into db, and g and
 // g * xhat into the row's two running sums (kept as pairs, added up once per row).
@@ -465,14 +459,18 @@ __device__ __forceinline__ void ln_bwd_dx(const float (&xf)[V], const float (&d)
     }
 }
 
-template <typename T, int VPT, bool ADDG, typename AfterReduce>
-__device__ __forceinline__ bool ln_bwd_row_body(const LnBwdArgs &a, int64_t row, int nvec,
+// One row of the backward with its x, dy (and d_ro) vectors in registers (this thread owns
+// vectors c = v * blockDim.x + threadIdx.x; mu, rs the row's mean and rstd): dx written, and
+// dy * xhat and dy added into this thread's dw and db registers. w is read where it is used,
+// from L1, rather than held in registers: this kernel's registers go to the dw and db sums.
+template <typename T, int VPT, bool ADDG>
+__device__ __forceinline__ void ln_bwd_row_body(const LnBwdArgs &a, int64_t row, int nvec,
                                                 const uint4 (&xv)[VPT], const uint4 (&dyv)[VPT],
                                                 const uint4 (&gv)[VPT],
                                                 float (&dw)[VPT][Elem<T>::kPerVec],
                                                 float (&db)[VPT][Elem<T>::kPerVec],
                                                 float (&slots)[2][2][32], int &parity, float mu,
-                                                float rs, AfterReduce after_reduce) {
+                                                float rs) {
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
     const int tid = threadIdx.x;
@@ -493,7 +491,6 @@ __device__ __forceinline__ bool ln_bwd_row_body(const LnBwdArgs &a, int64_t row,
     }
     const float2 t = cta_sum2(sg.x + sg.y, sgx.x + sgx.y, slots[parity]);
     parity ^= 1;
-    if (!after_reduce()) return false;
     const float cx = -rs * (t.y / n_f), cc = -rs * (t.x / n_f);
     const int64_t base = row * nvec;
 #pragma unroll
@@ -514,7 +511,6 @@ __device__ __forceinline__ bool ln_bwd_row_body(const LnBwdArgs &a, int64_t row,
             st_stream(static_cast<uint4 *>(a.dx) + base + c, E::pack(o));
         }
     }
-    return true;
 }
 
 // This CTA's dw and db partial sums -> row blockIdx.x of the two [P, N] workspace halves.
@@ -573,7 +569,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_cta(const LnB
             }
         }
         ln_bwd_row_body<T, VPT, ADDG>(a, row, nvec, xv, dyv, gv, dw, db, slots, parity,
-                                      __ldg(a.mean + row), __ldg(a.rstd + row), [] { return true; });
+                                      __ldg(a.mean + row), __ldg(a.rstd + row));
     }
     ln_bwd_store_partial<T, VPT>(a, nvec, dw, db);
 }
