@@ -665,6 +665,14 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) __maxnreg__(ln_bwd_ring_
             fence_proxy_async();
             ring.issue(k - 1 + ring.S);
         }
+        // and the row after the ring's reach asked into L2, so that its bulk copy finds it there
+        // (16384 x 4096 plain: 90.8 -> 86.5 us; 8192 x 8192: 97.1 -> 90.9 plain, 113.3 -> 105.5
+        // fused; 16384 x 4096 fused: 102.6 -> 103.6)
+        if (tid == 0 && k + ring.S < ring.nrows) {
+            const int64_t off = (ring.first + (k + ring.S) * ring.stride) * static_cast<int64_t>(ring.row_bytes);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) prefetch_l2_bulk(ring.src[t] + off, ring.row_bytes);
+        }
         const float cx = -rs * (t.y / n_f), cc = -rs * (t.x / n_f);
         const int64_t base = (ring.first + k * ring.stride) * nvec;
 #pragma unroll
