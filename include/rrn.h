@@ -38,8 +38,11 @@
  *   - Aliasing: an output may be the same buffer as an input of the same shape
  *     (residual_out == residual or x; y == x; dx == dy or x; d_r == dy, d_residual_out or
  *     residual_out). Any other overlap is undefined.
- *   - M == 0 is a no-op that returns RRN_OK and launches nothing (after dtype, N and eps are
- *     checked); the pointers are then not examined and may be NULL.
+ *   - M == 0 returns RRN_OK after dtype, N and eps are checked. The forward calls then launch
+ *     nothing and examine no pointer (all may be NULL). The backward calls read no row either,
+ *     but dw (and db) are sums over no rows: they are set to zero on `stream`, so dw (and db,
+ *     where given) must then be valid, 4-byte aligned device pointers; the other pointers and
+ *     the workspace are not examined.
  *   - Work is enqueued on `stream` (NULL: the legacy default stream) and the call returns
  *     without waiting. Argument errors return a nonzero code before anything is launched;
  *     a failed launch returns RRN_ERR_CUDA (rrn_last_cuda_error() gives the cudaError_t);
@@ -117,7 +120,11 @@ RRN_API int add_rmsnorm_fwd(const void *x, const void *residual, void *residual_
 RRN_API int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t *bytes);
 
 /*
- * rmsnorm_bwd - RMSNorm backward of rmsnorm_fwd, with a two-stage deterministic dw.
+ * rmsnorm_bwd - RMSNorm backward of rmsnorm_fwd, with a two-stage deterministic dw: the
+ * gradients of the Machete page's RMSNorm op (section "Built-In Areas", which lists autograd
+ * helpers beside the ops). The pages write no backward formula; the one at the top of this
+ * file is the exact derivative of the forward definition (d rstd / d x_k = -rstd^3 x_k / N),
+ * dx plus a dw summed over the rows.
  *   dy        [M, N] dtype, read (upstream gradient of y).
  *   x         [M, N] dtype, read (the forward input).
  *   w         [N] dtype, read.
@@ -130,7 +137,7 @@ RRN_API int rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N, int dtype, size_t 
  *             one stream.
  *   eps       validated (>= 0, finite) and otherwise unused: rstd carries it.
  * Stage 1 writes per-CTA fp32 partial sums of dy * xhat to the workspace; stage 2 adds
- * them in a fixed order. With M == 0 nothing is launched and dw is left untouched.
+ * them in a fixed order. With M == 0 dw is set to zero (an empty sum) and no workspace is used.
  * Returns an rrn_status.
  */
 RRN_API int rmsnorm_bwd(const void *dy, const void *x, const void *w, const float *rstd, void *dx,
@@ -139,14 +146,21 @@ RRN_API int rmsnorm_bwd(const void *dy, const void *x, const void *w, const floa
 
 /*
  * rmsnorm_bwd_noalloc - rmsnorm_bwd without a caller-provided workspace, for callers that
- * cannot allocate device memory: code running while a CUDA graph is captured, plugins inside an
- * engine that owns all device allocations, C callers without a caching allocator for whom a
- * cudaMalloc/cudaFree pair per call would synchronise the device. (The source pages have no
+ * cannot allocate device memory: plugins inside an engine that owns every device allocation and
+ * hands a plugin only its inputs and outputs, and C callers without a caching allocator, for whom
+ * a cudaMalloc/cudaFree pair per call would synchronise the device. (The source pages have no
  * counterpart of this entry point; it is a deployment convenience of this library.)
- *   Arguments, layout, results and determinism as for rmsnorm_bwd; no workspace arguments.
+ *   Arguments, layout and error codes as for rmsnorm_bwd, without the workspace arguments; the
+ *   argument checks run first, and M == 0 sets dw to zero as rmsnorm_bwd does.
  *   The dw partial sums live in one 8 MiB array of fp32 inside the library (a __device__
  *   variable, held by every GPU that loads the library until the process exits). The stage-1
- *   CTA count is lowered so that CTAs * N <= 2,097,152; N > 2,097,152 returns RRN_ERR_SCRATCH.
+ *   launch is rmsnorm_bwd's, with the rows of partial sums it writes (one per CTA, or one per
+ *   cluster when each row is split over a cluster) lowered until rows * N <= 2,097,152;
+ *   N > 2,097,152 returns RRN_ERR_SCRATCH.
+ *   Determinism: dw is bitwise reproducible from one rmsnorm_bwd_noalloc call to the next (same
+ *   M, N, dtype and device). Where the rows of partial sums had to be lowered, the sums are
+ *   added in another order than rmsnorm_bwd adds them, so dw can differ from rmsnorm_bwd's in
+ *   the last bits (within the dw tolerance); dx is the same.
  *   Nothing in the array needs to start at zero (stage 1 writes all that stage 2 reads).
  *   All calls on a device share the array: calls whose kernels overlap on the GPU race - order
  *   them on one stream. The first call on each device looks the array's address up (with that

@@ -568,7 +568,7 @@ int check_bwd(const void *dy, const void *d_ro, const void *x, const void *w, co
               const void *dx, const float *dw, int64_t M, int64_t N, float eps, int dtype) {
     int st = check_common(M, N, eps, dtype);
     if (st != RRN_OK) return st;
-    if (M == 0) return RRN_OK;  // nothing is read or written: pointers are not examined
+    if (M == 0) return RRN_OK;  // no row is read or written: row pointers are not examined
     if (!dy || !x || !w || !rstd || !dx || !dw) return RRN_ERR_NULL;
     const uintptr_t es = elem_size(dtype);
     if (!aligned(dy, es) || !aligned(x, es) || !aligned(w, es) || !aligned(dx, es) ||
@@ -577,12 +577,25 @@ int check_bwd(const void *dy, const void *d_ro, const void *x, const void *w, co
     return RRN_OK;
 }
 
+// M == 0: dw (and db) are sums over no rows, so they are set to zero on the stream; no row
+// data is examined.
+int zero_sums(float *dw, float *db, int64_t N, cudaStream_t stream) {
+    if (!dw) return RRN_ERR_NULL;
+    if (!aligned(dw, 4) || (db && !aligned(db, 4))) return RRN_ERR_ALIGN;
+    for (float *p : {dw, db}) {
+        if (!p) continue;
+        const cudaError_t e = cudaMemsetAsync(p, 0, static_cast<size_t>(N) * sizeof(float), stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return RRN_OK;
+}
+
 int run_bwd(const void *dy, const void *d_ro, const void *x, const void *w, const float *rstd,
             void *dx, float *dw, void *workspace, size_t workspace_bytes, int64_t M, int64_t N,
             float eps, int dtype, const rrn_launch *cfg, cudaStream_t stream) {
     int st = check_bwd(dy, d_ro, x, w, rstd, dx, dw, M, N, eps, dtype);
     if (st != RRN_OK) return st;
-    if (M == 0) return RRN_OK;
+    if (M == 0) return zero_sums(dw, nullptr, N, stream);
     Launch l;
     int64_t rpc = 0;
     st = plan_bwd_impl(vec_path_ok({dy, d_ro, x, w, dx}, N, dtype), d_ro != nullptr, M, N, dtype,
@@ -795,7 +808,7 @@ int run_ln_bwd(const void *dy, const void *d_ro, const void *x, const void *w, c
                const rrn_launch *cfg, cudaStream_t stream) {
     int st = check_bwd(dy, d_ro, x, w, rstd, dx, dw, M, N, eps, dtype);
     if (st != RRN_OK) return st;
-    if (M == 0) return RRN_OK;
+    if (M == 0) return zero_sums(dw, db, N, stream);
     if (!mean) return RRN_ERR_NULL;
     if (!aligned(mean, 4) || (db && !aligned(db, 4))) return RRN_ERR_ALIGN;
     Launch l;
@@ -898,6 +911,11 @@ void to_public(const Launch &l, rrn_launch *out) {
 }
 
 }  // namespace
+
+int validate_bwd(const void *dy, const void *x, const void *w, const float *rstd, const void *dx,
+                 const float *dw, int64_t M, int64_t N, float eps, int dtype) {
+    return check_bwd(dy, nullptr, x, w, rstd, dx, dw, M, N, eps, dtype);
+}
 
 cudaError_t allow_dynamic_smem(const void *kernel, int bytes) {
     static std::mutex mu;

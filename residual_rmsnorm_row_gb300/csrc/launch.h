@@ -118,6 +118,11 @@ constexpr int kReduceThreads = 512;  // dw stage-2 CTA size: 32 columns x 16 row
 constexpr int kMaxStages = 8;        // deepest shared-memory ring of the TMA variants
 constexpr int kMaxCluster = 8;       // largest (portable) thread-block cluster
 
+// The argument checks of rmsnorm_bwd (shape, dtype, eps, and - for M > 0 - pointers and their
+// alignment), without the workspace; an rrn_status (defined in api.cu).
+int validate_bwd(const void *dy, const void *x, const void *w, const float *rstd, const void *dx,
+                 const float *dw, int64_t M, int64_t N, float eps, int dtype);
+
 // Raise a kernel's dynamic shared-memory limit to `bytes` on the current device (done once
 // per kernel, device and size; defined in api.cu).
 cudaError_t allow_dynamic_smem(const void *kernel, int bytes);

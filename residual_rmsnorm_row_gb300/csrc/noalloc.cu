@@ -1,11 +1,11 @@
 // rmsnorm_bwd_noalloc: the RMSNorm backward for callers that cannot allocate device memory.
 //
 // The regular backward takes a caller-provided workspace for its per-CTA dw partial sums. Some
-// callers have no way to provide one: code that runs while a CUDA graph is being captured (a
-// cudaMalloc there fails or breaks the capture), plugins inside an inference engine that owns
-// every device allocation, and plain C callers with no caching allocator, for whom a cudaMalloc
-// and cudaFree around each call would synchronise the device. This entry point keeps the
-// partial sums in a fixed array in the library's own device memory instead.
+// callers have no way to provide one: plugins inside an inference or training engine that owns
+// every device allocation and hands a plugin only its inputs and outputs, and plain C callers
+// with no caching allocator, for whom a cudaMalloc and cudaFree around each call would
+// synchronise the device. This entry point keeps the partial sums in a fixed array in the
+// library's own device memory instead.
 //
 // The array is a file-scope __device__ variable of kScratchFloats floats (8 MiB): every GPU that
 // loads the library holds it until the process exits. All calls on a device share it, and it
@@ -63,22 +63,22 @@ extern "C" RRN_API int rmsnorm_bwd_noalloc(const void *dy, const void *x, const 
                                            const float *rstd, void *dx, float *dw, int64_t M,
                                            int64_t N, float eps, int dtype, rrn_stream_t stream) {
     using namespace rrn;
-    if (N > kScratchFloats) return RRN_ERR_SCRATCH;  // not even one row of partial sums fits
-    if (M == 0 || N < 1) {
-        // nothing to launch (or a shape error the regular entry point reports)
+    // the regular entry point's argument checks first, so that their codes win
+    int st = validate_bwd(dy, x, w, rstd, dx, dw, M, N, eps, dtype);
+    if (st != RRN_OK) return st;
+    if (M == 0) {
+        // an empty sum: the regular entry point sets dw to zero and uses no workspace
         return rmsnorm_bwd(dy, x, w, rstd, dx, dw, nullptr, 0, M, N, eps, dtype, stream);
     }
-    // The regular plan, with the number of stage-1 CTAs (one row of partial sums each) lowered
-    // until the partial sums fit the array.
+    if (N > kScratchFloats) return RRN_ERR_SCRATCH;  // not even one row of partial sums fits
+    // The regular plan, with the rows of partial sums stage 1 writes (one per CTA, or one per
+    // cluster when a row is split over a cluster) lowered until they fit the array.
     rrn_launch cfg{};
-    int st = rrn_plan_bwd(dy, nullptr, x, w, dx, M, N, dtype, &cfg);
+    st = rrn_plan_bwd(dy, nullptr, x, w, dx, M, N, dtype, &cfg);
     if (st != RRN_OK) return st;
     const int64_t fit = kScratchFloats / N;
-    if (cfg.ctas > fit) {
-        cfg.ctas = static_cast<int>(fit);
-        // a row split over clusters needs whole clusters (it then writes a row per cluster)
-        if (cfg.variant == RRN_VARIANT_ROW_CLUSTER) cfg.ctas -= cfg.ctas % cfg.cluster;
-    }
+    const int per_row = cfg.cluster > 0 ? cfg.cluster : 1;  // CTAs sharing one row of sums
+    if (cfg.ctas / per_row > fit) cfg.ctas = static_cast<int>(fit) * per_row;
     float *scratch = nullptr;
     st = scratch_address(&scratch);
     if (st != RRN_OK) return st;

@@ -114,10 +114,15 @@ def test_misaligned_elements(lib):
 
 
 def test_empty_problem_launches_nothing(lib):
-    # M == 0 returns before any CUDA call, so it succeeds even without a GPU.
+    # A forward with M == 0 returns before any CUDA call, so it succeeds even without a GPU.
     assert fwd(lib, M=0) == OK
     assert add_fwd(lib, M=0) == OK
-    assert bwd(lib, M=0, ws=None, wsb=0) == OK
+    # A backward with M == 0 sets dw (a sum over no rows) to zero on the stream, so dw is
+    # checked even then; the row pointers and the workspace are not (the zeroing itself is a
+    # GPU test).
+    assert bwd(lib, M=0, dy=None, x=None, w=None, rstd=None, dx=None, dw=None, ws=None,
+               wsb=0) == ERR_NULL
+    assert bwd(lib, M=0, dw=A + 2, ws=None, wsb=0) == ERR_ALIGN
     n = ctypes.c_size_t(123)
     assert lib.rmsnorm_bwd_workspace_bytes(0, 4096, BF16, ctypes.byref(n)) == OK
     assert n.value == 0

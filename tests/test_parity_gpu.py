@@ -188,16 +188,34 @@ def test_wide_rows_automatic_plan(dtype, N, fused, variant, extra):
     compare_fwd(h["x"], h.get("residual"), h["w"], dtype, wl.eps, y, ro, rstd)
 
 
-def test_empty_matrix_writes_nothing():
-    x = torch.zeros(0, 4096, dtype=torch.bfloat16, device="cuda")
-    w = torch.ones(4096, dtype=torch.bfloat16, device="cuda")
-    rrn.rmsnorm_fwd(x, w, x, None, 1e-6)
-    rrn.add_rmsnorm_fwd(x, x, x, w, x, None, 1e-6)
-    dw = torch.full((4096,), 7.0, device="cuda")
-    rrn.rmsnorm_bwd(x, x, w, torch.zeros(0, device="cuda"), x, dw,
-                    torch.zeros(4, device="cuda"), 1e-6)
+def test_empty_matrix():
+    # M == 0: the forward writes nothing; the backward's dw (and LayerNorm's db) are sums over
+    # no rows, which the oracle's definition makes zero - the GPU calls must overwrite them so.
+    N = 4096
+    x = torch.zeros(0, N, dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(N, dtype=torch.bfloat16, device="cuda")
+    rstd = torch.full((1,), 5.0, device="cuda")
+    rrn.rmsnorm_fwd(x, w, x, rstd[:0], 1e-6)
+    rrn.add_rmsnorm_fwd(x, x, x, w, x, rstd[:0], 1e-6)
+    empty = np.zeros((0, N), dtype=np.uint16)
+    _, dw_ref = oracle.rmsnorm_bwd(empty, empty, to_host(w), 1e-6)
+    _, dwf_ref = oracle.add_rmsnorm_bwd(empty, empty, empty, to_host(w), 1e-6)
+    _, dwl_ref, db_ref = oracle.add_layernorm_bwd(empty, None, empty, to_host(w), 1e-5)
+    assert dw_ref.shape == (N,)
+    ws = torch.zeros(4, device="cuda")
+    dw = torch.full((N,), 7.0, device="cuda")
+    rrn.rmsnorm_bwd(x, x, w, rstd[:0], x, dw, ws, 1e-6)
+    dwf = torch.full((N,), 7.0, device="cuda")
+    rrn.add_rmsnorm_bwd(x, x, x, w, rstd[:0], x, dwf, ws, 1e-6)
+    dwl = torch.full((N,), 7.0, device="cuda")
+    db = torch.full((N,), 7.0, device="cuda")
+    rrn.layernorm_bwd(x, None, x, w, rstd[:0], rstd[:0], x, dwl, db, ws, 1e-5)
     torch.cuda.synchronize()
-    assert torch.all(dw == 7.0)
+    assert float(rstd[0]) == 5.0, "a forward with M == 0 wrote"
+    for got, ref, what in ((dw, dw_ref, "rmsnorm_bwd dw"), (dwf, dwf_ref, "add_rmsnorm_bwd dw"),
+                           (dwl, dwl_ref, "layernorm_bwd dw"), (db, db_ref, "layernorm_bwd db")):
+        check_dw(got.cpu().numpy().astype(np.float64), ref, what)
+        assert np.array_equal(got.cpu().numpy(), np.zeros(N, np.float32)), what
 
 
 # ------------------------------------------------------------------ alignment and aliasing
@@ -436,11 +454,19 @@ def test_backward_workspace_too_small_is_rejected():
     w = torch.ones(4096, dtype=torch.bfloat16, device="cuda")
     rstd = torch.ones(64, device="cuda")
     dw = torch.empty(4096, device="cuda")
-    need = rrn.rmsnorm_bwd_workspace_bytes(64, 4096, torch.bfloat16)
+    # the query covers the plain and the fused backward; this call (plain) needs one row of N
+    # floats per stage-1 CTA (clusters: per cluster) and no more
+    plan = rrn.plan_bwd(x, x, w, x)
+    rows = plan.ctas // plan.cluster if plan.cluster > 1 else plan.ctas
+    need = rows * 4096 * 4
+    assert rrn.rmsnorm_bwd_workspace_bytes(64, 4096, torch.bfloat16) >= need
     ws = torch.empty(need // 4 - 1, device="cuda")
     with pytest.raises(rrn.RRNError) as e:
         rrn.rmsnorm_bwd(x, x, w, rstd, x, dw, ws, 1e-6)
     assert e.value.status == 6
+    ws = torch.empty(need // 4, device="cuda")
+    rrn.rmsnorm_bwd(x, x, w, rstd, x, dw, ws, 1e-6)
+    torch.cuda.synchronize()
 
 
 def test_bad_launch_configuration_is_rejected():
