@@ -142,7 +142,7 @@ __device__ __forceinline__ void bwd_store_partial(const BwdArgs &a, int nvec,
 
 template <typename T, int VPT, bool ADDG, bool CLUSTER>
 __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_cta(const BwdArgs a) {
-    pdl_allow_dependents();  // stage 2 may be scheduled now; it waits for our results
+    pdl_enter();  // stage 2 may be scheduled from now on; it waits for our results
     constexpr int V = Elem<T>::kPerVec;
     extern __shared__ __align__(16) float red[];  // N floats when CLUSTER
     __shared__ float slots[2][32];
@@ -183,7 +183,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_cta(const BwdArg
 // slot as soon as the CTA-wide dot product of its row is done.
 template <typename T, int VPT, bool ADDG, bool CLUSTER>
 __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArgs a) {
-    pdl_allow_dependents();  // stage 2 may be scheduled now; it waits for our results
+    pdl_enter();  // stage 2 may be scheduled from now on; it waits for our results
     constexpr int V = Elem<T>::kPerVec;
     constexpr int NT = ADDG ? 3 : 2;  // rows per slot: x, dy (, d_ro)
     extern __shared__ __align__(128) unsigned char ring_buf[];
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArg
 // each CTA its column slice - to row k of the [K, N] workspace.
 template <typename T, int VPT, bool ADDG>
 __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_split(const BwdArgs a) {
-    pdl_allow_dependents();  // stage 2 may be scheduled now; it waits for our results
+    pdl_enter();  // stage 2 may be scheduled from now on; it waits for our results
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
     __shared__ float slots[2][32];
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_split(const BwdA
 // workspace row instead of registers. Each workspace element is owned by one thread.
 template <typename T, bool VEC, bool ADDG>
 __global__ void __launch_bounds__(1024) bwd_stream(const BwdArgs a) {
-    pdl_allow_dependents();  // stage 2 may be scheduled now; it waits for our results
+    pdl_enter();  // stage 2 may be scheduled from now on; it waits for our results
     using E = Elem<T>;
     constexpr int W = E::kPerVec;
     constexpr int V = VEC ? W : 1;
@@ -476,6 +476,7 @@ template <int THREADS>
 __global__ void __launch_bounds__(THREADS)
     bwd_dw_reduce(const float *__restrict__ partial, float *__restrict__ out0,
                   float *__restrict__ out1, int P, int N) {
+    pdl_enter();  // stage 1 has finished and its partial sums are visible
     constexpr int G = THREADS / 32;
     constexpr int U = 48;
     __shared__ float sums[G][33];
@@ -483,7 +484,6 @@ __global__ void __launch_bounds__(THREADS)
     const int grp = threadIdx.x >> 5;
     const int col = blockIdx.x * 32 + lane;
     float *dw = blockIdx.y ? out1 : out0;
-    pdl_wait();  // stage 1 has finished and its partial sums are visible
     float acc = 0.f;
     if (col < N) {
         const float *src = partial + static_cast<int64_t>(blockIdx.y) * P * N + col;
@@ -581,25 +581,7 @@ cudaError_t launch_bwd(const BwdArgs &a, const Launch &l, cudaStream_t stream) {
     BwdArgs args = a;
     args.stages = l.stages;
     void *params[] = {&args};
-    cudaError_t e;
-    if (l.cluster) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(l.ctas);
-        cfg.blockDim = dim3(l.threads);
-        cfg.dynamicSmemBytes = static_cast<size_t>(l.smem);
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(l.cluster);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelExC(&cfg, k, params);
-    } else {
-        e = cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, static_cast<size_t>(l.smem),
-                             stream);
-    }
+    cudaError_t e = enqueue(k, l, l.cluster, params, stream);
     if (e != cudaSuccess) return e;
     return launch_dw_reduce(a.partial, a.dw, nullptr, l.cluster ? l.ctas / l.cluster : l.ctas, a.N,
                             stream);

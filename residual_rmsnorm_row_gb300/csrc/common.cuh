@@ -113,6 +113,14 @@ __device__ __forceinline__ void pdl_allow_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// The first statement of every kernel of the library (each may be launched as a programmatic
+// dependent of the kernel before it on the stream): let the next kernel be scheduled once every
+// CTA of this one is running, then wait until the previous kernel has completed and its memory
+// is visible, before any access to global memory. Both are no-ops for an ordinary launch.
+__device__ __forceinline__ void pdl_enter() {
+    pdl_allow_dependents();
+    pdl_wait();
+}
 
 // ----------------------------------------------------------------------------------------
 // Reductions: butterfly over the warp with shfl_xor (every lane ends with the total), then

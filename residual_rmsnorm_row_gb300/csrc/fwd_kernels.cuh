@@ -118,6 +118,7 @@ __device__ __forceinline__ void prefetch_w(const FwdArgs &a, int nvec) {
 
 template <typename T, int VPT, bool FUSED>
 __global__ void __maxnreg__(fwd_max_regs(VPT)) fwd_row_cta(const FwdArgs a) {
+    pdl_enter();
     constexpr int V = Elem<T>::kPerVec;
     __shared__ float slots[2][32];
     const int nvec = a.N / V;
@@ -152,6 +153,7 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) fwd_row_cta(const FwdArgs a) {
 template <typename T, int VPT, bool FUSED>
 __global__ void __launch_bounds__(fwd_max_threads(VPT))
     fwd_row_tma(const FwdArgs a) {
+    pdl_enter();
     constexpr int V = Elem<T>::kPerVec;
     constexpr int NT = FUSED ? 2 : 1;
     extern __shared__ __align__(128) unsigned char ring_buf[];
@@ -220,6 +222,7 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT))
 // few-row (decode) problems over more SMs.
 template <typename T, int VPT, bool FUSED>
 __global__ void __launch_bounds__(fwd_max_threads(VPT)) fwd_row_cluster(const FwdArgs a) {
+    pdl_enter();
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
     __shared__ float slots[2][32];
@@ -332,6 +335,7 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT)) fwd_row_cluster(const Fw
 
 template <typename T, int VPT, bool FUSED>
 __global__ void __launch_bounds__(256) fwd_row_warp(const FwdArgs a) {
+    pdl_enter();
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
 
@@ -447,6 +451,7 @@ __device__ __forceinline__ void load_r_chunk(const FwdArgs &a, int64_t base, int
 // later writes it, before it writes it.
 template <typename T, bool VEC, bool FUSED>
 __global__ void __launch_bounds__(1024) fwd_stream(const FwdArgs a) {
+    pdl_enter();
     using E = Elem<T>;
     constexpr int W = E::kPerVec;
     constexpr int V = VEC ? W : 1;
@@ -587,23 +592,7 @@ cudaError_t launch_fwd(const FwdArgs &a, const Launch &l, cudaStream_t stream) {
     FwdArgs args = a;
     args.stages = l.stages;
     void *params[] = {&args};
-    if (l.variant == RRN_VARIANT_ROW_CLUSTER) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(l.ctas);
-        cfg.blockDim = dim3(l.threads);
-        cfg.dynamicSmemBytes = static_cast<size_t>(l.smem);
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(l.cluster);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelExC(&cfg, k, params);
-    }
-    return cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, static_cast<size_t>(l.smem),
-                            stream);
+    return enqueue(k, l, l.variant == RRN_VARIANT_ROW_CLUSTER ? l.cluster : 0, params, stream);
 }
 
 template <typename T>

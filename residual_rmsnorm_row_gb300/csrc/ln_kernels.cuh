@@ -264,6 +264,7 @@ __device__ __forceinline__ void ln_out(const float (&f)[V], const float (&wf)[V]
 // CTAs - more rows in flight - per SM, as in the RMSNorm forward.
 template <typename T, int VPT, bool FUSED>
 __global__ void __maxnreg__(fwd_max_regs(VPT)) ln_fwd_row_cta(const LnFwdArgs a) {
+    pdl_enter();
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
     constexpr bool P = VPT >= 4;  // packed fp32 pairs
@@ -351,6 +352,7 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) ln_fwd_row_cta(const LnFwdArgs a)
 // Any N, any alignment: every pass re-reads the row (from L2); VEC selects 128-bit vectors.
 template <typename T, bool VEC, bool FUSED>
 __global__ void __launch_bounds__(1024) ln_fwd_stream(const LnFwdArgs a) {
+    pdl_enter();
     using E = Elem<T>;
     constexpr int W = E::kPerVec;
     constexpr int V = VEC ? W : 1;
@@ -540,7 +542,7 @@ __device__ __forceinline__ void ln_bwd_store_partial(const LnBwdArgs &a, int nve
 // registers and go to rows p of the two [P, N] workspace halves.
 template <typename T, int VPT, bool ADDG>
 __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_cta(const LnBwdArgs a) {
-    pdl_allow_dependents();  // the stage-2 reduction may be scheduled now
+    pdl_enter();  // the stage-2 reduction may be scheduled from now on
     constexpr int V = Elem<T>::kPerVec;
     __shared__ float slots[2][2][32];
     const int nvec = a.N / V;
@@ -586,7 +588,7 @@ constexpr int ln_bwd_ring_max_regs(int vpt) { return vpt == 2 ? 80 : vpt >= 4 ? 
 template <typename T, int VPT, bool ADDG>
 __global__ void __launch_bounds__(bwd_max_threads(VPT)) __maxnreg__(ln_bwd_ring_max_regs(VPT))
     ln_bwd_row_tma(const LnBwdArgs a) {
-    pdl_allow_dependents();  // the stage-2 reduction may be scheduled now
+    pdl_enter();  // the stage-2 reduction may be scheduled from now on
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
     constexpr int NT = ADDG ? 3 : 2;
@@ -713,7 +715,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) __maxnreg__(ln_bwd_ring_
 // of the workspace.
 template <typename T, int VPT, bool ADDG>
 __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_split(const LnBwdArgs a) {
-    pdl_allow_dependents();  // the stage-2 reduction may be scheduled now
+    pdl_enter();  // the stage-2 reduction may be scheduled from now on
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
     __shared__ float slots[2][2][32];
@@ -834,7 +836,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_split(const L
 // CTA's own workspace rows (each element owned by one thread).
 template <typename T, bool VEC, bool ADDG>
 __global__ void __launch_bounds__(1024) ln_bwd_stream(const LnBwdArgs a) {
-    pdl_allow_dependents();  // the stage-2 reductions may be scheduled now
+    pdl_enter();  // the stage-2 reductions may be scheduled from now on
     using E = Elem<T>;
     constexpr int W = E::kPerVec;
     constexpr int V = VEC ? W : 1;
@@ -963,7 +965,7 @@ cudaError_t launch_ln_fwd(const LnFwdArgs &a, const Launch &l, cudaStream_t stre
     if (!k) return cudaErrorInvalidConfiguration;
     LnFwdArgs args = a;
     void *params[] = {&args};
-    return cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, 0, stream);
+    return enqueue(k, l, 0, params, stream);
 }
 
 // Stage 1, then stage 2 twice (dw from the first workspace half, db from the second).
@@ -978,25 +980,7 @@ cudaError_t launch_ln_bwd(const LnBwdArgs &a, const Launch &l, cudaStream_t stre
     LnBwdArgs args = a;
     args.stages = l.stages;
     void *params[] = {&args};
-    cudaError_t e;
-    if (l.cluster) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(l.ctas);
-        cfg.blockDim = dim3(l.threads);
-        cfg.dynamicSmemBytes = static_cast<size_t>(l.smem);
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(l.cluster);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelExC(&cfg, k, params);
-    } else {
-        e = cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, static_cast<size_t>(l.smem),
-                             stream);
-    }
+    cudaError_t e = enqueue(k, l, l.cluster, params, stream);
     if (e != cudaSuccess) return e;
     // dw and db together, from the rows stage 1 wrote: one per CTA, or one per cluster
     const int rows = l.cluster ? l.ctas / l.cluster : l.ctas;

@@ -82,6 +82,7 @@ __device__ __forceinline__ void store_codes(uint8_t *dst, const float (&f)[V], c
 // Only when some |r * w| overflows fp32 does the row take a second step, for the amax of y.
 template <typename T, int VPT, bool FUSED>
 __global__ void __maxnreg__(fwd_max_regs(VPT)) quant_row_cta(const QuantArgs a) {
+    pdl_enter();
     using E = Elem<T>;
     constexpr int V = E::kPerVec;  // 8 (bf16) or 4 (fp32) codes per vector: 8 or 4 bytes
     __shared__ float slots[2][2][32];
@@ -184,6 +185,7 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) quant_row_cta(const QuantArgs a) 
 // |r * w| overflows) exchange one more value each, as the row-per-CTA kernel reduces one more.
 template <typename T, int VPT, bool FUSED>
 __global__ void __launch_bounds__(fwd_max_threads(VPT)) quant_row_cluster(const QuantArgs a) {
+    pdl_enter();
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
     __shared__ float slots[2][2][32];
@@ -326,6 +328,7 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT)) quant_row_cluster(const 
 // buffers).
 template <typename T, bool VEC, bool FUSED>
 __global__ void __launch_bounds__(1024) quant_stream(const QuantArgs a) {
+    pdl_enter();
     using E = Elem<T>;
     constexpr int W = E::kPerVec;
     constexpr int V = VEC ? W : 1;  // values per chunk
@@ -446,21 +449,7 @@ cudaError_t launch_quant(const QuantArgs &a, const Launch &l, cudaStream_t strea
     if (!k) return cudaErrorInvalidConfiguration;
     QuantArgs args = a;
     void *params[] = {&args};
-    if (l.variant == RRN_VARIANT_ROW_CLUSTER) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(l.ctas);
-        cfg.blockDim = dim3(l.threads);
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(l.cluster);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelExC(&cfg, k, params);
-    }
-    return cudaLaunchKernel(k, dim3(l.ctas), dim3(l.threads), params, 0, stream);
+    return enqueue(k, l, l.variant == RRN_VARIANT_ROW_CLUSTER ? l.cluster : 0, params, stream);
 }
 
 template <typename T>
