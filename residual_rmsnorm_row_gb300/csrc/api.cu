@@ -894,7 +894,11 @@ int run_quant(const void *x, const void *res, void *res_out, const void *w, void
     Launch l{};
     st = plan_quant(vec_path_ok({x, res, res_out, w, q}, N, dtype), fused, M, N, dtype, cfg, &l);
     if (st != RRN_OK) return st;
-    QuantArgs a{x, res, fused ? res_out : nullptr, w, q, scale, rstd, M, static_cast<int>(N), eps};
+    unsigned int *faults = nullptr;
+    st = fault_word(&faults);
+    if (st != RRN_OK) return st;
+    QuantArgs a{x, res, fused ? res_out : nullptr, w, q, scale, rstd, M, static_cast<int>(N), eps,
+                faults};
     cudaError_t e = dtype == RRN_BF16 ? launch_quant_bf16(a, l, stream) : launch_quant_f32(a, l, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return RRN_OK;

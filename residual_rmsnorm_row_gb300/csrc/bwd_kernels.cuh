@@ -263,18 +263,21 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArg
 // thread-block cluster (C = 2..8): CTA rank q owns the vectors [q * chunk, (q + 1) * chunk) of
 // every row its cluster handles (chunk = ceil(nvec / C)), holds that slice of x, dy (, d_ro) in
 // registers and keeps the dw partial sums of its columns across rows. A row's dot product
-// sum(g * xhat) is the sum of the C CTAs' parts, exchanged through distributed shared memory as
-// the split forward exchanges its sums of squares (each CTA writes its part into slot q of every
-// peer, one cluster barrier, every CTA adds the C slots in rank order: the same bits
-// everywhere). Cluster k owns rows k, k + K, ... (K clusters) and writes its dw partial sums -
-// each CTA its column slice - to row k of the [K, N] workspace.
+// sum(g * xhat) is the sum of the C CTAs' parts, added in rank order after an exchange through
+// distributed shared memory (ClusterExchange: asynchronous remote stores counted on mbarriers, no
+// cluster barrier in the row loop - a barrier's release would also wait for the previous row's
+// dx stores; measured on 8192 x 16384 bf16: 193 -> 175 us, fused 215 -> 177 us). Cluster k owns
+// rows k, k + K, ... (K clusters) and writes its dw partial sums - each CTA its column slice - to
+// row k of the [K, N] workspace.
 template <typename T, int VPT, bool ADDG>
 __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_split(const BwdArgs a) {
     pdl_enter();  // stage 2 may be scheduled from now on; it waits for our results
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
     __shared__ float slots[2][32];
-    __shared__ float part[2][kMaxCluster];  // one buffer per exchange, alternating
+    __shared__ float part[2][kMaxCluster];
+    __shared__ __align__(8) uint64_t xbar[2];
+    ClusterExchange<float, kMaxCluster> exchange(part, xbar);
 
     const int nvec = a.N / V;
     const int C = static_cast<int>(cluster_nctarank());
@@ -288,6 +291,8 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_split(const BwdA
     const uint4 *x4 = static_cast<const uint4 *>(a.x);
     const uint4 *dy4 = static_cast<const uint4 *>(a.dy);
     const uint4 *g4 = static_cast<const uint4 *>(a.d_ro);
+    if (tid == 0) exchange.init();
+    cluster_sync();  // every CTA of the cluster runs and has its barriers initialised
 
     uint4 wv[VPT];
     float dw[VPT][V];
@@ -298,7 +303,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_split(const BwdA
 #pragma unroll
         for (int k = 0; k < V; ++k) dw[v][k] = 0.f;
     }
-    int parity = 0, pbuf = 0;
+    int parity = 0;
     const int64_t first = cluster_id_x();
     const int64_t ncl = cluster_nclusters_x();
     float rs_next = first < a.M ? __ldg(a.rstd + first) : 0.f;
@@ -347,12 +352,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_split(const BwdA
         }
         dot = cta_sum(dot, slots[parity]);
         parity ^= 1;
-        if (tid < C) st_cluster_f32(&part[pbuf][q], static_cast<uint32_t>(tid), dot);
-        cluster_sync();
-        float t = 0.f;
-        for (int i = 0; i < C; ++i) t += part[pbuf][i];
-        pbuf ^= 1;
-        const float cm = t / n_f;
+        const float cm = exchange(dot, 0.f, [](float u, float v) { return u + v; }, a.faults) / n_f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = c0 + v * nthr + tid;
@@ -384,6 +384,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_split(const BwdA
                 dst[k] = make_float4(dw[v][4 * k], dw[v][4 * k + 1], dw[v][4 * k + 2], dw[v][4 * k + 3]);
         }
     }
+    cluster_sync();  // no CTA leaves while a peer's remote stores may still be on their way to it
 }
 
 // Two passes over each row (any N, any alignment); the dw partials live in the CTA's own

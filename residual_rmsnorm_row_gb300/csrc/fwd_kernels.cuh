@@ -216,8 +216,8 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT))
 // One row split across the C CTAs of a thread-block cluster (C = 2..8): CTA rank q owns the
 // vectors [q * chunk, (q + 1) * chunk) of every row its cluster handles (chunk = ceil(nvec / C)),
 // held in registers. The CTAs' partial sums of squares are exchanged through distributed shared
-// memory: each CTA writes its partial into slot q of every peer's array, then one cluster
-// barrier, then every CTA adds the C slots in rank order (the same bits everywhere). Clusters
+// memory (ClusterExchange: asynchronous remote stores counted on mbarriers, no cluster barrier per
+// row) and every CTA adds the C values in rank order (the same bits everywhere). Clusters
 // walk rows with a grid-sized stride. For rows too wide for one CTA's registers, and to spread
 // few-row (decode) problems over more SMs.
 template <typename T, int VPT, bool FUSED>
@@ -226,7 +226,9 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT)) fwd_row_cluster(const Fw
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
     __shared__ float slots[2][32];
-    __shared__ float part[2][kMaxCluster];  // one buffer per exchange, alternating
+    __shared__ float part[2][kMaxCluster];
+    __shared__ __align__(8) uint64_t xbar[2];
+    ClusterExchange<float, kMaxCluster> xchg(part, xbar);
 
     const int nvec = a.N / V;
     const int C = static_cast<int>(cluster_nctarank());
@@ -239,6 +241,8 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT)) fwd_row_cluster(const Fw
     const float n_f = static_cast<float>(a.N);
     const uint4 *x4 = static_cast<const uint4 *>(a.x);
     const uint4 *r4 = static_cast<const uint4 *>(a.res);
+    if (tid == 0) xchg.init();
+    cluster_sync();  // every CTA of the cluster runs and has its barriers initialised
 
     uint4 wv[VPT];
 #pragma unroll
@@ -246,15 +250,11 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT)) fwd_row_cluster(const Fw
         const int c = c0 + v * nthr + tid;
         if (c < c1) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
     }
-    int parity = 0, pbuf = 0;
-    // Cluster-wide total of one float per CTA; every CTA gets the same bits.
+    int parity = 0;
+    // Cluster-wide total (or maximum) of one float per CTA; every CTA gets the same bits.
     auto exchange = [&](float mine, bool take_max) {
-        if (tid < C) st_cluster_f32(&part[pbuf][q], static_cast<uint32_t>(tid), mine);
-        cluster_sync();
-        float t = 0.f;
-        for (int i = 0; i < C; ++i) t = take_max ? fmaxf(t, part[pbuf][i]) : t + part[pbuf][i];
-        pbuf ^= 1;
-        return t;
+        return take_max ? xchg(mine, 0.f, [](float u, float v) { return fmaxf(u, v); }, a.faults)
+                        : xchg(mine, 0.f, [](float u, float v) { return u + v; }, a.faults);
     };
 
     const int64_t ncl = cluster_nclusters_x();

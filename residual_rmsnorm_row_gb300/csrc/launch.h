@@ -88,6 +88,7 @@ struct QuantArgs {
     int64_t M;
     int N;
     float eps;
+    unsigned int *faults;  // the library's device fault word (cluster exchanges' bounded waits)
 };
 
 // A resolved launch (all fields set).

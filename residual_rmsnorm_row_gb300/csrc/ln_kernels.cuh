@@ -709,8 +709,9 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) __maxnreg__(ln_bwd_ring_
 // of a thread-block cluster (as the RMSNorm backward's bwd_row_split): CTA rank q owns the
 // vectors [q * chunk, (q + 1) * chunk) of every row its cluster handles and keeps the dw and db
 // partial sums of those columns; the row's two sums (of g and of g * xhat) are the sums of the C
-// CTAs' parts, exchanged through distributed shared memory (each CTA writes its pair into slot q
-// of every peer, one cluster barrier, every CTA adds the C pairs in rank order). Cluster k owns
+// CTAs' parts, exchanged through distributed shared memory (ClusterExchange: asynchronous remote
+// stores counted on mbarriers, no cluster barrier per row; every CTA adds the C pairs in rank
+// order). Cluster k owns
 // rows k, k + K, ... (K clusters) and writes its dw sums to row k and its db sums to row K + k
 // of the workspace.
 template <typename T, int VPT, bool ADDG>
@@ -719,7 +720,9 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_split(const L
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
     __shared__ float slots[2][2][32];
-    __shared__ float part[2][2][kMaxCluster];  // [exchange buffer][sum][rank]
+    __shared__ float2 part[2][kMaxCluster];
+    __shared__ __align__(8) uint64_t xbar[2];
+    ClusterExchange<float2, kMaxCluster> xchg(part, xbar);
 
     const int nvec = a.N / V;
     const int C = static_cast<int>(cluster_nctarank());
@@ -731,6 +734,8 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_split(const L
     const int nthr = blockDim.x;
     const float n_f = static_cast<float>(a.N);
     const uint4 *w4 = static_cast<const uint4 *>(a.w);
+    if (tid == 0) xchg.init();
+    cluster_sync();  // every CTA of the cluster runs and has its barriers initialised
 
     float dw[VPT][V], db[VPT][V];
 #pragma unroll
@@ -740,7 +745,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_split(const L
 #pragma unroll
         for (int k = 0; k < V; ++k) dw[v][k] = db[v][k] = 0.f;
     }
-    int parity = 0, pbuf = 0;
+    int parity = 0;
     const int64_t first = cluster_id_x();
     const int64_t ncl = cluster_nclusters_x();
     for (int64_t row = first; row < a.M; row += ncl) {
@@ -784,18 +789,10 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_split(const L
         }
         const float2 t = cta_sum2(sg.x + sg.y, sgx.x + sgx.y, slots[parity]);
         parity ^= 1;
-        if (tid < C) {
-            st_cluster_f32(&part[pbuf][0][q], static_cast<uint32_t>(tid), t.x);
-            st_cluster_f32(&part[pbuf][1][q], static_cast<uint32_t>(tid), t.y);
-        }
-        cluster_sync();
-        float tg = 0.f, tgx = 0.f;
-        for (int i = 0; i < C; ++i) {
-            tg += part[pbuf][0][i];
-            tgx += part[pbuf][1][i];
-        }
-        pbuf ^= 1;
-        const float cx = -rs * (tgx / n_f), cc = -rs * (tg / n_f);
+        const float2 tt = xchg(t, make_float2(0.f, 0.f),
+                               [](float2 u, float2 v) { return make_float2(u.x + v.x, u.y + v.y); },
+                               a.faults);
+        const float cx = -rs * (tt.y / n_f), cc = -rs * (tt.x / n_f);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = c0 + v * nthr + tid;
@@ -830,6 +827,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_split(const L
             }
         }
     }
+    cluster_sync();  // no CTA leaves while a peer's remote stores may still be on their way to it
 }
 
 // Stage 1 for any N and alignment: two passes over each row; the partials accumulate in the

@@ -179,9 +179,9 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) quant_row_cta(const QuantArgs a) 
 // Rows too wide for one CTA's registers, split over the C CTAs of a thread-block cluster as the
 // plain forward's fwd_row_cluster splits them: CTA rank q holds the vectors
 // [q * chunk, (q + 1) * chunk) of every row its cluster handles, w in registers. Each CTA's
-// sum(r^2) and max|r * w| are exchanged through distributed shared memory (each CTA writes its
-// pair into slot q of every peer, one cluster barrier, every CTA combines the C pairs in rank
-// order: the same bits everywhere); the rare paths (rescaled rstd, the amax of y itself when some
+// sum(r^2) and max|r * w| are exchanged through distributed shared memory (ClusterExchange:
+// asynchronous remote stores counted on mbarriers, no cluster barrier per row; every CTA combines
+// the C pairs in rank order: the same bits everywhere); the rare paths (rescaled rstd, the amax of y itself when some
 // |r * w| overflows) exchange one more value each, as the row-per-CTA kernel reduces one more.
 template <typename T, int VPT, bool FUSED>
 __global__ void __launch_bounds__(fwd_max_threads(VPT)) quant_row_cluster(const QuantArgs a) {
@@ -189,7 +189,9 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT)) quant_row_cluster(const 
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
     __shared__ float slots[2][2][32];
-    __shared__ float part[2][2][kMaxCluster];  // [exchange buffer][value][rank]
+    __shared__ float2 part[2][kMaxCluster];
+    __shared__ __align__(8) uint64_t xbar[2];
+    ClusterExchange<float2, kMaxCluster> xchg(part, xbar);
 
     const int nvec = a.N / V;
     const int C = static_cast<int>(cluster_nctarank());
@@ -207,21 +209,14 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT)) quant_row_cluster(const 
         const int c = c0 + v * nthr + tid;
         if (c < c1) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
     }
-    int parity = 0, pbuf = 0;
+    if (tid == 0) xchg.init();
+    cluster_sync();  // every CTA of the cluster runs and has its barriers initialised
+    int parity = 0;
     // cluster-wide (sum of the first values, max of the second values)
     auto exchange = [&](float s, float m) {
-        if (tid < C) {
-            st_cluster_f32(&part[pbuf][0][q], static_cast<uint32_t>(tid), s);
-            st_cluster_f32(&part[pbuf][1][q], static_cast<uint32_t>(tid), m);
-        }
-        cluster_sync();
-        float2 t = make_float2(0.f, 0.f);
-        for (int i = 0; i < C; ++i) {
-            t.x += part[pbuf][0][i];
-            t.y = fmaxf(t.y, part[pbuf][1][i]);
-        }
-        pbuf ^= 1;
-        return t;
+        return xchg(make_float2(s, m), make_float2(0.f, 0.f),
+                    [](float2 u, float2 v) { return make_float2(u.x + v.x, fmaxf(u.y, v.y)); },
+                    a.faults);
     };
 
     const int64_t ncl = cluster_nclusters_x();

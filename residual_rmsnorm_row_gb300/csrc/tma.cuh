@@ -131,11 +131,29 @@ __device__ __forceinline__ uint32_t cluster_nclusters_x() {
 }
 
 // Store one float into the shared memory of CTA `rank` of this cluster, at the address that
-// `local` has in this CTA.
-__device__ __forceinline__ void st_cluster_f32(const float *local, uint32_t rank, float v) {
-    uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+// `local` has in this CTA, and count its 4 bytes as a completed transaction on that CTA's
+// mbarrier at the address `bar` has in this CTA. The store is asynchronous: the receiver, having
+// announced the bytes it expects (mbar_arrive_expect_tx), waits on its own mbarrier. No cluster
+// barrier (and no release of this thread's other memory operations) is involved.
+__device__ __forceinline__ void st_async_cluster_f32(const float *local, uint32_t rank, float v,
+                                                     const uint64_t *bar) {
+    uint32_t rd, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rd) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_addr(bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(rd),
+                 "r"(__float_as_uint(v)), "r"(rb)
+                 : "memory");
+}
+
+// The same for a pair of floats (8 bytes; both addresses 8-byte aligned).
+__device__ __forceinline__ void st_async_cluster_f32x2(const float2 *local, uint32_t rank, float2 v,
+                                                       const uint64_t *bar) {
+    uint32_t rd, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rd) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_addr(bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(rd),
+                 "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(rb)
+                 : "memory");
 }
 
 // All threads of all CTAs of the cluster: release this CTA's prior memory operations (incl.
@@ -144,6 +162,56 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+
+// One value per CTA combined across the C CTAs of a thread-block cluster, through distributed
+// shared memory and without a cluster barrier (whose release would also wait for this thread's
+// earlier global stores). In each exchange every CTA stores its value into slot q (its rank) of
+// every CTA's buffer with an asynchronous remote store that completes a transaction on the
+// receiving CTA's mbarrier; each CTA waits on its own mbarrier for the C values and combines them
+// in rank order, so every CTA gets the same bits. Two buffers alternate: a CTA sends the value of
+// exchange e + 2 only after it has received every peer's value of exchange e + 1, which each peer
+// sends after it has read its buffer of exchange e, so no value is overwritten before it is read.
+// Waits are bounded; once one runs out the fault word is set and later exchanges no longer wait
+// (their results are invalid). The kernel initialises the barriers (init, one thread) and then
+// synchronises the cluster once before the first exchange, and once more before any CTA exits.
+template <typename VAL, int MAXC>  // VAL: float or float2
+struct ClusterExchange {
+    VAL (*part)[MAXC];  // [2][MAXC] in shared memory
+    uint64_t *bar;      // [2] mbarriers in shared memory
+    int C, q;
+    int buf;
+    uint32_t phase;     // bit b: the phase parity bar[b] completes next
+    bool ok;
+
+    __device__ __forceinline__ ClusterExchange(VAL (*p)[MAXC], uint64_t *b)
+        : part(p), bar(b), C(static_cast<int>(cluster_nctarank())),
+          q(static_cast<int>(cluster_ctarank())), buf(0), phase(0), ok(true) {}
+    // One thread, before the cluster synchronisation that precedes the first exchange.
+    __device__ __forceinline__ void init() const {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbarrier_init();
+    }
+    // Every thread of the CTA: send `mine`; return op(...op(op(seed, v_0), v_1)..., v_{C-1}),
+    // the C values combined in rank order.
+    template <typename Op>
+    __device__ __forceinline__ VAL operator()(VAL mine, VAL seed, Op op, unsigned int *faults) {
+        const int tid = threadIdx.x;
+        if (tid == 0) mbar_arrive_expect_tx(&bar[buf], static_cast<uint32_t>(C * sizeof(VAL)));
+        if (tid < C) {
+            if constexpr (sizeof(VAL) == 8)
+                st_async_cluster_f32x2(&part[buf][q], static_cast<uint32_t>(tid), mine, &bar[buf]);
+            else
+                st_async_cluster_f32(&part[buf][q], static_cast<uint32_t>(tid), mine, &bar[buf]);
+        }
+        if (ok && !mbar_wait(&bar[buf], (phase >> buf) & 1u, faults)) ok = false;
+        phase ^= 1u << buf;
+        VAL t = seed;
+        for (int i = 0; i < C; ++i) t = op(t, part[buf][i]);
+        buf ^= 1;
+        return t;
+    }
+};
 
 // A CTA's ring of S shared-memory slots fed by bulk copies. Slot k % S holds row k of the CTA
 // (global row first + k * stride, k < nrows) of NT tensors - src[t] + row * row_bytes - and
