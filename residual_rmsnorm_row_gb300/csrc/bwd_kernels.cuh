@@ -582,7 +582,7 @@ cudaError_t launch_bwd(const BwdArgs &a, const Launch &l, cudaStream_t stream) {
     BwdArgs args = a;
     args.stages = l.stages;
     void *params[] = {&args};
-    cudaError_t e = enqueue(k, l, l.cluster, params, stream);
+    cudaError_t e = enqueue(k, l, l.cluster, false, params, stream);
     if (e != cudaSuccess) return e;
     return launch_dw_reduce(a.partial, a.dw, nullptr, l.cluster ? l.ctas / l.cluster : l.ctas, a.N,
                             stream);

@@ -592,7 +592,8 @@ cudaError_t launch_fwd(const FwdArgs &a, const Launch &l, cudaStream_t stream) {
     FwdArgs args = a;
     args.stages = l.stages;
     void *params[] = {&args};
-    return enqueue(k, l, l.variant == RRN_VARIANT_ROW_CLUSTER ? l.cluster : 0, params, stream);
+    const bool per_row = (l.variant == RRN_VARIANT_ROW_CTA || l.variant == RRN_VARIANT_ROW_WARP) && l.smem == 0;
+    return enqueue(k, l, l.variant == RRN_VARIANT_ROW_CLUSTER ? l.cluster : 0, per_row, params, stream);
 }
 
 template <typename T>

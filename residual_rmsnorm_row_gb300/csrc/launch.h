@@ -126,18 +126,19 @@ int validate_bwd(const void *dy, const void *x, const void *w, const float *rstd
 
 // Enqueue `kernel` on `stream` as l describes (l.ctas CTAs of l.threads threads, l.smem bytes of
 // dynamic shared memory), in thread-block clusters of `cluster` CTAs when cluster > 0.
-// A kernel without a shared-memory ring (l.smem == 0) is launched as a programmatic dependent of
-// the kernel before it on the stream: it may be scheduled while that kernel drains, overlapping
-// its launch and CTA start-up with the other's tail, and it waits for that kernel to complete,
-// memory included, before its first access to global memory (pdl_enter in common.cuh); after
-// any other kind of predecessor the launch is an ordinary one. Measured on GB300: one-row
-// forwards of few rows in a CUDA graph 2.2 -> 2.0 us per launch, 16384 x 4096 forwards back to
-// back 82.8 -> 81.4 us. The ring kernels are launched the ordinary way: as dependents of the
-// previous call's stage 2 the fused backward's stage 1 ran 25-30 % slower back to back (89 ->
-// 114-118 us on 16384 x 4096 bf16), its CTAs, each with 48 KB of shared memory, scheduled onto SMs
-// the other kernel still held.
-inline cudaError_t enqueue(const void *kernel, const Launch &l, int cluster, void **params,
-                           cudaStream_t stream) {
+// With `programmatic`, the kernel is launched as a programmatic dependent of the kernel before it
+// on the stream: it may be scheduled while that kernel drains, overlapping its launch and CTA
+// start-up with the other's tail, and it waits for that kernel to complete, memory included,
+// before its first access to global memory (pdl_enter in common.cuh); after any other kind of
+// predecessor the launch is an ordinary one. Callers ask for it only for grids of one CTA per row
+// (many waves, or few rows) with no shared-memory ring. Measured on GB300: one-row forwards of
+// few rows in a CUDA graph 2.2 -> 2.0 us per launch, 16384 x 4096 forwards back to back 82.8 ->
+// 81.4 us. Grids sized to one wave of resident CTAs (the backward's stage 1, cluster and ring
+// kernels) keep ordinary launches: scheduled while the previous kernel still held SMs, part of
+// such a grid waited for a second wave (back to back: the fused backward 89 -> 114-118 us with a
+// ring on 16384 x 4096, the split-row backward 140 -> 216 us on 8192 x 16384 bf16).
+inline cudaError_t enqueue(const void *kernel, const Launch &l, int cluster, bool programmatic,
+                           void **params, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(l.ctas));
     cfg.blockDim = dim3(static_cast<unsigned>(l.threads));
@@ -145,7 +146,7 @@ inline cudaError_t enqueue(const void *kernel, const Launch &l, int cluster, voi
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     int n = 0;
-    if (l.smem == 0) {
+    if (programmatic) {
         attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[n].val.programmaticStreamSerializationAllowed = 1;
         ++n;

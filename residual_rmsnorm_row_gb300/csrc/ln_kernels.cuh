@@ -963,7 +963,7 @@ cudaError_t launch_ln_fwd(const LnFwdArgs &a, const Launch &l, cudaStream_t stre
     if (!k) return cudaErrorInvalidConfiguration;
     LnFwdArgs args = a;
     void *params[] = {&args};
-    return enqueue(k, l, 0, params, stream);
+    return enqueue(k, l, 0, l.variant == RRN_VARIANT_ROW_CTA, params, stream);
 }
 
 // Stage 1, then stage 2 twice (dw from the first workspace half, db from the second).
@@ -978,7 +978,7 @@ cudaError_t launch_ln_bwd(const LnBwdArgs &a, const Launch &l, cudaStream_t stre
     LnBwdArgs args = a;
     args.stages = l.stages;
     void *params[] = {&args};
-    cudaError_t e = enqueue(k, l, l.cluster, params, stream);
+    cudaError_t e = enqueue(k, l, l.cluster, false, params, stream);
     if (e != cudaSuccess) return e;
     // dw and db together, from the rows stage 1 wrote: one per CTA, or one per cluster
     const int rows = l.cluster ? l.ctas / l.cluster : l.ctas;

@@ -456,7 +456,8 @@ cudaError_t launch_quant(const QuantArgs &a, const Launch &l, cudaStream_t strea
     if (!k) return cudaErrorInvalidConfiguration;
     QuantArgs args = a;
     void *params[] = {&args};
-    return enqueue(k, l, l.variant == RRN_VARIANT_ROW_CLUSTER ? l.cluster : 0, params, stream);
+    return enqueue(k, l, l.variant == RRN_VARIANT_ROW_CLUSTER ? l.cluster : 0,
+                   l.variant == RRN_VARIANT_ROW_CTA, params, stream);
 }
 
 template <typename T>

@@ -42,6 +42,7 @@ class Workload:
     outlier_frac: float = 0.0    # fraction of residual entries replaced by +/- outlier_value
     outlier_value: float = 50.0
     w_kind: str = "normal"       # "normal": 1 + 0.1*N(0,1); "uniform": U(0.5, 1.5)
+    residual_grad: bool = True   # layernorm_bwd: a gradient arrives at residual_out (d_ro)
     meta: Dict[str, str] = field(default_factory=dict)
 
     def with_shape(self, M: int, N: Optional[int] = None) -> "Workload":
@@ -80,6 +81,9 @@ _add(Workload("add_layernorm_fwd_16384x4096_bf16", "add_layernorm_fwd", 16384, 4
               x_mean=0.5))
 _add(Workload("layernorm_bwd_16384x4096_bf16", "layernorm_bwd", 16384, 4096, BF16, 1e-5, 7,
               x_mean=0.5))
+# The plain LayerNorm backward (no gradient at residual_out: two input rows, as RMSNorm's).
+_add(Workload("layernorm_bwd_plain_16384x4096_bf16", "layernorm_bwd", 16384, 4096, BF16, 1e-5, 14,
+              x_mean=0.5, residual_grad=False))
 # The fused Add+RMSNorm feeding fp8 e4m3 codes with a per-row scale (inputs as the fused forward).
 _add(Workload("add_rmsnorm_fp8_16384x4096_bf16", "add_rmsnorm_fp8", 16384, 4096, BF16, 1e-6, 8))
 # Rows wider than one CTA holds in registers: split over a thread-block cluster (16384 wide) or
@@ -149,7 +153,7 @@ def make(w: Workload) -> Dict[str, np.ndarray]:
         out["b"] = _store(np.float32(0.1) * rng.standard_normal(w.N, dtype=np.float32), w.dtype)
     if w.op in ("rmsnorm_bwd", "add_rmsnorm_bwd", "layernorm_bwd"):
         out["dy"] = _store(rng.standard_normal(shape, dtype=np.float32), w.dtype)
-    if w.op in ("add_rmsnorm_bwd", "layernorm_bwd"):
+    if w.op == "add_rmsnorm_bwd" or (w.op == "layernorm_bwd" and w.residual_grad):
         out["d_ro"] = _store(rng.standard_normal(shape, dtype=np.float32), w.dtype)
     return out
 
@@ -162,7 +166,8 @@ def min_bytes(w: Workload) -> int:
     rmsnorm_bwd: x, dy, dx (M*N each), w (N), rstd (M, fp32), dw (N, fp32).
     add_rmsnorm_bwd: residual_out, dy, d_residual_out, d_r (M*N each), w, rstd, dw.
     add_layernorm_fwd: x, residual, residual_out, y (M*N each), w, b (N), mean, rstd (M, fp32).
-    layernorm_bwd: x, dy, d_residual_out, dx (M*N each), w (N), mean, rstd (M), dw, db (N, fp32).
+    layernorm_bwd: x, dy, d_residual_out (when residual_grad), dx (M*N each), w (N), mean, rstd
+    (M), dw, db (N, fp32).
     add_rmsnorm_fp8: x, residual, residual_out (M*N each), the codes (M*N bytes), w (N),
     scale (M, fp32).
     """
@@ -178,7 +183,7 @@ def min_bytes(w: Workload) -> int:
     if w.op == "add_layernorm_fwd":
         return 4 * w.M * w.N * e + 2 * w.N * e + 8 * w.M
     if w.op == "layernorm_bwd":
-        return 4 * w.M * w.N * e + w.N * e + 8 * w.M + 8 * w.N
+        return (4 if w.residual_grad else 3) * w.M * w.N * e + w.N * e + 8 * w.M + 8 * w.N
     if w.op == "add_rmsnorm_fp8":
         return 3 * w.M * w.N * e + w.M * w.N + w.N * e + 4 * w.M
     raise ValueError(w.op)

@@ -66,6 +66,20 @@ def test_layernorm_backward_full_size():
     check_dw(db.cpu().numpy().astype(np.float64), ref_db, "LN db")
 
 
+def test_layernorm_backward_plain_full_size():
+    # no gradient at residual_out: the two-input-row backward, in the layout the benchmark times
+    wl = synth.get("layernorm_bwd_plain_16384x4096_bf16")
+    h = synth.make(wl)
+    x, w = to_dev(h["x"], "bf16"), to_dev(h["w"], "bf16")
+    _, mean, rstd = rrn.layer_norm(x, w, to_dev(h["b"], "bf16"), wl.eps)
+    dx, dw, db = rrn.layer_norm_backward(to_dev(h["dy"], "bf16"), x, w, mean, rstd, wl.eps)
+    torch.cuda.synchronize()
+    ref_dx, ref_dw, ref_db = oracle.add_layernorm_bwd(h["dy"], None, h["x"], h["w"], wl.eps)
+    check_out(values(dx), ref_dx, "bf16", "LN dx")
+    check_dw(dw.cpu().numpy().astype(np.float64), ref_dw, "LN dw")
+    check_dw(db.cpu().numpy().astype(np.float64), ref_db, "LN db")
+
+
 def _fwd_launches(dtype, N):
     V = 8 if dtype == "bf16" else 4
     out = [None, rrn.Launch(rrn.VARIANT_STREAM, 0, 128, 0), rrn.Launch(rrn.VARIANT_STREAM, 0, 1024, 7)]

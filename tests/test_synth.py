@@ -11,7 +11,8 @@ def test_every_workload_draws_its_tensors():
         want = {"x", "w"} | ({"residual"} if w.op in ("add_rmsnorm_fwd", "add_layernorm_fwd",
                                                        "add_rmsnorm_fp8") else set()) | (
             {"dy"} if w.op in ("rmsnorm_bwd", "add_rmsnorm_bwd", "layernorm_bwd") else set()) | (
-            {"d_ro"} if w.op in ("add_rmsnorm_bwd", "layernorm_bwd") else set()) | (
+            {"d_ro"} if w.op == "add_rmsnorm_bwd" or (w.op == "layernorm_bwd" and w.residual_grad)
+            else set()) | (
             {"b"} if "layernorm" in w.op else set())
         assert want <= set(t), name
         enc = np.uint16 if w.dtype == synth.BF16 else np.float32
@@ -54,6 +55,10 @@ def test_min_bytes_matches_tensor_sizes():
     assert synth.min_bytes(synth.get("add_rmsnorm_fwd_16384x4096_bf16")) == 536_944_640
     assert synth.min_bytes(synth.get("add_rmsnorm_fwd_16384x7168_bf16")) == 939_603_968
     assert synth.min_bytes(synth.get("rmsnorm_bwd_16384x4096_bf16")) == 402_743_296
+    # LayerNorm backward: x, dy (, d_residual_out), dx + w + mean, rstd + dw, db
+    assert synth.min_bytes(synth.get("layernorm_bwd_plain_16384x4096_bf16")) == \
+        3 * 16384 * 4096 * 2 + 4096 * 2 + 8 * 16384 + 8 * 4096
+    assert "d_ro" not in synth.make(synth.get("layernorm_bwd_plain_16384x4096_bf16").with_shape(4))
     assert synth.min_bytes(synth.get("rmsnorm_fwd_65536x2048_f32")) == 1_074_012_160
     # 16384 x 4096: x, residual, residual_out (bf16) + codes (1 byte) + w + scale
     assert synth.min_bytes(synth.get("add_rmsnorm_fp8_16384x4096_bf16")) == \
