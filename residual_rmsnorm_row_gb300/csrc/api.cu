@@ -187,6 +187,11 @@ constexpr int kClusterChunkVec = 512;
 
 // Vectors per CTA of the forward's row split for a fused or plain forward.
 int cluster_chunk_vec(bool fused) { return fused ? kClusterChunkVec : 2 * kClusterChunkVec; }
+// Widest row (in vectors) the forward kernels split over a cluster: 8 CTAs of up to 1024 vectors.
+// Fused rows of 4096-8192 vectors take chunks above kClusterChunkVec: with the asynchronous
+// cluster exchange that measured faster than the two-pass kernel (4096 x 65536 bf16: 365 vs 400
+// us; fp32 4096 x 32768: 321 vs 375; fp8 output 294 vs 390).
+constexpr int64_t kClusterMaxVec = static_cast<int64_t>(kMaxCluster) * 2 * kClusterChunkVec;
 // CTAs per cluster for the backward's distributed-shared-memory pre-reduction of dw when the
 // caller leaves the choice to the planner (0: no clusters).
 constexpr int kBwdCluster = 0;
@@ -237,11 +242,13 @@ bool vec_path_ok(std::initializer_list<const void *> ptrs, int64_t N, int dtype)
 }
 
 // The layout of a forward-type kernel with each row split over a cluster (fwd_row_cluster,
-// quant_row_cluster): the cluster size from cluster_chunk_vec unless given, the vectors per thread
-// as the row-per-CTA forward picks them for one CTA's chunk, and - unless given - one wave of
-// clusters: as many as the GPU holds at once (`occ` gives that number for a layout).
+// quant_row_cluster): the cluster size from cluster_chunk_vec unless given (8 for wider rows), the
+// vectors per thread as the row-per-CTA forward picks them for one CTA's chunk with about
+// `target_threads` threads, and - unless given - one wave of clusters: as many as the GPU holds
+// at once (`occ` gives that number for a layout).
 template <typename Occ>
-int fwd_cluster_layout(int64_t nvec, int64_t M, bool fused, const rrn_launch *cfg, Occ occ, Launch *l) {
+int fwd_cluster_layout(int64_t nvec, int64_t M, bool fused, const rrn_launch *cfg, Occ occ, Launch *l,
+                       int target_threads = kFwdTargetThreads) {
     if (cfg && cfg->cluster) {
         l->cluster = cfg->cluster;
     } else {
@@ -253,7 +260,7 @@ int fwd_cluster_layout(int64_t nvec, int64_t M, bool fused, const rrn_launch *cf
     if (cfg && cfg->vpt) {
         l->vpt = cfg->vpt;
     } else {
-        l->vpt = ceil_pow2_vpt((chunk + kFwdTargetThreads - 1) / kFwdTargetThreads, kMaxVpt);
+        l->vpt = ceil_pow2_vpt((chunk + target_threads - 1) / target_threads, kMaxVpt);
         while (l->vpt < kMaxVpt && chunk > static_cast<int64_t>(l->vpt) * fwd_max_threads(l->vpt)) l->vpt *= 2;
     }
     l->threads = cfg && cfg->threads ? cfg->threads : round_up32((chunk + l->vpt - 1) / l->vpt);
@@ -294,7 +301,7 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
         if (!vec_ok) l.variant = RRN_VARIANT_STREAM;
         else if (nvec <= 32 * kMaxVpt && M >= 4LL * sms) l.variant = RRN_VARIANT_ROW_WARP;
         else if (nvec <= cta_max) l.variant = RRN_VARIANT_ROW_CTA;
-        else if (nvec <= static_cast<int64_t>(kMaxCluster) * cluster_chunk_vec(fused)) l.variant = RRN_VARIANT_ROW_CLUSTER;
+        else if (nvec <= kClusterMaxVec) l.variant = RRN_VARIANT_ROW_CLUSTER;
         else l.variant = RRN_VARIANT_STREAM;
     }
     l.vec = (l.variant == RRN_VARIANT_STREAM) ? vec_ok : true;
@@ -844,8 +851,8 @@ int plan_quant(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const r
         const int64_t cta_max = M < 2LL * sms || !fused ? kRowCtaMaxVec : 128 * kMaxVpt;
         l.variant = !vec_ok          ? RRN_VARIANT_STREAM
                     : nvec <= cta_max ? RRN_VARIANT_ROW_CTA
-                    : nvec <= static_cast<int64_t>(kMaxCluster) * cluster_chunk_vec(fused) ? RRN_VARIANT_ROW_CLUSTER
-                                                                                            : RRN_VARIANT_STREAM;
+                    : nvec <= kClusterMaxVec ? RRN_VARIANT_ROW_CLUSTER
+                                             : RRN_VARIANT_STREAM;
     }
     l.vec = l.variant == RRN_VARIANT_STREAM ? vec_ok : true;
     auto occ = [&](const Launch &t) {
@@ -858,7 +865,10 @@ int plan_quant(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const r
         l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid(M);
     } else if (l.variant == RRN_VARIANT_ROW_CLUSTER) {
         if (!vec_ok) return RRN_ERR_CONFIG;
-        st = fwd_cluster_layout(nvec, M, fused, cfg, occ, &l);
+        // chunks above 512 vectors: 256-thread CTAs (4096 x 65536 bf16 with a residual: 294 us
+        // at 4 x 256 against 432 at 8 x 128)
+        const int64_t chunk = (nvec + kMaxCluster - 1) / kMaxCluster;
+        st = fwd_cluster_layout(nvec, M, fused, cfg, occ, &l, chunk > kClusterChunkVec ? 256 : kFwdTargetThreads);
         if (st != RRN_OK) return st;
     } else if (l.variant == RRN_VARIANT_STREAM) {
         l.vpt = 1;

@@ -192,7 +192,8 @@ def test_fp8_in_place(dtype, N):
 
 def test_fp8_plans():
     """The forward's layouts: one row per CTA, cluster split for wide rows with a residual (and
-    beyond 2048 vectors without one), the 128-bit two-pass kernel beyond 8 chunks."""
+    beyond 2048 vectors without one; 256-thread CTAs for chunks above 512 vectors), the 128-bit
+    two-pass kernel beyond 8192 vectors."""
     def plan(M, N, fused):
         x = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
         w = torch.empty(N, device="cuda", dtype=torch.bfloat16)
@@ -206,6 +207,8 @@ def test_fp8_plans():
     p = plan(16384, 16384, False)
     assert (p.variant, p.vpt) == (rrn.VARIANT_ROW_CTA, 8), p
     p = plan(4096, 65536, True)
+    assert (p.variant, p.cluster, p.vpt, p.threads) == (rrn.VARIANT_ROW_CLUSTER, 8, 4, 256), p
+    p = plan(2048, 131072, True)
     assert (p.variant, p.threads, p.vec) == (rrn.VARIANT_STREAM, 1024, 1), p
     p = plan(64, 4095, False)
     assert p.variant == rrn.VARIANT_STREAM and p.vec == 0, p

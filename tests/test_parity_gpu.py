@@ -152,21 +152,22 @@ def test_edge_shapes_forward(dtype, N, M):
 
 # The automatic plan for wide rows when rows are not few (M >= 2 x SMs). Fused (two input
 # rows): one row per CTA up to 1024 vectors, a cluster split of at most 512 vectors per CTA up
-# to 4096 vectors. Plain (one input row, so twice the vectors for the same bytes in flight):
-# one row per CTA up to 2048 vectors, cluster chunks of at most 1024 up to 8192. Wider: the
-# two-pass kernel (1024 threads from 8192 vectors or elements), as for unaligned rows.
+# to 4096 vectors, then clusters of 8 up to 8192. Plain (one input row, so twice the vectors for
+# the same bytes in flight): one row per CTA up to 2048 vectors, cluster chunks of at most 1024
+# up to 8192. Wider: the two-pass kernel (1024 threads from 8192 vectors or elements), as for
+# unaligned rows.
 R, C, S = rrn.VARIANT_ROW_CTA, rrn.VARIANT_ROW_CLUSTER, rrn.VARIANT_STREAM
 WIDE_PLANS = [  # (dtype, N, fused, variant, cluster size or threads)
     ("bf16", 8192, True, R, None), ("bf16", 8192, False, R, None),
     ("bf16", 16384, True, C, 4), ("bf16", 16384, False, R, None),
     ("bf16", 24576, True, C, 8), ("bf16", 24576, False, C, 4),
     ("bf16", 32768, True, C, 8), ("bf16", 32768, False, C, 4),
-    ("bf16", 40000, True, S, 512), ("bf16", 40000, False, C, 8),
-    ("bf16", 65536, True, S, 1024), ("bf16", 65536, False, C, 8),
+    ("bf16", 40000, True, C, 8), ("bf16", 40000, False, C, 8),
+    ("bf16", 65536, True, C, 8), ("bf16", 65536, False, C, 8),
     ("bf16", 80000, False, S, 1024),
     ("bf16", 9001, True, S, 1024), ("bf16", 9001, False, S, 1024),   # unaligned: element-wise
     ("f32", 16384, True, C, 8), ("f32", 16384, False, C, 4),
-    ("f32", 32768, True, S, 1024), ("f32", 32768, False, C, 8),
+    ("f32", 32768, True, C, 8), ("f32", 32768, False, C, 8),
 ]
 
 
