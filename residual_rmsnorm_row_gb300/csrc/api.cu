@@ -167,11 +167,13 @@ constexpr int kFwdTargetThreads = 128;
 constexpr int kBwdTargetThreads = 256;
 // Threads per CTA for few-row (decode) problems: one CTA per row, as wide as this.
 constexpr int kDecodeTargetThreads = 512;
-// LayerNorm backward of rows split over a cluster: 256-thread CTAs when the gradient at
-// residual_out is a third input row, 128 without it (8192 x 16384 bf16: 353 us fused, 271 us
-// plain vs 338 at 256 threads). Rows held by one CTA: see ln_bwd_vpt.
-constexpr int kLnBwdSplitThreadsFused = 256;
-constexpr int kLnBwdSplitThreadsPlain = 128;
+// LayerNorm backward of rows split over a cluster: chunks of up to 256 vectors per CTA (clusters
+// of 8 from 1024 vectors a row, wider chunks at 8), two vectors a thread. Measured on
+// 8192 x 16384 bf16 with the asynchronous exchange and the next row asked into L2: 194 us fused,
+// 173 us plain, against 213 / 191 us for clusters of 4 with 2 x 256 and 227 / 208 us with
+// 4 x 128. Rows held by one CTA: see ln_bwd_vpt.
+constexpr int kLnBwdSplitChunkVec = 256;
+constexpr int kLnBwdSplitThreads = 128;
 // Narrowest CTA the LayerNorm backward feeds through the TMA ring at 2 vectors per thread;
 // narrower ones hold their rows in registers (65536 x 1024 bf16 plain: 96.6 us at 64 threads
 // without the ring, 105 with it). At 4 vectors per thread the ring wins at any width
@@ -718,14 +720,15 @@ int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, con
             l.cluster = cfg->cluster;
         } else {
             l.cluster = 2;
-            while (l.cluster < kMaxCluster && nvec > static_cast<int64_t>(l.cluster) * kClusterChunkVec) l.cluster *= 2;
+            while (l.cluster < kMaxCluster && nvec > static_cast<int64_t>(l.cluster) * kLnBwdSplitChunkVec) l.cluster *= 2;
         }
         if (l.cluster < 2 || l.cluster > kMaxCluster) return RRN_ERR_CONFIG;
         const int64_t chunk = (nvec + l.cluster - 1) / l.cluster;
-        // kLnBwdSplitThreads*: CTAs of 256 threads with the gradient at residual_out, 128
-        // without
-        st = pick_row_layout(chunk, 1LL << 40, sms, cfg, kBwdMaxVpt, bwd_threads_limit,
-                             add_grad ? kLnBwdSplitThreadsFused : kLnBwdSplitThreadsPlain, &l);
+        // two vectors a thread while a CTA of up to 512 threads covers the chunk (4096 x 32768:
+        // 220 us fused, 202 plain at 2 x 256 against 246 / 228 at 4 x 128)
+        rrn_launch pick = cfg ? *cfg : rrn_launch{};
+        if (!pick.vpt && !pick.threads) pick.vpt = chunk <= 2 * bwd_max_threads(2) ? 2 : kBwdMaxVpt;
+        st = pick_row_layout(chunk, 1LL << 40, sms, &pick, kBwdMaxVpt, bwd_threads_limit, kLnBwdSplitThreads, &l);
         if (st != RRN_OK) return st;
         if (cfg && cfg->ctas) {
             l.ctas = cfg->ctas;

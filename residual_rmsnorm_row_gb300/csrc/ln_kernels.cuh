@@ -752,17 +752,17 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_split(const L
         const float mu = __ldg(a.mean + row);
         const float rs = __ldg(a.rstd + row);
         const int64_t base = row * nvec;
-        if constexpr (ADDG) {
-            // three input rows: ask L2 for this CTA's slices of the cluster's next row now, so
-            // that its loads find them there (measured 10-17 % faster on 8192 x 16384 and
-            // 4096 x 32768 bf16; no gain, or a loss, with two input rows)
+        {
+            // ask L2 for this CTA's slices of the cluster's next row now, so that its loads find
+            // them there (8192 x 16384 bf16 with the gradient at residual_out: 347 -> 297 us behind
+            // a cluster barrier per row)
             const int64_t nxt = row + ncl;
             if (tid == 0 && c1 > c0 && nxt < a.M) {
                 const int64_t nb = nxt * nvec + c0;
                 const uint32_t bytes = static_cast<uint32_t>(c1 - c0) * 16u;
                 prefetch_l2_bulk(static_cast<const uint4 *>(a.x) + nb, bytes);
                 prefetch_l2_bulk(static_cast<const uint4 *>(a.dy) + nb, bytes);
-                prefetch_l2_bulk(static_cast<const uint4 *>(a.d_ro) + nb, bytes);
+                if constexpr (ADDG) prefetch_l2_bulk(static_cast<const uint4 *>(a.d_ro) + nb, bytes);
             }
         }
         uint4 xv[VPT], dyv[VPT], gv[VPT];

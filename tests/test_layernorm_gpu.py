@@ -275,7 +275,11 @@ def test_layernorm_plans():
     p = bwd(8192, 8192, True)
     assert (p.variant, p.vpt, p.threads) == (rrn.VARIANT_ROW_TMA, 4, 256) and p.stages >= 2, p
     p = bwd(8192, 16384, True)
-    assert p.variant == rrn.VARIANT_ROW_CLUSTER and 2 <= p.cluster <= 8, p
+    assert (p.variant, p.cluster, p.vpt, p.threads) == (rrn.VARIANT_ROW_CLUSTER, 8, 2, 128), p
+    p = bwd(8192, 16384, False)
+    assert (p.variant, p.cluster, p.vpt, p.threads) == (rrn.VARIANT_ROW_CLUSTER, 8, 2, 128), p
+    p = bwd(4096, 32768, True)
+    assert (p.variant, p.cluster, p.vpt, p.threads) == (rrn.VARIANT_ROW_CLUSTER, 8, 2, 256), p
     p = bwd(64, 4095, False)
     assert p.variant == rrn.VARIANT_STREAM and p.vec == 0, p
     x = torch.empty(16384, 4096, device="cuda", dtype=torch.bfloat16)
