@@ -77,3 +77,40 @@ def test_fp8_and_layernorm_forward_are_bitwise_reproducible():
         return q.view(torch.uint8), scale, ro, y, mean, rstd
 
     assert _same(run(), run())
+
+
+def test_split_row_kernels_are_bitwise_reproducible():
+    # rows split over thread-block clusters: the CTAs' partial sums meet through distributed
+    # shared memory (asynchronous remote stores counted on mbarriers) and are added in rank order
+    M, N = 2048, 16384
+    wl = synth.Workload("split-det", "layernorm_bwd", M, N, "bf16", 1e-5, 61, x_mean=0.5)
+    h = synth.make(wl)
+    x, w = to_dev(h["x"], "bf16"), to_dev(h["w"], "bf16")
+    dy, dro = to_dev(h["dy"], "bf16"), to_dev(h["d_ro"], "bf16")
+    _, rstd = rrn.rms_norm(x, w, wl.eps)
+    _, mean, lrstd = rrn.layer_norm(x, w, None, wl.eps)
+    ws = torch.empty(2 * M * N, device="cuda")
+    for d in (dro, None):
+        plan = rrn.plan_bwd(dy, x, w, x, d)
+        assert plan.variant == rrn.VARIANT_ROW_CLUSTER, plan.name
+        lplan = rrn.plan_layernorm_bwd(dy, x, w, x, d)
+        assert lplan.variant == rrn.VARIANT_ROW_CLUSTER, lplan.name
+
+    def run():
+        out = []
+        for d in (dro, None):
+            dr = torch.empty_like(x)
+            dw = torch.empty(N, device="cuda")
+            rrn.add_rmsnorm_bwd(dy, d, x, w, rstd, dr, dw, ws, wl.eps)
+            dx = torch.empty_like(x)
+            lw = torch.empty(N, device="cuda")
+            lb = torch.empty(N, device="cuda")
+            rrn.layernorm_bwd(dy, d, x, w, mean, lrstd, dx, lw, lb, ws, wl.eps)
+            out += [dr, dw, dx, lw, lb]
+        y, ro, rs = rrn.add_rms_norm(x, dy, w, wl.eps)
+        q, scale, ro2 = rrn.rms_norm_fp8(x, w, wl.eps, residual=dy)
+        torch.cuda.synchronize()
+        return out + [y, ro, rs, q.view(torch.uint8), scale, ro2]
+
+    assert rrn.plan_fwd(x, dy, x, w, x).variant == rrn.VARIANT_ROW_CLUSTER
+    assert _same(run(), run())
