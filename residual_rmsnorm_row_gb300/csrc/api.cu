@@ -854,8 +854,8 @@ int plan_quant(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const r
         const int64_t cta_max = M < 2LL * sms || !fused ? kRowCtaMaxVec : 128 * kMaxVpt;
         l.variant = !vec_ok          ? RRN_VARIANT_STREAM
                     : nvec <= cta_max ? RRN_VARIANT_ROW_CTA
-                    : nvec <= kClusterMaxVec ? RRN_VARIANT_ROW_CLUSTER
-                                             : RRN_VARIANT_STREAM;
+                    : nvec <= 2 * kClusterMaxVec ? RRN_VARIANT_ROW_CLUSTER
+                                                 : RRN_VARIANT_STREAM;
     }
     l.vec = l.variant == RRN_VARIANT_STREAM ? vec_ok : true;
     auto occ = [&](const Launch &t) {
@@ -869,9 +869,11 @@ int plan_quant(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const r
     } else if (l.variant == RRN_VARIANT_ROW_CLUSTER) {
         if (!vec_ok) return RRN_ERR_CONFIG;
         // chunks above 512 vectors: 256-thread CTAs (4096 x 65536 bf16 with a residual: 294 us
-        // at 4 x 256 against 432 at 8 x 128)
+        // at 4 x 256 against 432 at 8 x 128), above 1024: 512 (rows up to 16384 vectors, twice
+        // the forward's limit: 2048 x 131072 357 us at 4 x 512, 516 at 8 x 256, 460 two-pass)
         const int64_t chunk = (nvec + kMaxCluster - 1) / kMaxCluster;
-        st = fwd_cluster_layout(nvec, M, fused, cfg, occ, &l, chunk > kClusterChunkVec ? 256 : kFwdTargetThreads);
+        const int target = chunk > 2 * kClusterChunkVec ? 512 : chunk > kClusterChunkVec ? 256 : kFwdTargetThreads;
+        st = fwd_cluster_layout(nvec, M, fused, cfg, occ, &l, target);
         if (st != RRN_OK) return st;
     } else if (l.variant == RRN_VARIANT_STREAM) {
         l.vpt = 1;

@@ -144,10 +144,11 @@ def test_fp8_row_whose_r_times_w_overflows():
         compare(h, "bf16", 1e-6, False, q, scale, rstd, None, str(launch))
 
 
-@pytest.mark.parametrize("dtype,N", [("bf16", 16384), ("bf16", 32768), ("bf16", 65536), ("f32", 16384)])
+@pytest.mark.parametrize("dtype,N", [("bf16", 16384), ("bf16", 32768), ("bf16", 65536), ("bf16", 131072),
+                                     ("f32", 16384)])
 def test_fp8_wide_rows(dtype, N):
-    """Rows wider than one CTA holds: split over clusters (automatic up to 8 CTAs of 512 vectors
-    with a residual, 1024 without), the 128-bit two-pass kernel beyond."""
+    """Rows wider than one CTA holds: split over clusters (automatic up to 8 CTAs of 2048
+    vectors), the 128-bit two-pass kernel beyond."""
     M = 40
     for fused in (False, True):
         wl = synth.Workload("fp8-wide", "add_rmsnorm_fwd" if fused else "rmsnorm_fwd", M, N, dtype,
@@ -193,7 +194,7 @@ def test_fp8_in_place(dtype, N):
 def test_fp8_plans():
     """The forward's layouts: one row per CTA, cluster split for wide rows with a residual (and
     beyond 2048 vectors without one; 256-thread CTAs for chunks above 512 vectors), the 128-bit
-    two-pass kernel beyond 8192 vectors."""
+    two-pass kernel beyond 16384 vectors."""
     def plan(M, N, fused):
         x = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
         w = torch.empty(N, device="cuda", dtype=torch.bfloat16)
@@ -209,6 +210,8 @@ def test_fp8_plans():
     p = plan(4096, 65536, True)
     assert (p.variant, p.cluster, p.vpt, p.threads) == (rrn.VARIANT_ROW_CLUSTER, 8, 4, 256), p
     p = plan(2048, 131072, True)
+    assert (p.variant, p.cluster, p.vpt, p.threads) == (rrn.VARIANT_ROW_CLUSTER, 8, 4, 512), p
+    p = plan(1024, 262144, True)
     assert (p.variant, p.threads, p.vec) == (rrn.VARIANT_STREAM, 1024, 1), p
     p = plan(64, 4095, False)
     assert p.variant == rrn.VARIANT_STREAM and p.vec == 0, p
