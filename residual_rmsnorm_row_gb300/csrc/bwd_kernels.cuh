@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArg
 // rows k, k + K, ... (K clusters) and writes its dw partial sums - each CTA its column slice - to
 // row k of the [K, N] workspace.
 template <typename T, int VPT, bool ADDG>
-__global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_split(const BwdArgs a) {
+__device__ __forceinline__ void bwd_row_split_body(const BwdArgs &a) {
     pdl_enter();  // stage 2 may be scheduled from now on; it waits for our results
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
@@ -385,6 +385,20 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_split(const BwdA
         }
     }
     cluster_sync();  // no CTA leaves while a peer's remote stores may still be on their way to it
+}
+
+// The split-row kernel without and with the gradient at residual_out. The latter, at 4 vectors
+// a thread, is compiled for 2 resident CTAs of 256 threads (at most 128 registers): it then fits
+// with no spills, 4 CTAs of 128 threads per SM instead of 3 at 164 registers (8192 x 16384 bf16:
+// 172 -> 166 us; 4096 x 32768: 181 -> 168 us). The plain kernel keeps the compiler's allocation
+// (128 at 4 vectors; asking for 2 CTAs gave 123 and ran 2 % slower).
+template <typename T, int VPT>
+__global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_split(const BwdArgs a) {
+    bwd_row_split_body<T, VPT, false>(a);
+}
+template <typename T, int VPT>
+__global__ void __launch_bounds__(bwd_max_threads(VPT), VPT == 4 ? 2 : 1) bwd_row_split_addg(const BwdArgs a) {
+    bwd_row_split_body<T, VPT, true>(a);
 }
 
 // Two passes over each row (any N, any alignment); the dw partials live in the CTA's own
@@ -538,9 +552,12 @@ const void *bwd_kernel_ptr(const Launch &l) {
                          : reinterpret_cast<const void *>(&bwd_stream<T, false, ADDG>);
         case RRN_VARIANT_ROW_CLUSTER:
             switch (l.vpt) {
-                case 1: return reinterpret_cast<const void *>(&bwd_row_split<T, 1, ADDG>);
-                case 2: return reinterpret_cast<const void *>(&bwd_row_split<T, 2, ADDG>);
-                case 4: return reinterpret_cast<const void *>(&bwd_row_split<T, 4, ADDG>);
+                case 1: return ADDG ? reinterpret_cast<const void *>(&bwd_row_split_addg<T, 1>)
+                                    : reinterpret_cast<const void *>(&bwd_row_split<T, 1>);
+                case 2: return ADDG ? reinterpret_cast<const void *>(&bwd_row_split_addg<T, 2>)
+                                    : reinterpret_cast<const void *>(&bwd_row_split<T, 2>);
+                case 4: return ADDG ? reinterpret_cast<const void *>(&bwd_row_split_addg<T, 4>)
+                                    : reinterpret_cast<const void *>(&bwd_row_split<T, 4>);
                 default: return nullptr;
             }
         case RRN_VARIANT_ROW_TMA:
