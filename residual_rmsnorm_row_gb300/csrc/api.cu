@@ -203,16 +203,30 @@ constexpr int kMaxDynSmem = 227 * 1024;
 
 // Pick the ring depth for a TMA variant whose one-row slot takes `slot_bytes`. Resident CTAs
 // per SM come first (measured on the 16384 x 4096 bf16 backward: 4 CTAs x 2 stages 71.8 us,
-// 2 CTAs x 7 stages 96.8 us); among the depths that keep the most CTAs resident, the shallowest
-// from 2 up that keeps kRingTargetBytes per SM in flight (else the deepest of them). Returns
-// the CTAs per SM (0: no depth fits); sets l->stages and l->smem.
+// 2 CTAs x 7 stages 96.8 us), at most `max_occ` of them when that is positive; among the
+// depths that keep the most CTAs resident, the shallowest from 2 up that keeps kRingTargetBytes
+// of ring per SM - `capped_target` when max_occ held the CTAs back - (else the deepest of
+// them). Returns the CTAs per SM (0: no depth fits); sets l->stages and l->smem.
 constexpr int64_t kRingTargetBytes = 64 * 1024;
+
+// The backward with two input rows (x, dy) measured best with at most about 48 KB of rows being
+// worked on per SM (resident CTAs x slot bytes, at least 2 CTAs) and, where that holds CTAs
+// back, a ring of about 128 KB per SM to keep the bytes in flight (bf16, 64 Mi elements per
+// matrix, back to back): 3072 columns 73.3 -> 69.2 us (4 CTAs x 3 stages instead of 5 x 2),
+// 4096 columns 73.5 -> 68.0 (3 x 3 instead of 4 x 2), 6144 columns 71.5 -> 69.5 (2 x 3 instead
+// of 2 x 2); 1024, 2048 and 8192 columns kept their layouts (there 3 or 4 stages measured 1-2 %
+// slower). With a third input row the most CTAs and 64 KB of ring per SM stayed the best
+// measured at every width.
+constexpr int64_t kBwdPlainWorkBytes = 48 * 1024;
+constexpr int64_t kBwdPlainRingBytes = 128 * 1024;
 
 // occ(t): resident CTAs per SM of launch t.
 template <typename Occ>
-int plan_ring(Occ occ, int slot_bytes, int want_stages, Launch *l) {
+int plan_ring(Occ occ, int slot_bytes, int want_stages, Launch *l, int max_occ = 0,
+              int64_t capped_target = kRingTargetBytes) {
     int occ_of[kMaxStages + 1] = {};
     int best_occ = 0;
+    bool capped = false;
     for (int S = 1; S <= kMaxStages; ++S) {
         if (want_stages && S != want_stages) continue;
         const int64_t smem = static_cast<int64_t>(S) * slot_bytes;
@@ -221,14 +235,19 @@ int plan_ring(Occ occ, int slot_bytes, int want_stages, Launch *l) {
         t.stages = S;
         t.smem = static_cast<int>(smem);
         occ_of[S] = occ(t);
+        if (max_occ > 0 && occ_of[S] >= max_occ) {
+            occ_of[S] = max_occ;
+            capped = true;
+        }
         if (occ_of[S] > best_occ) best_occ = occ_of[S];
     }
     if (best_occ < 1) return 0;
+    const int64_t target = capped && best_occ == max_occ ? capped_target : kRingTargetBytes;
     int pick = 0;
     for (int S = 1; S <= kMaxStages; ++S) {
         if (occ_of[S] != best_occ) continue;
         pick = S;
-        if (S >= 2 && static_cast<int64_t>(best_occ) * S * slot_bytes >= kRingTargetBytes) break;
+        if (S >= 2 && static_cast<int64_t>(best_occ) * S * slot_bytes >= target) break;
     }
     l->stages = pick;
     l->smem = pick * slot_bytes;
@@ -519,8 +538,11 @@ int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
                 if (want < 0 || want > kMaxStages) return RRN_ERR_CONFIG;
                 const int64_t slot = (add_grad ? 3 : 2) * N * elem_size(dtype);
                 if (slot > kMaxDynSmem) return RRN_ERR_CONFIG;
+                const int64_t work_cap = kBwdPlainWorkBytes / slot;
                 ring_occ = plan_ring([&](const Launch &t) { return occupancy(true, dtype, add_grad, t); },
-                                     static_cast<int>(slot), want, &l);
+                                     static_cast<int>(slot), want, &l,
+                                     add_grad ? 0 : static_cast<int>(work_cap < 2 ? 2 : work_cap),
+                                     kBwdPlainRingBytes);
                 if (ring_occ < 1) return RRN_ERR_CONFIG;
             }
             break;

@@ -38,7 +38,7 @@ __device__ __forceinline__ bool bwd_row_body(const BwdArgs &a, int64_t row, int 
     constexpr int V = E::kPerVec;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
-    float dot = 0.f;
+    float2 dot2 = splat(0.f);  // packed fp32 pairs: half the FMA instructions
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int c = v * nthr + tid;
@@ -48,14 +48,17 @@ __device__ __forceinline__ bool bwd_row_body(const BwdArgs &a, int64_t row, int 
             E::unpack(dyv[v], d);
             E::unpack(wv[v], wf);
 #pragma unroll
-            for (int k = 0; k < V; ++k) {
-                const float xh = xf[k] * rs;
-                dot = fmaf(d[k] * wf[k], xh, dot);
-                dw[v][k] = fmaf(d[k], xh, dw[v][k]);
+            for (int k = 0; k < V; k += 2) {
+                const float2 xh = mul2(pair(xf[k], xf[k + 1]), splat(rs));
+                const float2 d2 = pair(d[k], d[k + 1]);
+                dot2 = fma2(mul2(d2, pair(wf[k], wf[k + 1])), xh, dot2);
+                const float2 w2 = fma2(d2, xh, pair(dw[v][k], dw[v][k + 1]));
+                dw[v][k] = w2.x;
+                dw[v][k + 1] = w2.y;
             }
         }
     }
-    dot = cta_sum(dot, slots[parity]);
+    const float dot = cta_sum(dot2.x + dot2.y, slots[parity]);
     parity ^= 1;
     if (!after_reduce()) return false;
     const float cm = dot / static_cast<float>(a.N);
@@ -69,7 +72,13 @@ __device__ __forceinline__ bool bwd_row_body(const BwdArgs &a, int64_t row, int 
             E::unpack(dyv[v], d);
             E::unpack(wv[v], wf);
 #pragma unroll
-            for (int k = 0; k < V; ++k) o[k] = rs * (d[k] * wf[k] - (xf[k] * rs) * cm);
+            for (int k = 0; k < V; k += 2) {
+                const float2 xh = mul2(pair(xf[k], xf[k + 1]), splat(rs));
+                const float2 g = mul2(pair(d[k], d[k + 1]), pair(wf[k], wf[k + 1]));
+                const float2 r = mul2(splat(rs), fma2(xh, splat(-cm), g));
+                o[k] = r.x;
+                o[k + 1] = r.y;
+            }
             if constexpr (ADDG) {
                 float g[V];
                 E::unpack(gv[v], g);
@@ -225,15 +234,15 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArg
     float rs = ring.nrows > 0 ? __ldg(a.rstd + ring.first) : 0.f;
     for (; k < ring.nrows; ++k) {
         const float rs_next = k + 1 < ring.nrows ? __ldg(a.rstd + ring.first + (k + 1) * ring.stride) : 0.f;
-        if (!ring.wait(k, a.faults)) abort_flag = 1;
+        if (!ring.wait(a.faults)) abort_flag = 1;
         uint4 xv[VPT], dyv[VPT], gv[VPT];
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * nthr + tid;
             if (c < nvec) {
-                xv[v] = ld_shared_v4(ring.slot(k, 0) + static_cast<size_t>(c) * 16);
-                dyv[v] = ld_shared_v4(ring.slot(k, 1) + static_cast<size_t>(c) * 16);
-                if constexpr (ADDG) gv[v] = ld_shared_v4(ring.slot(k, NT - 1) + static_cast<size_t>(c) * 16);
+                xv[v] = ld_shared_v4(ring.slot(0) + static_cast<size_t>(c) * 16);
+                dyv[v] = ld_shared_v4(ring.slot(1) + static_cast<size_t>(c) * 16);
+                if constexpr (ADDG) gv[v] = ld_shared_v4(ring.slot(NT - 1) + static_cast<size_t>(c) * 16);
             }
         }
         const bool done = bwd_row_body<T, VPT, ADDG>(a, ring.first + k * ring.stride, nvec, xv, dyv, gv,
@@ -241,11 +250,12 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_tma(const BwdArg
             if (abort_flag) return false;
             if (tid == 0 && k + ring.S < ring.nrows) {
                 fence_proxy_async();
-                ring.issue(k + ring.S);
+                ring.issue(k + ring.S, ring.cur);
             }
             return true;
         });
         if (!done) break;
+        ring.advance();
         rs = rs_next;
     }
     if (k < ring.nrows) {

@@ -187,14 +187,14 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT))
     int parity = 0;
     int64_t k = 0;
     for (; k < ring.nrows; ++k) {
-        if (!ring.wait(k, a.faults)) abort_flag = 1;
+        if (!ring.wait(a.faults)) abort_flag = 1;
         uint4 xv[VPT], rv[VPT];
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * nthr + tid;
             if (c < nvec) {
-                xv[v] = ld_shared_v4(ring.slot(k, 0) + static_cast<size_t>(c) * 16);
-                if (FUSED) rv[v] = ld_shared_v4(ring.slot(k, NT - 1) + static_cast<size_t>(c) * 16);
+                xv[v] = ld_shared_v4(ring.slot(0) + static_cast<size_t>(c) * 16);
+                if (FUSED) rv[v] = ld_shared_v4(ring.slot(NT - 1) + static_cast<size_t>(c) * 16);
             }
         }
         const bool done = row_cta_body<T, VPT, FUSED>(
@@ -202,11 +202,12 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT))
                 if (abort_flag) return false;  // written before the barrier: uniform
                 if (tid == 0 && k + ring.S < ring.nrows) {
                     fence_proxy_async();       // our generic reads of the slot come first
-                    ring.issue(k + ring.S);
+                    ring.issue(k + ring.S, ring.cur);
                 }
                 return true;
             });
         if (!done) break;
+        ring.advance();
     }
     // A wait ran out: let the copies already issued land before the CTA's shared memory is
     // released, then leave; the fault word tells the host.

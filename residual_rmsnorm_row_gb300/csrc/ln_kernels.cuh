@@ -629,8 +629,8 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) __maxnreg__(ln_bwd_ring_
 #pragma unroll
         for (int k = 0; k < V; ++k) dw[v][k] = db[v][k] = 0.f;
     }
-    auto vec = [&](int64_t k, int t, int c) {  // vector c of tensor t of row k, from the ring
-        return ld_shared_v4(ring.slot(k, t) + static_cast<size_t>(c) * 16);
+    auto vec = [&](int t, int c) {  // vector c of tensor t of the row under the ring's cursor
+        return ld_shared_v4(ring.slot(t) + static_cast<size_t>(c) * 16);
     };
     int parity = 0;
     int64_t k = 0;
@@ -646,15 +646,15 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) __maxnreg__(ln_bwd_ring_
             mu_next = __ldg(a.mean + nxt);
             rs_next = __ldg(a.rstd + nxt);
         }
-        if (!ring.wait(k, a.faults)) abort_flag = 1;
+        if (!ring.wait(a.faults)) abort_flag = 1;
         float2 sg = splat(0.f), sgx = splat(0.f);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = v * nthr + tid;
             if (c < nvec) {
                 float xf[V], d[V], wf[V];
-                E::unpack(vec(k, 0, c), xf);
-                E::unpack(vec(k, 1, c), d);
+                E::unpack(vec(0, c), xf);
+                E::unpack(vec(1, c), d);
                 E::unpack(ld_keep(w4 + c), wf);
                 ln_bwd_accumulate<V>(xf, d, wf, mu, rs, dw[v], db[v], sg, sgx);
             }
@@ -665,7 +665,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) __maxnreg__(ln_bwd_ring_
         if (abort_flag) break;  // written before the barrier: uniform
         if (tid == 0 && k >= 1 && k - 1 + ring.S < ring.nrows) {
             fence_proxy_async();
-            ring.issue(k - 1 + ring.S);
+            ring.issue(k - 1 + ring.S, ring.prev());
         }
         // and the row after the ring's reach asked into L2, so that its bulk copy finds it there
         // (16384 x 4096 plain: 90.8 -> 86.5 us; 8192 x 8192: 97.1 -> 90.9 plain, 113.3 -> 105.5
@@ -682,19 +682,20 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) __maxnreg__(ln_bwd_ring_
             const int c = v * nthr + tid;
             if (c < nvec) {
                 float xf[V], d[V], wf[V], o[V];
-                E::unpack(vec(k, 0, c), xf);
-                E::unpack(vec(k, 1, c), d);
+                E::unpack(vec(0, c), xf);
+                E::unpack(vec(1, c), d);
                 E::unpack(ld_keep(w4 + c), wf);
                 ln_bwd_dx<V>(xf, d, wf, mu, rs, cx, cc, o);
                 if constexpr (ADDG) {
                     float gg[V];
-                    E::unpack(vec(k, NT - 1, c), gg);
+                    E::unpack(vec(NT - 1, c), gg);
 #pragma unroll
                     for (int j = 0; j < V; ++j) o[j] += gg[j];
                 }
                 st_stream(static_cast<uint4 *>(a.dx) + base + c, E::pack(o));
             }
         }
+        ring.advance();
         mu = mu_next;
         rs = rs_next;
     }

@@ -217,6 +217,8 @@ struct ClusterExchange {
 // (global row first + k * stride, k < nrows) of NT tensors - src[t] + row * row_bytes - and
 // completes on the mbarrier full[k % S]. One thread initialises the barriers and issues the
 // copies; every thread waits. A slot may be refilled once every thread is done reading it.
+// The row being worked on is followed by a cursor (its slot `cur` and the parity `phase` of
+// that slot's fill), advanced once per row, so the hot loop divides nothing by S.
 template <int NT>
 struct RowRing {
     unsigned char *buf;  // S * NT * row_bytes bytes of dynamic shared memory
@@ -225,9 +227,21 @@ struct RowRing {
     uint32_t row_bytes;
     int S;
     int64_t first, stride, nrows;
+    int cur = 0;
+    uint32_t phase = 0;
 
-    __device__ __forceinline__ unsigned char *slot(int64_t k, int t) const {
-        return buf + static_cast<size_t>(static_cast<int>(k % S) * NT + t) * row_bytes;
+    __device__ __forceinline__ unsigned char *at(int s, int t) const {
+        return buf + static_cast<uint32_t>(s * NT + t) * row_bytes;
+    }
+    // tensor t of the row under the cursor
+    __device__ __forceinline__ unsigned char *slot(int t) const { return at(cur, t); }
+    // the slot the cursor held one row earlier
+    __device__ __forceinline__ int prev() const { return cur == 0 ? S - 1 : cur - 1; }
+    __device__ __forceinline__ void advance() {
+        if (++cur == S) {
+            cur = 0;
+            phase ^= 1u;
+        }
     }
     // One thread, before the CTA barrier that precedes any use.
     __device__ __forceinline__ void init() const {
@@ -235,22 +249,23 @@ struct RowRing {
         fence_mbarrier_init();
         fence_proxy_async();
     }
-    // One thread: request row k of every tensor into its slot. The caller has ordered its own
-    // earlier reads of that slot (fence_proxy_async) when the slot is being refilled.
-    __device__ __forceinline__ void issue(int64_t k) const {
-        uint64_t *bar = &full[k % S];
+    // One thread: request row k of every tensor into slot s (= k % S). The caller has ordered
+    // its own earlier reads of that slot (fence_proxy_async) when the slot is being refilled.
+    __device__ __forceinline__ void issue(int64_t k, int s) const {
+        uint64_t *bar = &full[s];
         const int64_t off = (first + k * stride) * static_cast<int64_t>(row_bytes);
         mbar_arrive_expect_tx(bar, NT * row_bytes);
 #pragma unroll
-        for (int t = 0; t < NT; ++t) bulk_g2s(slot(k, t), src[t] + off, row_bytes, bar);
+        for (int t = 0; t < NT; ++t) bulk_g2s(at(s, t), src[t] + off, row_bytes, bar);
     }
     // One thread: fill the ring with the first rows.
     __device__ __forceinline__ void prime() const {
-        for (int64_t k = 0; k < nrows && k < S; ++k) issue(k);
+        for (int s = 0; s < S && s < nrows; ++s) issue(s, s);
     }
-    // Every thread: wait (bounded) until row k has landed; false after a timeout.
-    __device__ __forceinline__ bool wait(int64_t k, unsigned int *faults) const {
-        return mbar_wait(&full[k % S], static_cast<uint32_t>((k / S) & 1), faults);
+    // Every thread: wait (bounded) until the row under the cursor has landed; false after a
+    // timeout.
+    __device__ __forceinline__ bool wait(unsigned int *faults) const {
+        return mbar_wait(&full[cur], phase, faults);
     }
     // One thread, after the CTA gave up at row k: let the copies already issued - rows k to
     // k + ahead - 1 - land before the shared memory is released (each wait bounded again).
