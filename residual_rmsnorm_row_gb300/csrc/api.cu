@@ -776,23 +776,17 @@ int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, con
         if (st != RRN_OK) return st;
         if (l.variant == RRN_VARIANT_ROW_TMA) {
             // The ring refills a slot one row late (ln_bwd_row_tma), so it needs 2 stages or
-            // more: S - 1 rows in flight. Measured on 16384 x 4096 bf16: 3 stages with the
-            // gradient at residual_out (102.6 us vs 108.7 at 2), 2 without (90.8 vs 94.4 at 3);
-            // fewer when more would cost CTAs per SM.
+            // more: S - 1 rows in flight. Measured back to back with as many CTAs per SM as fit,
+            // bf16: 2 stages with or without the gradient at residual_out (16384 x 4096: 92.5 us
+            // fused vs 95.1 at 3, 77.2 plain vs 84.9; 32768 x 2048 fused: 92.0 vs 94.5).
             const int want = cfg ? cfg->stages : 0;
             if (want < 0 || want == 1 || want > kMaxStages || 2 * slot > kMaxDynSmem) return RRN_ERR_CONFIG;
-            auto occ_at = [&](int S) {
-                Launch t = l;
-                t.stages = S;
-                t.smem = static_cast<int>(S * slot);
-                return S * slot <= kMaxDynSmem ? occupancy_ln(true, dtype, add_grad, t) : 0;
-            };
-            int S = want ? want : add_grad ? 3 : 2;
-            ring_occ = occ_at(S);
-            if (!want && ring_occ < occ_at(2)) {
-                S = 2;
-                ring_occ = occ_at(2);
-            }
+            const int S = want ? want : 2;
+            if (S * slot > kMaxDynSmem) return RRN_ERR_CONFIG;
+            Launch t = l;
+            t.stages = S;
+            t.smem = static_cast<int>(S * slot);
+            ring_occ = occupancy_ln(true, dtype, add_grad, t);
             if (ring_occ < 1) return RRN_ERR_CONFIG;
             l.stages = S;
             l.smem = static_cast<int>(S * slot);

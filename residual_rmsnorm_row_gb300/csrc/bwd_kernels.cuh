@@ -61,7 +61,7 @@ __device__ __forceinline__ bool bwd_row_body(const BwdArgs &a, int64_t row, int 
     const float dot = cta_sum(dot2.x + dot2.y, slots[parity]);
     parity ^= 1;
     if (!after_reduce()) return false;
-    const float cm = dot / static_cast<float>(a.N);
+    const float cm = dot * (1.f / static_cast<float>(a.N));  // 1 / N is hoisted out of the row loop
     const int64_t base = row * nvec;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
@@ -297,7 +297,7 @@ __device__ __forceinline__ void bwd_row_split_body(const BwdArgs &a) {
     const int c1 = min(nvec, c0 + chunk);
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
-    const float n_f = static_cast<float>(a.N);
+    const float inv_n = 1.f / static_cast<float>(a.N);
     const uint4 *x4 = static_cast<const uint4 *>(a.x);
     const uint4 *dy4 = static_cast<const uint4 *>(a.dy);
     const uint4 *g4 = static_cast<const uint4 *>(a.d_ro);
@@ -362,7 +362,7 @@ __device__ __forceinline__ void bwd_row_split_body(const BwdArgs &a) {
         }
         dot = cta_sum(dot, slots[parity]);
         parity ^= 1;
-        const float cm = exchange(dot, 0.f, [](float u, float v) { return u + v; }, a.faults) / n_f;
+        const float cm = exchange(dot, 0.f, [](float u, float v) { return u + v; }, a.faults) * inv_n;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = c0 + v * nthr + tid;
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(1024) bwd_stream(const BwdArgs a) {
     const int nchunk = a.N / V;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
-    const float n_f = static_cast<float>(a.N);
+    const float inv_n = 1.f / static_cast<float>(a.N);
     float *prow = a.partial + static_cast<int64_t>(blockIdx.x) * a.N;
 
     int parity = 0;
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(1024) bwd_stream(const BwdArgs a) {
         }
         dot = cta_sum(dot, slots[parity]);
         parity ^= 1;
-        const float cm = dot / n_f;
+        const float cm = dot * inv_n;
         const bool first = (row == blockIdx.x);
         for (int c = tid; c < nchunk; c += nthr) {
             float xf[W], df[W], wf[W], o[W];

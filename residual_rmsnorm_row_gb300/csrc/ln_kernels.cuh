@@ -477,7 +477,7 @@ __device__ __forceinline__ void ln_bwd_row_body(const LnBwdArgs &a, int64_t row,
     constexpr int V = E::kPerVec;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
-    const float n_f = static_cast<float>(a.N);
+    const float inv_n = 1.f / static_cast<float>(a.N);
     const uint4 *w4 = static_cast<const uint4 *>(a.w);
     float2 sg = splat(0.f), sgx = splat(0.f);
 #pragma unroll
@@ -493,7 +493,7 @@ __device__ __forceinline__ void ln_bwd_row_body(const LnBwdArgs &a, int64_t row,
     }
     const float2 t = cta_sum2(sg.x + sg.y, sgx.x + sgx.y, slots[parity]);
     parity ^= 1;
-    const float cx = -rs * (t.y / n_f), cc = -rs * (t.x / n_f);
+    const float cx = -rs * (t.y * inv_n), cc = -rs * (t.x * inv_n);
     const int64_t base = row * nvec;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
@@ -600,7 +600,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) __maxnreg__(ln_bwd_ring_
     const int nvec = a.N / V;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
-    const float n_f = static_cast<float>(a.N);
+    const float inv_n = 1.f / static_cast<float>(a.N);  // the row means below: one product each
     const uint4 *w4 = static_cast<const uint4 *>(a.w);
     RowRing<NT> ring;
     ring.buf = ring_buf;
@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) __maxnreg__(ln_bwd_ring_
 #pragma unroll
             for (int t = 0; t < NT; ++t) prefetch_l2_bulk(ring.src[t] + off, ring.row_bytes);
         }
-        const float cx = -rs * (t.y / n_f), cc = -rs * (t.x / n_f);
+        const float cx = -rs * (t.y * inv_n), cc = -rs * (t.x * inv_n);
         const int64_t base = (ring.first + k * ring.stride) * nvec;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
@@ -733,7 +733,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_split(const L
     const int c1 = min(nvec, c0 + chunk);
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
-    const float n_f = static_cast<float>(a.N);
+    const float inv_n = 1.f / static_cast<float>(a.N);
     const uint4 *w4 = static_cast<const uint4 *>(a.w);
     if (tid == 0) xchg.init();
     cluster_sync();  // every CTA of the cluster runs and has its barriers initialised
@@ -793,7 +793,7 @@ __global__ void __launch_bounds__(bwd_max_threads(VPT)) ln_bwd_row_split(const L
         const float2 tt = xchg(t, make_float2(0.f, 0.f),
                                [](float2 u, float2 v) { return make_float2(u.x + v.x, u.y + v.y); },
                                a.faults);
-        const float cx = -rs * (tt.y / n_f), cc = -rs * (tt.x / n_f);
+        const float cx = -rs * (tt.y * inv_n), cc = -rs * (tt.x * inv_n);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             const int c = c0 + v * nthr + tid;
@@ -843,7 +843,7 @@ __global__ void __launch_bounds__(1024) ln_bwd_stream(const LnBwdArgs a) {
     const int nchunk = a.N / V;
     const int tid = threadIdx.x;
     const int nthr = blockDim.x;
-    const float n_f = static_cast<float>(a.N);
+    const float inv_n = 1.f / static_cast<float>(a.N);
     float *pw = a.partial + static_cast<int64_t>(blockIdx.x) * a.N;
     float *pb = a.partial + (static_cast<int64_t>(gridDim.x) + blockIdx.x) * a.N;
 
@@ -877,7 +877,7 @@ __global__ void __launch_bounds__(1024) ln_bwd_stream(const LnBwdArgs a) {
         }
         const float2 t = cta_sum2(sg, sgx, slots[parity]);
         parity ^= 1;
-        const float mg = t.x / n_f, mgx = t.y / n_f;
+        const float mg = t.x * inv_n, mgx = t.y * inv_n;
         const bool first = (row == blockIdx.x);
         for (int c = tid; c < nchunk; c += nthr) {
             float xf[W], df[W], wf[W], o[W];
