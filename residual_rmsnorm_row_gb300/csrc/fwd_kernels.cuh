@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT))
 // walk rows with a grid-sized stride. For rows too wide for one CTA's registers, and to spread
 // few-row (decode) problems over more SMs.
 template <typename T, int VPT, bool FUSED>
-__global__ void __launch_bounds__(fwd_max_threads(VPT)) fwd_row_cluster(const FwdArgs a) {
+__device__ __forceinline__ void fwd_row_cluster_body(const FwdArgs &a) {
     pdl_enter();
     using E = Elem<T>;
     constexpr int V = E::kPerVec;
@@ -332,6 +332,20 @@ __global__ void __launch_bounds__(fwd_max_threads(VPT)) fwd_row_cluster(const Fw
         if (q == 0 && tid == 0 && a.rstd) a.rstd[row] = rs;
     }
     cluster_sync();  // no CTA exits while a peer may still write into its shared memory
+}
+
+// The cluster kernel; at 8 vectors a thread compiled for 2 CTAs of 256 threads (at most 128
+// registers instead of 166 with a residual, 88 bytes of it spilled to local memory: 4 CTAs of
+// 128 threads per SM instead of 3; 4096 x 65536 bf16 with a residual 369.8 -> 350.3 us). Fewer
+// vectors a thread keep the compiler's own allocation (the same bound there cost 6-7 % on
+// 16384- and 32768-wide rows).
+template <typename T, int VPT, bool FUSED>
+__global__ void __launch_bounds__(fwd_max_threads(VPT)) fwd_row_cluster(const FwdArgs a) {
+    fwd_row_cluster_body<T, VPT, FUSED>(a);
+}
+template <typename T, bool FUSED>
+__global__ void __launch_bounds__(fwd_max_threads(8), 2) fwd_row_cluster_v8(const FwdArgs a) {
+    fwd_row_cluster_body<T, 8, FUSED>(a);
 }
 
 template <typename T, int VPT, bool FUSED>
@@ -562,7 +576,7 @@ const void *fwd_kernel_ptr(const Launch &l) {
                 case 1: return reinterpret_cast<const void *>(&fwd_row_cluster<T, 1, FUSED>);
                 case 2: return reinterpret_cast<const void *>(&fwd_row_cluster<T, 2, FUSED>);
                 case 4: return reinterpret_cast<const void *>(&fwd_row_cluster<T, 4, FUSED>);
-                case 8: return reinterpret_cast<const void *>(&fwd_row_cluster<T, 8, FUSED>);
+                case 8: return reinterpret_cast<const void *>(&fwd_row_cluster_v8<T, FUSED>);
                 default: return nullptr;
             }
         case RRN_VARIANT_ROW_TMA:
