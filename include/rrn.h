@@ -283,7 +283,9 @@ RRN_API int rrn_selftest_wait_timeout(uint64_t limit_ns, rrn_stream_t stream);
 typedef enum {
     RRN_VARIANT_AUTO = 0,    /* let the library choose */
     RRN_VARIANT_ROW_CTA = 1, /* one row per CTA, row held in registers, 128-bit vectors */
-    RRN_VARIANT_ROW_WARP = 2,/* one row per warp, row held in registers, 128-bit vectors */
+    RRN_VARIANT_ROW_WARP = 2,/* one row per warp, row held in registers, 128-bit vectors
+                                (rows of at most 8 x 32 vectors; the RMSNorm, fp8 and LayerNorm
+                                forwards) */
     RRN_VARIANT_STREAM = 3,  /* one row per CTA, two passes over the row (any N / alignment) */
     RRN_VARIANT_ROW_TMA = 4, /* persistent row per CTA fed by bulk async copies (TMA engine)
                                 into a shared-memory ring of `stages` rows, 128-bit vectors */
@@ -349,16 +351,16 @@ RRN_API int add_rmsnorm_fwd_ex(const void *x, const void *residual, void *residu
                                const void *w, void *y, float *rstd, int64_t M, int64_t N,
                                float eps, int dtype, const rrn_launch *cfg, rrn_stream_t stream);
 
-/* rmsnorm_fwd_fp8 with an explicit launch configuration (row-per-CTA, cluster split or
- * two-pass). */
+/* rmsnorm_fwd_fp8 with an explicit launch configuration (row-per-CTA, row-per-warp, cluster
+ * split or two-pass). */
 RRN_API int rmsnorm_fwd_fp8_ex(const void *x, const void *residual, void *residual_out,
                                const void *w, void *q, float *scale, float *rstd, int64_t M,
                                int64_t N, float eps, int dtype, const rrn_launch *cfg,
                                rrn_stream_t stream);
 
-/* LayerNorm with an explicit launch configuration: the forward row-per-CTA or two-pass; the
- * backward also the TMA ring (ROW_TMA) and the cluster split (ROW_CLUSTER; workspace: one dw and
- * one db row per cluster). */
+/* LayerNorm with an explicit launch configuration: the forward row-per-CTA, row-per-warp or
+ * two-pass; the backward row-per-CTA, two-pass, the TMA ring (ROW_TMA) and the cluster split
+ * (ROW_CLUSTER; workspace: one dw and one db row per cluster). */
 RRN_API int add_layernorm_fwd_ex(const void *x, const void *residual, void *residual_out,
                                  const void *w, const void *b, void *y, float *mean, float *rstd,
                                  int64_t M, int64_t N, float eps, int dtype, const rrn_launch *cfg,

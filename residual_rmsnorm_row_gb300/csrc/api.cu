@@ -181,6 +181,10 @@ constexpr int kLnBwdSplitThreads = 128;
 constexpr int kLnBwdMinRingThreads = 128;
 // Widest row (in 128-bit vectors) one CTA holds in registers: 8 vectors x 256 threads.
 constexpr int kRowCtaMaxVec = 2048;
+constexpr int kLnFwdMaxVpt = 4;         // LayerNorm forward row layouts (plan_ln_fwd)
+constexpr int kLnFwdTargetThreads = 64;
+// fp8 output: one row per warp up to this many vectors over many rows (plan_quant)
+constexpr int kQuantWarpMaxVec = 256;
 // Vectors of a row each CTA of the cluster split takes when the planner chooses the cluster
 // size, for the fused forward (two input rows): measured best at 4 vectors x 128 threads a CTA.
 // The plain forward (one input row) keeps the same bytes in flight per thread with twice as
@@ -674,14 +678,37 @@ int plan_ln_fwd(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const 
     if (st != RRN_OK) return st;
     Launch l{};
     l.variant = cfg && cfg->variant ? cfg->variant : RRN_VARIANT_AUTO;
-    if (l.variant == RRN_VARIANT_AUTO)
-        l.variant = vec_ok && nvec <= kRowCtaMaxVec ? RRN_VARIANT_ROW_CTA : RRN_VARIANT_STREAM;
+    if (l.variant == RRN_VARIANT_AUTO) {
+        // Measured on bf16 rows with a residual and bias (64 Mi elements, back to back): a row
+        // per warp up to 128 vectors over many rows (512 columns 200.9 -> 84.6 us, 768 142.9 ->
+        // 95.1, 1024 120.6 -> 85.7 against a row per CTA; 2048: 96.2 against 86.6 for a CTA of
+        // 4 x 64), a row per CTA up to kRowCtaMaxVec, the two-pass kernel beyond.
+        if (!vec_ok) l.variant = RRN_VARIANT_STREAM;
+        else if (nvec <= 32 * kLnFwdMaxVpt && M >= 4LL * sms) l.variant = RRN_VARIANT_ROW_WARP;
+        else if (nvec <= kRowCtaMaxVec) l.variant = RRN_VARIANT_ROW_CTA;
+        else l.variant = RRN_VARIANT_STREAM;
+    }
     l.vec = l.variant == RRN_VARIANT_STREAM ? vec_ok : true;
     if (l.variant == RRN_VARIANT_ROW_CTA) {
         if (!vec_ok) return RRN_ERR_CONFIG;
-        st = pick_row_layout(nvec, M, sms, cfg, kMaxVpt, fwd_threads_limit, kFwdTargetThreads, &l);
+        // 4 vectors a thread (more threads instead) from 256 vectors up: the LayerNorm row
+        // kernel keeps more per-row state than RMSNorm's, and 8 vectors a thread took 141-175
+        // registers, 2 CTAs per SM (bf16 with a residual and bias, back to back: 6144 columns
+        // 135.4 -> 84.8 us at 4 x 192, 8192 columns 109.7 -> 85.3 at 4 x 256, 12288 columns
+        // 149.1 -> 88.5 at 4 x 384; 2048 columns 92.9 -> 86.6 at 4 x 64 instead of 2 x 128)
+        // (given explicitly, 8 vectors a thread still run)
+        st = pick_row_layout(nvec, M, sms, cfg, cfg && cfg->vpt ? kMaxVpt : kLnFwdMaxVpt, fwd_threads_limit,
+                             kLnFwdTargetThreads, &l);
         if (st != RRN_OK) return st;
         l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid(M);
+    } else if (l.variant == RRN_VARIANT_ROW_WARP) {
+        if (!vec_ok) return RRN_ERR_CONFIG;
+        l.vpt = cfg && cfg->vpt ? cfg->vpt : ceil_pow2_vpt((nvec + 31) / 32, kMaxVpt);
+        if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4 && l.vpt != 8) return RRN_ERR_CONFIG;
+        if (static_cast<int64_t>(l.vpt) * 32 < nvec) return RRN_ERR_CONFIG;
+        l.threads = cfg && cfg->threads ? cfg->threads : 128;
+        if (l.threads < 32 || l.threads % 32 || l.threads > 256) return RRN_ERR_CONFIG;
+        l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid((M + l.threads / 32 - 1) / (l.threads / 32));
     } else if (l.variant == RRN_VARIANT_STREAM) {
         l.vpt = 1;
         const int64_t chunks = l.vec ? nvec : N;
@@ -695,7 +722,7 @@ int plan_ln_fwd(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const 
             l.ctas = clamp_grid(M < cap ? M : cap);
         }
     } else {
-        return RRN_ERR_CONFIG;  // LayerNorm runs the row-per-CTA and two-pass variants
+        return RRN_ERR_CONFIG;  // the LayerNorm forward runs the row-per-CTA, row-per-warp and two-pass variants
     }
     if (l.ctas < 1) return RRN_ERR_CONFIG;
     *out = l;
@@ -865,13 +892,16 @@ int plan_quant(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const r
     Launch l{};
     l.variant = cfg && cfg->variant ? cfg->variant : RRN_VARIANT_AUTO;
     if (l.variant == RRN_VARIANT_AUTO) {
-        // as the forward: one row per CTA while the CTA holds it, wider rows split over a
-        // cluster, wider still the two-pass kernel
+        // as the forward: one row per warp for short rows over many rows (bf16 with a residual,
+        // 64 Mi elements, back to back: 512 columns 198.1 -> 74.3 us, 1024 110.0 -> 71.7, 2048
+        // 77.4 -> 72.1 against a row per CTA), one row per CTA while the CTA holds it, wider rows
+        // split over a cluster, wider still the two-pass kernel
         const int64_t cta_max = M < 2LL * sms || !fused ? kRowCtaMaxVec : 128 * kMaxVpt;
-        l.variant = !vec_ok          ? RRN_VARIANT_STREAM
-                    : nvec <= cta_max ? RRN_VARIANT_ROW_CTA
-                    : nvec <= 2 * kClusterMaxVec ? RRN_VARIANT_ROW_CLUSTER
-                                                 : RRN_VARIANT_STREAM;
+        l.variant = !vec_ok                                  ? RRN_VARIANT_STREAM
+                    : nvec <= kQuantWarpMaxVec && M >= 4LL * sms ? RRN_VARIANT_ROW_WARP
+                    : nvec <= cta_max                        ? RRN_VARIANT_ROW_CTA
+                    : nvec <= 2 * kClusterMaxVec             ? RRN_VARIANT_ROW_CLUSTER
+                                                             : RRN_VARIANT_STREAM;
     }
     l.vec = l.variant == RRN_VARIANT_STREAM ? vec_ok : true;
     auto occ = [&](const Launch &t) {
@@ -882,6 +912,14 @@ int plan_quant(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const r
         st = pick_row_layout(nvec, M, sms, cfg, kMaxVpt, fwd_threads_limit, kFwdTargetThreads, &l);
         if (st != RRN_OK) return st;
         l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid(M);
+    } else if (l.variant == RRN_VARIANT_ROW_WARP) {
+        if (!vec_ok) return RRN_ERR_CONFIG;
+        l.vpt = cfg && cfg->vpt ? cfg->vpt : ceil_pow2_vpt((nvec + 31) / 32, kMaxVpt);
+        if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4 && l.vpt != 8) return RRN_ERR_CONFIG;
+        if (static_cast<int64_t>(l.vpt) * 32 < nvec) return RRN_ERR_CONFIG;
+        l.threads = cfg && cfg->threads ? cfg->threads : 128;
+        if (l.threads < 32 || l.threads % 32 || l.threads > 256) return RRN_ERR_CONFIG;
+        l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid((M + l.threads / 32 - 1) / (l.threads / 32));
     } else if (l.variant == RRN_VARIANT_ROW_CLUSTER) {
         if (!vec_ok) return RRN_ERR_CONFIG;
         // chunks above 512 vectors: 256-thread CTAs (4096 x 65536 bf16 with a residual: 294 us

@@ -97,6 +97,12 @@ __device__ __forceinline__ void r_of(const uint4 &xv, const uint4 &rv,
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) { __stcs(p, v); }
 __device__ __forceinline__ uint4 ld_keep(const uint4 *p) { return __ldg(p); }
+// The same bits, opaque to the compiler: a loop-invariant packed vector passed through this in
+// the loop is unpacked there, rather than once before the loop into twice the registers.
+__device__ __forceinline__ uint4 opaque(uint4 v) {
+    asm volatile("" : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w));
+    return v;
+}
 // Pull a line into L1 ahead of its use, without holding a register for it.
 __device__ __forceinline__ void prefetch_l1(const void *p) {
     asm volatile("prefetch.global.L1 [%0];" ::"l"(p));

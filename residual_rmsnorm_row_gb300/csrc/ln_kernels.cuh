@@ -42,8 +42,8 @@ __device__ __forceinline__ float2 cta_sum2(float a, float b, float (*slots)[32])
 // The row statistics from per-thread access to the row values: `each(fn)` calls fn(v) for
 // every fp32 value of the row this thread owns. Returns (mean, rstd) as a reference value m0,
 // a small correction corr (mean = m0 + corr) and rstd: deviations are formed as
-// (r - m0) - corr, so the fp32 rounding of the mean itself never enters them. Reductions
-// alternate between the two slot pairs (parity), as cta_sum callers do.
+// (r - m0) - corr, so the fp32 rounding of the mean itself never enters them. The reductions
+// are those of `red` (CtaReduce or WarpReduce, below).
 // ln_stats_two_pass: pass 1 gives a first mean m0 = sum(r) / N; pass 2 sums d = r - m0 and d^2
 // together (one barrier) and corrects both: corr = sum(d) / N and
 // sum((r - mean)^2) = sum(d^2) - sum(d)^2 / N (the corrected two-pass algorithm), so the
@@ -56,6 +56,34 @@ struct LnStats {
     float rstd;
     __device__ __forceinline__ float mean() const { return m0 + corr; }
     __device__ __forceinline__ float dev(float r) const { return (r - m0) - corr; }
+};
+
+// The reductions the statistics take, over the CTA (two slot pairs in shared memory, used
+// alternately, as cta_sum callers do) or over one warp (shuffles only, for a row per warp). Both
+// add in a fixed order, so every thread of the group gets the same bits.
+struct CtaReduce {
+    float (&slots)[2][2][32];
+    int &parity;
+    __device__ __forceinline__ float sum(float v) {
+        const float t = cta_sum(v, slots[parity][0]);
+        parity ^= 1;
+        return t;
+    }
+    __device__ __forceinline__ float max(float v) {
+        const float t = cta_max(v, slots[parity][0]);
+        parity ^= 1;
+        return t;
+    }
+    __device__ __forceinline__ float2 sum2(float a, float b) {
+        const float2 t = cta_sum2(a, b, slots[parity]);
+        parity ^= 1;
+        return t;
+    }
+};
+struct WarpReduce {
+    __device__ __forceinline__ float sum(float v) const { return warp_sum(v); }
+    __device__ __forceinline__ float max(float v) const { return warp_max(v); }
+    __device__ __forceinline__ float2 sum2(float a, float b) const { return make_float2(warp_sum(a), warp_sum(b)); }
 };
 
 // The shift of the one-step statistics: the mean of the row's first min(N, 8) values r (formed
@@ -99,26 +127,22 @@ __device__ __forceinline__ float ln_shift_vec(const void *x, const void *res, in
 }
 
 // The corrected two-pass statistics (the fallback of ln_stats).
-template <typename Each>
-__device__ __forceinline__ LnStats ln_stats_two_pass(Each each, float n_f, float eps,
-                                                  float (&slots)[2][2][32], int &parity) {
+template <typename Red, typename Each>
+__device__ __forceinline__ LnStats ln_stats_two_pass(Each each, float n_f, float eps, Red &red) {
     float s1 = 0.f;
     each([&](float v) { s1 += v; });
-    s1 = cta_sum(s1, slots[parity][0]);
-    parity ^= 1;
+    s1 = red.sum(s1);
     float m0;
     if (isfinite(s1)) {
         m0 = s1 / n_f;
     } else {  // rare: the sum overflowed fp32 - add the row scaled by a power of two
         float am = 0.f;
         each([&](float v) { am = fmaxf(am, fabsf(v)); });
-        am = cta_max(am, slots[parity][0]);
-        parity ^= 1;
+        am = red.max(am);
         const int e = rescale_exponent(am);
         float t = 0.f;
         each([&](float v) { t += ldexpf(v, -e); });
-        t = cta_sum(t, slots[parity][0]);
-        parity ^= 1;
+        t = red.sum(t);
         m0 = ldexpf(t / n_f, e);
     }
     float d1 = 0.f, d2 = 0.f;
@@ -127,8 +151,7 @@ __device__ __forceinline__ LnStats ln_stats_two_pass(Each each, float n_f, float
         d1 += d;
         d2 = fmaf(d, d, d2);
     });
-    const float2 t2 = cta_sum2(d1, d2, slots[parity]);
-    parity ^= 1;
+    const float2 t2 = red.sum2(d1, d2);
     LnStats st;
     st.m0 = m0;
     st.corr = isfinite(t2.x) ? t2.x / n_f : 0.f;
@@ -139,16 +162,14 @@ __device__ __forceinline__ LnStats ln_stats_two_pass(Each each, float n_f, float
     } else {  // rare: squared deviations out of fp32 range, or a constant row
         float am = 0.f;
         each([&](float v) { am = fmaxf(am, fabsf(st.dev(v))); });
-        am = cta_max(am, slots[parity][0]);
-        parity ^= 1;
+        am = red.max(am);
         const int e = rescale_exponent(am);
         float t = 0.f;
         each([&](float v) {
             const float d = ldexpf(st.dev(v), -e);
             t = fmaf(d, d, t);
         });
-        t = cta_sum(t, slots[parity][0]);
-        parity ^= 1;
+        t = red.sum(t);
         rs = rstd_rescaled(t, n_f, eps, e);
     }
     st.rstd = rs;
@@ -167,11 +188,10 @@ __device__ __forceinline__ LnStats ln_stats_two_pass(Each each, float n_f, float
 // ln_stats_shifted takes this thread's sums d1 = sum(r - K), d2 = sum((r - K)^2), which a kernel
 // may have formed in a pass of its own (the row-per-CTA forward forms them while it stores
 // residual_out); ln_stats forms them itself.
-template <typename Each>
+template <typename Red, typename Each>
 __device__ __forceinline__ LnStats ln_stats_shifted(Each each, float K, float d1, float d2, float n_f,
-                                                    float eps, float (&slots)[2][2][32], int &parity) {
-    const float2 t = cta_sum2(d1, d2, slots[parity]);
-    parity ^= 1;
+                                                    float eps, Red &red) {
+    const float2 t = red.sum2(d1, d2);
     if (isfinite(t.x) && !needs_rescale(t.y)) {
         const float corr = t.x / n_f;
         const float ssd = t.y - t.x * corr;
@@ -183,19 +203,18 @@ __device__ __forceinline__ LnStats ln_stats_shifted(Each each, float K, float d1
             return st;
         }
     }
-    return ln_stats_two_pass(each, n_f, eps, slots, parity);
+    return ln_stats_two_pass(each, n_f, eps, red);
 }
 
-template <typename Each>
-__device__ __forceinline__ LnStats ln_stats(Each each, float K, float n_f, float eps,
-                                            float (&slots)[2][2][32], int &parity) {
+template <typename Red, typename Each>
+__device__ __forceinline__ LnStats ln_stats(Each each, float K, float n_f, float eps, Red &red) {
     float d1 = 0.f, d2 = 0.f;
     each([&](float v) {
         const float d = v - K;
         d1 += d;
         d2 = fmaf(d, d, d2);
     });
-    return ln_stats_shifted(each, K, d1, d2, n_f, eps, slots, parity);
+    return ln_stats_shifted(each, K, d1, d2, n_f, eps, red);
 }
 
 // The forward's per-vector arithmetic, in packed fp32 pairs (PACKED) or one value at a time;
@@ -321,7 +340,8 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) ln_fwd_row_cta(const LnFwdArgs a)
                     for (int k = 0; k < V; ++k) fn(f[k]);
                 }
         };
-        const LnStats st = ln_stats_shifted(each, K, d1.x + d1.y, d2.x + d2.y, n_f, a.eps, slots, parity);
+        CtaReduce red{slots, parity};
+        const LnStats st = ln_stats_shifted(each, K, d1.x + d1.y, d2.x + d2.y, n_f, a.eps, red);
         const float ncr = -st.corr * st.rstd;
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
@@ -343,6 +363,103 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) ln_fwd_row_cta(const LnFwdArgs a)
             }
         }
         if (tid == 0) {
+            if (a.mean) a.mean[row] = st.mean();
+            if (a.rstd) a.rstd[row] = st.rstd;
+        }
+    }
+}
+
+// Row per warp, for short rows over many rows (as the RMSNorm forward's fwd_row_warp): lane l
+// owns vectors v * 32 + l, the statistics are warp-wide (shuffles, no barrier), and warps walk
+// rows with a grid-sized stride. Nothing but the row's own loads stands before its arithmetic:
+// w and b are loaded into registers once, and the shift K (the mean of the row's first 8
+// values, added up per vector and then over the lanes that hold them) is passed round by
+// shuffles from the lanes that loaded those values.
+template <typename T, int VPT, bool FUSED>
+__global__ void __launch_bounds__(256) ln_fwd_row_warp(const LnFwdArgs a) {
+    pdl_enter();
+    using E = Elem<T>;
+    constexpr int V = E::kPerVec;
+    constexpr int KL = (8 + V - 1) / V;  // lanes whose vector 0 holds the row's first 8 values
+    constexpr bool P = VPT >= 4;  // packed fp32 pairs
+    const int nvec = a.N / V;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const float n_f = static_cast<float>(a.N);
+    const int nk = a.N < 8 ? a.N : 8;
+    const float inv_nk = 1.f / static_cast<float>(nk);
+    uint4 wv[VPT], bv[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * 32 + lane;
+        if (c < nvec) {
+            wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
+            bv[v] = a.b ? ld_keep(static_cast<const uint4 *>(a.b) + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    WarpReduce red;
+    for (int64_t row = warp0; row < a.M; row += nwarps) {
+        const int64_t base = row * nvec;
+        uint4 xv[VPT], rv[VPT];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * 32 + lane;
+            if (c < nvec) {
+                xv[v] = ld_stream(static_cast<const uint4 *>(a.x) + base + c);
+                if (FUSED) rv[v] = ld_stream(static_cast<const uint4 *>(a.res) + base + c);
+            }
+        }
+        float ks = 0.f;
+        if (lane < KL && lane < nvec) {
+            float f[V];
+            r_of<T, FUSED>(xv[0], rv[0], f);
+#pragma unroll
+            for (int k = 0; k < V; ++k)
+                if (lane * V + k < nk) ks += f[k];
+        }
+        float K = __shfl_sync(0xffffffffu, ks, 0);
+#pragma unroll
+        for (int l = 1; l < KL; ++l) K += __shfl_sync(0xffffffffu, ks, l);
+        K *= inv_nk;
+        // (residual_out may be the buffer of x or residual: each lane stores only the vectors it
+        // has itself loaded, and the values K is formed from travelled by shuffle)
+        float2 d1 = splat(0.f), d2 = splat(0.f);  // sums of d = r - K and d^2
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * 32 + lane;
+            if (c < nvec) {
+                float f[V];
+                ln_r_of<T, FUSED, P>(xv[v], rv[v], f);
+                if (FUSED) st_stream(static_cast<uint4 *>(a.res_out) + base + c, E::pack(f));
+                ln_moments<V, P>(f, K, d1, d2);
+            }
+        }
+        auto each = [&](auto fn) {
+#pragma unroll
+            for (int v = 0; v < VPT; ++v)
+                if (v * 32 + lane < nvec) {
+                    float f[V];
+                    r_of<T, FUSED>(xv[v], rv[v], f);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) fn(f[k]);
+                }
+        };
+        const LnStats st = ln_stats_shifted(each, K, d1.x + d1.y, d2.x + d2.y, n_f, a.eps, red);
+        const float ncr = -st.corr * st.rstd;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * 32 + lane;
+            if (c < nvec) {
+                float f[V], wf[V], bf[V], o[V];
+                ln_r_of<T, FUSED, P>(xv[v], rv[v], f);
+                E::unpack(opaque(wv[v]), wf);
+                E::unpack(opaque(bv[v]), bf);
+                ln_out<V, P>(f, wf, bf, st.m0, st.rstd, ncr, o);
+                st_stream(static_cast<uint4 *>(a.y) + base + c, E::pack(o));
+            }
+        }
+        if (lane == 0) {
             if (a.mean) a.mean[row] = st.mean();
             if (a.rstd) a.rstd[row] = st.rstd;
         }
@@ -389,7 +506,8 @@ __global__ void __launch_bounds__(1024) ln_fwd_stream(const LnFwdArgs a) {
             }
         };
         const float K = ln_shift<T, FUSED>(a.x, a.res, base, a.N);
-        const LnStats st = ln_stats(each, K, n_f, a.eps, slots, parity);
+        CtaReduce red{slots, parity};
+        const LnStats st = ln_stats(each, K, n_f, a.eps, red);
         for (int c = tid; c < nchunk; c += nthr) {
             float f[W], wf[W], bf[W], o[W];
             load_r(base, c, f);
@@ -933,6 +1051,14 @@ const void *ln_fwd_kernel_ptr(const Launch &l) {
                 case 8: return reinterpret_cast<const void *>(&ln_fwd_row_cta<T, 8, FUSED>);
                 default: return nullptr;
             }
+        case RRN_VARIANT_ROW_WARP:
+            switch (l.vpt) {
+                case 1: return reinterpret_cast<const void *>(&ln_fwd_row_warp<T, 1, FUSED>);
+                case 2: return reinterpret_cast<const void *>(&ln_fwd_row_warp<T, 2, FUSED>);
+                case 4: return reinterpret_cast<const void *>(&ln_fwd_row_warp<T, 4, FUSED>);
+                case 8: return reinterpret_cast<const void *>(&ln_fwd_row_warp<T, 8, FUSED>);
+                default: return nullptr;
+            }
         case RRN_VARIANT_STREAM:
             return l.vec ? reinterpret_cast<const void *>(&ln_fwd_stream<T, true, FUSED>)
                          : reinterpret_cast<const void *>(&ln_fwd_stream<T, false, FUSED>);
@@ -978,7 +1104,7 @@ cudaError_t launch_ln_fwd(const LnFwdArgs &a, const Launch &l, cudaStream_t stre
     if (!k) return cudaErrorInvalidConfiguration;
     LnFwdArgs args = a;
     void *params[] = {&args};
-    return enqueue(k, l, 0, l.variant == RRN_VARIANT_ROW_CTA, params, stream);
+    return enqueue(k, l, 0, l.variant == RRN_VARIANT_ROW_CTA || l.variant == RRN_VARIANT_ROW_WARP, params, stream);
 }
 
 // Stage 1, then stage 2 twice (dw from the first workspace half, db from the second).

@@ -36,6 +36,21 @@ __device__ __forceinline__ float rms_rstd(Each each, float ss, float n_f, float 
     return rstd_rescaled(s2, n_f, eps, e);
 }
 
+// rms_rstd over one warp (a row per warp): the warp-wide sum of squares, shuffles only.
+template <typename Each>
+__device__ __forceinline__ float rms_rstd_warp(Each each, float ss, float n_f, float eps) {
+    if (!needs_rescale(ss)) return rstd_plain(ss, n_f, eps);
+    float am = 0.f;
+    each([&](float v) { am = fmaxf(am, fabsf(v)); });
+    const int e = rescale_exponent(warp_max(am));
+    float s2 = 0.f;
+    each([&](float v) {
+        const float t = ldexpf(v, -e);
+        s2 = fmaf(t, t, s2);
+    });
+    return rstd_rescaled(warp_sum(s2), n_f, eps, e);
+}
+
 __device__ __forceinline__ uint16_t e4m3x2(float a, float b) {
     return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
@@ -170,6 +185,100 @@ __global__ void __maxnreg__(fwd_max_regs(VPT)) quant_row_cta(const QuantArgs a) 
             }
         }
         if (tid == 0) {
+            a.scale[row] = am / 448.f;
+            if (a.rstd) a.rstd[row] = rs;
+        }
+    }
+}
+
+// Row per warp, for short rows over many rows (as the forward's fwd_row_warp): w in registers
+// (loaded once), the row's sum(r^2) and max|r * w| warp-wide (shuffles, no barrier), rows walked
+// with a grid-sized stride; otherwise the arithmetic of quant_row_cta.
+template <typename T, int VPT, bool FUSED>
+__global__ void __launch_bounds__(256) quant_row_warp(const QuantArgs a) {
+    pdl_enter();
+    using E = Elem<T>;
+    constexpr int V = E::kPerVec;
+    const int nvec = a.N / V;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const float n_f = static_cast<float>(a.N);
+    uint4 wv[VPT];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * 32 + lane;
+        if (c < nvec) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
+    }
+    for (int64_t row = warp0; row < a.M; row += nwarps) {
+        const int64_t base = row * nvec;
+        uint4 xv[VPT], rv[VPT];
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * 32 + lane;
+            if (c < nvec) {
+                xv[v] = ld_stream(static_cast<const uint4 *>(a.x) + base + c);
+                if (FUSED) rv[v] = ld_stream(static_cast<const uint4 *>(a.res) + base + c);
+            }
+        }
+        float ss = 0.f, mw = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * 32 + lane;
+            if (c < nvec) {
+                float f[V], wf[V];
+                r_of<T, FUSED>(xv[v], rv[v], f);
+                if (FUSED) st_stream(static_cast<uint4 *>(a.res_out) + base + c, E::pack(f));
+                E::unpack(opaque(wv[v]), wf);
+#pragma unroll
+                for (int k = 0; k < V; ++k) {
+                    ss = fmaf(f[k], f[k], ss);
+                    mw = fmaxf(mw, fabsf(f[k] * wf[k]));
+                }
+            }
+        }
+        ss = warp_sum(ss);
+        mw = warp_max(mw);
+        auto each = [&](auto fn) {
+#pragma unroll
+            for (int v = 0; v < VPT; ++v)
+                if (v * 32 + lane < nvec) {
+                    float f[V];
+                    r_of<T, FUSED>(xv[v], rv[v], f);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) fn(f[k]);
+                }
+        };
+        const float rs = rms_rstd_warp(each, ss, n_f, a.eps);
+        float am = rs * mw;
+        if (!isfinite(mw)) {
+            // rare: some |r * w| beyond the fp32 range - the amax over the y values themselves
+            float m = 0.f;
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int c = v * 32 + lane;
+                if (c < nvec) {
+                    float f[V], wf[V];
+                    r_of<T, FUSED>(xv[v], rv[v], f);
+                    E::unpack(opaque(wv[v]), wf);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) m = fmaxf(m, fabsf(f[k] * rs * wf[k]));
+                }
+            }
+            am = warp_max(m);
+        }
+        const float inv = am > 0.f ? 448.f / am : 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * 32 + lane;
+            if (c < nvec) {
+                float f[V], wf[V];
+                r_of<T, FUSED>(xv[v], rv[v], f);
+                E::unpack(opaque(wv[v]), wf);
+                store_codes<V>(static_cast<uint8_t *>(a.q) + (base + c) * V, f, wf, rs, inv);
+            }
+        }
+        if (lane == 0) {
             a.scale[row] = am / 448.f;
             if (a.rstd) a.rstd[row] = rs;
         }
@@ -443,6 +552,14 @@ const void *quant_kernel_ptr(const Launch &l) {
                 case 8: return reinterpret_cast<const void *>(&quant_row_cluster<T, 8, FUSED>);
                 default: return nullptr;
             }
+        case RRN_VARIANT_ROW_WARP:
+            switch (l.vpt) {
+                case 1: return reinterpret_cast<const void *>(&quant_row_warp<T, 1, FUSED>);
+                case 2: return reinterpret_cast<const void *>(&quant_row_warp<T, 2, FUSED>);
+                case 4: return reinterpret_cast<const void *>(&quant_row_warp<T, 4, FUSED>);
+                case 8: return reinterpret_cast<const void *>(&quant_row_warp<T, 8, FUSED>);
+                default: return nullptr;
+            }
         case RRN_VARIANT_STREAM:
             return l.vec ? reinterpret_cast<const void *>(&quant_stream<T, true, FUSED>)
                          : reinterpret_cast<const void *>(&quant_stream<T, false, FUSED>);
@@ -457,7 +574,7 @@ cudaError_t launch_quant(const QuantArgs &a, const Launch &l, cudaStream_t strea
     QuantArgs args = a;
     void *params[] = {&args};
     return enqueue(k, l, l.variant == RRN_VARIANT_ROW_CLUSTER ? l.cluster : 0,
-                   l.variant == RRN_VARIANT_ROW_CTA, params, stream);
+                   l.variant == RRN_VARIANT_ROW_CTA || l.variant == RRN_VARIANT_ROW_WARP, params, stream);
 }
 
 template <typename T>

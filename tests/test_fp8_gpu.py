@@ -92,7 +92,7 @@ def test_fp8_fused_full_size():
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("N", [1, 7, 1000, 1024, 4095, 4096, 7168, 8192, 20000])
+@pytest.mark.parametrize("N", [1, 7, 1000, 1024, 2048, 4095, 4096, 7168, 8192, 20000])
 def test_fp8_variants(dtype, N):
     M = 61
     for fused in (False, True):
@@ -115,31 +115,41 @@ def test_fp8_variants(dtype, N):
                     launches += [rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 1, 0, 6, 0, 2)]
             if 8 <= nvec <= 8 * 2048:
                 launches += [rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 0, 0, 8)]
+            if nvec <= 256:  # one row per warp: a grid for every row, and 3 CTAs of 2 warps walking rows
+                vpt = next(v for v in (1, 2, 4, 8) if 32 * v >= nvec)
+                launches += [rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 128, 0), rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 64, 3)]
         for launch in launches:
             q, scale, rstd, ro = run(h, dtype, wl.eps, fused, launch)
             compare(h, dtype, wl.eps, fused, q, scale, rstd, ro, str(launch))
 
 
-def test_fp8_zero_and_extreme_rows():
-    N = 4096
+def _warp_launch(N):
+    # one row per warp where a warp holds the row (bf16: 8 values a vector, 8 vectors a lane)
+    return [rrn.Launch(rrn.VARIANT_ROW_WARP, 0, 64, 0)] if N <= 2048 else []
+
+
+@pytest.mark.parametrize("N", [4096, 1024])
+def test_fp8_zero_and_extreme_rows(N):
     rng = np.random.default_rng(102)
     rows = np.stack([np.zeros(N, np.float32), rng.standard_normal(N).astype(np.float32) * 1e30,
                      np.full(N, 2.0, np.float32), rng.standard_normal(N).astype(np.float32)])
     h = {"x": bits_of(rows, "bf16"), "w": bits_of(np.ones(N, np.float32), "bf16")}
-    for launch in (None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0), rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 0, 0, 4)):
+    for launch in [None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0),
+                   rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 0, 0, 4)] + _warp_launch(N):
         q, scale, rstd, _ = run(h, "bf16", 1e-6, False, launch)
         compare(h, "bf16", 1e-6, False, q, scale, rstd, None, str(launch))
         assert float(scale[0]) == 0.0 and int(q[0].max()) == 0
 
 
-def test_fp8_row_whose_r_times_w_overflows():
+@pytest.mark.parametrize("N", [4096, 1024])
+def test_fp8_row_whose_r_times_w_overflows(N):
     # |r| near 1e38 with w = 8: r * w is beyond fp32 although y = r * rstd * w is about 8
-    N = 4096
     rng = np.random.default_rng(103)
     z = np.clip(rng.standard_normal(N), -3.0, 3.0).astype(np.float32)  # |r| <= 3e38 stays finite
     rows = np.stack([z * np.float32(1e38), rng.standard_normal(N).astype(np.float32)])
     h = {"x": bits_of(rows, "bf16"), "w": bits_of(np.full(N, 8.0, np.float32), "bf16")}
-    for launch in (None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0), rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 0, 0, 4)):
+    for launch in [None, rrn.Launch(rrn.VARIANT_STREAM, 0, 256, 0),
+                   rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 0, 0, 4)] + _warp_launch(N):
         q, scale, rstd, _ = run(h, "bf16", 1e-6, False, launch)
         compare(h, "bf16", 1e-6, False, q, scale, rstd, None, str(launch))
 
@@ -160,7 +170,7 @@ def test_fp8_wide_rows(dtype, N):
             compare(h, dtype, wl.eps, fused, q, scale, rstd, ro, f"{N} {launch}")
 
 
-@pytest.mark.parametrize("dtype,N", [("bf16", 4096), ("f32", 4096), ("bf16", 4095), ("bf16", 32768)])
+@pytest.mark.parametrize("dtype,N", [("bf16", 4096), ("f32", 4096), ("bf16", 4095), ("bf16", 32768), ("bf16", 1024)])
 def test_fp8_in_place(dtype, N):
     """residual_out written over residual, and over x."""
     M = 96
@@ -175,6 +185,8 @@ def test_fp8_in_place(dtype, N):
         launches += [rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 0, 0, 4)]
         if N // V <= 1024:
             launches += [rrn.Launch(rrn.VARIANT_ROW_CTA, 0, 0, 0)]
+        if N // V <= 256:
+            launches += [rrn.Launch(rrn.VARIANT_ROW_WARP, 0, 128, 0)]
     for launch in launches:
         for target in ("residual", "x"):
             x, res = to_dev(h["x"], dtype), to_dev(h["residual"], dtype)
@@ -192,7 +204,7 @@ def test_fp8_in_place(dtype, N):
 
 
 def test_fp8_plans():
-    """The forward's layouts: one row per CTA, cluster split for wide rows with a residual (and
+    """The forward's layouts: one row per warp for short rows over many rows, one row per CTA, cluster split for wide rows with a residual (and
     beyond 2048 vectors without one; 256-thread CTAs for chunks above 512 vectors), the 128-bit
     two-pass kernel beyond 16384 vectors."""
     def plan(M, N, fused):
@@ -203,6 +215,10 @@ def test_fp8_plans():
 
     p = plan(16384, 4096, True)
     assert (p.variant, p.vpt, p.threads) == (rrn.VARIANT_ROW_CTA, 4, 128), p
+    p = plan(65536, 1024, True)  # short rows over many rows: one row per warp
+    assert (p.variant, p.vpt, p.threads, p.ctas) == (rrn.VARIANT_ROW_WARP, 4, 128, 65536 // 4), p
+    p = plan(32768, 2048, False)
+    assert (p.variant, p.vpt, p.threads) == (rrn.VARIANT_ROW_WARP, 8, 128), p
     p = plan(16384, 16384, True)
     assert (p.variant, p.cluster) == (rrn.VARIANT_ROW_CLUSTER, 4), p
     p = plan(16384, 16384, False)

@@ -89,11 +89,14 @@ def _fwd_launches(dtype, N):
             thr = -(-(-(-nvec // vpt)) // 32) * 32
             if thr <= (256 if vpt == 8 else 512 if vpt == 4 else 1024):
                 out += [rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 0), rrn.Launch(rrn.VARIANT_ROW_CTA, vpt, thr, 9)]
+        if nvec <= 256:  # one row per warp: a grid for every row, and 5 CTAs of 2 warps walking rows
+            vpt = next(v for v in (1, 2, 4, 8) if 32 * v >= nvec)
+            out += [rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 128, 0), rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 64, 5)]
     return out
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("N", [1, 7, 1000, 1024, 4095, 4096, 7168, 8192, 20000])
+@pytest.mark.parametrize("N", [1, 7, 8, 256, 1000, 1024, 2048, 4095, 4096, 7168, 8192, 20000])
 def test_layernorm_forward_variants(dtype, N):
     M = 67
     for fused in (False, True):
@@ -286,3 +289,15 @@ def test_layernorm_plans():
     w = torch.empty(4096, device="cuda", dtype=torch.bfloat16)
     p = rrn.plan_layernorm_fwd(x, w, x, w, x, x)
     assert (p.variant, p.vpt, p.threads) == (rrn.VARIANT_ROW_CTA, 4, 128), p
+    # wider rows: at most 4 vectors a thread, more threads instead
+    for N, thr in ((2048, 64), (6144, 192), (8192, 256), (12288, 384), (16384, 512)):
+        x = torch.empty(4096, N, device="cuda", dtype=torch.bfloat16)
+        w = torch.empty(N, device="cuda", dtype=torch.bfloat16)
+        p = rrn.plan_layernorm_fwd(x, w, x, w, x, x)
+        assert (p.variant, p.vpt, p.threads) == (rrn.VARIANT_ROW_CTA, 4, thr), (N, p)
+    # short rows over many rows: one row per warp
+    for N, vpt in ((512, 2), (768, 4), (1024, 4)):
+        x = torch.empty(65536, N, device="cuda", dtype=torch.bfloat16)
+        w = torch.empty(N, device="cuda", dtype=torch.bfloat16)
+        p = rrn.plan_layernorm_fwd(x, w, x, w, x, x)
+        assert (p.variant, p.vpt, p.threads, p.ctas) == (rrn.VARIANT_ROW_WARP, vpt, 128, 65536 // 4), (N, p)
