@@ -185,6 +185,11 @@ constexpr int kLnFwdMaxVpt = 4;         // LayerNorm forward row layouts (plan_l
 constexpr int kLnFwdTargetThreads = 64;
 // fp8 output: one row per warp up to this many vectors over many rows (plan_quant)
 constexpr int kQuantWarpMaxVec = 256;
+// RMSNorm backward: one row per warp (bwd_row_warp) up to this many vectors over many rows
+// (bf16, 64 Mi elements, back to back: 512 columns 89.1 -> 81.7 us plain, 100.9 -> 96.2 with
+// the gradient at residual_out; from 128 vectors the ring measured faster: 1024 columns 75.3
+// against 85.2, 2048 69.3 against 82.2)
+constexpr int kBwdWarpMaxVec = 64;
 // Vectors of a row each CTA of the cluster split takes when the planner chooses the cluster
 // size, for the fused forward (two input rows): measured best at 4 vectors x 128 threads a CTA.
 // The plain forward (one input row) keeps the same bytes in flight per thread with twice as
@@ -476,7 +481,9 @@ int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
         // kClusterChunkVec vectors (4 a thread x 128 threads, as the ring's CTAs), else the
         // two-pass kernel.
         const int64_t slot = (add_grad ? 3 : 2) * N * elem_size(dtype);
-        l.variant = regs ? (slot <= kMaxDynSmem / 2 ? RRN_VARIANT_ROW_TMA : RRN_VARIANT_ROW_CTA)
+        l.variant = regs ? (nvec <= kBwdWarpMaxVec && M >= 4LL * sms ? RRN_VARIANT_ROW_WARP
+                            : slot <= kMaxDynSmem / 2                ? RRN_VARIANT_ROW_TMA
+                                                                     : RRN_VARIANT_ROW_CTA)
                   : vec_ok && nvec <= static_cast<int64_t>(kMaxCluster) * kClusterChunkVec ? RRN_VARIANT_ROW_CLUSTER
                                                                                            : RRN_VARIANT_STREAM;
     }
@@ -549,6 +556,17 @@ int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
                                      kBwdPlainRingBytes);
                 if (ring_occ < 1) return RRN_ERR_CONFIG;
             }
+            break;
+        }
+        case RRN_VARIANT_ROW_WARP: {
+            // a row per warp; the CTA's warps add their dw sums in N floats of shared memory
+            if (!vec_ok) return RRN_ERR_CONFIG;
+            l.vpt = cfg && cfg->vpt ? cfg->vpt : ceil_pow2_vpt((nvec + 31) / 32, kMaxVpt);
+            if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4 && l.vpt != 8) return RRN_ERR_CONFIG;
+            if (static_cast<int64_t>(l.vpt) * 32 < nvec) return RRN_ERR_CONFIG;
+            l.threads = cfg && cfg->threads ? cfg->threads : 128;
+            if (l.threads < 32 || l.threads % 32 || l.threads > 256) return RRN_ERR_CONFIG;
+            l.smem = static_cast<int>(N * static_cast<int64_t>(sizeof(float)));
             break;
         }
         case RRN_VARIANT_STREAM: {

@@ -149,6 +149,146 @@ __device__ __forceinline__ void bwd_store_partial(const BwdArgs &a, int nvec,
     }
 }
 
+// Stage 1 for short rows: a row per warp. Warp w of CTA p takes rows p * W + w, then every
+// (P * W)-th row after it (W warps a CTA, P CTAs); lane l owns vectors v * 32 + l. The row's dot
+// product is warp-wide (shuffles, no barrier per row); each thread adds dy * xhat into its dw
+// registers, and at the end the W warps' sums are added in warp order through shared memory
+// (N floats of dynamic shared memory) into row p of the workspace, as a row-per-CTA stage 1
+// writes it. Up to 4 vectors a lane the next row is loaded before the current row's arithmetic:
+// two rows per warp in flight.
+template <typename T, int VPT, bool ADDG>
+__global__ void __launch_bounds__(256) bwd_row_warp(const BwdArgs a) {
+    pdl_enter();  // stage 2 may be scheduled from now on; it waits for our results
+    using E = Elem<T>;
+    constexpr int V = E::kPerVec;
+    constexpr bool PIPE = VPT <= 4;
+    extern __shared__ __align__(16) float red[];
+    const int nvec = a.N / V;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int W = blockDim.x >> 5;
+    const int64_t nw = static_cast<int64_t>(gridDim.x) * W;
+    const float inv_n = 1.f / static_cast<float>(a.N);
+    const uint4 *dy4 = static_cast<const uint4 *>(a.dy);
+    const uint4 *g4 = static_cast<const uint4 *>(a.d_ro);
+    const uint4 *x4 = static_cast<const uint4 *>(a.x);
+
+    uint4 wv[VPT];
+    float dw[VPT][V];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * 32 + lane;
+        if (c < nvec) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
+#pragma unroll
+        for (int k = 0; k < V; ++k) dw[v][k] = 0.f;
+    }
+    auto load = [&](int64_t r, uint4 (&xo)[VPT], uint4 (&dyo)[VPT], uint4 (&go)[VPT]) {
+        const int64_t base = r * nvec;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * 32 + lane;
+            if (c < nvec) {
+                xo[v] = ld_stream(x4 + base + c);
+                dyo[v] = ld_stream(dy4 + base + c);
+                if constexpr (ADDG) go[v] = ld_stream(g4 + base + c);
+            }
+        }
+    };
+    int64_t row = static_cast<int64_t>(blockIdx.x) * W + warp;
+    uint4 xv[VPT], dyv[VPT], gv[VPT];
+    float rs = 0.f;
+    if (PIPE && row < a.M) {
+        load(row, xv, dyv, gv);
+        rs = __ldg(a.rstd + row);
+    }
+    for (; row < a.M; row += nw) {
+        const int64_t nxt = row + nw;
+        uint4 xn[VPT], dyn[VPT], gn[VPT];
+        float rsn = 0.f;
+        if constexpr (PIPE) {
+            if (nxt < a.M) {
+                load(nxt, xn, dyn, gn);
+                rsn = __ldg(a.rstd + nxt);
+            }
+        } else {
+            load(row, xv, dyv, gv);
+            rs = __ldg(a.rstd + row);
+        }
+        float2 dot2 = splat(0.f);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * 32 + lane;
+            if (c < nvec) {
+                float xf[V], d[V], wf[V];
+                E::unpack(xv[v], xf);
+                E::unpack(dyv[v], d);
+                E::unpack(opaque(wv[v]), wf);
+#pragma unroll
+                for (int k = 0; k < V; k += 2) {
+                    const float2 xh = mul2(pair(xf[k], xf[k + 1]), splat(rs));
+                    const float2 d2 = pair(d[k], d[k + 1]);
+                    dot2 = fma2(mul2(d2, pair(wf[k], wf[k + 1])), xh, dot2);
+                    const float2 w2 = fma2(d2, xh, pair(dw[v][k], dw[v][k + 1]));
+                    dw[v][k] = w2.x;
+                    dw[v][k + 1] = w2.y;
+                }
+            }
+        }
+        const float cm = warp_sum(dot2.x + dot2.y) * inv_n;
+        const int64_t base = row * nvec;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * 32 + lane;
+            if (c < nvec) {
+                float xf[V], d[V], wf[V], o[V];
+                E::unpack(xv[v], xf);
+                E::unpack(dyv[v], d);
+                E::unpack(opaque(wv[v]), wf);
+#pragma unroll
+                for (int k = 0; k < V; k += 2) {
+                    const float2 xh = mul2(pair(xf[k], xf[k + 1]), splat(rs));
+                    const float2 g = mul2(pair(d[k], d[k + 1]), pair(wf[k], wf[k + 1]));
+                    const float2 r = mul2(splat(rs), fma2(xh, splat(-cm), g));
+                    o[k] = r.x;
+                    o[k + 1] = r.y;
+                }
+                if constexpr (ADDG) {
+                    float gg[V];
+                    E::unpack(gv[v], gg);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) o[k] += gg[k];
+                }
+                st_stream(static_cast<uint4 *>(a.dx) + base + c, E::pack(o));
+            }
+        }
+        if constexpr (PIPE) {
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                xv[v] = xn[v];
+                dyv[v] = dyn[v];
+                if constexpr (ADDG) gv[v] = gn[v];
+            }
+            rs = rsn;
+        }
+    }
+    // the W warps' sums, added in warp order, then row blockIdx.x of the workspace
+    for (int w = 0; w < W; ++w) {
+        if (warp == w) {
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int c = v * 32 + lane;
+                if (c < nvec) {
+#pragma unroll
+                    for (int k = 0; k < V; ++k) red[c * V + k] = w == 0 ? dw[v][k] : red[c * V + k] + dw[v][k];
+                }
+            }
+        }
+        __syncthreads();
+    }
+    float *prow = a.partial + static_cast<int64_t>(blockIdx.x) * a.N;
+    for (int j = threadIdx.x; j < a.N; j += blockDim.x) prow[j] = red[j];
+}
+
 template <typename T, int VPT, bool ADDG, bool CLUSTER>
 __global__ void __launch_bounds__(bwd_max_threads(VPT)) bwd_row_cta(const BwdArgs a) {
     pdl_enter();  // stage 2 may be scheduled from now on; it waits for our results
@@ -555,6 +695,14 @@ const void *bwd_kernel_ptr(const Launch &l) {
                 case 5: return reinterpret_cast<const void *>(&bwd_row_cta<T, 2, ADDG, true>);
                 case 8: return reinterpret_cast<const void *>(&bwd_row_cta<T, 4, ADDG, false>);
                 case 9: return reinterpret_cast<const void *>(&bwd_row_cta<T, 4, ADDG, true>);
+                default: return nullptr;
+            }
+        case RRN_VARIANT_ROW_WARP:
+            switch (l.vpt) {
+                case 1: return reinterpret_cast<const void *>(&bwd_row_warp<T, 1, ADDG>);
+                case 2: return reinterpret_cast<const void *>(&bwd_row_warp<T, 2, ADDG>);
+                case 4: return reinterpret_cast<const void *>(&bwd_row_warp<T, 4, ADDG>);
+                case 8: return reinterpret_cast<const void *>(&bwd_row_warp<T, 8, ADDG>);
                 default: return nullptr;
             }
         case RRN_VARIANT_STREAM:

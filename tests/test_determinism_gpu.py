@@ -45,6 +45,28 @@ def test_fused_backward_is_bitwise_reproducible(launch):
 
 
 @pytest.mark.parametrize("with_dro", [True, False])
+def test_short_row_backward_is_bitwise_reproducible(with_dro):
+    # 512 columns over many rows: one row per warp, the CTA's warps adding their dw sums in order
+    wl = synth.get("add_rmsnorm_bwd_16384x4096_bf16").with_shape(16384, 512)
+    h = synth.make(wl)
+    x, w = to_dev(h["x"], "bf16"), to_dev(h["w"], "bf16")
+    dy = to_dev(h["dy"], "bf16")
+    dro = to_dev(h["d_ro"], "bf16") if with_dro else None
+    _, rstd = rrn.rms_norm(x, w, wl.eps)
+    assert rrn.plan_bwd(dy, x, w, x, dro).variant == rrn.VARIANT_ROW_WARP
+    ws = torch.empty(wl.M * wl.N, device="cuda")
+
+    def run():
+        dr = torch.empty_like(x)
+        dw = torch.empty(wl.N, device="cuda")
+        rrn.add_rmsnorm_bwd(dy, dro, x, w, rstd, dr, dw, ws, wl.eps)
+        torch.cuda.synchronize()
+        return dr, dw
+
+    assert _same(run(), run())
+
+
+@pytest.mark.parametrize("with_dro", [True, False])
 def test_layernorm_backward_is_bitwise_reproducible(with_dro):
     wl = synth.get("layernorm_bwd_16384x4096_bf16").with_shape(4096)
     h = synth.make(wl)

@@ -58,6 +58,9 @@ def _launches(dtype, N):
                         rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 0, 0),
                         rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 0, 2, 4),
                         rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 11, 2)]
+        if nvec <= 256:  # one row per warp (the planner's grid; 3 CTAs of 2 warps walking rows)
+            vpt = next(v for v in (1, 2, 4, 8) if 32 * v >= nvec)
+            out += [rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 128, 0), rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 64, 3)]
     return out
 
 

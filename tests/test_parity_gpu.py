@@ -362,7 +362,7 @@ def _bwd_case(h, dtype, eps, launch=None, M=None):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("N", [1, 7, 9, 1000, 1024, 4095, 4096, 7168, 8192, 16384])
+@pytest.mark.parametrize("N", [1, 7, 8, 9, 256, 1000, 1024, 2048, 4095, 4096, 7168, 8192, 16384])
 def test_backward_shapes(dtype, N):
     M = 203
     wl = synth.Workload("bwd", "rmsnorm_bwd", M, N, dtype, 1e-6, 61)
@@ -389,6 +389,11 @@ def test_backward_shapes(dtype, N):
                              rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 13, 1),
                              rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 13, 1, 2),
                              rrn.Launch(rrn.VARIANT_ROW_TMA, vpt, thr, 7, 3)]
+    if N % V == 0 and N // V <= 256:
+        # one row per warp: the planner's grid, 64-thread CTAs, and 5 CTAs of 4 warps walking rows
+        vpt = next(v for v in (1, 2, 4, 8) if 32 * v >= N // V)
+        launches += [rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 128, 0), rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 64, 0),
+                     rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 128, 5)]
     if N % V == 0 and N // V >= 512:
         # each row split over a cluster (CTA q owning a column slice); 3 x C CTAs: ragged rows
         for C in (2, 4, 8):
@@ -418,6 +423,27 @@ def test_wide_rows_backward_automatic_plan(dtype, N, variant, cluster):
     cond = bwd_cond(h["x"], h["dy"], h["w"], wl.eps)
     dx, dw = _bwd_case(h, dtype, wl.eps)
     check_out(values(dx), dx_ref, dtype, "dx", cond)
+    check_dw(dw.cpu().numpy().astype(np.float64), dw_ref, "dw")
+
+
+def test_short_rows_backward_plan():
+    """Rows of at most 64 vectors over many rows: one row per warp (with or without the gradient
+    at residual_out); from 128 vectors the ring."""
+    for N, variant in ((512, rrn.VARIANT_ROW_WARP), (256, rrn.VARIANT_ROW_WARP), (1024, rrn.VARIANT_ROW_TMA)):
+        x = torch.empty(65536, N, device="cuda", dtype=torch.bfloat16)
+        w = torch.empty(N, device="cuda", dtype=torch.bfloat16)
+        for g in (None, x):
+            p = rrn.plan_bwd(x, x, w, x, g)
+            assert p.variant == variant, (N, p)
+            if variant == rrn.VARIANT_ROW_WARP:
+                assert p.vpt * 32 >= N // 8 and p.threads == 128, p
+    # and the full-size workload through the automatic plan matches the oracle
+    M, N = 16384, 512
+    wl = synth.Workload("bwd-short", "rmsnorm_bwd", M, N, "bf16", 1e-6, 62)
+    h = synth.make(wl)
+    dx_ref, dw_ref = oracle.rmsnorm_bwd(h["dy"], h["x"], h["w"], wl.eps)
+    dx, dw = _bwd_case(h, "bf16", wl.eps)
+    check_out(values(dx), dx_ref, "bf16", "dx", bwd_cond(h["x"], h["dy"], h["w"], wl.eps))
     check_dw(dw.cpu().numpy().astype(np.float64), dw_ref, "dw")
 
 
