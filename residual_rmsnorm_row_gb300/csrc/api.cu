@@ -190,6 +190,11 @@ constexpr int kQuantWarpMaxVec = 256;
 // the gradient at residual_out; from 128 vectors the ring measured faster: 1024 columns 75.3
 // against 85.2, 2048 69.3 against 82.2)
 constexpr int kBwdWarpMaxVec = 64;
+// LayerNorm backward: one row per warp (ln_bwd_row_warp) up to this many vectors over many rows
+// (bf16, back to back, against a row per CTA of 2 vectors a thread: 512 columns 97.2 -> 91.5 us
+// plain, 106.9 -> 106.3 with the gradient at residual_out; 1024 columns 91.8 -> 86.7 and
+// 101.0 -> 100.0)
+constexpr int kLnBwdWarpMaxVec = 128;
 // Vectors of a row each CTA of the cluster split takes when the planner chooses the cluster
 // size, for the fused forward (two input rows): measured best at 4 vectors x 128 threads a CTA.
 // The plain forward (one input row) keeps the same bytes in flight per thread with twice as
@@ -775,7 +780,9 @@ int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, con
         const int vpt = ln_bwd_vpt(nvec, add_grad);
         const bool ring = slot <= kMaxDynSmem / 2 &&
                           (vpt >= 4 || round_up32((nvec + vpt - 1) / vpt) >= kLnBwdMinRingThreads);
-        l.variant = regs ? (ring ? RRN_VARIANT_ROW_TMA : RRN_VARIANT_ROW_CTA)
+        l.variant = regs ? (nvec <= kLnBwdWarpMaxVec && M >= 4LL * sms ? RRN_VARIANT_ROW_WARP
+                            : ring                                     ? RRN_VARIANT_ROW_TMA
+                                                                       : RRN_VARIANT_ROW_CTA)
                   : vec_ok && nvec <= static_cast<int64_t>(kMaxCluster) * kClusterChunkVec ? RRN_VARIANT_ROW_CLUSTER
                                                                                            : RRN_VARIANT_STREAM;
     }
@@ -836,6 +843,15 @@ int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, con
             l.stages = S;
             l.smem = static_cast<int>(S * slot);
         }
+    } else if (l.variant == RRN_VARIANT_ROW_WARP) {
+        // a row per warp; the CTA's warps add their dw and db sums in 2 N floats of shared memory
+        if (!vec_ok) return RRN_ERR_CONFIG;
+        l.vpt = cfg && cfg->vpt ? cfg->vpt : ceil_pow2_vpt((nvec + 31) / 32, kMaxVpt);
+        if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4 && l.vpt != 8) return RRN_ERR_CONFIG;
+        if (static_cast<int64_t>(l.vpt) * 32 < nvec) return RRN_ERR_CONFIG;
+        l.threads = cfg && cfg->threads ? cfg->threads : 128;
+        if (l.threads < 32 || l.threads % 32 || l.threads > 256) return RRN_ERR_CONFIG;
+        l.smem = static_cast<int>(2 * N * static_cast<int64_t>(sizeof(float)));
     } else if (l.variant == RRN_VARIANT_STREAM) {
         l.vpt = 1;
         const int64_t chunks = l.vec ? nvec : N;

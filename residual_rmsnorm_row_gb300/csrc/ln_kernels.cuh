@@ -80,6 +80,7 @@ struct CtaReduce {
         return t;
     }
 };
+__device__ __forceinline__ float2 red_warp_sum2(float a, float b) { return make_float2(warp_sum(a), warp_sum(b)); }
 struct WarpReduce {
     __device__ __forceinline__ float sum(float v) const { return warp_sum(v); }
     __device__ __forceinline__ float max(float v) const { return warp_max(v); }
@@ -633,6 +634,143 @@ __device__ __forceinline__ void ln_bwd_row_body(const LnBwdArgs &a, int64_t row,
     }
 }
 
+// Stage 1 for short rows: a row per warp (as the RMSNorm backward's bwd_row_warp). Warp w of CTA
+// p takes rows p * W + w, then every (P * W)-th row; lane l owns vectors v * 32 + l; the row's
+// two sums are warp-wide (no barrier per row); dw and db stay in registers, and at the end the
+// W warps' sums are added in warp order through shared memory (2 N floats) into rows p of the
+// two workspace halves. Up to 2 vectors a lane the next row is loaded before the current row's
+// arithmetic.
+template <typename T, int VPT, bool ADDG>
+__global__ void __launch_bounds__(256) ln_bwd_row_warp(const LnBwdArgs a) {
+    pdl_enter();  // the stage-2 reduction may be scheduled from now on
+    using E = Elem<T>;
+    constexpr int V = E::kPerVec;
+    constexpr bool PIPE = VPT <= 2;
+    extern __shared__ __align__(16) float red[];  // [2][N]: dw, then db
+    const int nvec = a.N / V;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int W = blockDim.x >> 5;
+    const int64_t nw = static_cast<int64_t>(gridDim.x) * W;
+    const float inv_n = 1.f / static_cast<float>(a.N);
+    const uint4 *dy4 = static_cast<const uint4 *>(a.dy);
+    const uint4 *g4 = static_cast<const uint4 *>(a.d_ro);
+    const uint4 *x4 = static_cast<const uint4 *>(a.x);
+
+    uint4 wv[VPT];
+    float dw[VPT][V], db[VPT][V];
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+        const int c = v * 32 + lane;
+        if (c < nvec) wv[v] = ld_keep(static_cast<const uint4 *>(a.w) + c);
+#pragma unroll
+        for (int k = 0; k < V; ++k) dw[v][k] = db[v][k] = 0.f;
+    }
+    auto load = [&](int64_t r, uint4 (&xo)[VPT], uint4 (&dyo)[VPT], uint4 (&go)[VPT]) {
+        const int64_t base = r * nvec;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * 32 + lane;
+            if (c < nvec) {
+                xo[v] = ld_stream(x4 + base + c);
+                dyo[v] = ld_stream(dy4 + base + c);
+                if constexpr (ADDG) go[v] = ld_stream(g4 + base + c);
+            }
+        }
+    };
+    int64_t row = static_cast<int64_t>(blockIdx.x) * W + warp;
+    uint4 xv[VPT], dyv[VPT], gv[VPT];
+    float mu = 0.f, rs = 0.f;
+    if (PIPE && row < a.M) {
+        load(row, xv, dyv, gv);
+        mu = __ldg(a.mean + row);
+        rs = __ldg(a.rstd + row);
+    }
+    for (; row < a.M; row += nw) {
+        const int64_t nxt = row + nw;
+        uint4 xn[VPT], dyn[VPT], gn[VPT];
+        float mun = 0.f, rsn = 0.f;
+        if constexpr (PIPE) {
+            if (nxt < a.M) {
+                load(nxt, xn, dyn, gn);
+                mun = __ldg(a.mean + nxt);
+                rsn = __ldg(a.rstd + nxt);
+            }
+        } else {
+            load(row, xv, dyv, gv);
+            mu = __ldg(a.mean + row);
+            rs = __ldg(a.rstd + row);
+        }
+        float2 sg = splat(0.f), sgx = splat(0.f);
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * 32 + lane;
+            if (c < nvec) {
+                float xf[V], d[V], wf[V];
+                E::unpack(xv[v], xf);
+                E::unpack(dyv[v], d);
+                E::unpack(opaque(wv[v]), wf);
+                ln_bwd_accumulate<V>(xf, d, wf, mu, rs, dw[v], db[v], sg, sgx);
+            }
+        }
+        const float2 t = red_warp_sum2(sg.x + sg.y, sgx.x + sgx.y);
+        const float cx = -rs * (t.y * inv_n), cc = -rs * (t.x * inv_n);
+        const int64_t base = row * nvec;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v) {
+            const int c = v * 32 + lane;
+            if (c < nvec) {
+                float xf[V], d[V], wf[V], o[V];
+                E::unpack(xv[v], xf);
+                E::unpack(dyv[v], d);
+                E::unpack(opaque(wv[v]), wf);
+                ln_bwd_dx<V>(xf, d, wf, mu, rs, cx, cc, o);
+                if constexpr (ADDG) {
+                    float gg[V];
+                    E::unpack(gv[v], gg);
+#pragma unroll
+                    for (int k = 0; k < V; ++k) o[k] += gg[k];
+                }
+                st_stream(static_cast<uint4 *>(a.dx) + base + c, E::pack(o));
+            }
+        }
+        if constexpr (PIPE) {
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                xv[v] = xn[v];
+                dyv[v] = dyn[v];
+                if constexpr (ADDG) gv[v] = gn[v];
+            }
+            mu = mun;
+            rs = rsn;
+        }
+    }
+    // the W warps' sums, added in warp order, then rows blockIdx.x of the workspace halves
+    float *rw = red, *rb = red + a.N;
+    for (int w = 0; w < W; ++w) {
+        if (warp == w) {
+#pragma unroll
+            for (int v = 0; v < VPT; ++v) {
+                const int c = v * 32 + lane;
+                if (c < nvec) {
+#pragma unroll
+                    for (int k = 0; k < V; ++k) {
+                        rw[c * V + k] = w == 0 ? dw[v][k] : rw[c * V + k] + dw[v][k];
+                        rb[c * V + k] = w == 0 ? db[v][k] : rb[c * V + k] + db[v][k];
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+    float *pw = a.partial + static_cast<int64_t>(blockIdx.x) * a.N;
+    float *pb = a.partial + (static_cast<int64_t>(gridDim.x) + blockIdx.x) * a.N;
+    for (int j = threadIdx.x; j < a.N; j += blockDim.x) {
+        pw[j] = rw[j];
+        pb[j] = rb[j];
+    }
+}
+
 // This CTA's dw and db partial sums -> row blockIdx.x of the two [P, N] workspace halves.
 template <typename T, int VPT>
 __device__ __forceinline__ void ln_bwd_store_partial(const LnBwdArgs &a, int nvec,
@@ -1069,6 +1207,14 @@ const void *ln_fwd_kernel_ptr(const Launch &l) {
 template <typename T, bool ADDG>
 const void *ln_bwd_kernel_ptr(const Launch &l) {
     switch (l.variant) {
+        case RRN_VARIANT_ROW_WARP:
+            switch (l.vpt) {
+                case 1: return reinterpret_cast<const void *>(&ln_bwd_row_warp<T, 1, ADDG>);
+                case 2: return reinterpret_cast<const void *>(&ln_bwd_row_warp<T, 2, ADDG>);
+                case 4: return reinterpret_cast<const void *>(&ln_bwd_row_warp<T, 4, ADDG>);
+                case 8: return reinterpret_cast<const void *>(&ln_bwd_row_warp<T, 8, ADDG>);
+                default: return nullptr;
+            }
         case RRN_VARIANT_ROW_CTA:
             switch (l.vpt) {
                 case 1: return reinterpret_cast<const void *>(&ln_bwd_row_cta<T, 1, ADDG>);

@@ -86,8 +86,8 @@ _add(Workload("layernorm_bwd_plain_16384x4096_bf16", "layernorm_bwd", 16384, 409
               x_mean=0.5, residual_grad=False))
 # The fused Add+RMSNorm feeding fp8 e4m3 codes with a per-row scale (inputs as the fused forward).
 _add(Workload("add_rmsnorm_fp8_16384x4096_bf16", "add_rmsnorm_fp8", 16384, 4096, BF16, 1e-6, 8))
-# Rows wider than one CTA holds in registers: split over a thread-block cluster (16384 wide) or
-# the two-pass kernel (65536 wide).
+# Rows wider than one CTA holds in registers: split over a thread-block cluster (16384 wide: 4
+# CTAs; 65536 wide: 8).
 _add(Workload("add_rmsnorm_fwd_16384x16384_bf16", "add_rmsnorm_fwd", 16384, 16384, BF16, 1e-6, 9))
 _add(Workload("add_rmsnorm_fwd_4096x65536_bf16", "add_rmsnorm_fwd", 4096, 65536, BF16, 1e-6, 9))
 # The backward of rows too wide for one CTA's registers (each row split over a cluster).
@@ -97,6 +97,16 @@ _add(Workload("layernorm_bwd_8192x16384_bf16", "layernorm_bwd", 8192, 16384, BF1
               x_mean=0.5))
 # The fp8 output of wide rows (split over a cluster).
 _add(Workload("add_rmsnorm_fp8_16384x16384_bf16", "add_rmsnorm_fp8", 16384, 16384, BF16, 1e-6, 13))
+# Short rows over many rows (one row per warp: the LayerNorm and fp8 forwards, the RMSNorm and
+# LayerNorm backwards) and a LayerNorm forward of 8192 columns (a CTA of 4 vectors a thread).
+_add(Workload("add_layernorm_fwd_65536x1024_bf16", "add_layernorm_fwd", 65536, 1024, BF16, 1e-5, 15,
+              x_mean=0.5))
+_add(Workload("add_layernorm_fwd_8192x8192_bf16", "add_layernorm_fwd", 8192, 8192, BF16, 1e-5, 16,
+              x_mean=0.5))
+_add(Workload("add_rmsnorm_fp8_65536x1024_bf16", "add_rmsnorm_fp8", 65536, 1024, BF16, 1e-6, 17))
+_add(Workload("rmsnorm_bwd_131072x512_bf16", "rmsnorm_bwd", 131072, 512, BF16, 1e-6, 18))
+_add(Workload("layernorm_bwd_plain_65536x1024_bf16", "layernorm_bwd", 65536, 1024, BF16, 1e-5, 19,
+              x_mean=0.5, residual_grad=False))
 
 
 def get(name: str) -> Workload:

@@ -67,6 +67,29 @@ def test_short_row_backward_is_bitwise_reproducible(with_dro):
 
 
 @pytest.mark.parametrize("with_dro", [True, False])
+def test_short_row_layernorm_backward_is_bitwise_reproducible(with_dro):
+    # 1024 columns over many rows: one row per warp, the warps adding dw and db in order
+    wl = synth.get("layernorm_bwd_16384x4096_bf16").with_shape(16384, 1024)
+    h = synth.make(wl)
+    x, w = to_dev(h["x"], "bf16"), to_dev(h["w"], "bf16")
+    dy = to_dev(h["dy"], "bf16")
+    dro = to_dev(h["d_ro"], "bf16") if with_dro else None
+    _, mean, rstd = rrn.layer_norm(x, w, None, wl.eps)
+    assert rrn.plan_layernorm_bwd(dy, x, w, x, dro).variant == rrn.VARIANT_ROW_WARP
+    ws = torch.empty(wl.M * wl.N * 2, device="cuda")
+
+    def run():
+        dx = torch.empty_like(x)
+        dw = torch.empty(wl.N, device="cuda")
+        db = torch.empty(wl.N, device="cuda")
+        rrn.layernorm_bwd(dy, dro, x, w, mean, rstd, dx, dw, db, ws, wl.eps)
+        torch.cuda.synchronize()
+        return dx, dw, db
+
+    assert _same(run(), run())
+
+
+@pytest.mark.parametrize("with_dro", [True, False])
 def test_layernorm_backward_is_bitwise_reproducible(with_dro):
     wl = synth.get("layernorm_bwd_16384x4096_bf16").with_shape(4096)
     h = synth.make(wl)

@@ -140,7 +140,7 @@ def test_layernorm_forward_in_place(dtype, N):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("N", [1, 9, 1000, 1024, 4095, 4096, 7168, 8192])
+@pytest.mark.parametrize("N", [1, 8, 9, 256, 512, 1000, 1024, 4095, 4096, 7168, 8192])
 def test_layernorm_backward_variants(dtype, N):
     M = 75
     wl = synth.Workload("ln-bwd", "layernorm_bwd", M, N, dtype, 1e-5, 92, x_mean=0.5)
@@ -165,6 +165,10 @@ def test_layernorm_backward_variants(dtype, N):
             if -(-(N // V) // C) <= 1024:
                 launches += [rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 0, 0, C),
                              rrn.Launch(rrn.VARIANT_ROW_CLUSTER, 0, 0, 3 * C, 0, C)]
+    if N % V == 0 and N // V <= 128:
+        # one row per warp: the planner's grid, and 4 CTAs of 2 warps walking rows
+        vpt = next(v for v in (1, 2, 4) if 32 * v >= N // V)
+        launches += [rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 128, 0), rrn.Launch(rrn.VARIANT_ROW_WARP, vpt, 64, 4)]
     cond0 = bwd_cond(h["x"], h["dy"], h["w"], wl.eps, layernorm=True)
     for with_dro in (True, False):
         ref_dx, ref_dw, ref_db = oracle.add_layernorm_bwd(h["dy"], h["d_ro"] if with_dro else None,
@@ -273,8 +277,10 @@ def test_layernorm_plans():
     assert (p.variant, p.vpt, p.threads, p.stages) == (rrn.VARIANT_ROW_TMA, 4, 128, 2), p
     p = bwd(32768, 2048, False)
     assert (p.variant, p.vpt, p.threads) == (rrn.VARIANT_ROW_TMA, 4, 64), p
-    p = bwd(65536, 1024, False)
-    assert (p.variant, p.vpt, p.threads) == (rrn.VARIANT_ROW_CTA, 2, 64), p
+    p = bwd(65536, 1024, False)  # short rows over many rows: one row per warp
+    assert (p.variant, p.vpt, p.threads) == (rrn.VARIANT_ROW_WARP, 4, 128), p
+    p = bwd(131072, 512, True)
+    assert (p.variant, p.vpt, p.threads) == (rrn.VARIANT_ROW_WARP, 2, 128), p
     p = bwd(8192, 8192, True)
     assert (p.variant, p.vpt, p.threads) == (rrn.VARIANT_ROW_TMA, 4, 256) and p.stages >= 2, p
     p = bwd(8192, 16384, True)
