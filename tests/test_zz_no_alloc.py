@@ -73,6 +73,16 @@ def test_noalloc_matches_oracle_and_regular_backward_on_calls_in_a_row():
     assert torch.equal(first[0], third[0]) and torch.equal(first[1], third[1])
 
 
+def test_noalloc_short_rows_one_per_warp():
+    # rows of 512 columns over many rows: the regular plan takes a row per warp (one row of
+    # partial sums per CTA); the array holds 4096 such rows, more than that plan's CTAs
+    M, N = 16384, 512
+    x = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+    w = torch.empty(N, device="cuda", dtype=torch.bfloat16)
+    assert rrn.plan_bwd(x, x, w, x).variant == rrn.VARIANT_ROW_WARP
+    _check(M, N, "bf16", 7)
+
+
 def test_noalloc_wide_rows_split_over_clusters():
     # rows of 24576 columns are split over clusters of 8 CTAs, one row of partial sums per
     # cluster: the array holds 85 such rows (2^21 // 24576), more than this GPU runs at once,
