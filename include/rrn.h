@@ -163,8 +163,8 @@ RRN_API int rmsnorm_bwd(const void *dy, const void *x, const void *w, const floa
  *   the last bits (within the dw tolerance); dx is the same.
  *   Nothing in the array needs to start at zero (stage 1 writes all that stage 2 reads).
  *   All calls on a device share the array: calls whose kernels overlap on the GPU race - order
- *   them on one stream. The first call on each device looks the array's address up (with that
- *   device current); make that first call before any stream capture begins.
+ *   them on one stream. The first call on each device looks the array's address up through the
+ *   CUDA runtime (with that device current); later calls on that device reuse it.
  *   No cudaMalloc, cudaFree or other allocation happens. Returns an rrn_status.
  */
 RRN_API int rmsnorm_bwd_noalloc(const void *dy, const void *x, const void *w, const float *rstd,

@@ -15,8 +15,7 @@
 //
 // Host code cannot use the array's name as a device address, so the first call on each device
 // looks the address up with cudaGetSymbolAddress (with that device current) and caches it. That
-// lookup is the first call's only extra work; make the first call on a device before any
-// stream capture begins.
+// lookup is the first call's only extra work.
 #include <cuda_runtime.h>
 
 #include <atomic>
