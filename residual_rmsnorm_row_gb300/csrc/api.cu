@@ -268,6 +268,19 @@ int plan_ring(Occ occ, int slot_bytes, int want_stages, Launch *l, int max_occ =
     return best_occ;
 }
 
+// The layout of a row-per-warp kernel (every op's ROW_WARP variant): a lane takes vpt vectors
+// (given, or the smallest power of two covering the row with 32 lanes), 128 threads a CTA unless
+// given (at most 256, a multiple of 32). The grid is the caller's: one row per warp for the
+// forwards, resident CTAs for the backwards.
+int warp_row_layout(int64_t nvec, const rrn_launch *cfg, Launch *l) {
+    l->vpt = cfg && cfg->vpt ? cfg->vpt : ceil_pow2_vpt((nvec + 31) / 32, kMaxVpt);
+    if (l->vpt != 1 && l->vpt != 2 && l->vpt != 4 && l->vpt != 8) return RRN_ERR_CONFIG;
+    if (static_cast<int64_t>(l->vpt) * 32 < nvec) return RRN_ERR_CONFIG;
+    l->threads = cfg && cfg->threads ? cfg->threads : 128;
+    if (l->threads < 32 || l->threads % 32 || l->threads > 256) return RRN_ERR_CONFIG;
+    return RRN_OK;
+}
+
 // ---------------------------------------------------------------- forward planning
 // True when every row of every matrix starts on a 16-byte boundary (128-bit vector path).
 bool vec_path_ok(std::initializer_list<const void *> ptrs, int64_t N, int dtype) {
@@ -367,11 +380,8 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
         }
         case RRN_VARIANT_ROW_WARP: {
             if (!vec_ok) return RRN_ERR_CONFIG;
-            l.vpt = cfg && cfg->vpt ? cfg->vpt : ceil_pow2_vpt((nvec + 31) / 32, kMaxVpt);
-            if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4 && l.vpt != 8) return RRN_ERR_CONFIG;
-            if (static_cast<int64_t>(l.vpt) * 32 < nvec) return RRN_ERR_CONFIG;
-            l.threads = cfg && cfg->threads ? cfg->threads : 128;
-            if (l.threads < 32 || l.threads % 32 || l.threads > 256) return RRN_ERR_CONFIG;
+            st = warp_row_layout(nvec, cfg, &l);
+            if (st != RRN_OK) return st;
             l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid((M + l.threads / 32 - 1) / (l.threads / 32));
             break;
         }
@@ -566,11 +576,8 @@ int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
         case RRN_VARIANT_ROW_WARP: {
             // a row per warp; the CTA's warps add their dw sums in N floats of shared memory
             if (!vec_ok) return RRN_ERR_CONFIG;
-            l.vpt = cfg && cfg->vpt ? cfg->vpt : ceil_pow2_vpt((nvec + 31) / 32, kMaxVpt);
-            if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4 && l.vpt != 8) return RRN_ERR_CONFIG;
-            if (static_cast<int64_t>(l.vpt) * 32 < nvec) return RRN_ERR_CONFIG;
-            l.threads = cfg && cfg->threads ? cfg->threads : 128;
-            if (l.threads < 32 || l.threads % 32 || l.threads > 256) return RRN_ERR_CONFIG;
+            st = warp_row_layout(nvec, cfg, &l);
+            if (st != RRN_OK) return st;
             l.smem = static_cast<int>(N * static_cast<int64_t>(sizeof(float)));
             break;
         }
@@ -726,11 +733,8 @@ int plan_ln_fwd(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const 
         l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid(M);
     } else if (l.variant == RRN_VARIANT_ROW_WARP) {
         if (!vec_ok) return RRN_ERR_CONFIG;
-        l.vpt = cfg && cfg->vpt ? cfg->vpt : ceil_pow2_vpt((nvec + 31) / 32, kMaxVpt);
-        if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4 && l.vpt != 8) return RRN_ERR_CONFIG;
-        if (static_cast<int64_t>(l.vpt) * 32 < nvec) return RRN_ERR_CONFIG;
-        l.threads = cfg && cfg->threads ? cfg->threads : 128;
-        if (l.threads < 32 || l.threads % 32 || l.threads > 256) return RRN_ERR_CONFIG;
+        st = warp_row_layout(nvec, cfg, &l);
+        if (st != RRN_OK) return st;
         l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid((M + l.threads / 32 - 1) / (l.threads / 32));
     } else if (l.variant == RRN_VARIANT_STREAM) {
         l.vpt = 1;
@@ -846,11 +850,8 @@ int plan_ln_bwd(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype, con
     } else if (l.variant == RRN_VARIANT_ROW_WARP) {
         // a row per warp; the CTA's warps add their dw and db sums in 2 N floats of shared memory
         if (!vec_ok) return RRN_ERR_CONFIG;
-        l.vpt = cfg && cfg->vpt ? cfg->vpt : ceil_pow2_vpt((nvec + 31) / 32, kMaxVpt);
-        if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4 && l.vpt != 8) return RRN_ERR_CONFIG;
-        if (static_cast<int64_t>(l.vpt) * 32 < nvec) return RRN_ERR_CONFIG;
-        l.threads = cfg && cfg->threads ? cfg->threads : 128;
-        if (l.threads < 32 || l.threads % 32 || l.threads > 256) return RRN_ERR_CONFIG;
+        st = warp_row_layout(nvec, cfg, &l);
+        if (st != RRN_OK) return st;
         l.smem = static_cast<int>(2 * N * static_cast<int64_t>(sizeof(float)));
     } else if (l.variant == RRN_VARIANT_STREAM) {
         l.vpt = 1;
@@ -948,11 +949,8 @@ int plan_quant(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, const r
         l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid(M);
     } else if (l.variant == RRN_VARIANT_ROW_WARP) {
         if (!vec_ok) return RRN_ERR_CONFIG;
-        l.vpt = cfg && cfg->vpt ? cfg->vpt : ceil_pow2_vpt((nvec + 31) / 32, kMaxVpt);
-        if (l.vpt != 1 && l.vpt != 2 && l.vpt != 4 && l.vpt != 8) return RRN_ERR_CONFIG;
-        if (static_cast<int64_t>(l.vpt) * 32 < nvec) return RRN_ERR_CONFIG;
-        l.threads = cfg && cfg->threads ? cfg->threads : 128;
-        if (l.threads < 32 || l.threads % 32 || l.threads > 256) return RRN_ERR_CONFIG;
+        st = warp_row_layout(nvec, cfg, &l);
+        if (st != RRN_OK) return st;
         l.ctas = cfg && cfg->ctas ? cfg->ctas : clamp_grid((M + l.threads / 32 - 1) / (l.threads / 32));
     } else if (l.variant == RRN_VARIANT_ROW_CLUSTER) {
         if (!vec_ok) return RRN_ERR_CONFIG;
