@@ -186,14 +186,16 @@ constexpr int kLnFwdTargetThreads = 64;
 // fp8 output: one row per warp up to this many vectors over many rows (plan_quant)
 constexpr int kQuantWarpMaxVec = 256;
 // RMSNorm backward: one row per warp (bwd_row_warp) up to this many vectors over many rows
-// (bf16, 64 Mi elements, back to back: 512 columns 89.1 -> 81.7 us plain, 100.9 -> 96.2 with
-// the gradient at residual_out; from 128 vectors the ring measured faster: 1024 columns 75.3
-// against 85.2, 2048 69.3 against 82.2)
-constexpr int kBwdWarpMaxVec = 64;
+// (bf16, 64 Mi elements, back to back, against the ring: 512 columns 89.1 -> 71.7 us plain,
+// 100.9 -> 88.5 with the gradient at residual_out; 1024 columns 75.1 -> 72.3 plain, while with
+// the gradient the ring stays ahead there, 87.6 against 89.2; 2048 columns the ring, 69.3
+// against 82.2)
+constexpr int kBwdWarpMaxVec = 128;
+constexpr int kBwdWarpMaxVecAddGrad = 64;
 // LayerNorm backward: one row per warp (ln_bwd_row_warp) up to this many vectors over many rows
-// (bf16, back to back, against a row per CTA of 2 vectors a thread: 512 columns 97.2 -> 91.5 us
-// plain, 106.9 -> 106.3 with the gradient at residual_out; 1024 columns 91.8 -> 86.7 and
-// 101.0 -> 100.0)
+// (bf16, back to back, against a row per CTA of 2 vectors a thread: 512 columns 97.2 -> 80.9 us
+// plain, 106.9 -> 97.2 with the gradient at residual_out; 1024 columns 91.8 -> 85.0 and
+// 101.0 -> 99.0)
 constexpr int kLnBwdWarpMaxVec = 128;
 // Vectors of a row each CTA of the cluster split takes when the planner chooses the cluster
 // size, for the fused forward (two input rows): measured best at 4 vectors x 128 threads a CTA.
@@ -496,7 +498,8 @@ int plan_bwd_impl(bool vec_ok, bool add_grad, int64_t M, int64_t N, int dtype,
         // kClusterChunkVec vectors (4 a thread x 128 threads, as the ring's CTAs), else the
         // two-pass kernel.
         const int64_t slot = (add_grad ? 3 : 2) * N * elem_size(dtype);
-        l.variant = regs ? (nvec <= kBwdWarpMaxVec && M >= 4LL * sms ? RRN_VARIANT_ROW_WARP
+        const int64_t warp_max = add_grad ? kBwdWarpMaxVecAddGrad : kBwdWarpMaxVec;
+        l.variant = regs ? (nvec <= warp_max && M >= 4LL * sms ? RRN_VARIANT_ROW_WARP
                             : slot <= kMaxDynSmem / 2                ? RRN_VARIANT_ROW_TMA
                                                                      : RRN_VARIANT_ROW_CTA)
                   : vec_ok && nvec <= static_cast<int64_t>(kMaxCluster) * kClusterChunkVec ? RRN_VARIANT_ROW_CLUSTER

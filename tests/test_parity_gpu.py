@@ -427,14 +427,17 @@ def test_wide_rows_backward_automatic_plan(dtype, N, variant, cluster):
 
 
 def test_short_rows_backward_plan():
-    """Rows of at most 64 vectors over many rows: one row per warp (with or without the gradient
-    at residual_out); from 128 vectors the ring."""
-    for N, variant in ((512, rrn.VARIANT_ROW_WARP), (256, rrn.VARIANT_ROW_WARP), (1024, rrn.VARIANT_ROW_TMA)):
+    """Short rows over many rows: one row per warp up to 128 vectors (64 with the gradient at
+    residual_out); beyond, the ring."""
+    for N, plain, fused in ((256, rrn.VARIANT_ROW_WARP, rrn.VARIANT_ROW_WARP),
+                            (512, rrn.VARIANT_ROW_WARP, rrn.VARIANT_ROW_WARP),
+                            (1024, rrn.VARIANT_ROW_WARP, rrn.VARIANT_ROW_TMA),
+                            (2048, rrn.VARIANT_ROW_TMA, rrn.VARIANT_ROW_TMA)):
         x = torch.empty(65536, N, device="cuda", dtype=torch.bfloat16)
         w = torch.empty(N, device="cuda", dtype=torch.bfloat16)
-        for g in (None, x):
+        for g, variant in ((None, plain), (x, fused)):
             p = rrn.plan_bwd(x, x, w, x, g)
-            assert p.variant == variant, (N, p)
+            assert p.variant == variant, (N, g is not None, p)
             if variant == rrn.VARIANT_ROW_WARP:
                 assert p.vpt * 32 >= N // 8 and p.threads == 128, p
     # and the full-size workload through the automatic plan matches the oracle
