@@ -82,19 +82,21 @@ def test_fused_backward_variants(dtype, N, with_dro):
         check_dw(dw.cpu().numpy().astype(np.float64), ref_dw, f"dw {launch}")
 
 
-def test_fused_backward_in_place():
-    M, N = 64, 4096
+@pytest.mark.parametrize("N,launch", [(4096, None), (512, rrn.Launch(rrn.VARIANT_ROW_WARP, 0, 128, 0))],
+                         ids=["auto", "row-per-warp"])
+def test_fused_backward_in_place(N, launch):
+    M = 64
     wl = synth.Workload("fused-bwd-alias", "add_rmsnorm_bwd", M, N, "bf16", 1e-6, 82)
     h = synth.make(wl)
     ref_dr, _ = oracle.add_rmsnorm_bwd(h["dy"], h["d_ro"], h["x"], h["w"], wl.eps)
     r, w = to_dev(h["x"], "bf16"), to_dev(h["w"], "bf16")
     _, rstd = rrn.rms_norm(r, w, wl.eps)
     dw = torch.empty(N, device="cuda")
-    ws = torch.empty(rrn.rmsnorm_bwd_workspace_bytes(M, N, r.dtype) // 4, device="cuda")
+    ws = torch.empty(max(rrn.rmsnorm_bwd_workspace_bytes(M, N, r.dtype), 4 * M * N) // 4, device="cuda")
     for target in ("dy", "d_ro", "r"):
         dy, dro, rr = to_dev(h["dy"], "bf16"), to_dev(h["d_ro"], "bf16"), r.clone()
         out = {"dy": dy, "d_ro": dro, "r": rr}[target]
-        rrn.add_rmsnorm_bwd(dy, dro, rr, w, rstd, out, dw, ws, wl.eps)
+        rrn.add_rmsnorm_bwd(dy, dro, rr, w, rstd, out, dw, ws, wl.eps, launch=launch)
         torch.cuda.synchronize()
         check_out(values(out), ref_dr, "bf16", f"d_r written over {target}")
 

@@ -188,6 +188,31 @@ def test_layernorm_backward_variants(dtype, N):
             check_dw(db.cpu().numpy().astype(np.float64), ref_db, f"LN db {launch}")
 
 
+@pytest.mark.parametrize("N,launch", [(4096, None), (1024, rrn.Launch(rrn.VARIANT_ROW_WARP, 0, 128, 0))],
+                         ids=["auto", "row-per-warp"])
+def test_layernorm_backward_in_place(N, launch):
+    """dx written over dy, over the gradient at residual_out, and over x."""
+    M = 70
+    wl = synth.Workload("ln-bwd-alias", "layernorm_bwd", M, N, "bf16", 1e-5, 94, x_mean=0.5)
+    h = synth.make(wl)
+    ref_dx, ref_dw, ref_db = oracle.add_layernorm_bwd(h["dy"], h["d_ro"], h["x"], h["w"], wl.eps)
+    cond = bwd_cond(h["x"], h["dy"], h["w"], wl.eps, layernorm=True) + np.abs(oracle.decode(h["d_ro"]))
+    w = to_dev(h["w"], "bf16")
+    x0 = to_dev(h["x"], "bf16")
+    _, mean, rstd = rrn.layer_norm(x0, w, None, wl.eps)
+    ws = torch.empty(max(rrn.layernorm_bwd_workspace_bytes(M, N, x0.dtype), 8 * M * N) // 4, device="cuda")
+    for target in ("dy", "d_ro", "x"):
+        x, dy, dro = x0.clone(), to_dev(h["dy"], "bf16"), to_dev(h["d_ro"], "bf16")
+        out = {"dy": dy, "d_ro": dro, "x": x}[target]
+        dw = torch.empty(N, device="cuda")
+        db = torch.empty(N, device="cuda")
+        rrn.layernorm_bwd(dy, dro, x, w, mean, rstd, out, dw, db, ws, wl.eps, launch=launch)
+        torch.cuda.synchronize()
+        check_out(values(out), ref_dx, "bf16", f"LN dx written over {target}, {launch}", cond)
+        check_dw(dw.cpu().numpy().astype(np.float64), ref_dw, f"LN dw ({target})")
+        check_dw(db.cpu().numpy().astype(np.float64), ref_db, f"LN db ({target})")
+
+
 def test_layernorm_backward_ring_needs_two_stages():
     """The backward's ring refills a slot one row late: one stage is refused before any launch."""
     M, N = 64, 4096

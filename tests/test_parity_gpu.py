@@ -460,8 +460,10 @@ def test_backward_is_deterministic():
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_backward_in_place(dtype):
-    M, N = 50, 4096
+@pytest.mark.parametrize("N,launch", [(4096, None), (512, rrn.Launch(rrn.VARIANT_ROW_WARP, 0, 128, 0))],
+                         ids=["auto", "row-per-warp"])
+def test_backward_in_place(dtype, N, launch):
+    M = 50
     wl = synth.Workload("bwd-alias", "rmsnorm_bwd", M, N, dtype, 1e-6, 71)
     h = synth.make(wl)
     dx_ref, dw_ref = oracle.rmsnorm_bwd(h["dy"], h["x"], h["w"], wl.eps)
@@ -469,11 +471,11 @@ def test_backward_in_place(dtype):
     x, w, dy = to_dev(h["x"], dtype), to_dev(h["w"], dtype), to_dev(h["dy"], dtype)
     _, rstd = rrn.rms_norm(x, w, wl.eps)
     dw = torch.empty(N, device="cuda")
-    ws = torch.empty(rrn.rmsnorm_bwd_workspace_bytes(M, N, x.dtype) // 4, device="cuda")
-    rrn.rmsnorm_bwd(dy, x, w, rstd, dy, dw, ws, wl.eps)      # dx over dy
+    ws = torch.empty(max(rrn.rmsnorm_bwd_workspace_bytes(M, N, x.dtype), 4 * M * N) // 4, device="cuda")
+    rrn.rmsnorm_bwd_ex(dy, x, w, rstd, dy, dw, ws, wl.eps, launch)      # dx over dy
     torch.cuda.synchronize()
     check_out(values(dy), dx_ref, dtype, "dx==dy", cond)
-    rrn.rmsnorm_bwd(to_dev(h["dy"], dtype), x, w, rstd, x, dw, ws, wl.eps)  # dx over x
+    rrn.rmsnorm_bwd_ex(to_dev(h["dy"], dtype), x, w, rstd, x, dw, ws, wl.eps, launch)  # dx over x
     torch.cuda.synchronize()
     check_out(values(x), dx_ref, dtype, "dx==x", cond)
     check_dw(dw.cpu().numpy().astype(np.float64), dw_ref)
