@@ -181,6 +181,11 @@ constexpr int kLnBwdSplitThreads = 128;
 constexpr int kLnBwdMinRingThreads = 128;
 // Widest row (in 128-bit vectors) one CTA holds in registers: 8 vectors x 256 threads.
 constexpr int kRowCtaMaxVec = 2048;
+// The fused forward takes a row per warp only up to this many vectors: from 129 to 256 vectors
+// a row per CTA measured faster (bf16, 64 Mi elements, back to back: 2048 columns 85.7 -> 79.7
+// us at 2 x 128, 1536 columns 95.7 -> 87.3 at 2 x 96; the plain forward keeps the row per warp
+// up to 256 vectors: 2048 columns 41.8 us against 64.3 for the best row-per-CTA layout).
+constexpr int kFwdWarpMaxVecFused = 128;
 constexpr int kLnFwdMaxVpt = 4;         // LayerNorm forward row layouts (plan_ln_fwd)
 constexpr int kLnFwdTargetThreads = 64;
 // fp8 output: one row per warp up to this many vectors over many rows (plan_quant)
@@ -349,7 +354,7 @@ int plan_fwd_impl(bool vec_ok, bool fused, int64_t M, int64_t N, int dtype, cons
         const bool few = M < 2LL * sms;
         const int64_t cta_max = few || !fused ? kRowCtaMaxVec : 128 * kMaxVpt;
         if (!vec_ok) l.variant = RRN_VARIANT_STREAM;
-        else if (nvec <= 32 * kMaxVpt && M >= 4LL * sms) l.variant = RRN_VARIANT_ROW_WARP;
+        else if (nvec <= (fused ? kFwdWarpMaxVecFused : 32 * kMaxVpt) && M >= 4LL * sms) l.variant = RRN_VARIANT_ROW_WARP;
         else if (nvec <= cta_max) l.variant = RRN_VARIANT_ROW_CTA;
         else if (nvec <= kClusterMaxVec) l.variant = RRN_VARIANT_ROW_CLUSTER;
         else l.variant = RRN_VARIANT_STREAM;

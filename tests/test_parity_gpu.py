@@ -189,6 +189,18 @@ def test_wide_rows_automatic_plan(dtype, N, fused, variant, extra):
     compare_fwd(h["x"], h.get("residual"), h["w"], dtype, wl.eps, y, ro, rstd)
 
 
+def test_short_rows_forward_plan():
+    """Many short rows: a row per warp up to 256 vectors plain, up to 128 fused (from 129 to 256
+    vectors the fused forward takes a row per CTA)."""
+    for N, fused, variant in ((1024, True, rrn.VARIANT_ROW_WARP), (1024, False, rrn.VARIANT_ROW_WARP),
+                              (2048, True, rrn.VARIANT_ROW_CTA), (2048, False, rrn.VARIANT_ROW_WARP),
+                              (1536, True, rrn.VARIANT_ROW_CTA)):
+        x = torch.empty(32768, N, device="cuda", dtype=torch.bfloat16)
+        w = torch.empty(N, device="cuda", dtype=torch.bfloat16)
+        p = rrn.plan_fwd(x, x if fused else None, x if fused else None, w, x)
+        assert p.variant == variant, (N, fused, p)
+
+
 def test_empty_matrix():
     # M == 0: the forward writes nothing; the backward's dw (and LayerNorm's db) are sums over
     # no rows, which the oracle's definition makes zero - the GPU calls must overwrite them so.
